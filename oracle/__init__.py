@@ -1,0 +1,16 @@
+"""fp64 CPU oracle of the selective-scan (S6) hot path.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline may import this package; the library in ``selective_state_space_145_b300``
+never does, and this package never imports it.
+"""
+
+from .oracle import (  # noqa: F401
+    causal_conv1d,
+    chunk_aggregates,
+    compose,
+    selective_scan,
+    silu,
+    softplus,
+    state_update,
+)

@@ -1,0 +1,151 @@
+"""ctypes front end of the fp64 CPU oracle (``ssm_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY. Inputs may be numpy arrays or CPU torch tensors of any
+float dtype; they are widened exactly to float64 (bf16 and fp32 values are
+representable in fp64) and passed to the C routines. Outputs are float64 numpy
+arrays. Nothing here does arithmetic of the method: it only marshals arguments.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+
+from . import build_oracle
+
+_lib = None
+_P = ctypes.POINTER(ctypes.c_double)
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = build_oracle.build()
+        lib = ctypes.CDLL(path)
+        L, I = ctypes.c_long, ctypes.c_int
+        lib.oracle_softplus.argtypes = [_P, _P, L]
+        lib.oracle_silu.argtypes = [_P, _P, L]
+        lib.oracle_causal_conv1d.argtypes = [_P, _P, _P, _P, _P, L, L, L, I, I, I]
+        lib.oracle_selective_scan.argtypes = ([_P] * 8 + [I] + [_P, _P, I] + [_P, _P, _P, _P, _P, _P]
+                                              + [L, L, L, L, I])
+        lib.oracle_compose.argtypes = [_P, _P, _P, _P, _P, _P, L]
+        lib.oracle_chunk_aggregates.argtypes = ([_P] * 5 + [I] + [_P, _P, I, _P, L, _P, _P]
+                                                + [L, L, L, L, I])
+        lib.oracle_state_update.argtypes = ([_P, _P] + [_P] * 8 + [I] + [_P, _P, I, _P] + [L, L, L, I])
+        for f in ("oracle_softplus", "oracle_silu", "oracle_causal_conv1d", "oracle_selective_scan",
+                  "oracle_compose", "oracle_chunk_aggregates", "oracle_state_update"):
+            getattr(lib, f).restype = None
+        _lib = lib
+    return _lib
+
+
+def _f64(a) -> Optional[np.ndarray]:
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().cpu().double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_P)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def softplus(x) -> np.ndarray:
+    x = _f64(x)
+    y = np.empty_like(x)
+    _load().oracle_softplus(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def silu(x) -> np.ndarray:
+    x = _f64(x)
+    y = np.empty_like(x)
+    _load().oracle_silu(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def causal_conv1d(x, w, bias=None, window=None, apply_silu: bool = True, nthreads: int = 1) -> np.ndarray:
+    """x [batch, dim, L], w [dim, K], bias [dim] or None, window [batch, dim, K-1] or None."""
+    x, w, bias, window = _f64(x), _f64(w), _f64(bias), _f64(window)
+    batch, dim, L = x.shape
+    K = w.shape[1]
+    out = np.empty_like(x)
+    _load().oracle_causal_conv1d(_ptr(x), _ptr(w), _ptr(bias), _ptr(window), _ptr(out), batch, dim, L, K,
+                                 int(apply_silu), nthreads)
+    return out
+
+
+def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True,
+                   conv_w=None, conv_b=None, conv_init=None, h0=None, want_conv_state: bool = False,
+                   want_trace: bool = False, nthreads: int = 1) -> Tuple[np.ndarray, ...]:
+    """Returns (out [b, d, L], h_last [b, d, N]) plus conv_state_out and/or h_trace [b, d, L, N] if asked."""
+    x, delta, A, B, C = _f64(x), _f64(delta), _f64(A), _f64(B), _f64(C)
+    D, z, delta_bias, conv_w, conv_b, conv_init, h0 = map(_f64, (D, z, delta_bias, conv_w, conv_b, conv_init, h0))
+    batch, dim, L = x.shape
+    N = A.shape[1]
+    K = conv_w.shape[1] if conv_w is not None else 0
+    out = np.empty((batch, dim, L))
+    h_last = np.empty((batch, dim, N))
+    cs = np.empty((batch, dim, max(K - 1, 0))) if (want_conv_state and K > 1) else None
+    tr = np.empty((batch, dim, L, N)) if want_trace else None
+    _load().oracle_selective_scan(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                  _ptr(delta_bias), int(delta_softplus), _ptr(conv_w), _ptr(conv_b), K,
+                                  _ptr(conv_init), _ptr(h0), _ptr(out), _ptr(h_last), _ptr(cs), _ptr(tr),
+                                  batch, dim, L, N, nthreads)
+    res = [out, h_last]
+    if want_conv_state:
+        res.append(cs)
+    if want_trace:
+        res.append(tr)
+    return tuple(res)
+
+
+def compose(a1, b1, a2, b2) -> Tuple[np.ndarray, np.ndarray]:
+    """(a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2), elementwise."""
+    a1, b1, a2, b2 = map(_f64, (a1, b1, a2, b2))
+    a = np.empty_like(a1)
+    b = np.empty_like(a1)
+    _load().oracle_compose(_ptr(a1), _ptr(b1), _ptr(a2), _ptr(b2), _ptr(a), _ptr(b), a1.size)
+    return a, b
+
+
+def chunk_aggregates(x, delta, A, B, delta_bias=None, delta_softplus: bool = True, conv_w=None, conv_b=None,
+                     conv_init=None, chunk_len: int = 64, nthreads: int = 1) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-chunk aggregates (a, b), each [batch, dim, nchunks, N]."""
+    x, delta, A, B = _f64(x), _f64(delta), _f64(A), _f64(B)
+    delta_bias, conv_w, conv_b, conv_init = map(_f64, (delta_bias, conv_w, conv_b, conv_init))
+    batch, dim, L = x.shape
+    N = A.shape[1]
+    K = conv_w.shape[1] if conv_w is not None else 0
+    q = (L + chunk_len - 1) // chunk_len
+    agg_a = np.empty((batch, dim, q, N))
+    agg_b = np.empty((batch, dim, q, N))
+    _load().oracle_chunk_aggregates(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(delta_bias),
+                                    int(delta_softplus), _ptr(conv_w), _ptr(conv_b), K, _ptr(conv_init),
+                                    chunk_len, _ptr(agg_a), _ptr(agg_b), batch, dim, L, N, nthreads)
+    return agg_a, agg_b
+
+
+def state_update(state, conv_state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                 delta_softplus: bool = True, conv_w=None, conv_b=None, nthreads: int = 1):
+    """One decode step. Returns (y [batch, dim], new state, new conv_state); the inputs are not modified."""
+    state = _f64(state).copy()
+    conv_state = _f64(conv_state).copy() if conv_state is not None else None
+    x, delta, A, B, C = _f64(x), _f64(delta), _f64(A), _f64(B), _f64(C)
+    D, z, delta_bias, conv_w, conv_b = map(_f64, (D, z, delta_bias, conv_w, conv_b))
+    batch, dim = x.shape
+    N = A.shape[1]
+    K = conv_w.shape[1] if conv_w is not None else 0
+    y = np.empty((batch, dim))
+    _load().oracle_state_update(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                _ptr(D), _ptr(z), _ptr(delta_bias), int(delta_softplus), _ptr(conv_w),
+                                _ptr(conv_b), K, _ptr(y), batch, dim, N, nthreads)
+    return y, state, conv_state

@@ -1,0 +1,325 @@
+"""Pins of the fp64 CPU oracle against what the pages and the mathematics fix.
+
+Each test ties the oracle to something other than itself: a closed form, a
+limit, brute-force products on tiny inputs, a library routine for a special
+case, an invariant of the method, or a worked example. Together they are chosen
+so that a dropped term, a wrong sign or index, or a transposed operand in the
+oracle fails at least one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+RNG = np.random.default_rng(145)
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(*shape):
+    return RNG.standard_normal(shape)
+
+
+def _neg_A(dim, N, lo=0.2, hi=2.0):
+    return -RNG.uniform(lo, hi, size=(dim, N))
+
+
+def _silu_lib(x):
+    return F.silu(torch.as_tensor(x, dtype=torch.float64)).numpy()
+
+
+# ---------------------------------------------------------------- library special cases
+
+def test_softplus_matches_torch():
+    # "Mamba" (ai360xpert.com), selection mechanism: Delta = softplus(.)
+    x = np.concatenate([np.linspace(-60, 60, 2001), _rand(1000) * 5])
+    ref = F.softplus(torch.as_tensor(x), beta=1.0, threshold=1e4).numpy()
+    np.testing.assert_allclose(oracle.softplus(x), ref, rtol=5e-16, atol=0)
+
+
+def test_silu_matches_torch():
+    x = np.concatenate([np.linspace(-40, 40, 801), _rand(1000) * 4])
+    np.testing.assert_allclose(oracle.silu(x), _silu_lib(x), rtol=4e-16, atol=1e-300)
+
+
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_causal_conv_matches_torch_conv1d(K):
+    # "Overview of Mamba (SSM) Model", block: depthwise causal conv then SiLU.
+    b, d, L = 2, 5, 19
+    x, w, bias = _rand(b, d, L), _rand(d, K), _rand(d)
+    ref = F.conv1d(torch.as_tensor(x), torch.as_tensor(w)[:, None, :], torch.as_tensor(bias),
+                   padding=K - 1, groups=d)[..., :L].numpy()
+    np.testing.assert_allclose(oracle.causal_conv1d(x, w, bias, apply_silu=False), ref, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(oracle.causal_conv1d(x, w, bias, apply_silu=True), _silu_lib(ref),
+                               rtol=1e-14, atol=1e-14)
+    # a supplied window plays the role of the inputs before t = 0
+    win = _rand(b, d, K - 1)
+    ref_w = F.conv1d(torch.as_tensor(np.concatenate([win, x], axis=-1)), torch.as_tensor(w)[:, None, :],
+                     torch.as_tensor(bias), groups=d).numpy()
+    np.testing.assert_allclose(oracle.causal_conv1d(x, w, bias, window=win, apply_silu=False), ref_w,
+                               rtol=1e-14, atol=1e-14)
+
+
+def test_scan_with_conv_equals_conv_then_scan():
+    # the fused prologue is the library conv (+SiLU) followed by the plain scan
+    b, d, L, N, K = 2, 3, 23, 4, 4
+    x, delta, z = _rand(b, d, L), 0.5 * _rand(b, d, L), _rand(b, d, L)
+    A, B, C, D, bias = _neg_A(d, N), _rand(b, N, L), _rand(b, N, L), _rand(d), _rand(d) - 2
+    w, cb = RNG.uniform(-0.5, 0.5, (d, K)), _rand(d)
+    u = _silu_lib(F.conv1d(torch.as_tensor(x), torch.as_tensor(w)[:, None, :], torch.as_tensor(cb),
+                           padding=K - 1, groups=d)[..., :L].numpy())
+    out1, h1 = oracle.selective_scan(x, delta, A, B, C, D, z, bias, True, w, cb)
+    out2, h2 = oracle.selective_scan(u, delta, A, B, C, D, z, bias, True)
+    np.testing.assert_allclose(out1, out2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(h1, h2, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_lti_closed_form_convolution():
+    """Delta, B, C constant in t: the scan is the LTI convolution
+    y_t = sum_k (sum_n C_n Abar_n^k Delta B_n) u_{t-k} + sum_n C_n Abar_n^{t+1} h0_n + D u_t
+    ("Mamba" ai360xpert.com: fixed-Delta SSM; "Mamba" ozercemkelahmet.com, step 1-2)."""
+    b, d, L, N = 2, 3, 40, 4
+    Delta = RNG.uniform(0.05, 0.6, (b, d))
+    Bc, Cc = _rand(b, N), _rand(b, N)
+    A, D, u, z, h0 = _neg_A(d, N), _rand(d), _rand(b, d, L), _rand(b, d, L), _rand(b, d, N)
+    delta = np.repeat(Delta[:, :, None], L, axis=2)
+    B = np.repeat(Bc[:, :, None], L, axis=2)
+    C = np.repeat(Cc[:, :, None], L, axis=2)
+    out, h_last = oracle.selective_scan(u, delta, A, B, C, D, z, None, False, h0=h0)
+    ref = np.zeros((b, d, L))
+    for bi in range(b):
+        for di in range(d):
+            Abar = np.exp(Delta[bi, di] * A[di])                                   # [N]
+            kern = np.array([np.sum(Cc[bi] * Abar ** k * Delta[bi, di] * Bc[bi]) for k in range(L)])
+            y = np.convolve(u[bi, di], kern)[:L] + D[di] * u[bi, di]
+            y += np.array([np.sum(Cc[bi] * Abar ** (t + 1) * h0[bi, di]) for t in range(L)])
+            ref[bi, di] = y * _silu_lib(z[bi, di])
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_lti_constant_input_geometric_sum():
+    """Constant u, Delta, B: h_t[n] = Delta B_n u (1 - Abar_n^{t+1}) / (1 - Abar_n) from h = 0."""
+    d, L, N = 3, 57, 5
+    Delta = RNG.uniform(0.01, 0.3, (1, d))
+    Bc, A = _rand(1, N), _neg_A(d, N)
+    uval = 1.7
+    u = np.full((1, d, L), uval)
+    delta = np.repeat(Delta[:, :, None], L, axis=2)
+    B = np.repeat(Bc[:, :, None], L, axis=2)
+    C = _rand(1, N, L)
+    _, _, trace = oracle.selective_scan(u, delta, A, B, C, None, None, None, False, want_trace=True)
+    for di in range(d):
+        Abar = np.exp(Delta[0, di] * A[di])
+        for t in (0, 1, 10, L - 1):
+            ref = Delta[0, di] * Bc[0] * uval * (1 - Abar ** (t + 1)) / (1 - Abar)
+            np.testing.assert_allclose(trace[0, di, t], ref, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- limits of the step size
+
+def test_small_delta_keeps_state():
+    """Delta -> 0: Abar -> 1 and Bbar -> 0, so h_t = h0 and y_t = C_t.h0 + D u_t
+    ("Mamba" ai360xpert.com: small Delta keeps the state; "Mamba" ozercemkelahmet.com step 3)."""
+    b, d, L, N = 2, 3, 33, 4
+    x, z, B, C = _rand(b, d, L), _rand(b, d, L), _rand(b, N, L), _rand(b, N, L)
+    A, D, h0 = _neg_A(d, N), _rand(d), _rand(b, d, N)
+    delta = np.full((b, d, L), -40.0)                     # softplus(-40) ~ 4.2e-18
+    out, h_last = oracle.selective_scan(x, delta, A, B, C, D, z, np.zeros(d), True, h0=h0)
+    np.testing.assert_allclose(h_last, h0, rtol=1e-15, atol=1e-15)
+    ref = (np.einsum("bnt,bdn->bdt", C, h0) + D[None, :, None] * x) * _silu_lib(z)
+    np.testing.assert_allclose(out, ref, rtol=1e-14, atol=1e-14)
+
+
+def test_large_delta_forgets_past():
+    """Large Delta with A <= -1: Abar ~ 0, so the output is memoryless:
+    y_t = Delta u_t (C_t . B_t) + D u_t ("Mamba" ai360xpert.com: large Delta resets the state)."""
+    b, d, L, N = 2, 3, 29, 4
+    x, z, B, C = _rand(b, d, L), _rand(b, d, L), _rand(b, N, L), _rand(b, N, L)
+    A, D, h0 = -1.0 - RNG.uniform(0, 1, (d, N)), _rand(d), _rand(b, d, N)
+    delta = np.full((b, d, L), 40.0)
+    out, h_last = oracle.selective_scan(x, delta, A, B, C, D, z, np.zeros(d), True, h0=h0)
+    Delta = 40.0 + math.log1p(math.exp(-40.0))
+    ref = (Delta * x * np.einsum("bnt,bnt->bt", C, B)[:, None, :] + D[None, :, None] * x) * _silu_lib(z)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(h_last, Delta * B[:, None, :, -1] * x[:, :, -1:], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute_force(x, delta, A, B, C, D, z, bias, w, cb, win, h0):
+    """Unrolled: h_T = (prod_{r<=T} Abar_r) h0 + sum_s (prod_{r=s+1}^{T} Abar_r) Bbar_s u_s, scalars only."""
+    b, d, L = x.shape
+    N = A.shape[1]
+    K = w.shape[1]
+    out = np.zeros((b, d, L))
+    hL = np.zeros((b, d, N))
+    for bi in range(b):
+        for di in range(d):
+            stream = list(win[bi, di]) + list(x[bi, di])
+            u = []
+            for t in range(L):
+                acc = sum(w[di, k] * stream[t + k] for k in range(K)) + cb[di]
+                u.append(acc / (1.0 + math.exp(-acc)))
+            Dl = [math.log1p(math.exp(delta[bi, di, t] + bias[di])) for t in range(L)]
+            for T in range(L):
+                y = 0.0
+                for n in range(N):
+                    Abar = [math.exp(Dl[r] * A[di, n]) for r in range(L)]
+                    p0 = 1.0
+                    for r in range(T + 1):
+                        p0 *= Abar[r]
+                    hT = p0 * h0[bi, di, n]
+                    for s in range(T + 1):
+                        p = 1.0
+                        for r in range(s + 1, T + 1):
+                            p *= Abar[r]
+                        hT += p * Dl[s] * B[bi, n, s] * u[s]
+                    y += C[bi, n, T] * hT
+                    if T == L - 1:
+                        hL[bi, di, n] = hT
+                y += D[di] * u[T]
+                out[bi, di, T] = y * z[bi, di, T] / (1.0 + math.exp(-z[bi, di, T]))
+    return out, hL
+
+
+def test_brute_force_tiny():
+    b, d, L, N, K = 2, 3, 7, 3, 3
+    x, delta, z = _rand(b, d, L), 0.8 * _rand(b, d, L), _rand(b, d, L)
+    A, B, C, D, bias = _neg_A(d, N), _rand(b, N, L), _rand(b, N, L), _rand(d), _rand(d) - 1
+    w, cb, win, h0 = RNG.uniform(-0.5, 0.5, (d, K)), _rand(d), _rand(b, d, K - 1), _rand(b, d, N)
+    out, hL = oracle.selective_scan(x, delta, A, B, C, D, z, bias, True, w, cb, conv_init=win, h0=h0)
+    ref, refL = _brute_force(x, delta, A, B, C, D, z, bias, w, cb, win, h0)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(hL, refL, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- invariants
+
+def _problem(b=2, d=3, L=21, N=4, K=4):
+    return dict(x=_rand(b, d, L), delta=0.7 * _rand(b, d, L), A=_neg_A(d, N), B=_rand(b, N, L), C=_rand(b, N, L),
+                D=_rand(d), z=_rand(b, d, L), delta_bias=_rand(d) - 1.5, conv_w=RNG.uniform(-0.5, 0.5, (d, K)),
+                conv_b=_rand(d), conv_init=_rand(b, d, K - 1), h0=_rand(b, d, N))
+
+
+def test_chunked_prompt_equals_whole_prompt():
+    """Processing a prompt in two calls that pass on (h, conv window) equals one call
+    ("Mamba" ozercemkelahmet.com, deployment notes: chunks pass the state on)."""
+    p = _problem()
+    L = p["x"].shape[-1]
+    full, hfull, csfull = oracle.selective_scan(**p, want_conv_state=True)
+    for L1 in range(1, L):
+        a = {k: (v[..., :L1] if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+        out1, h1, cs1 = oracle.selective_scan(**a, want_conv_state=True)
+        bpart = {k: (v[..., L1:] if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+        bpart["h0"], bpart["conv_init"] = h1, cs1
+        out2, h2, cs2 = oracle.selective_scan(**bpart, want_conv_state=True)
+        np.testing.assert_array_equal(np.concatenate([out1, out2], axis=-1), full)
+        np.testing.assert_array_equal(h2, hfull)
+        np.testing.assert_array_equal(cs2, csfull)
+
+
+def test_recurrent_mode_equals_parallel_mode():
+    """K decode steps from (state, window) equal one scan over the same K tokens with
+    h0 = state and the conv window as the inputs before t = 0
+    ("Mamba" ozercemkelahmet.com, sanity checks: recurrent and parallel mode agree)."""
+    p = _problem(L=9)
+    out, hL, cs = oracle.selective_scan(**p, want_conv_state=True)
+    state, window = p["h0"], p["conv_init"]
+    for t in range(p["x"].shape[-1]):
+        y, state, window = oracle.state_update(state, window, p["x"][..., t], p["delta"][..., t], p["A"],
+                                               p["B"][..., t], p["C"][..., t], p["D"], p["z"][..., t],
+                                               p["delta_bias"], True, p["conv_w"], p["conv_b"])
+        np.testing.assert_array_equal(y, out[..., t])
+    np.testing.assert_array_equal(state, hL)
+    np.testing.assert_array_equal(window, cs)
+
+
+def test_compose_is_function_composition_and_associative():
+    n = 1000
+    a1, a2, a3 = (RNG.uniform(0, 1, n) for _ in range(3))
+    b1, b2, b3 = (_rand(n) for _ in range(3))
+    h = _rand(n)
+    a12, b12 = oracle.compose(a1, b1, a2, b2)
+    # applying (a1, b1) then (a2, b2) to h
+    np.testing.assert_allclose(a12 * h + b12, a2 * (a1 * h + b1) + b2, rtol=1e-14, atol=1e-14)
+    left = oracle.compose(a12, b12, a3, b3)
+    a23, b23 = oracle.compose(a2, b2, a3, b3)
+    right = oracle.compose(a1, b1, a23, b23)
+    np.testing.assert_allclose(left[0], right[0], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(left[1], right[1], rtol=1e-14, atol=1e-14)
+    one, zero = np.ones(n), np.zeros(n)
+    for got in (oracle.compose(one, zero, a1, b1), oracle.compose(a1, b1, one, zero)):
+        np.testing.assert_array_equal(got[0], a1)
+        np.testing.assert_array_equal(got[1], b1)
+
+
+@pytest.mark.parametrize("chunk", [1, 4, 5, 8, 21, 64])
+def test_chunk_carry_equals_sequential(chunk):
+    """Chunk aggregates composed in order give the state at every chunk boundary, and each
+    chunk rerun from that state reproduces the sequential output (the cross-chunk carry)."""
+    p = _problem(L=21)
+    L = p["x"].shape[-1]
+    out, hL, trace = oracle.selective_scan(**p, want_trace=True)
+    agg_a, agg_b = oracle.chunk_aggregates(p["x"], p["delta"], p["A"], p["B"], p["delta_bias"], True,
+                                           p["conv_w"], p["conv_b"], p["conv_init"], chunk_len=chunk)
+    h = p["h0"].copy()
+    K = p["conv_w"].shape[1]
+    stream = np.concatenate([p["conv_init"], p["x"]], axis=-1)
+    for q in range(agg_a.shape[2]):
+        t0, t1 = q * chunk, min(L, (q + 1) * chunk)
+        sub = {k: (v[..., t0:t1] if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+        sub["h0"], sub["conv_init"] = h, stream[..., t0:t0 + K - 1]
+        o, _ = oracle.selective_scan(**sub)
+        np.testing.assert_allclose(o, out[..., t0:t1], rtol=1e-12, atol=1e-12)
+        h = agg_a[:, :, q] * h + agg_b[:, :, q]
+        np.testing.assert_allclose(h, trace[:, :, t1 - 1], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(h, hL, rtol=1e-12, atol=1e-12)
+
+
+def test_decay_is_monotone_without_input():
+    """A < 0 and Delta > 0 give 0 < Abar < 1: with no input the state shrinks every step."""
+    b, d, L, N = 1, 4, 50, 6
+    x, delta = _rand(b, d, L), _rand(b, d, L)
+    out, hL, trace = oracle.selective_scan(x, delta, _neg_A(d, N), np.zeros((b, N, L)), _rand(b, N, L),
+                                           None, None, np.zeros(d), True, h0=_rand(b, d, N), want_trace=True)
+    ratio = trace[:, :, 1:] / trace[:, :, :-1]
+    assert np.all(ratio > 0) and np.all(ratio < 1)
+
+
+def test_decode_window_shifts_raw_inputs():
+    """The decode window keeps the last K-1 raw inputs, oldest first."""
+    d, N, K = 3, 2, 4
+    win = _rand(1, d, K - 1)
+    xs = _rand(5, 1, d)
+    state = np.zeros((1, d, N))
+    for t in range(5):
+        _, state, win2 = oracle.state_update(state, win, xs[t], np.zeros((1, d)), _neg_A(d, N), _rand(1, N),
+                                             _rand(1, N), None, None, None, True, RNG.uniform(-1, 1, (d, K)), None)
+        np.testing.assert_array_equal(win2, np.concatenate([win[..., 1:], xs[t][..., None]], axis=-1))
+        win = win2
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_scalar_walkthrough_golden():
+    """The pages' scalar walk-through with the step sizes fixed by the fixture."""
+    with open(os.path.join(GOLDEN, "scalar_walkthrough.json")) as f:
+        g = json.load(f)
+    L = len(g["inputs"])
+    x = np.array(g["inputs"], dtype=np.float64).reshape(1, 1, L)
+    Delta = np.array([math.log(v) for v in g["delta_as_log_of"]]).reshape(1, 1, L)
+    A = np.array([[-g["a"]]])
+    ones = np.ones((1, 1, L))
+    out, hL, tr = oracle.selective_scan(x, Delta, A, ones, ones, None, None, None, False, want_trace=True)
+    ln2 = math.log(2.0)
+    expect = np.array([num / den * ln2 for num, den in g["state_over_ln2"]])
+    np.testing.assert_allclose(tr[0, 0, :, 0], expect, rtol=1e-14, atol=0)
+    np.testing.assert_allclose(out[0, 0], expect, rtol=1e-14, atol=0)
