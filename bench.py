@@ -1,0 +1,446 @@
+"""Benchmark of the selective-scan hot path on B300: state updates/s and achieved HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input: for a prefill
+workload one call of ssm_selective_scan_fwd (conv prologue + Delta + discretisation +
+recurrence + readout + gate, plus the chunk-carry kernel when the scan is chunked); for the
+decode workload its 64 consecutive ssm_selective_state_update calls. Inputs are resident in
+HBM; L2 is flushed (a 256 MiB write) before every timed step, outside the step's events.
+Each step is timed with CUDA events on the launching stream.
+
+Prints ONE JSON line (rank 0). Under torchrun every rank runs its own copy of the workload
+(weak scaling, no collective on the data path); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "block_f32_b2_d1024_l1024_n16_k4"
+METRIC = "selective-scan state updates/s (B*L*D*N) and HBM GB/s vs B300 peak"
+UNIT = "updates/s"
+FALLBACK_HBM_GBS = 6400.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes every input read once / every output written once, per step (no per-step state)."""
+    es = 2 if w.io == "bf16" else 4
+    N, K = w.dstate, w.d_conv
+    if w.kind == "decode":
+        ch = w.batch * w.dim
+        per = (ch * N * 4 * 2                      # state read + write
+               + ch * (K - 1) * es * 2             # window read + write
+               + ch * es * 4                       # x, delta, z in; y out
+               + w.batch * N * es * 2              # B, C
+               + w.dim * N * 4                     # A
+               + w.dim * 4 * 3                     # D, delta_bias, conv bias
+               + w.dim * K * 4)                    # conv weights
+        return per * w.steps
+    tokens = w.batch * w.dim * w.seqlen
+    b = tokens * es * 4                            # x (or u), delta, z in; y out
+    b += 2 * w.batch * N * w.seqlen * es           # B, C
+    b += w.batch * w.dim * N * 4                   # h_last out
+    b += w.dim * N * 4                             # A
+    b += w.dim * 4 * 2                             # D, delta_bias
+    if K:
+        b += w.dim * 4 + w.dim * K * 4             # conv bias, conv weights
+    return b
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_145_b300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(workload: str):
+    """DRAM bytes per step from a committed ncu summary, if its kernel-source hash is current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_step")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        rows = []
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[2 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def oracle_sample_rate(w, target_s: float = 10.0, max_channels: int = 1024):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the workload's channels.
+
+    Returns (updates/s, cores, sample description)."""
+    import numpy as np
+
+    import oracle
+    from selective_state_space_145_b300 import inputs
+
+    cores = oracle.oracle.default_threads()
+    if w.kind == "decode":
+        q = inputs.decode_inputs(min(w.batch, 16), w.dim, w.dstate, w.d_conv, w.io, w.seed, steps=1)
+        state, win = q["state"].double().numpy(), q["conv_state"].double().numpy()
+        ups = 0
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < target_s:
+            _, state, win = oracle.state_update(state, win, q["x"][0], q["delta"][0], q["A"], q["B"][0], q["C"][0],
+                                                q["D"], q["z"][0], q["delta_bias"], True, q["conv_w"], q["conv_b"],
+                                                nthreads=cores)
+            ups += state.size
+            reps += 1
+        dt = time.perf_counter() - t0
+        return ups / dt, cores, f"{reps} decode steps of {state.shape[0]} sequences x {w.dim} channels"
+    # prefill: full-length rows of a subset of channels
+    nch = max(1, min(max_channels, w.batch * w.dim))
+    bsub = 1
+    dsub = min(w.dim, nch)
+    p = inputs.scan_inputs(bsub, dsub, w.seqlen, w.dstate, w.d_conv, w.io, w.seed, salient_frac=w.salient_frac)
+    # size the sample so it takes about target_s
+    L = w.seqlen
+    probe_len = min(L, 256)
+    t0 = time.perf_counter()
+    oracle.selective_scan(p["x"][..., :probe_len], p["delta"][..., :probe_len], p["A"], p["B"][..., :probe_len],
+                          p["C"][..., :probe_len], p["D"], p["z"][..., :probe_len], p["delta_bias"], True,
+                          p["conv_w"], p["conv_b"], nthreads=cores)
+    per_step = (time.perf_counter() - t0) / probe_len
+    use_len = int(max(probe_len, min(L, target_s / max(per_step, 1e-9))))
+    sub = {k: (v[..., :use_len] if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.selective_scan(sub["x"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"], sub["z"],
+                              sub["delta_bias"], True, sub["conv_w"], sub["conv_b"], nthreads=cores)
+        reps += 1
+        if time.perf_counter() - t0 >= target_s or reps >= 10000:
+            break
+    dt = time.perf_counter() - t0
+    ups = reps * dsub * use_len * w.dstate
+    return ups / dt, cores, (f"{reps} pass(es) over {dsub} channels x {use_len} steps x N={w.dstate} "
+                             f"of the workload's inputs (fp64, {cores} threads)")
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    rates = []
+    desc, cores = "", 1
+    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        r, cores, desc = oracle_sample_rate(w, target_s=budget)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.mean(rates)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    c = {"workload": w.name, "kind": w.kind, "io": w.io, "batch": w.batch, "d_inner": w.dim, "seqlen": w.seqlen,
+         "d_state": w.dstate, "d_conv": w.d_conv, "l2": "flushed before every timed step (256 MiB write)"}
+    if w.d_model:
+        c.update({"d_model": w.d_model, "expand": w.expand})
+    if w.kind == "decode":
+        c["decode_steps_per_step"] = w.steps
+    if w.salient_frac:
+        c["salient_frac"] = w.salient_frac
+    return c
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w):
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import selective_state_space_145_b300 as ssm
+    from selective_state_space_145_b300 import inputs
+
+    p = inputs.workload_inputs(w) if world == 1 else inputs.workload_inputs(
+        inputs.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank}))
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    if w.kind == "decode":
+        state0, win0 = g["state"].clone(), g["conv_state"].clone()
+
+        def step():
+            for t in range(w.steps):
+                ssm.ssm_selective_state_update(g["state"], g["conv_state"], g["x"][t], g["delta"][t], g["A"],
+                                               g["B"][t], g["C"][t], g["D"], g["z"][t], g["delta_bias"], True,
+                                               g["conv_w"], g["conv_b"], y=ybuf[t])
+
+        ybuf = torch.empty(w.steps, w.batch, w.dim, dtype=g["x"].dtype, device=dev)
+        launches_per_step = w.steps
+        kernels = ["decode_kernel"]
+    else:
+        cl = ssm.ssm_scan_default_chunk_len(w.batch, w.dim, w.seqlen, w.dstate, g["x"].dtype)
+        nchunks = (w.seqlen + cl - 1) // cl
+        ws_bytes = ssm.ssm_scan_workspace_bytes(w.batch, w.dim, w.seqlen, w.dstate, 0, g["x"].dtype)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(g["x"])
+        h_last = torch.empty(w.batch, w.dim, w.dstate, dtype=torch.float32, device=dev)
+
+        def step():
+            ssm.ssm_selective_scan_fwd(g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"],
+                                       True, g["conv_w"], g["conv_b"], None, None, workspace=ws, out=out,
+                                       h_last=h_last)
+
+        launches_per_step = 2 if nchunks > 1 else 1
+        kernels = ["scan_kernel<carry>", "scan_kernel<main>"] if nchunks > 1 else ["scan_kernel<main>"]
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = statistics.mean(step_ms)
+    ms = reduce_max(ms_local, world, dev)
+
+    updates = w.updates
+    value = updates * world / (ms * 1e-3)
+    bytes_step = algorithmic_bytes(w)
+    peak, peak_kind = _peaks()
+    achieved = bytes_step / (ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: pinned H2D of the step's inputs,
+    # the call(s), D2H of the results, all inside the events
+    e2e = None
+    if rank == 0 or world > 1:
+        host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+        dev_in = {k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+        if w.kind == "decode":
+            res_host = torch.empty(w.steps, w.batch, w.dim, dtype=host["x"].dtype).pin_memory()
+            st_host = torch.empty_like(host["state"]).pin_memory()
+
+            def e2e_step():
+                for k, v in host.items():
+                    if isinstance(v, torch.Tensor):
+                        dev_in[k].copy_(v, non_blocking=True)
+                for t in range(w.steps):
+                    ssm.ssm_selective_state_update(dev_in["state"], dev_in["conv_state"], dev_in["x"][t],
+                                                   dev_in["delta"][t], dev_in["A"], dev_in["B"][t], dev_in["C"][t],
+                                                   dev_in["D"], dev_in["z"][t], dev_in["delta_bias"], True,
+                                                   dev_in["conv_w"], dev_in["conv_b"], y=ybuf[t])
+                res_host.copy_(ybuf, non_blocking=True)
+                st_host.copy_(dev_in["state"], non_blocking=True)
+
+            d2h = res_host.numel() * res_host.element_size() + st_host.numel() * 4
+        else:
+            out_host = torch.empty_like(host["x"]).pin_memory()
+            hl_host = torch.empty(w.batch, w.dim, w.dstate, dtype=torch.float32).pin_memory()
+
+            def e2e_step():
+                for k, v in host.items():
+                    if isinstance(v, torch.Tensor):
+                        dev_in[k].copy_(v, non_blocking=True)
+                ssm.ssm_selective_scan_fwd(dev_in["x"], dev_in["delta"], dev_in["A"], dev_in["B"], dev_in["C"],
+                                           dev_in["D"], dev_in["z"], dev_in["delta_bias"], True, dev_in["conv_w"],
+                                           dev_in["conv_b"], None, None, workspace=ws, out=out, h_last=h_last)
+                out_host.copy_(out, non_blocking=True)
+                hl_host.copy_(h_last, non_blocking=True)
+
+            d2h = out_host.numel() * out_host.element_size() + hl_host.numel() * 4
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 20))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, world, dev)
+        e2e = {"value": updates * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r, cores, desc = oracle_sample_rate(w, target_s=args.cpu_seconds)
+        cpu = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": config_of(w),
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic_from_profiles(w.name), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_step": bytes_step,
+                     "timed": "whole step (" + " + ".join(kernels) + "), CUDA events on the launching stream"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    from selective_state_space_145_b300 import inputs
+
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

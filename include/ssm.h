@@ -1,0 +1,177 @@
+/*
+ * ssm.h -- C ABI of the B300 selective state-space (S6) library, libssm.so.
+ *
+ * Three operations, each on the caller's CUDA stream:
+ *   ssm_causal_conv1d_fwd       depthwise causal conv1d (+ SiLU), the block's short conv
+ *   ssm_selective_scan_fwd      selective scan forward (optionally with the conv fused in
+ *                               front), returning y and the final state h_L
+ *   ssm_selective_state_update  one recurrent (decode) step for a batch of sequences
+ *
+ * Sources (page title, section):
+ *   "Mamba" (ai360xpert.com, core ML), "The selection mechanism":
+ *       Delta_t = softplus(W x_t + b), Abar_t = exp(Delta_t A), Bbar_t ~ Delta_t B.
+ *   "Mamba (Selective State-Space Model)" (gunjandhanuka.github.io), "Key math":
+ *       B_t, C_t, Delta_t computed from the input; A learned; hardware-aware parallel scan.
+ *   "Mamba" (ozercemkelahmet.com/tools/mamba), "How it works" steps 1-5,
+ *       "A minimal selective scan in PyTorch", "Deployment notes" (state passed between
+ *       prompt chunks; constant-size state at inference).
+ *   "Overview of Mamba (SSM) Model" (bembew.net), "How the Mamba Block Works":
+ *       depthwise conv + SiLU before the SSM, SiLU(z) gate, Mamba(d_model, d_state, d_conv, expand).
+ *
+ * Conventions shared by every call
+ *   - Device pointers only (cudaMalloc'd or equivalent), contiguous, row-major, in the
+ *     layouts stated per argument. The caller owns every buffer, including the scan's
+ *     workspace; the library allocates nothing and keeps no state between calls.
+ *   - Per-token tensors use the I/O dtype `io` (SSM_F32 = float, SSM_BF16 = bfloat16).
+ *     Parameters (A, D, delta_bias, conv weight/bias) and states (h0, h_last, the decode
+ *     state) are always float32. Arithmetic is float32 throughout; bf16 results are
+ *     rounded to nearest-even once, on store.
+ *   - Pointers must be aligned to their element size. Per-token base pointers that are
+ *     16-byte aligned, with rows whose byte length is a multiple of 16, take the
+ *     vectorised path; anything else takes a slower element-wise path with the same
+ *     results.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call is
+ *     asynchronous with respect to the host and does not synchronise.
+ *   - Errors: argument checks happen on the host before any launch and return
+ *     SSM_ERR_INVALID_ARG or SSM_ERR_UNSUPPORTED without touching device memory. A
+ *     failed launch returns SSM_ERR_CUDA. No call aborts, prints or throws.
+ *   - Empty work (batch == 0 or dim == 0) returns SSM_OK without a launch.
+ *   - dstate (N) is 1..16. d_conv (K) is 1..4 when a conv weight is given.
+ *   - Tensors named as inputs are only read; outputs must not alias inputs, except the
+ *     decode state and window, which are updated in place.
+ */
+#ifndef SSM_H_
+#define SSM_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_INVALID_ARG = 1, /* a required pointer is NULL, a size is negative, a buffer is too small */
+  SSM_ERR_UNSUPPORTED = 2, /* a valid request outside the compiled limits (dstate > 16, d_conv > 4,
+                              misaligned pointer, unknown dtype) */
+  SSM_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+SSM_API int ssm_version(void);
+
+/* Static, human-readable name of a status code. */
+SSM_API const char* ssm_status_string(int status);
+
+/*
+ * Causal depthwise conv1d of every channel, optionally followed by SiLU:
+ *   out[b,d,t] = act( sum_{k=0}^{K-1} w[d,k] * x[b,d,t-(K-1)+k] + bias[d] ),
+ * where x[b,d,s] for s < 0 is conv_init[b,d,(K-1)+s] (or 0 when conv_init is NULL).
+ * ("Overview of Mamba (SSM) Model", block: depthwise convolution and SiLU before the SSM;
+ *  "Mamba" ozercemkelahmet.com, glossary: a causal conv only sees current and past positions.)
+ *
+ *   x          [batch, dim, seqlen] io        input
+ *   w          [dim, d_conv] float32          filter taps; w[d, K-1] multiplies the current input
+ *   bias       [dim] float32 or NULL (= 0)
+ *   conv_init  [batch, dim, d_conv-1] io or NULL: raw inputs preceding t = 0, oldest first
+ *   out        [batch, dim, seqlen] io        output (must not alias x)
+ *   apply_silu 0 or 1
+ */
+SSM_API ssm_status ssm_causal_conv1d_fwd(const void* x, const float* w, const float* bias, const void* conv_init,
+                                 void* out, int batch, int dim, int seqlen, int d_conv, int apply_silu,
+                                 ssm_dtype io, void* stream);
+
+/*
+ * Chunk length the scan uses when asked for chunk_len = 0, for this problem on the
+ * current device (a multiple of 64, or seqlen rounded up to 64 when no chunking pays).
+ */
+SSM_API int ssm_scan_default_chunk_len(int batch, int dim, int seqlen, int dstate, ssm_dtype io);
+
+/*
+ * Workspace bytes ssm_selective_scan_fwd needs for this problem and chunk length
+ * (chunk_len = 0 means ssm_scan_default_chunk_len). 0 when the scan runs as one chunk.
+ */
+SSM_API size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate, int chunk_len, ssm_dtype io);
+
+/*
+ * Selective scan forward, for every batch element b and channel d:
+ *   u_t     = x_t, or silu(causal conv of x)_t when conv_w != NULL (as ssm_causal_conv1d_fwd)
+ *   Delta_t = softplus(delta_t + delta_bias[d])      (delta_t + delta_bias[d] if delta_softplus == 0)
+ *   h_t[n]  = exp(Delta_t A[d,n]) h_{t-1}[n] + Delta_t B[b,n,t] u_t,    h_{-1} = h0 (or 0)
+ *   y_t     = sum_n C[b,n,t] h_t[n] + D[d] u_t
+ *   out_t   = y_t * silu(z_t)                        (y_t when z == NULL)
+ * ("Mamba" ai360xpert.com, selection mechanism; "Mamba" ozercemkelahmet.com, steps 1-4 and the
+ *  PyTorch slow reference; "Overview of Mamba (SSM) Model", the SiLU gate.)
+ * The per-step state never leaves the chip. Time is cut into chunks of chunk_len steps; when
+ * there is more than one chunk, a first kernel writes each chunk's carry (the sum of Delta
+ * and the chunk's end state from zero) to the workspace, and the main kernel starts every
+ * chunk from the composition of its predecessors' carries,
+ *   (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2),  a = exp(A * sum Delta),
+ * the associative operator of the parallel scan ("Mamba" ai360xpert.com, "Why this breaks
+ * the parallel form"; "Mamba" ozercemkelahmet.com, step 4).
+ *
+ *   x           [batch, dim, seqlen] io   the scan input u, or the conv input when conv_w != NULL
+ *   delta       [batch, dim, seqlen] io   step-size pre-activation
+ *   A           [dim, dstate] float32     (negative for a stable decay)
+ *   B, C        [batch, dstate, seqlen] io  per-token input / output maps, shared by all channels
+ *   D           [dim] float32 or NULL (no skip term)
+ *   z           [batch, dim, seqlen] io or NULL (no gate)
+ *   delta_bias  [dim] float32 or NULL (= 0)
+ *   delta_softplus  0 or 1
+ *   conv_w      [dim, d_conv] float32 or NULL (no conv prologue); conv_b [dim] float32 or NULL
+ *   conv_init   [batch, dim, d_conv-1] io or NULL: raw inputs before t = 0 (a previous chunk's tail)
+ *   h0          [batch, dim, dstate] float32 or NULL (zero initial state)
+ *   out         [batch, dim, seqlen] io   output
+ *   h_last      [batch, dim, dstate] float32 or NULL: the state after the last step (h0 if seqlen == 0)
+ *   conv_state_out [batch, dim, d_conv-1] io or NULL: the last d_conv-1 raw inputs of the stream
+ *               conv_init ++ x, ready to be passed as the decode window or the next conv_init
+ *   chunk_len   0 = library default; otherwise >= 1, rounded up to a multiple of 64
+ *   workspace   device buffer of at least ssm_scan_workspace_bytes(...) bytes, 256-byte aligned,
+ *               or NULL/0 bytes. With chunk_len = 0 the library lowers the chunk count until the
+ *               given workspace suffices (one chunk needs none); with an explicit chunk_len a
+ *               too-small workspace is SSM_ERR_INVALID_ARG. Its contents need no initialisation.
+ */
+SSM_API ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                                  const float* D, const void* z, const float* delta_bias, int delta_softplus,
+                                  const float* conv_w, const float* conv_b, int d_conv, const void* conv_init,
+                                  const float* h0, void* out, float* h_last, void* conv_state_out, int batch,
+                                  int dim, int seqlen, int dstate, ssm_dtype io, int chunk_len, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * One recurrent (decode) step for every sequence b and channel d, state updated in place:
+ *   window   = [conv_state[b,d,0 .. K-2], x[b,d]]          (oldest first)
+ *   u        = silu(sum_k conv_w[d,k] window[k] + conv_b[d]);   conv_state <- window[1 .. K-1]
+ *              (u = x[b,d] when conv_w == NULL; conv_state is then unused and may be NULL)
+ *   Delta    = softplus(delta[b,d] + delta_bias[d])
+ *   state[n] = exp(Delta A[d,n]) state[n] + Delta B[b,n] u
+ *   y[b,d]   = (sum_n C[b,n] state[n] + D[d] u) * silu(z[b,d])
+ * ("Mamba" ozercemkelahmet.com, step 5 and deployment notes: a fixed-size state per sequence
+ *  updated once per token; "Mamba (Selective State-Space Model)", constant inference state.)
+ *
+ *   state       [batch, dim, dstate] float32, in/out
+ *   conv_state  [batch, dim, d_conv-1] io, in/out (the raw-input window)
+ *   x, delta    [batch, dim] io;   z [batch, dim] io or NULL
+ *   A           [dim, dstate] float32;   B, C [batch, dstate] io
+ *   D, delta_bias, conv_w, conv_b as for the scan
+ *   y           [batch, dim] io output
+ */
+SSM_API ssm_status ssm_selective_state_update(float* state, void* conv_state, const void* x, const void* delta,
+                                      const float* A, const void* B, const void* C, const float* D, const void* z,
+                                      const float* delta_bias, int delta_softplus, const float* conv_w,
+                                      const float* conv_b, int d_conv, void* y, int batch, int dim, int dstate,
+                                      ssm_dtype io, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_H_ */

@@ -1,0 +1,31 @@
+"""B300-native selective state-space (S6) hot path: causal conv prologue, selective scan
+forward and the decode state update, as hand-written sm_103a CUDA behind a C ABI
+(``libssm.so``, declared in ``include/ssm.h``) with a thin ctypes binding.
+
+The binding loads the library on first use and raises if it is missing.
+"""
+
+from .ssm import (  # noqa: F401
+    EXPORTS,
+    LIB_PATH,
+    SSMError,
+    lib,
+    ssm_causal_conv1d_fwd,
+    ssm_scan_default_chunk_len,
+    ssm_scan_workspace_bytes,
+    ssm_selective_scan_fwd,
+    ssm_selective_state_update,
+    status_string,
+    version,
+)
+
+__all__ = [
+    "ssm_causal_conv1d_fwd",
+    "ssm_selective_scan_fwd",
+    "ssm_selective_state_update",
+    "ssm_scan_default_chunk_len",
+    "ssm_scan_workspace_bytes",
+    "version",
+    "status_string",
+    "SSMError",
+]

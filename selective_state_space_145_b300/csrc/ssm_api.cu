@@ -1,0 +1,221 @@
+// ssm_api.cu -- the C ABI (include/ssm.h): host-side argument checks, the chunking policy
+// and dispatch to the kernels. No device memory is allocated here and nothing is cached
+// between calls except which kernels have had their shared-memory limit raised.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssm.h"
+#include "ssm_internal.h"
+
+namespace {
+
+using ssm::kChunkQuantum;
+using ssm::kMaxConv;
+using ssm::kMaxDstate;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int io_bytes(ssm_dtype io) { return io == SSM_BF16 ? 2 : 4; }
+
+bool io_ok(ssm_dtype io) { return io == SSM_F32 || io == SSM_BF16; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+// States per thread of the scan: 4 when there are enough channels to fill the GPU with four
+// threads per channel, else 1 (sixteen threads per channel).
+int choose_npt(long long channels) { return channels >= 8192 ? 4 : 1; }
+
+long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
+
+// Time-chunk length: one chunk when the channels alone give every SM enough CTAs; otherwise
+// the fewest chunks that do, keeping chunks at least 256 steps long.
+int default_chunk_len_impl(int batch, int dim, int seqlen) {
+  const long long channels = (long long)batch * dim;
+  const int npt = choose_npt(channels);
+  const int dt = 128 / (kMaxDstate / npt);
+  const long long ctas = ((dim + dt - 1) / dt) * (long long)batch;
+  const long long target = (long long)sm_count() * 4;
+  const long long whole = round_up(seqlen > 0 ? seqlen : 1, kChunkQuantum);
+  if (ctas >= target || seqlen <= 512) return (int)whole;
+  long long q = (target + ctas - 1) / ctas;
+  const long long qmax = (seqlen + 255) / 256;
+  if (q > qmax) q = qmax;
+  if (q < 1) q = 1;
+  long long cl = round_up((seqlen + q - 1) / q, kChunkQuantum);
+  return (int)cl;
+}
+
+int nchunks_for(int seqlen, int chunk_len) {
+  if (seqlen <= 0) return 1;
+  return (int)((seqlen + (long long)chunk_len - 1) / chunk_len);
+}
+
+bool dims_ok(int batch, int dim, int seqlen, int dstate) {
+  return batch >= 0 && dim >= 0 && seqlen >= 0 && dstate >= 1 && batch <= 65535;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_version(void) { return 100; }
+
+const char* ssm_status_string(int status) {
+  switch (status) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+    default: return "SSM_UNKNOWN_STATUS";
+  }
+}
+
+int ssm_scan_default_chunk_len(int batch, int dim, int seqlen, int dstate, ssm_dtype io) {
+  (void)dstate;
+  (void)io;
+  if (batch <= 0 || dim <= 0 || seqlen < 0) return kChunkQuantum;
+  return default_chunk_len_impl(batch, dim, seqlen);
+}
+
+size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate, int chunk_len, ssm_dtype io) {
+  if (batch <= 0 || dim <= 0 || seqlen <= 0 || chunk_len < 0) return 0;
+  int cl = chunk_len == 0 ? ssm_scan_default_chunk_len(batch, dim, seqlen, dstate, io)
+                          : (int)round_up(chunk_len, kChunkQuantum);
+  return ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl));
+}
+
+ssm_status ssm_causal_conv1d_fwd(const void* x, const float* w, const float* bias, const void* conv_init, void* out,
+                                 int batch, int dim, int seqlen, int d_conv, int apply_silu, ssm_dtype io,
+                                 void* stream) {
+  if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (batch < 0 || dim < 0 || seqlen < 0) return SSM_ERR_INVALID_ARG;
+  if (d_conv < 1) return SSM_ERR_INVALID_ARG;
+  if (d_conv > kMaxConv) return SSM_ERR_UNSUPPORTED;
+  if (apply_silu != 0 && apply_silu != 1) return SSM_ERR_INVALID_ARG;
+  if ((long long)batch * dim == 0 || seqlen == 0) return SSM_OK;
+  if (!x || !w || !out) return SSM_ERR_INVALID_ARG;
+  const size_t es = io_bytes(io);
+  if (!aligned(x, es) || !aligned(out, es) || !aligned(w, 4) || (bias && !aligned(bias, 4)) ||
+      (conv_init && !aligned(conv_init, es)))
+    return SSM_ERR_UNSUPPORTED;
+  ssm::ConvArgs a;
+  a.x = x; a.w = w; a.bias = bias; a.conv_init = conv_init; a.out = out;
+  a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.d_conv = d_conv; a.apply_silu = apply_silu;
+  a.bf16 = io == SSM_BF16;
+  a.vec = (seqlen % 4 == 0) && aligned(x, 16) && aligned(out, 16);
+  return ssm::launch_conv(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                                  const float* D, const void* z, const float* delta_bias, int delta_softplus,
+                                  const float* conv_w, const float* conv_b, int d_conv, const void* conv_init,
+                                  const float* h0, void* out, float* h_last, void* conv_state_out, int batch,
+                                  int dim, int seqlen, int dstate, ssm_dtype io, int chunk_len, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (!dims_ok(batch, dim, seqlen, dstate)) return SSM_ERR_INVALID_ARG;
+  if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
+  if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+  if (chunk_len < 0) return SSM_ERR_INVALID_ARG;
+  const bool conv = conv_w != nullptr;
+  if (conv || conv_init || conv_state_out) {
+    if (d_conv < 1) return SSM_ERR_INVALID_ARG;
+    if (d_conv > kMaxConv) return SSM_ERR_UNSUPPORTED;
+  }
+  if (!conv && (conv_b || conv_init)) return SSM_ERR_INVALID_ARG;
+  if ((long long)batch * dim == 0) return SSM_OK;
+  // per-token tensors may be NULL only when there are no tokens
+  if (!A || (seqlen > 0 && (!x || !delta || !B || !C || !out))) return SSM_ERR_INVALID_ARG;
+  const size_t es = io_bytes(io);
+  const void* io_ptrs[] = {x, delta, B, C, z, out, conv_init, conv_state_out};
+  for (const void* p : io_ptrs)
+    if (p && !aligned(p, es)) return SSM_ERR_UNSUPPORTED;
+  const void* f_ptrs[] = {A, D, delta_bias, conv_w, conv_b, h0, h_last};
+  for (const void* p : f_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_UNSUPPORTED;
+
+  // chunking
+  int cl;
+  if (chunk_len == 0) {
+    cl = default_chunk_len_impl(batch, dim, seqlen);
+    // lower the chunk count until the given workspace suffices
+    while (nchunks_for(seqlen, cl) > 1 &&
+           ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl)) >
+               (workspace ? workspace_bytes : 0)) {
+      const int q = nchunks_for(seqlen, cl) - 1;
+      cl = (int)round_up((seqlen + q - 1) / q, kChunkQuantum);
+    }
+  } else {
+    if (chunk_len > (1 << 30)) chunk_len = 1 << 30;
+    cl = (int)round_up(chunk_len, kChunkQuantum);
+  }
+  const int nchunks = nchunks_for(seqlen, cl);
+  if (nchunks > 65535) return SSM_ERR_INVALID_ARG;
+  const size_t need = ssm::scan_workspace_bytes((long long)batch * dim, nchunks);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return SSM_ERR_UNSUPPORTED;
+  }
+
+  ssm::ScanArgs a;
+  a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
+  a.delta_softplus = delta_softplus; a.conv_w = conv_w; a.conv_b = conv_b; a.d_conv = d_conv;
+  a.conv_init = conv_init; a.h0 = h0; a.out = out; a.h_last = h_last; a.conv_state_out = conv_state_out;
+  a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.dstate = dstate;
+  a.bf16 = io == SSM_BF16;
+  const bool rows16 = ((long long)seqlen * (long long)es) % 16 == 0;
+  a.vec = rows16 && aligned(x, 16) && aligned(delta, 16) && aligned(B, 16) && aligned(C, 16) &&
+          aligned(out, 16) && (!z || aligned(z, 16));
+  a.chunk_len = cl;
+  a.nchunks = nchunks;
+  ssm::scan_workspace_split(workspace, (long long)batch * dim, nchunks, &a.ws_S, &a.ws_h);
+  a.npt = choose_npt((long long)batch * dim);
+  return ssm::launch_scan(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_selective_state_update(float* state, void* conv_state, const void* x, const void* delta,
+                                      const float* A, const void* B, const void* C, const float* D, const void* z,
+                                      const float* delta_bias, int delta_softplus, const float* conv_w,
+                                      const float* conv_b, int d_conv, void* y, int batch, int dim, int dstate,
+                                      ssm_dtype io, void* stream) {
+  if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (batch < 0 || dim < 0 || dstate < 1) return SSM_ERR_INVALID_ARG;
+  if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
+  if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+  const bool conv = conv_w != nullptr;
+  if (conv) {
+    if (d_conv < 1) return SSM_ERR_INVALID_ARG;
+    if (d_conv > kMaxConv) return SSM_ERR_UNSUPPORTED;
+    if (d_conv > 1 && !conv_state) return SSM_ERR_INVALID_ARG;
+  } else if (conv_b) {
+    return SSM_ERR_INVALID_ARG;
+  }
+  if ((long long)batch * dim == 0) return SSM_OK;
+  if (!state || !x || !delta || !A || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+  const size_t es = io_bytes(io);
+  const void* io_ptrs[] = {x, delta, B, C, z, y, conv ? conv_state : nullptr};
+  for (const void* p : io_ptrs)
+    if (p && !aligned(p, es)) return SSM_ERR_UNSUPPORTED;
+  const void* f_ptrs[] = {state, A, D, delta_bias, conv_w, conv_b};
+  for (const void* p : f_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_UNSUPPORTED;
+  ssm::DecodeArgs a;
+  a.state = state; a.conv_state = conv ? conv_state : nullptr; a.x = x; a.delta = delta; a.A = A; a.B = B;
+  a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias; a.delta_softplus = delta_softplus;
+  a.conv_w = conv_w; a.conv_b = conv_b; a.d_conv = conv ? d_conv : 0; a.y = y;
+  a.batch = batch; a.dim = dim; a.dstate = dstate; a.bf16 = io == SSM_BF16;
+  return ssm::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"

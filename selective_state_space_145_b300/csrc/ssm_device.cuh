@@ -1,0 +1,119 @@
+// ssm_device.cuh -- device-side helpers shared by the scan, conv and decode kernels:
+// I/O dtype conversion, vector moves, and the transcendental building blocks
+// (exp2, sigmoid/SiLU, softplus) in the two precision tiers the library uses.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- MUFU primitives (PTX)
+
+// 2^x on the special-function unit; flushes subnormal results to zero.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- activations
+
+// silu(x) = x * sigmoid(x) = x / (1 + e^-x). For x -> -inf, e^-x -> inf and the
+// reciprocal gives 0; for x -> +inf it gives x.
+__device__ __forceinline__ float silu_f(float x) {
+  return x * rcp_approx(1.0f + ex2_approx(-x * kLog2e));
+}
+
+// softplus(v) = log(1 + e^v); v itself above 20 (the remainder is below e^-20 relative).
+// PRECISE uses log1pf (accurate for the small step sizes, where 1 + e^v rounds);
+// the fast tier uses lg2(1 + e^v), whose relative error near Delta ~ 1e-3 is ~2e-4,
+// well inside the bf16 output tolerance.
+template <bool PRECISE>
+__device__ __forceinline__ float softplus_f(float v) {
+  if (v > 20.0f) return v;
+  float e = ex2_approx(v * kLog2e);
+  if (PRECISE) return log1pf(e);
+  return lg2_approx(1.0f + e) * kLn2;
+}
+
+// ---------------------------------------------------------------- I/O dtype
+
+template <typename T> struct IoTraits;
+template <> struct IoTraits<float> {
+  static constexpr int kBytes = 4;
+  static constexpr bool kPrecise = true;   // fp32 I/O: accurate softplus
+};
+template <> struct IoTraits<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  static constexpr bool kPrecise = false;  // bf16 I/O: fast transcendental tier
+};
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Load 4 consecutive elements (t .. t+3) as floats. The pointer must be 4-element aligned
+// in the vector path (16 B for fp32, 8 B for bf16).
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  float4 q = *reinterpret_cast<const float4*>(p);
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  uint2 q = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(q.x << 16);
+  v[1] = __uint_as_float(q.x & 0xffff0000u);
+  v[2] = __uint_as_float(q.y << 16);
+  v[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+
+__device__ __forceinline__ void store4(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&v)[4]) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 q;
+  q.x = *reinterpret_cast<uint32_t*>(&a);
+  q.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = q;
+}
+
+// ---------------------------------------------------------------- async copies (sm_80+ cp.async)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared copy; src_bytes = 0 zero-fills the destination without reading.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+}  // namespace ssm

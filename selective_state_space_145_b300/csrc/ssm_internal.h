@@ -1,0 +1,84 @@
+// ssm_internal.h -- host-side launch interface between the C ABI (ssm_api.cu) and the
+// kernels. Plain structs of pointers and sizes; no torch types.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace ssm {
+
+// Largest state size the kernels hold in registers.
+constexpr int kMaxDstate = 16;
+// Largest conv width; narrower filters are zero-padded on the old side to this width.
+constexpr int kMaxConv = 4;
+// Chunk lengths are multiples of the scan's time tile.
+constexpr int kChunkQuantum = 64;
+
+struct ScanArgs {
+  const void* x;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  int delta_softplus;
+  const float* conv_w;   // NULL: no conv prologue
+  const float* conv_b;
+  int d_conv;
+  const void* conv_init;
+  const float* h0;
+  void* out;
+  float* h_last;
+  void* conv_state_out;
+  int batch, dim, seqlen, dstate;
+  int bf16;              // io dtype: 0 = fp32, 1 = bf16
+  int vec;               // 1: 16-byte vector path is legal for every per-token tensor
+  int chunk_len;         // multiple of kChunkQuantum, >= 1 chunk
+  int nchunks;
+  float* ws_S;           // [nchunks-1][batch*dim] sum of Delta per chunk
+  float* ws_h;           // [nchunks-1][batch*dim][kMaxDstate] chunk end state from zero
+  int npt;               // states per thread (1 or 4)
+};
+
+struct ConvArgs {
+  const void* x;
+  const float* w;
+  const float* bias;
+  const void* conv_init;
+  void* out;
+  int batch, dim, seqlen, d_conv, apply_silu;
+  int bf16;
+  int vec;
+};
+
+struct DecodeArgs {
+  float* state;
+  void* conv_state;
+  const void* x;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  int delta_softplus;
+  const float* conv_w;
+  const float* conv_b;
+  int d_conv;
+  void* y;
+  int batch, dim, dstate;
+  int bf16;
+};
+
+// Workspace layout of the chunked scan.
+size_t scan_workspace_bytes(long long channels, int nchunks);
+void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, float** h);
+
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
+cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace ssm

@@ -1,0 +1,239 @@
+"""Python binding of libssm.so (argument marshalling only).
+
+Each function takes CUDA torch tensors, checks shapes, dtypes and contiguity, and calls
+the C entry point of the same name on the current torch stream with raw device pointers.
+Every step of the computation runs in the library's kernels; nothing here computes.
+The library must have been built (``__graft_entry__.build()`` or ``python -m
+selective_state_space_145_b300.build``): a missing library raises, there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssm.so")
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA = 0, 1, 2, 3
+SSM_F32, SSM_BF16 = 0, 1
+
+_DTYPE_CODE = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16}
+
+_lib = None
+
+# Exported C symbols, as declared in include/ssm.h.
+EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_scan_default_chunk_len",
+           "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update")
+
+
+class SSMError(RuntimeError):
+    """A libssm call returned a non-OK status."""
+
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libssm.so once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                               "(python -m selective_state_space_145_b300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, fp, i, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.ssm_version.restype = i
+        L.ssm_version.argtypes = []
+        L.ssm_status_string.restype = ctypes.c_char_p
+        L.ssm_status_string.argtypes = [i]
+        L.ssm_causal_conv1d_fwd.restype = i
+        L.ssm_causal_conv1d_fwd.argtypes = [vp, fp, fp, vp, vp, i, i, i, i, i, i, vp]
+        L.ssm_scan_default_chunk_len.restype = i
+        L.ssm_scan_default_chunk_len.argtypes = [i, i, i, i, i]
+        L.ssm_scan_workspace_bytes.restype = sz
+        L.ssm_scan_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        L.ssm_selective_scan_fwd.restype = i
+        L.ssm_selective_scan_fwd.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, vp, fp, vp]
+                                             + [i] * 6 + [vp, sz, vp])
+        L.ssm_selective_state_update.restype = i
+        L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
+                                                 i, i, i, i, vp]
+        _lib = L
+    return _lib
+
+
+def version() -> int:
+    return lib().ssm_version()
+
+
+def status_string(status: int) -> str:
+    return lib().ssm_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != SSM_OK:
+        raise SSMError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _io_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPE_CODE:
+        raise TypeError(f"unsupported I/O dtype {t.dtype}; use float32 or bfloat16")
+    return _DTYPE_CODE[t.dtype]
+
+
+def _need(t: Optional[torch.Tensor], name: str, shape, dtype, device, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ssm_causal_conv1d_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                          conv_init: Optional[torch.Tensor] = None, apply_silu: bool = True,
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Causal depthwise conv1d (+SiLU). x [batch, dim, L] (f32/bf16), w [dim, K] f32."""
+    batch, dim, L = x.shape
+    K = w.shape[1]
+    dev, io = x.device, x.dtype
+    _need(x, "x", (batch, dim, L), io, dev)
+    _need(w, "w", (dim, K), torch.float32, dev)
+    _need(bias, "bias", (dim,), torch.float32, dev, optional=True)
+    _need(conv_init, "conv_init", (batch, dim, K - 1), io, dev, optional=True)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", (batch, dim, L), io, dev)
+    st = lib().ssm_causal_conv1d_fwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(conv_init), _ptr(out), batch, dim, L, K,
+                                     int(bool(apply_silu)), _io_code(x), _stream(dev))
+    _check("ssm_causal_conv1d_fwd", st)
+    return out
+
+
+def ssm_scan_default_chunk_len(batch: int, dim: int, seqlen: int, dstate: int, io: torch.dtype) -> int:
+    return lib().ssm_scan_default_chunk_len(batch, dim, seqlen, dstate, _DTYPE_CODE[io])
+
+
+def ssm_scan_workspace_bytes(batch: int, dim: int, seqlen: int, dstate: int, chunk_len: int,
+                             io: torch.dtype) -> int:
+    return int(lib().ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, chunk_len, _DTYPE_CODE[io]))
+
+
+def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                           C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                           delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+                           conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
+                           conv_init: Optional[torch.Tensor] = None, h0: Optional[torch.Tensor] = None,
+                           return_last_state: bool = True, return_conv_state: bool = False,
+                           d_conv: Optional[int] = None, chunk_len: int = 0,
+                           workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                           h_last: Optional[torch.Tensor] = None,
+                           conv_state_out: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, ...]:
+    """Selective scan forward. Returns (out, h_last) [+ conv_state_out when asked].
+
+    x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (all float32 or bfloat16, one dtype);
+    A [dim, dstate], D / delta_bias / conv_b [dim], conv_w [dim, K], h0 [batch, dim, dstate]: float32.
+    The workspace (if the chosen chunking needs one) is allocated here unless passed in.
+    """
+    batch, dim, L = x.shape
+    N = A.shape[1]
+    dev, io = x.device, x.dtype
+    K = conv_w.shape[1] if conv_w is not None else (d_conv or 0)
+    _need(x, "x", (batch, dim, L), io, dev)
+    _need(delta, "delta", (batch, dim, L), io, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B, "B", (batch, N, L), io, dev)
+    _need(C, "C", (batch, N, L), io, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(z, "z", (batch, dim, L), io, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    if conv_w is not None:
+        _need(conv_w, "conv_w", (dim, K), torch.float32, dev)
+    _need(conv_b, "conv_b", (dim,), torch.float32, dev, optional=True)
+    _need(conv_init, "conv_init", (batch, dim, K - 1), io, dev, optional=True)
+    _need(h0, "h0", (batch, dim, N), torch.float32, dev, optional=True)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", (batch, dim, L), io, dev)
+    if return_last_state and h_last is None:
+        h_last = torch.empty(batch, dim, N, dtype=torch.float32, device=dev)
+    _need(h_last, "h_last", (batch, dim, N), torch.float32, dev, optional=True)
+    if return_conv_state and conv_state_out is None:
+        if K < 1:
+            raise ValueError("return_conv_state needs a conv width (conv_w or d_conv)")
+        conv_state_out = torch.empty(batch, dim, K - 1, dtype=io, device=dev)
+    _need(conv_state_out, "conv_state_out", (batch, dim, K - 1), io, dev, optional=True)
+    io_code = _io_code(x)
+    need = ssm_scan_workspace_bytes(batch, dim, L, N, chunk_len, io)
+    ws_bytes = 0
+    if workspace is not None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    elif need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = need
+    st = lib().ssm_selective_scan_fwd(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+        _ptr(conv_w), _ptr(conv_b), K, _ptr(conv_init), _ptr(h0), _ptr(out), _ptr(h_last), _ptr(conv_state_out),
+        batch, dim, L, N, io_code, int(chunk_len), _ptr(workspace), ws_bytes, _stream(dev))
+    _check("ssm_selective_scan_fwd", st)
+    res = (out, h_last)
+    if return_conv_state:
+        res = res + (conv_state_out,)
+    return res
+
+
+def ssm_selective_state_update(state: torch.Tensor, conv_state: Optional[torch.Tensor], x: torch.Tensor,
+                               delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                               D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                               delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+                               conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
+                               y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step; updates ``state`` [batch, dim, N] f32 and ``conv_state`` [batch, dim, K-1] in place.
+
+    x, delta, z: [batch, dim]; B, C: [batch, N]. Returns y [batch, dim].
+    """
+    batch, dim = x.shape
+    N = A.shape[1]
+    dev, io = x.device, x.dtype
+    K = conv_w.shape[1] if conv_w is not None else 0
+    _need(state, "state", (batch, dim, N), torch.float32, dev)
+    if conv_w is not None:
+        _need(conv_w, "conv_w", (dim, K), torch.float32, dev)
+        _need(conv_state, "conv_state", (batch, dim, K - 1), io, dev, optional=(K == 1))
+    _need(x, "x", (batch, dim), io, dev)
+    _need(delta, "delta", (batch, dim), io, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B, "B", (batch, N), io, dev)
+    _need(C, "C", (batch, N), io, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(z, "z", (batch, dim), io, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    _need(conv_b, "conv_b", (dim,), torch.float32, dev, optional=True)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", (batch, dim), io, dev)
+    st = lib().ssm_selective_state_update(
+        _ptr(state), _ptr(conv_state if conv_w is not None else None), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+        _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(conv_w), _ptr(conv_b), K, _ptr(y),
+        batch, dim, N, _io_code(x), _stream(dev))
+    _check("ssm_selective_state_update", st)
+    return y

@@ -1,0 +1,131 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every symbol include/ssm.h
+declares, and rejects bad arguments on the host before any launch (no GPU needed: every call
+here returns from the argument checks)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from selective_state_space_145_b300 import build
+
+    build.build()
+    import selective_state_space_145_b300 as ssm
+
+    return ssm.lib()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "ssm.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"SSM_API\s+[\w\s\*]+?\b(ssm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    decl = _declared_symbols()
+    for name in ("ssm_causal_conv1d_fwd", "ssm_selective_scan_fwd", "ssm_selective_state_update"):
+        assert name in decl
+
+
+def test_library_exports_every_declared_symbol(L):
+    import selective_state_space_145_b300 as ssm
+
+    decl = _declared_symbols()
+    assert sorted(ssm.EXPORTS) == decl
+    for name in decl:
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    import selective_state_space_145_b300 as ssm
+
+    assert ssm.version() >= 100
+    assert ssm.status_string(0) == "SSM_OK"
+    assert ssm.status_string(1) == "SSM_ERR_INVALID_ARG"
+    assert ssm.status_string(2) == "SSM_ERR_UNSUPPORTED"
+    assert ssm.status_string(3) == "SSM_ERR_CUDA"
+
+
+# A non-null, 64 KiB-aligned address that is not device memory. Every call below is built to
+# FAIL the host-side checks (or to be empty work), so nothing is ever launched with it.
+FAKE = 0x10000
+
+
+def _scan(L, **kw):
+    a = dict(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, delta_bias=None, sp=1, conv_w=None,
+             conv_b=None, d_conv=0, conv_init=None, h0=None, out=FAKE, h_last=None, cs_out=None, batch=1, dim=4,
+             seqlen=8, dstate=16, io=0, chunk_len=0, ws=None, ws_bytes=0)
+    a.update(kw)
+    return L.ssm_selective_scan_fwd(a["x"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["delta_bias"],
+                                    a["sp"], a["conv_w"], a["conv_b"], a["d_conv"], a["conv_init"], a["h0"],
+                                    a["out"], a["h_last"], a["cs_out"], a["batch"], a["dim"], a["seqlen"],
+                                    a["dstate"], a["io"], a["chunk_len"], a["ws"], a["ws_bytes"], None)
+
+
+def test_scan_argument_checks(L):
+    assert _scan(L, x=None) == 1
+    assert _scan(L, out=None) == 1
+    assert _scan(L, seqlen=-1) == 1
+    assert _scan(L, dstate=0) == 1
+    assert _scan(L, dstate=17) == 2
+    assert _scan(L, io=7) == 2
+    assert _scan(L, sp=2) == 1
+    assert _scan(L, conv_w=FAKE, d_conv=5) == 2
+    assert _scan(L, conv_w=FAKE, d_conv=0) == 1
+    assert _scan(L, conv_b=FAKE) == 1              # conv bias without conv weight
+    assert _scan(L, x=FAKE + 2) == 2               # misaligned fp32 pointer
+    assert _scan(L, chunk_len=-5) == 1
+    assert _scan(L, seqlen=1 << 20, chunk_len=64, batch=1, dim=4) == 1   # chunked: workspace missing
+    # empty work: no launch, OK
+    assert _scan(L, batch=0) == 0
+    assert _scan(L, dim=0, x=None) == 0
+
+
+def test_workspace_query(L):
+    import selective_state_space_145_b300 as ssm
+    import torch
+
+    assert ssm.ssm_scan_workspace_bytes(1, 64, 256, 16, 256, torch.float32) == 0
+    ws = ssm.ssm_scan_workspace_bytes(2, 100, 1000, 16, 64, torch.float32)
+    q = (1000 + 63) // 64
+    s_bytes = ((q - 1) * 200 * 4 + 255) // 256 * 256
+    assert ws == s_bytes + (q - 1) * 200 * 16 * 4
+    cl = ssm.ssm_scan_default_chunk_len(1, 1536, 131072, 16, torch.bfloat16)
+    assert cl % 64 == 0 and 256 <= cl <= 131072
+
+
+def test_decode_and_conv_argument_checks(L):
+    f = L.ssm_selective_state_update
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, FAKE, None, 4, FAKE, 2, 8, 16, 1, None]
+    bad = list(base)
+    bad[0] = None
+    assert f(*bad) == 1                            # state missing
+    bad = list(base)
+    bad[17] = 32
+    assert f(*bad) == 2                            # dstate > 16
+    bad = list(base)
+    bad[1] = None
+    assert f(*bad) == 1                            # conv window missing with a conv
+    bad = list(base)
+    bad[13] = 6
+    assert f(*bad) == 2                            # d_conv > 4
+    c = L.ssm_causal_conv1d_fwd
+    assert c(None, FAKE, None, None, FAKE, 1, 4, 8, 4, 1, 0, None) == 1
+    assert c(FAKE, FAKE, None, None, FAKE, 1, 4, 8, 0, 1, 0, None) == 1
+    assert c(FAKE, FAKE, None, None, FAKE, 1, 4, 8, 5, 1, 0, None) == 2
+    assert c(FAKE, FAKE, None, None, FAKE, 0, 4, 8, 4, 1, 0, None) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import selective_state_space_145_b300.ssm as s
+
+    monkeypatch.setattr(s, "_lib", None)
+    monkeypatch.setattr(s, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        s.lib()

@@ -1,0 +1,274 @@
+"""GPU parity: the CUDA library, called through its C ABI (ctypes binding), against the fp64
+CPU oracle on the same seeded inputs, element by element.
+
+Small problems are compared whole; they span several time tiles, several channel tiles,
+ragged tails, several chunks and the degenerate cases. The five synthetic workloads run at
+full size in the launch configuration the benchmark uses and are compared on sampled
+channels that the oracle computes one by one.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_145_b300 import inputs
+from ssm_testutil import (TOL, assert_close, channel_slice, gpu_scan, oracle_scan, sample_channels, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _ssm():
+    import selective_state_space_145_b300 as ssm
+
+    return ssm
+
+
+# ---------------------------------------------------------------- whole small problems
+
+SMALL = [
+    # batch, dim, L, N, K, io, with_h0, with_init, random_A, chunk_len
+    (1, 64, 256, 16, 0, "f32", False, False, False, 0),      # the small scan workload's shape
+    (2, 37, 101, 16, 4, "f32", True, True, True, 0),         # ragged L (element-wise path), partial channel tile
+    (2, 40, 96, 5, 3, "bf16", True, True, True, 0),          # N < 16, K < 4
+    (3, 130, 200, 16, 4, "bf16", False, False, False, 64),   # 4 chunks, ragged last chunk
+    (2, 33, 333, 7, 2, "f32", True, True, True, 64),         # chunks + ragged + odd N
+    (1, 20000, 40, 16, 4, "bf16", True, False, False, 0),    # many channels: 4 states per thread
+    (2, 5000, 300, 16, 4, "f32", True, True, True, 128),     # 4 states per thread, chunked
+    (1, 3, 1, 1, 4, "f32", True, True, True, 0),             # L = 1, N = 1
+    (1, 8, 3, 16, 4, "bf16", False, True, False, 0),         # L < K-1: the window comes from conv_init
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "b{}_d{}_l{}_n{}_k{}_{}_h0{}_ci{}_rA{}_cl{}".format(*c))
+def test_scan_small_whole(cuda_device, case):
+    batch, dim, L, N, K, io, h0, ci, rA, cl = case
+    p = inputs.scan_inputs(batch, dim, L, N, K, io, seed=1000 + dim + L, with_h0=h0, with_conv_init=ci,
+                           random_A=rA)
+    g = to_dev(p, cuda_device)
+    out, hL, cs = gpu_scan(g, chunk_len=cl, return_conv_state=K > 0, d_conv=K or None) if K > 0 else \
+        (*gpu_scan(g, chunk_len=cl), None)
+    ref, refL, *rest = oracle_scan(p, want_conv_state=K > 0)
+    assert_close(out, ref, io, "out")
+    assert_close(hL, refL, io, "h_last")
+    if K > 1:
+        # the raw-input window is moved bit for bit
+        np.testing.assert_array_equal(cs.float().cpu().numpy(), rest[0])
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_scan_options_off(cuda_device, io):
+    """No gate, no skip, no bias, softplus off (Delta = delta, positive), no conv."""
+    p = inputs.scan_inputs(2, 70, 130, 16, 0, io, seed=5, with_z=False, with_D=False, random_A=True)
+    p["delta_bias"] = None
+    p["delta"] = (p["delta"].float().abs() * 0.2 + 0.01).to(p["delta"].dtype)
+    g = to_dev(p, cuda_device)
+    out, hL = gpu_scan(g, delta_softplus=False)
+    ref, refL = oracle_scan(p, delta_softplus=False)
+    assert_close(out, ref, io, "out")
+    assert_close(hL, refL, io, "h_last")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_chunked_equals_unchunked(cuda_device, io):
+    """The cross-chunk carry: every chunk length gives the oracle's result, and the same
+    result as one chunk to within rounding."""
+    p = inputs.scan_inputs(2, 48, 700, 16, 4, io, seed=77, with_h0=True, with_conv_init=True, salient_frac=0.02)
+    g = to_dev(p, cuda_device)
+    ref, refL = oracle_scan(p)
+    one, one_h = gpu_scan(g, chunk_len=1 << 20)
+    for cl in (64, 128, 192, 320):
+        out, hL = gpu_scan(g, chunk_len=cl)
+        assert_close(out, ref, io, f"out chunk_len={cl}")
+        assert_close(hL, refL, io, f"h_last chunk_len={cl}")
+        assert_close(out, one.float().cpu().double().numpy(), io, f"chunked vs whole cl={cl}")
+
+
+def test_chunked_prompt_on_gpu(cuda_device):
+    """Two GPU calls passing (h_last, conv window) equal one call (prompts processed in chunks)."""
+    p = inputs.scan_inputs(2, 50, 257, 16, 4, "f32", seed=9, with_h0=True, with_conv_init=True)
+    g = to_dev(p, cuda_device)
+    full, hfull, csfull = gpu_scan(g, return_conv_state=True)
+    L1 = 100
+    g1 = {k: (v[..., :L1].contiguous() if k in ("x", "delta", "z", "B", "C") else v) for k, v in g.items()}
+    o1, h1, cs1 = gpu_scan(g1, return_conv_state=True)
+    g2 = {k: (v[..., L1:].contiguous() if k in ("x", "delta", "z", "B", "C") else v) for k, v in g.items()}
+    g2["h0"], g2["conv_init"] = h1, cs1
+    o2, h2, cs2 = gpu_scan(g2, return_conv_state=True)
+    ref, refL = oracle_scan(p)
+    assert_close(torch.cat([o1, o2], dim=-1), ref, "f32", "two calls vs oracle")
+    assert_close(h2, refL, "f32", "h_last after two calls")
+    assert torch.equal(cs2, csfull)
+
+
+def test_empty_and_zero_length(cuda_device):
+    ssm = _ssm()
+    p = inputs.scan_inputs(2, 24, 0, 16, 4, "f32", seed=3, with_h0=True, with_conv_init=True)
+    g = to_dev(p, cuda_device)
+    out, hL, cs = gpu_scan(g, return_conv_state=True)
+    torch.cuda.synchronize()
+    assert out.numel() == 0
+    assert torch.equal(hL, g["h0"])
+    assert torch.equal(cs, g["conv_init"])
+    # batch 0 / dim 0: nothing to do
+    e = torch.empty(0, 8, 16, device=cuda_device)
+    A = -torch.ones(8, 16, device=cuda_device)
+    Bm = torch.empty(0, 16, 16, device=cuda_device)
+    out, hL = ssm.ssm_selective_scan_fwd(e, e, A, Bm, Bm)
+    assert out.shape == (0, 8, 16)
+
+
+def test_deterministic(cuda_device):
+    p = inputs.scan_inputs(2, 64, 512, 16, 4, "bf16", seed=21, with_h0=True)
+    g = to_dev(p, cuda_device)
+    a1, h1 = gpu_scan(g, chunk_len=128)
+    a2, h2 = gpu_scan(g, chunk_len=128)
+    assert torch.equal(a1, a2) and torch.equal(h1, h2)
+
+
+# ---------------------------------------------------------------- standalone conv
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+@pytest.mark.parametrize("L", [1, 37, 256])
+def test_conv1d(cuda_device, io, K, L):
+    ssm = _ssm()
+    p = inputs.scan_inputs(2, 19, L, 4, K, io, seed=K * 100 + L, with_conv_init=True)
+    g = to_dev(p, cuda_device)
+    for silu in (True, False):
+        for init in (True, False):
+            y = ssm.ssm_causal_conv1d_fwd(g["x"], g["conv_w"], g["conv_b"], g["conv_init"] if init else None,
+                                          apply_silu=silu)
+            ref = oracle.causal_conv1d(p["x"], p["conv_w"], p["conv_b"], p["conv_init"] if init else None,
+                                       apply_silu=silu)
+            assert_close(y, ref, io, f"conv silu={silu} init={init}")
+
+
+# ---------------------------------------------------------------- decode
+
+DECODE_SMALL = [
+    # batch, dim, N, K, io, steps
+    (3, 50, 16, 4, "bf16", 5),
+    (2, 33, 5, 2, "f32", 4),     # N not a multiple of 4: element-wise state path
+    (4, 64, 16, 4, "f32", 3),
+    (1, 7, 16, 1, "bf16", 2),    # K = 1: no window
+]
+
+
+@pytest.mark.parametrize("case", DECODE_SMALL, ids=lambda c: "b{}_d{}_n{}_k{}_{}_s{}".format(*c))
+def test_decode_small(cuda_device, case):
+    ssm = _ssm()
+    batch, dim, N, K, io, steps = case
+    q = inputs.decode_inputs(batch, dim, N, K, io, seed=batch * dim + N, steps=steps, random_A=True)
+    g = to_dev(q, cuda_device)
+    state, win = q["state"].double().numpy(), (q["conv_state"].double().numpy() if q["conv_state"] is not None else None)
+    for t in range(steps):
+        y = ssm.ssm_selective_state_update(g["state"], g["conv_state"], g["x"][t], g["delta"][t], g["A"], g["B"][t],
+                                           g["C"][t], g["D"], g["z"][t], g["delta_bias"], True, g["conv_w"],
+                                           g["conv_b"])
+        yr, state, win = oracle.state_update(state, win, q["x"][t], q["delta"][t], q["A"], q["B"][t], q["C"][t], q["D"],
+                                             q["z"][t], q["delta_bias"], True, q["conv_w"], q["conv_b"])
+        assert_close(y, yr, io, f"y step {t}")
+        assert_close(g["state"], state, io, f"state step {t}")
+        if K > 1:
+            np.testing.assert_array_equal(g["conv_state"].float().cpu().numpy(), win)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_recurrent_equals_parallel_on_gpu(cuda_device, io):
+    """K decode steps from (state, window) equal one scan over the same K tokens with h0 = state
+    and conv_init = window (recurrent and parallel mode agree)."""
+    ssm = _ssm()
+    batch, dim, N, K, T = 2, 40, 16, 4, 12
+    p = inputs.scan_inputs(batch, dim, T, N, K, io, seed=31, with_h0=True, with_conv_init=True)
+    g = to_dev(p, cuda_device)
+    out, hL, cs = gpu_scan(g, return_conv_state=True)
+    state, win = g["h0"].clone(), g["conv_init"].clone()
+    ys = []
+    for t in range(T):
+        ys.append(ssm.ssm_selective_state_update(state, win, g["x"][..., t].contiguous(), g["delta"][..., t].contiguous(),
+                                                 g["A"], g["B"][..., t].contiguous(), g["C"][..., t].contiguous(),
+                                                 g["D"], g["z"][..., t].contiguous(), g["delta_bias"], True,
+                                                 g["conv_w"], g["conv_b"]))
+    yd = torch.stack(ys, dim=-1)
+    rtol, atol = TOL[io]
+    assert_close(yd, out.float().cpu().double().numpy(), io, "decode vs scan")
+    assert_close(state, hL.cpu().double().numpy(), io, "decode state vs scan h_last")
+    assert torch.equal(win, cs)
+
+
+# ---------------------------------------------------------------- the five workloads, full size
+
+def _workload_scan(name, n_sample, cuda_device, seed):
+    w = inputs.WORKLOADS[name]
+    p = inputs.workload_inputs(w)
+    g = to_dev(p, cuda_device)
+    out, hL = gpu_scan(g)   # default chunking: the launch configuration the benchmark times
+    torch.cuda.synchronize()
+    chans = sample_channels(w.batch, w.dim, n_sample, seed)
+    for (b, d) in chans:
+        q = channel_slice(p, b, d)
+        ref, refL = oracle_scan(q, nthreads=1)
+        assert_close(out[b:b + 1, d:d + 1], ref, w.io, f"{name} out[{b},{d}]")
+        assert_close(hL[b:b + 1, d:d + 1], refL, w.io, f"{name} h_last[{b},{d}]")
+    # properties that hold at any size
+    assert torch.isfinite(out.float()).all()
+    assert torch.isfinite(hL).all()
+    return p, g, out, hL
+
+
+def test_workload_small_scan_whole(cuda_device):
+    w = inputs.WORKLOADS["scan_f32_b1_d64_l256_n16"]
+    p = inputs.workload_inputs(w)
+    out, hL = gpu_scan(to_dev(p, cuda_device))
+    ref, refL = oracle_scan(p)
+    assert_close(out, ref, "f32", "out")
+    assert_close(hL, refL, "f32", "h_last")
+
+
+def test_workload_block_f32_whole(cuda_device):
+    w = inputs.WORKLOADS["block_f32_b2_d1024_l1024_n16_k4"]
+    p = inputs.workload_inputs(w)
+    out, hL = gpu_scan(to_dev(p, cuda_device))
+    ref, refL = oracle_scan(p)
+    assert_close(out, ref, "f32", "out")
+    assert_close(hL, refL, "f32", "h_last")
+
+
+@pytest.mark.slow
+def test_workload_block_bf16_sampled(cuda_device):
+    _workload_scan("block_bf16_b8_d2048_l2048_n16_k4", 64, cuda_device, seed=2)
+
+
+@pytest.mark.slow
+def test_workload_longscan_bf16_sampled(cuda_device):
+    _workload_scan("longscan_bf16_b1_d1536_l131072_n16", 12, cuda_device, seed=3)
+
+
+@pytest.mark.slow
+def test_workload_decode_sampled(cuda_device):
+    ssm = _ssm()
+    w = inputs.WORKLOADS["decode_bf16_b256_d5120_n16_k4_x64"]
+    q = inputs.workload_inputs(w)
+    g = to_dev(q, cuda_device)
+    chans = sample_channels(w.batch, w.dim, 64, seed=4)
+    idx_b = [b for b, _ in chans]
+    idx_d = [d for _, d in chans]
+    state = q["state"][idx_b, idx_d].double().numpy()[:, None, :]       # [S, 1, N]
+    win = q["conv_state"][idx_b, idx_d].double().numpy()[:, None, :]
+    ys = []
+    for t in range(w.steps):
+        ys.append(ssm.ssm_selective_state_update(g["state"], g["conv_state"], g["x"][t], g["delta"][t], g["A"],
+                                                 g["B"][t], g["C"][t], g["D"], g["z"][t], g["delta_bias"], True,
+                                                 g["conv_w"], g["conv_b"]).float().cpu())
+    for s, (b, d) in enumerate(chans):
+        st, wn = state[s:s + 1], win[s:s + 1]
+        for t in range(w.steps):
+            yr, st, wn = oracle.state_update(st, wn, q["x"][t][b:b + 1, d:d + 1], q["delta"][t][b:b + 1, d:d + 1],
+                                             q["A"][d:d + 1], q["B"][t][b:b + 1], q["C"][t][b:b + 1], q["D"][d:d + 1],
+                                             q["z"][t][b:b + 1, d:d + 1], q["delta_bias"][d:d + 1], True,
+                                             q["conv_w"][d:d + 1], q["conv_b"][d:d + 1])
+            assert_close(ys[t][b:b + 1, d:d + 1], yr, "bf16", f"decode y[{b},{d}] step {t}")
+        assert_close(g["state"][b:b + 1, d:d + 1], st, "bf16", f"decode state[{b},{d}]")
+        np.testing.assert_array_equal(g["conv_state"][b:b + 1, d:d + 1].float().cpu().numpy(), wn)
+    assert torch.isfinite(g["state"]).all()
