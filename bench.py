@@ -272,8 +272,9 @@ def run_gpu(args, w):
     import selective_state_space_145_b300 as ssm
     from selective_state_space_145_b300 import inputs
 
-    p = inputs.workload_inputs(w) if world == 1 else inputs.workload_inputs(
-        inputs.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank}))
+    import dataclasses
+
+    p = inputs.workload_inputs(w if world == 1 else dataclasses.replace(w, seed=w.seed + 1000 * rank))
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -432,11 +433,20 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="override the workload's sequence length (smaller cases for profiling)")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
     args = ap.parse_args(argv)
+    import dataclasses
+
     from selective_state_space_145_b300 import inputs
 
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     w = inputs.WORKLOADS[args.workload]
+    if args.seqlen is not None or args.batch is not None:
+        w = dataclasses.replace(w, seqlen=args.seqlen if args.seqlen is not None else w.seqlen,
+                                batch=args.batch if args.batch is not None else w.batch)
+        w = dataclasses.replace(w, name=f"{w.name}[batch={w.batch},seqlen={w.seqlen}]")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gpu(args, w)

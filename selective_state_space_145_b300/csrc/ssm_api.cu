@@ -32,22 +32,18 @@ int sm_count() {
   return n;
 }
 
-// States per thread of the scan: 4 when there are enough channels to fill the GPU with four
-// threads per channel, else 1 (sixteen threads per channel).
-int choose_npt(long long channels) { return channels >= 8192 ? 4 : 1; }
-
 long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 
-// Time-chunk length: one chunk when the channels alone give every SM enough CTAs; otherwise
-// the fewest chunks that do, keeping chunks at least 256 steps long.
+// Time-chunk length. Chunking costs a carry pass over all but the last chunk, so the scan
+// runs as one chunk whenever the channels alone give every SM at least two CTAs; otherwise
+// it takes the fewest chunks that give four CTAs per SM, keeping chunks >= 256 steps.
 int default_chunk_len_impl(int batch, int dim, int seqlen) {
-  const long long channels = (long long)batch * dim;
-  const int npt = choose_npt(channels);
-  const int dt = 128 / (kMaxDstate / npt);
+  const int dt = ssm::scan_channels_per_cta();
   const long long ctas = ((dim + dt - 1) / dt) * (long long)batch;
-  const long long target = (long long)sm_count() * 4;
+  const long long sms = sm_count();
+  const long long target = sms * 4;
   const long long whole = round_up(seqlen > 0 ? seqlen : 1, kChunkQuantum);
-  if (ctas >= target || seqlen <= 512) return (int)whole;
+  if (ctas >= sms * 2 || seqlen <= 512) return (int)whole;
   long long q = (target + ctas - 1) / ctas;
   const long long qmax = (seqlen + 255) / 256;
   if (q > qmax) q = qmax;
@@ -180,7 +176,6 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   a.chunk_len = cl;
   a.nchunks = nchunks;
   ssm::scan_workspace_split(workspace, (long long)batch * dim, nchunks, &a.ws_S, &a.ws_h);
-  a.npt = choose_npt((long long)batch * dim);
   return ssm::launch_scan(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

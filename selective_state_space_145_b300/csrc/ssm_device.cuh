@@ -33,6 +33,42 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs (sm_100+ f32x2)
+// One instruction computes two fp32 lanes; the FMA pipe throughput per element is unchanged,
+// the issue slots are halved.
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
 // ---------------------------------------------------------------- activations
 
 // silu(x) = x * sigmoid(x) = x / (1 + e^-x). For x -> -inf, e^-x -> inf and the
@@ -51,6 +87,23 @@ __device__ __forceinline__ float softplus_f(float v) {
   float e = ex2_approx(v * kLog2e);
   if (PRECISE) return log1pf(e);
   return lg2_approx(1.0f + e) * kLn2;
+}
+
+// Pairwise forms of the same functions: the FMA-pipe work packed two lanes per instruction,
+// the MUFU work per element unchanged.
+__device__ __forceinline__ float2 silu2(float2 x) {
+  const float2 t = fmul2(x, f2(-kLog2e));
+  const float2 den = fadd2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), f2(1.0f));
+  return fmul2(x, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ float2 softplus2(float2 v) {
+  if (PRECISE) return make_float2(softplus_f<true>(v.x), softplus_f<true>(v.y));
+  const float2 t = fmul2(v, f2(kLog2e));
+  const float2 s = fadd2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), f2(1.0f));
+  const float2 r = fmul2(make_float2(lg2_approx(s.x), lg2_approx(s.y)), f2(kLn2));
+  return make_float2(v.x > 20.0f ? v.x : r.x, v.y > 20.0f ? v.y : r.y);
 }
 
 // ---------------------------------------------------------------- I/O dtype
@@ -98,6 +151,35 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&v)[4]) {
   q.x = *reinterpret_cast<uint32_t*>(&a);
   q.y = *reinterpret_cast<uint32_t*>(&b);
   *reinterpret_cast<uint2*>(p) = q;
+}
+
+// 8 consecutive elements; 16-byte aligned pointer (bf16: one 16-byte access, fp32: two).
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ---------------------------------------------------------------- async copies (sm_80+ cp.async)

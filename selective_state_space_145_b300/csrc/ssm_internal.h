@@ -39,7 +39,6 @@ struct ScanArgs {
   int nchunks;
   float* ws_S;           // [nchunks-1][batch*dim] sum of Delta per chunk
   float* ws_h;           // [nchunks-1][batch*dim][kMaxDstate] chunk end state from zero
-  int npt;               // states per thread (1 or 4)
 };
 
 struct ConvArgs {
@@ -72,6 +71,9 @@ struct DecodeArgs {
   int batch, dim, dstate;
   int bf16;
 };
+
+// Channels one scan CTA covers.
+int scan_channels_per_cta();
 
 // Workspace layout of the chunked scan.
 size_t scan_workspace_bytes(long long channels, int nchunks);

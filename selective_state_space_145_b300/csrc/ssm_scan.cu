@@ -8,22 +8,25 @@
 //   h_t[n] = exp(Delta_t A[d,n]) h_{t-1}[n] + Delta_t B[b,n,t] u_t,
 //   out_t = (sum_n C[b,n,t] h_t[n] + D_d u_t) * silu(z_t).
 //
-// Design (one CTA = DT channels of one batch element x one time chunk):
-//  * per time tile of kTT steps, the raw x / delta / z rows and the shared B / C rows are
-//    copied global->shared with 16-byte cp.async, double-buffered so tile i+1 lands
-//    while tile i is computed;
-//  * an element-wise phase turns each (t, d) into Delta, Delta*u and u once (conv, SiLU,
-//    softplus), in fp32 shared memory, so no per-(t, d) work is repeated per state;
-//  * the scan phase gives each channel TPC = 16 / NPT threads holding NPT states each in
-//    registers; a thread walks the tile sequentially, one exp2 per state update, and
-//    leaves its partial C.h per step in shared memory;
-//  * an epilogue sums the partials, adds D*u, applies the gate and stores coalesced rows.
+// Design. One CTA = 32 channels of one batch element x one time chunk; 128 threads, four
+// per channel, each holding four of the (up to) 16 states in registers. Per time tile of
+// 32 steps:
+//  * the raw x / delta / z rows of the 32 channels and the 16 shared B / C rows are copied
+//    global->shared with 16-byte cp.async into a ring of 3-4 tiles, so several tiles are
+//    always in flight;
+//  * element-wise phase: each thread turns 8 steps of its channel into Delta and Delta*u
+//    (conv, SiLU and softplus once per (t, d), never per state), keeps D*u and silu(z) for
+//    those steps in registers, and the block transposes B, C to fp32 [t][n];
+//  * scan phase: each thread walks the 32 steps sequentially with packed f32x2 math, one
+//    exp2 per state update, and leaves its partial C.h per step in shared memory;
+//  * epilogue: the same thread sums the four partials of its 8 steps (written by its own
+//    warp), adds D*u, applies the gate and stores straight to global memory.
 //  The per-step state never leaves registers. With more than one chunk, a carry kernel
-//  (same code, CARRY = true) first writes every chunk's sum of Delta and its end state
-//  from zero; the main kernel starts chunk q from h0 composed with the carries of chunks
-//  0..q-1 through (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2), a = exp(A sum Delta).
+//  (same code, CARRY = true: no C, no gate, no output) first writes every chunk's sum of
+//  Delta and its end state from zero; the main kernel starts chunk q from h0 composed with
+//  the carries of chunks 0..q-1 through (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) with
+//  a = exp(A sum Delta).
 #include <algorithm>
-#include <cstdio>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -31,48 +34,46 @@
 namespace ssm {
 namespace {
 
-constexpr int kThreads = 128;   // threads per CTA
-constexpr int kTT = 32;         // time steps per tile
-constexpr int kTP = kTT + 4;    // padded row stride of the fp32 tile arrays (keeps float4 alignment)
+constexpr int kThreads = 128;  // threads per CTA
+constexpr int kTPC = 4;        // threads per channel
+constexpr int kNPT = 4;        // states per thread
+constexpr int kDT = 32;        // channels per CTA
+constexpr int kTT = 32;        // time steps per tile
+constexpr int kTP = kTT + 4;   // padded row stride of the fp32 tile arrays (keeps float4 alignment)
+constexpr int kSeg = kTT / kTPC;  // steps per thread in the element-wise phase and the epilogue
+constexpr int kRows = 3 * kDT + 2 * kMaxDstate;  // staged rows per tile: x, delta, z, B, C
+static_assert(kTPC * kNPT == kMaxDstate, "four threads x four states cover N = 16");
+static_assert(kDT * kTPC == kThreads, "one thread group per channel");
+static_assert(kSeg == 8, "element-wise segment of 8 steps");
 
-template <int NPT>
-struct Cfg {
-  static constexpr int TPC = kMaxDstate / NPT;  // threads per channel
-  static constexpr int DT = kThreads / TPC;     // channels per CTA
-};
+// Depth of the raw-tile ring: 3 tiles of 8 KB (bf16) or 2 of 16 KB (fp32) per CTA, which
+// keeps four (bf16) or three (fp32) CTAs resident per SM.
+template <typename T>
+constexpr int stages() { return sizeof(T) == 2 ? 3 : 2; }
 
-template <typename T, int NPT>
+template <typename T>
 struct __align__(16) Smem {
-  static constexpr int DT = Cfg<NPT>::DT;
-  static constexpr int TPC = Cfg<NPT>::TPC;
-  // raw staging in the I/O dtype, double-buffered
-  T raw_x[2][DT][kTT];
-  T raw_d[2][DT][kTT];
-  T raw_z[2][DT][kTT];
-  T raw_B[2][kMaxDstate][kTT];
-  T raw_C[2][kMaxDstate][kTT];
-  // fp32 tile arrays
-  float s_delta[DT][kTP];
-  float s_du[DT][kTP];
-  float s_u[DT][kTP];
-  float s_y[TPC][DT][kTP];
-  float s_B[kTT][kMaxDstate];
+  static constexpr int S = stages<T>();
+  T raw[S][kRows][kTT];          // rows 0..31 x, 32..63 delta, 64..95 z, 96..111 B, 112..127 C
+  float s_dl[kDT][kTP];          // Delta
+  float s_du[kDT][kTP];          // Delta * u
+  float s_y[kDT][kTPC][kTP];     // partial C.h of each thread, per step
+  float s_B[kTT][kMaxDstate];    // B, fp32, t-major
   float s_C[kTT][kMaxDstate];
-  float s_halo[2][DT][4];   // the 3 raw inputs before the tile (ping-pong by tile parity)
-  float s_par[DT][8];       // delta_bias, D, conv taps w0..w3 (zero-padded on the old side), conv bias
+  float s_halo[2][kDT][4];       // the 3 raw inputs before the tile (ping-pong by tile parity)
 };
 
-template <typename T, int NPT, bool CONV, bool VEC, bool CARRY>
-__global__ void __launch_bounds__(kThreads) scan_kernel(const ScanArgs a) {
-  using Cf = Cfg<NPT>;
-  constexpr int TPC = Cf::TPC;
-  constexpr int DT = Cf::DT;
+template <typename T, bool CONV, bool VEC, bool CARRY>
+__global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
+  constexpr int kS = stages<T>();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Smem<T, NPT>& S = *reinterpret_cast<Smem<T, NPT>*>(smem_raw);
+  Smem<T>& S = *reinterpret_cast<Smem<T>*>(smem_raw);
 
   const int tid = threadIdx.x;
-  const int d0 = blockIdx.x * DT;
+  const int c = tid / kTPC;          // channel within the CTA
+  const int g = tid % kTPC;          // state group: n = 4g .. 4g+3; element-wise steps 8g .. 8g+7
+  const int d0 = blockIdx.x * kDT;
   const int q = blockIdx.y;
   const int b = blockIdx.z;
   const int L = a.seqlen, N = a.dstate, dim = a.dim;
@@ -80,301 +81,313 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanArgs a) {
   const int t_begin = q * a.chunk_len;
   const int t_end = min(L, t_begin + a.chunk_len);
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kTT - 1) / kTT : 0;
+  const int d = d0 + c;
+  const bool valid = d < dim;
+  const long long cc = (long long)b * dim + d;
 
   const T* __restrict__ gx = static_cast<const T*>(a.x);
-  const T* __restrict__ gd = static_cast<const T*>(a.delta);
   const T* __restrict__ gz = static_cast<const T*>(a.z);
-  const T* __restrict__ gB = static_cast<const T*>(a.B);
-  const T* __restrict__ gC = static_cast<const T*>(a.C);
   const bool has_z = (gz != nullptr) && !CARRY;
 
-  // ---- per-channel parameters and the conv halo before the chunk
-  for (int i = tid; i < DT; i += kThreads) {
-    const int d = d0 + i;
-    float par[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // ---- per-channel parameters, in registers; the conv filter is zero-padded to 4 taps
+  float bias = 0.f, Dd = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f, cb = 0.f;
+  if (valid) {
+    bias = a.delta_bias ? a.delta_bias[d] : 0.f;
+    Dd = a.D ? a.D[d] : 0.f;
+    if (CONV) {
+      const int K = a.d_conv;
+      const float* wp = a.conv_w + (long long)d * K;
+      w3 = wp[K - 1];
+      if (K >= 2) w2 = wp[K - 2];
+      if (K >= 3) w1 = wp[K - 3];
+      if (K >= 4) w0 = wp[K - 4];
+      cb = a.conv_b ? a.conv_b[d] : 0.f;
+    }
+  }
+  if (CONV && g == 0) {
+    // the 3 raw inputs before the chunk: conv_init (or zeros) for the first chunk, else x
     float hv[3] = {0.f, 0.f, 0.f};
-    if (d < dim) {
-      par[0] = a.delta_bias ? a.delta_bias[d] : 0.f;
-      par[1] = a.D ? a.D[d] : 0.f;
-      if (CONV) {
-        const int K = a.d_conv;
-        for (int k = 0; k < K; ++k) par[2 + (kMaxConv - K) + k] = a.conv_w[(long long)d * K + k];
-        par[6] = a.conv_b ? a.conv_b[d] : 0.f;
-        const long long c = (long long)b * dim + d;
-        if (q == 0) {
-          if (a.conv_init) {
-            const T* ci = static_cast<const T*>(a.conv_init) + c * (K - 1);
-            for (int j = 0; j < K - 1; ++j) hv[3 - (K - 1) + j] = to_f32(ci[j]);
-          }
-        } else {
-          for (int j = 0; j < 3; ++j) hv[j] = to_f32(gx[c * L + (t_begin - 3 + j)]);
+    if (valid) {
+      const int K = a.d_conv;
+      if (q == 0) {
+        if (a.conv_init) {
+          const T* ci = static_cast<const T*>(a.conv_init) + cc * (K - 1);
+          if (K >= 2) hv[2] = to_f32(ci[K - 2]);
+          if (K >= 3) hv[1] = to_f32(ci[K - 3]);
+          if (K >= 4) hv[0] = to_f32(ci[K - 4]);
         }
+      } else {
+        hv[0] = to_f32(gx[cc * L + (t_begin - 3)]);
+        hv[1] = to_f32(gx[cc * L + (t_begin - 2)]);
+        hv[2] = to_f32(gx[cc * L + (t_begin - 1)]);
       }
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) S.s_par[i][k] = par[k];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) S.s_halo[0][i][j] = hv[j];
-    S.s_halo[0][i][3] = 0.f;
+    S.s_halo[0][c][0] = hv[0];
+    S.s_halo[0][c][1] = hv[1];
+    S.s_halo[0][c][2] = hv[2];
+    S.s_halo[0][c][3] = 0.f;
   }
 
-  // ---- scan role of this thread: channel c_loc, states g*NPT .. g*NPT+NPT-1
-  const int c_loc = tid / TPC;
-  const int g = tid % TPC;
-  const int d_me = d0 + c_loc;
-  const bool valid = d_me < dim;
-  const long long c_me = (long long)b * dim + d_me;
-  float h[NPT], a2[NPT];
+  // ---- states n = 4g .. 4g+3 and A * log2(e)
+  float2 h01 = make_float2(0.f, 0.f), h23 = make_float2(0.f, 0.f);
+  float2 a01, a23;
+  {
+    float av[4];
 #pragma unroll
-  for (int k = 0; k < NPT; ++k) {
-    const int n = g * NPT + k;
-    a2[k] = (valid && n < N) ? a.A[(long long)d_me * N + n] * kLog2e : 0.f;
-    h[k] = 0.f;
+    for (int k = 0; k < 4; ++k) {
+      const int n = 4 * g + k;
+      av[k] = (valid && n < N) ? a.A[(long long)d * N + n] * kLog2e : 0.f;
+    }
+    a01 = make_float2(av[0], av[1]);
+    a23 = make_float2(av[2], av[3]);
   }
   if (!CARRY && valid) {
     if (a.h0) {
+      float hv[4];
 #pragma unroll
-      for (int k = 0; k < NPT; ++k) {
-        const int n = g * NPT + k;
-        if (n < N) h[k] = a.h0[c_me * N + n];
+      for (int k = 0; k < 4; ++k) {
+        const int n = 4 * g + k;
+        hv[k] = n < N ? a.h0[cc * N + n] : 0.f;
       }
+      h01 = make_float2(hv[0], hv[1]);
+      h23 = make_float2(hv[2], hv[3]);
     }
     // carry-in: compose the aggregates of chunks 0 .. q-1 onto h0
     for (int j = 0; j < q; ++j) {
-      const float Sj = a.ws_S[(long long)j * BD + c_me];
-      const float* hj = a.ws_h + ((long long)j * BD + c_me) * kMaxDstate + g * NPT;
-#pragma unroll
-      for (int k = 0; k < NPT; ++k) h[k] = fmaf(ex2_approx(Sj * a2[k]), h[k], hj[k]);
+      const float Sj = a.ws_S[(long long)j * BD + cc];
+      const float4 hb = *reinterpret_cast<const float4*>(a.ws_h + ((long long)j * BD + cc) * kMaxDstate + 4 * g);
+      const float2 x01 = fmul2(f2(Sj), a01), x23 = fmul2(f2(Sj), a23);
+      h01 = ffma2(make_float2(ex2_approx(x01.x), ex2_approx(x01.y)), h01, make_float2(hb.x, hb.y));
+      h23 = ffma2(make_float2(ex2_approx(x23.x), ex2_approx(x23.y)), h23, make_float2(hb.z, hb.w));
     }
   }
   float dsum = 0.f;  // CARRY: sum of Delta over the chunk
 
-  // ---- raw tile loaders
-  constexpr int kRowsMain = 3 * DT + 2 * kMaxDstate;
-  constexpr int kRowsCarry = 2 * DT + kMaxDstate;
-  constexpr int kRows = CARRY ? kRowsCarry : kRowsMain;
-  // map a staging row to (global row pointer, shared row pointer); returns false for padding rows
-  auto row_ptrs = [&](int r, int bf, const T*& src, T*& dst) -> bool {
-    if (r < DT) {
-      dst = S.raw_x[bf][r];
-      const int d = d0 + r;
-      src = gx + ((long long)b * dim + d) * L;
-      return d < dim;
+  // ---- staging: every thread copies the same 16-byte column of a fixed set of rows for
+  // every tile, so the global row pointers are computed once. Row r of a slot is
+  // x (r < 32), delta, z, B (96..111) or C (112..127); rows past dim / N, z rows without a
+  // gate and steps past the chunk end are zero-filled.
+  constexpr int kEPC = 16 / (int)sizeof(T);        // elements per 16-byte chunk
+  constexpr int kCPR = kTT / kEPC;                 // chunks per row
+  constexpr int kRowStep = kThreads / kCPR;        // rows between one thread's chunks
+  constexpr int kCopies = kRows / kRowStep;        // chunks per thread per tile
+  static_assert(kThreads % kCPR == 0 && kRows % kRowStep == 0, "copy tiling");
+  const int col = (tid % kCPR) * kEPC;             // this thread's column within a row
+  const T* src_row[kCopies];
+  bool row_ok[kCopies];
+#pragma unroll
+  for (int k = 0; k < kCopies; ++k) {
+    const int r = tid / kCPR + k * kRowStep;
+    const T* base = gx;
+    bool ok = false;
+    if (r < 3 * kDT) {
+      const int arr = r / kDT, rr = r % kDT;
+      const T* arrp = arr == 0 ? gx : (arr == 1 ? static_cast<const T*>(a.delta) : gz);
+      ok = d0 + rr < dim && (arr < 2 || has_z);
+      if (ok) base = arrp + ((long long)b * dim + d0 + rr) * L;
+    } else {
+      const int rr = r - 3 * kDT;
+      const int n = rr % kMaxDstate;
+      const bool isC = rr >= kMaxDstate;
+      ok = n < N && !(CARRY && isC);
+      if (ok) base = static_cast<const T*>(isC ? a.C : a.B) + ((long long)b * N + n) * L;
     }
-    r -= DT;
-    if (r < DT) {
-      dst = S.raw_d[bf][r];
-      const int d = d0 + r;
-      src = gd + ((long long)b * dim + d) * L;
-      return d < dim;
+    src_row[k] = base + col;
+    row_ok[k] = ok;
+  }
+
+  auto issue_tile_async = [&](int it, int slot) {
+    const int t0 = t_begin + it * kTT;
+    const bool tin = col < t_end - t0;
+    T* dst = &S.raw[slot][tid / kCPR][col];
+#pragma unroll
+    for (int k = 0; k < kCopies; ++k) {
+      const bool ok = row_ok[k] && tin;
+      cp_async16(dst + k * kRowStep * kTT, ok ? (const void*)(src_row[k] + t0) : (const void*)gx, ok ? 16u : 0u);
     }
-    r -= DT;
-    if (!CARRY) {
-      if (r < DT) {
-        dst = S.raw_z[bf][r];
-        const int d = d0 + r;
-        src = has_z ? gz + ((long long)b * dim + d) * L : gx;
-        return has_z && d < dim;
-      }
-      r -= DT;
-    }
-    if (r < kMaxDstate) {
-      dst = S.raw_B[bf][r];
-      src = gB + ((long long)b * N + r) * L;
-      return r < N;
-    }
-    r -= kMaxDstate;
-    dst = S.raw_C[bf][r];
-    src = gC + ((long long)b * N + r) * L;
-    return r < N;
   };
 
-  auto issue_tile_async = [&](int it, int bf) {
-    constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
-    constexpr int CPR = kTT / EPC;            // chunks per row
+  auto load_tile_sync = [&](int it, int slot) {
     const int t0 = t_begin + it * kTT;
     const int tl = min(kTT, t_end - t0);
-    for (int e = tid; e < kRows * CPR; e += kThreads) {
-      const int r = e / CPR, tt = (e % CPR) * EPC;
-      const T* src;
-      T* dst;
-      const bool ok = row_ptrs(r, bf, src, dst) && tt < tl;
-      cp_async16(dst + tt, ok ? (const void*)(src + t0 + tt) : (const void*)gx, ok ? 16u : 0u);
+#pragma unroll
+    for (int k = 0; k < kCopies; ++k) {
+      T* dst = &S.raw[slot][tid / kCPR + k * kRowStep][col];
+#pragma unroll
+      for (int e = 0; e < kEPC; ++e)
+        dst[e] = (row_ok[k] && col + e < tl) ? src_row[k][t0 + e] : from_f32<T>(0.f);
     }
   };
 
-  auto load_tile_sync = [&](int it, int bf) {
-    const int t0 = t_begin + it * kTT;
-    const int tl = min(kTT, t_end - t0);
-    for (int e = tid; e < kRows * kTT; e += kThreads) {
-      const int r = e / kTT, tt = e % kTT;
-      const T* src;
-      T* dst;
-      const bool ok = row_ptrs(r, bf, src, dst) && tt < tl;
-      dst[tt] = ok ? src[t0 + tt] : from_f32<T>(0.f);
+  if (VEC) {
+    // prologue: tiles 0 .. kS-2 in flight (one commit group per tile, empty past the end)
+#pragma unroll 1
+    for (int st = 0; st < kS - 1; ++st) {
+      if (st < ntiles) issue_tile_async(st, st);
+      cp_async_commit();
     }
-  };
-
-  if (VEC && ntiles > 0) {
-    issue_tile_async(0, 0);
-    cp_async_commit();
   }
 
   for (int it = 0; it < ntiles; ++it) {
-    const int bf = it & 1;
+    const int bf = it % kS;     // ring slot of tile `it`
+    const int hb = it & 1;      // halo ping-pong
     const int t0 = t_begin + it * kTT;
     const int tl = min(kTT, t_end - t0);
     if (VEC) {
-      cp_async_wait<0>();
+      cp_async_wait<kS - 2>();  // groups 0 .. it are complete
     } else {
       load_tile_sync(it, bf);
     }
-    __syncthreads();  // (A) tile `it` visible; every thread is past iteration it-1
-    if (VEC && it + 1 < ntiles) {
-      issue_tile_async(it + 1, bf ^ 1);
+    __syncthreads();  // (A) tile `it` visible; every thread is past iteration it-1, so the
+                      //     slot of tile it-1 can be refilled
+    if (VEC) {
+      const int nt = it + kS - 1;
+      if (nt < ntiles) issue_tile_async(nt, nt % kS);
       cp_async_commit();
     }
+    const T (*raw)[kTT] = S.raw[bf];
 
-    // ---- element-wise phase: B, C -> fp32 t-major; x, delta -> u, Delta, Delta*u
-    for (int e = tid; e < kMaxDstate * kTT; e += kThreads) {
-      const int n = e / kTT, t = e % kTT;
-      const bool ok = n < N && t < tl;
-      S.s_B[t][n] = ok ? to_f32(S.raw_B[bf][n][t]) : 0.f;
-      if (!CARRY) S.s_C[t][n] = ok ? to_f32(S.raw_C[bf][n][t]) : 0.f;
+    // ---- B, C -> fp32 t-major, in 4x4 blocks (rows past N / steps past the end are zero)
+    if (tid < (CARRY ? 32 : 64)) {
+      const int blk = tid & 31;
+      const int n0 = (blk & 3) * 4, s0 = (blk >> 2) * 4;
+      const T (*src)[kTT] = raw + 3 * kDT + (tid >= 32 ? kMaxDstate : 0);
+      float (*dst)[kMaxDstate] = tid >= 32 ? S.s_C : S.s_B;
+      float v[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) load4(&src[n0 + i][s0], v[i]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float4*>(&dst[s0 + j][n0]) = make_float4(v[0][j], v[1][j], v[2][j], v[3][j]);
     }
-    for (int e = tid; e < DT * (kTT / 4); e += kThreads) {
-      const int i = e / (kTT / 4), tt = (e % (kTT / 4)) * 4;
-      float xv[4], dv[4], u[4];
-      load4(&S.raw_x[bf][i][tt], xv);
-      load4(&S.raw_d[bf][i][tt], dv);
-      const float bias = S.s_par[i][0];
+
+    // ---- element-wise phase: steps tt .. tt+7 of channel c
+    const int tt = g * kSeg;
+    float2 skip[kSeg / 2], gate[kSeg / 2];
+    {
+      float xv[kSeg], dv[kSeg], zv[kSeg];
+      load8(&raw[c][tt], xv);
+      load8(&raw[kDT + c][tt], dv);
+      if (has_z) load8(&raw[2 * kDT + c][tt], zv);
+      float p0 = 0.f, p1 = 0.f, p2 = 0.f;  // x[tt-3], x[tt-2], x[tt-1]
       if (CONV) {
-        float win[7];
-        if (tt == 0) {
-          win[0] = S.s_halo[bf][i][0];
-          win[1] = S.s_halo[bf][i][1];
-          win[2] = S.s_halo[bf][i][2];
+        if (g == 0) {
+          p0 = S.s_halo[hb][c][0];
+          p1 = S.s_halo[hb][c][1];
+          p2 = S.s_halo[hb][c][2];
         } else {
           float pv[4];
-          load4(&S.raw_x[bf][i][tt - 4], pv);
-          win[0] = pv[1];
-          win[1] = pv[2];
-          win[2] = pv[3];
+          load4(&raw[c][tt - 4], pv);
+          p0 = pv[1];
+          p1 = pv[2];
+          p2 = pv[3];
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) win[3 + j] = xv[j];
-        const float w0 = S.s_par[i][2], w1 = S.s_par[i][3], w2 = S.s_par[i][4], w3 = S.s_par[i][5];
-        const float cb = S.s_par[i][6];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float acc = fmaf(w0, win[j], cb);
-          acc = fmaf(w1, win[j + 1], acc);
-          acc = fmaf(w2, win[j + 2], acc);
-          acc = fmaf(w3, win[j + 3], acc);
-          u[j] = silu_f(acc);
+        if (g == kTPC - 1) {
+          S.s_halo[hb ^ 1][c][0] = xv[kSeg - 3];
+          S.s_halo[hb ^ 1][c][1] = xv[kSeg - 2];
+          S.s_halo[hb ^ 1][c][2] = xv[kSeg - 1];
         }
-        if (tt == kTT - 4) {
-          S.s_halo[bf ^ 1][i][0] = xv[1];
-          S.s_halo[bf ^ 1][i][1] = xv[2];
-          S.s_halo[bf ^ 1][i][2] = xv[3];
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) u[j] = xv[j];
       }
-      float dl[4], du[4];
+      float win[kSeg + 3];
+      win[0] = p0;
+      win[1] = p1;
+      win[2] = p2;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float v = dv[j] + bias;
-        float D_ = a.delta_softplus ? softplus_f<PRECISE>(v) : v;
-        const bool tin = tt + j < tl;
-        D_ = tin ? D_ : 0.f;
-        u[j] = tin ? u[j] : 0.f;
-        dl[j] = D_;
-        du[j] = D_ * u[j];
+      for (int j = 0; j < kSeg; ++j) win[3 + j] = xv[j];
+      float dl[kSeg], du[kSeg];
+      const bool full = tt + kSeg <= tl;
+#pragma unroll
+      for (int j = 0; j < kSeg; j += 2) {
+        float2 u;
+        if (CONV) {
+          float2 acc = ffma2(f2(w0), make_float2(win[j], win[j + 1]), f2(cb));
+          acc = ffma2(f2(w1), make_float2(win[j + 1], win[j + 2]), acc);
+          acc = ffma2(f2(w2), make_float2(win[j + 2], win[j + 3]), acc);
+          acc = ffma2(f2(w3), make_float2(win[j + 3], win[j + 4]), acc);
+          u = silu2(acc);
+        } else {
+          u = make_float2(xv[j], xv[j + 1]);
+        }
+        const float2 v = fadd2(make_float2(dv[j], dv[j + 1]), f2(bias));
+        float2 D2 = a.delta_softplus ? softplus2<PRECISE>(v) : v;
+        if (!full) {  // steps past the tile end are identity updates: Delta = 0, u = 0
+          const bool i0 = tt + j < tl, i1 = tt + j + 1 < tl;
+          D2 = make_float2(i0 ? D2.x : 0.f, i1 ? D2.y : 0.f);
+          u = make_float2(i0 ? u.x : 0.f, i1 ? u.y : 0.f);
+        }
+        const float2 du2 = fmul2(D2, u);
+        dl[j] = D2.x;
+        dl[j + 1] = D2.y;
+        du[j] = du2.x;
+        du[j + 1] = du2.y;
+        if (!CARRY) {
+          skip[j / 2] = fmul2(f2(Dd), u);
+          gate[j / 2] = has_z ? silu2(make_float2(zv[j], zv[j + 1])) : f2(1.f);
+        }
       }
-      store4(&S.s_delta[i][tt], dl);
-      store4(&S.s_du[i][tt], du);
-      if (!CARRY) store4(&S.s_u[i][tt], u);
+      store8(&S.s_dl[c][tt], dl);
+      store8(&S.s_du[c][tt], du);
     }
     __syncthreads();  // (B)
 
-    // ---- scan phase: sequential in t, NPT states per thread in registers
+    // ---- scan phase: sequential in t; steps past tl have Delta = 0 and Delta*u = 0 (identity)
     {
-      const int tl4 = (tl + 3) & ~3;  // steps past tl have Delta = 0, Delta*u = 0: identity updates
+      const int tl4 = (tl + 3) & ~3;
       for (int t = 0; t < tl4; t += 4) {
-        const float4 dl4 = *reinterpret_cast<const float4*>(&S.s_delta[c_loc][t]);
-        const float4 du4 = *reinterpret_cast<const float4*>(&S.s_du[c_loc][t]);
+        const float4 dl4 = *reinterpret_cast<const float4*>(&S.s_dl[c][t]);
+        const float4 du4 = *reinterpret_cast<const float4*>(&S.s_du[c][t]);
         const float dl[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
         const float du[4] = {du4.x, du4.y, du4.z, du4.w};
         float yv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float bq[NPT], cq[NPT];
-          if (NPT % 4 == 0) {
-#pragma unroll
-            for (int k = 0; k < NPT; k += 4) {
-              const float4 bb = *reinterpret_cast<const float4*>(&S.s_B[t + j][g * NPT + k]);
-              bq[k] = bb.x; bq[k + 1] = bb.y; bq[k + 2] = bb.z; bq[k + 3] = bb.w;
-              if (!CARRY) {
-                const float4 cc = *reinterpret_cast<const float4*>(&S.s_C[t + j][g * NPT + k]);
-                cq[k] = cc.x; cq[k + 1] = cc.y; cq[k + 2] = cc.z; cq[k + 3] = cc.w;
-              }
-            }
+          const float4 bv = *reinterpret_cast<const float4*>(&S.s_B[t + j][4 * g]);
+          const float2 dd = f2(dl[j]);
+          const float2 x01 = fmul2(dd, a01), x23 = fmul2(dd, a23);
+          const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+          const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+          const float2 uu = f2(du[j]);
+          h01 = ffma2(e01, h01, fmul2(uu, make_float2(bv.x, bv.y)));
+          h23 = ffma2(e23, h23, fmul2(uu, make_float2(bv.z, bv.w)));
+          if (!CARRY) {
+            const float4 cv = *reinterpret_cast<const float4*>(&S.s_C[t + j][4 * g]);
+            const float2 p = ffma2(h23, make_float2(cv.z, cv.w), fmul2(h01, make_float2(cv.x, cv.y)));
+            yv[j] = p.x + p.y;
           } else {
-#pragma unroll
-            for (int k = 0; k < NPT; ++k) {
-              bq[k] = S.s_B[t + j][g * NPT + k];
-              if (!CARRY) cq[k] = S.s_C[t + j][g * NPT + k];
-            }
+            dsum += dl[j];
           }
-          float acc = 0.f;
-#pragma unroll
-          for (int k = 0; k < NPT; ++k) {
-            const float ab = ex2_approx(dl[j] * a2[k]);
-            h[k] = fmaf(ab, h[k], du[j] * bq[k]);
-            if (!CARRY) acc = fmaf(cq[k], h[k], acc);
-          }
-          if (CARRY) dsum += dl[j];
-          yv[j] = acc;
         }
-        if (!CARRY) store4(&S.s_y[g][c_loc][t], yv);
+        if (!CARRY) store4(&S.s_y[c][g][t], yv);
       }
     }
 
     if (!CARRY) {
-      __syncthreads();  // (C)
-      // ---- epilogue: y = sum of partials + D u, gate, store
-      for (int e = tid; e < DT * (kTT / 4); e += kThreads) {
-        const int i = e / (kTT / 4), tt = (e % (kTT / 4)) * 4;
-        const int d = d0 + i;
-        if (d >= dim || tt >= tl) continue;
-        float y[4], uu[4];
-        load4(&S.s_y[0][i][tt], y);
+      __syncwarp();  // the four partials of channel c come from this thread's own warp
+      // ---- epilogue: y = sum of the four partials + D u, gate, store steps tt .. tt+7
+      if (valid && tt < tl) {
+        float y0[kSeg], y1[kSeg], y2[kSeg], y3[kSeg];
+        load8(&S.s_y[c][0][tt], y0);
+        load8(&S.s_y[c][1][tt], y1);
+        load8(&S.s_y[c][2][tt], y2);
+        load8(&S.s_y[c][3][tt], y3);
+        float o[kSeg];
 #pragma unroll
-        for (int gg = 1; gg < TPC; ++gg) {
-          float p[4];
-          load4(&S.s_y[gg][i][tt], p);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) y[j] += p[j];
+        for (int j = 0; j < kSeg; j += 2) {
+          float2 y = fadd2(fadd2(make_float2(y0[j], y0[j + 1]), make_float2(y1[j], y1[j + 1])),
+                           fadd2(make_float2(y2[j], y2[j + 1]), make_float2(y3[j], y3[j + 1])));
+          y = fmul2(fadd2(y, skip[j / 2]), gate[j / 2]);
+          o[j] = y.x;
+          o[j + 1] = y.y;
         }
-        load4(&S.s_u[i][tt], uu);
-        const float Dd = S.s_par[i][1];
-        float o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = fmaf(Dd, uu[j], y[j]);
-        if (has_z) {
-          float zz[4];
-          load4(&S.raw_z[bf][i][tt], zz);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) o[j] *= silu_f(zz[j]);
-        }
-        T* dst = static_cast<T*>(a.out) + ((long long)b * dim + d) * L + t0 + tt;
-        if (VEC) {
-          store4(dst, o);
+        T* dst = static_cast<T*>(a.out) + cc * L + t0 + tt;
+        if (VEC && tt + kSeg <= tl) {
+          store8(dst, o);
+        } else if (VEC && tt + 4 <= tl) {  // fp32 rows can end on a 4-step boundary
+          const float o4[4] = {o[0], o[1], o[2], o[3]};
+          store4(dst, o4);
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < kSeg; ++j)
             if (tt + j < tl) dst[j] = from_f32<T>(o[j]);
         }
       }
@@ -384,40 +397,35 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const ScanArgs a) {
   // ---- chunk results
   if (valid) {
     if (CARRY) {
-      float* hw = a.ws_h + ((long long)q * BD + c_me) * kMaxDstate + g * NPT;
-#pragma unroll
-      for (int k = 0; k < NPT; ++k) hw[k] = h[k];
-      if (g == 0) a.ws_S[(long long)q * BD + c_me] = dsum;
+      *reinterpret_cast<float4*>(a.ws_h + ((long long)q * BD + cc) * kMaxDstate + 4 * g) =
+          make_float4(h01.x, h01.y, h23.x, h23.y);
+      if (g == 0) a.ws_S[(long long)q * BD + cc] = dsum;
     } else if (q == a.nchunks - 1 && a.h_last) {
+      const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
 #pragma unroll
-      for (int k = 0; k < NPT; ++k) {
-        const int n = g * NPT + k;
-        if (n < N) a.h_last[c_me * N + n] = h[k];
+      for (int k = 0; k < 4; ++k) {
+        const int n = 4 * g + k;
+        if (n < N) a.h_last[cc * N + n] = hv[k];
       }
     }
   }
-  if (!CARRY && q == a.nchunks - 1 && a.conv_state_out && a.d_conv > 1) {
-    // the last K-1 raw inputs of the stream conv_init ++ x (copied bit for bit)
+  if (!CARRY && q == a.nchunks - 1 && a.conv_state_out && a.d_conv > 1 && valid) {
+    // the last K-1 raw inputs of the stream conv_init ++ x, copied bit for bit
     const int K1 = a.d_conv - 1;
-    for (int e = tid; e < DT * K1; e += kThreads) {
-      const int i = e / K1, j = e % K1;
-      const int d = d0 + i;
-      if (d >= dim) continue;
-      const long long c = (long long)b * dim + d;
+    for (int j = g; j < K1; j += kTPC) {
       const int s = L - K1 + j;
       T v;
-      if (s >= 0) v = gx[c * L + s];
-      else v = a.conv_init ? static_cast<const T*>(a.conv_init)[c * K1 + (K1 + s)] : from_f32<T>(0.f);
-      static_cast<T*>(a.conv_state_out)[c * K1 + j] = v;
+      if (s >= 0) v = gx[cc * L + s];
+      else v = a.conv_init ? static_cast<const T*>(a.conv_init)[cc * K1 + (K1 + s)] : from_f32<T>(0.f);
+      static_cast<T*>(a.conv_state_out)[cc * K1 + j] = v;
     }
   }
 }
 
-template <typename T, int NPT, bool CONV, bool VEC, bool CARRY>
+template <typename T, bool CONV, bool VEC, bool CARRY>
 cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, cudaStream_t stream) {
-  constexpr int DT = Cfg<NPT>::DT;
-  const size_t smem = sizeof(Smem<T, NPT>);
-  auto kern = scan_kernel<T, NPT, CONV, VEC, CARRY>;
+  const size_t smem = sizeof(Smem<T>);
+  auto kern = scan_kernel<T, CONV, VEC, CARRY>;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -427,34 +435,30 @@ cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, cudaStream_t stream)
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  dim3 grid((a.dim + DT - 1) / DT, nchunks_grid, a.batch);
+  dim3 grid((a.dim + kDT - 1) / kDT, nchunks_grid, a.batch);
   kern<<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <typename T, int NPT, bool CONV, bool VEC>
+template <typename T, bool CONV, bool VEC>
 cudaError_t launch_pair(const ScanArgs& a, cudaStream_t stream) {
   if (a.nchunks > 1) {
-    cudaError_t err = launch_one<T, NPT, CONV, VEC, true>(a, a.nchunks - 1, stream);
+    cudaError_t err = launch_one<T, CONV, VEC, true>(a, a.nchunks - 1, stream);
     if (err != cudaSuccess) return err;
   }
-  return launch_one<T, NPT, CONV, VEC, false>(a, a.nchunks, stream);
-}
-
-template <typename T, int NPT>
-cudaError_t dispatch_conv_vec(const ScanArgs& a, cudaStream_t s) {
-  const bool conv = a.conv_w != nullptr;
-  if (conv) return a.vec ? launch_pair<T, NPT, true, true>(a, s) : launch_pair<T, NPT, true, false>(a, s);
-  return a.vec ? launch_pair<T, NPT, false, true>(a, s) : launch_pair<T, NPT, false, false>(a, s);
+  return launch_one<T, CONV, VEC, false>(a, a.nchunks, stream);
 }
 
 template <typename T>
-cudaError_t dispatch_npt(const ScanArgs& a, cudaStream_t s) {
-  if (a.npt == 1) return dispatch_conv_vec<T, 1>(a, s);
-  return dispatch_conv_vec<T, 4>(a, s);
+cudaError_t dispatch(const ScanArgs& a, cudaStream_t s) {
+  const bool conv = a.conv_w != nullptr;
+  if (conv) return a.vec ? launch_pair<T, true, true>(a, s) : launch_pair<T, true, false>(a, s);
+  return a.vec ? launch_pair<T, false, true>(a, s) : launch_pair<T, false, false>(a, s);
 }
 
 }  // namespace
+
+int scan_channels_per_cta() { return kDT; }
 
 size_t scan_workspace_bytes(long long channels, int nchunks) {
   if (nchunks <= 1) return 0;
@@ -476,8 +480,8 @@ void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, 
 }
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
-  if (a.bf16) return dispatch_npt<__nv_bfloat16>(a, stream);
-  return dispatch_npt<float>(a, stream);
+  if (a.bf16) return dispatch<__nv_bfloat16>(a, stream);
+  return dispatch<float>(a, stream);
 }
 
 }  // namespace ssm
