@@ -170,6 +170,41 @@ SSM_API ssm_status ssm_selective_state_update(float* state, void* conv_state, co
                                       const float* conv_b, int d_conv, void* y, int batch, int dim, int dstate,
                                       ssm_dtype io, void* stream);
 
+/*
+ * Size in bytes of the fixed device array that ssm_selective_scan_fwd_noalloc uses as its
+ * chunk-carry scratch. Every GPU that loads the library holds this much memory until exit.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * ssm_selective_scan_fwd for callers that cannot allocate device memory: callers that own
+ * only their inputs and outputs (for example a host framework's plugin interface that hands
+ * over tensor pointers but no workspace) or a serving loop that must not call cudaMalloc,
+ * which can block on device-wide synchronisation. The pages have no counterpart to this
+ * call; it is a deployment convenience of this library.
+ *
+ * Arguments, layouts and results are those of ssm_selective_scan_fwd without the workspace:
+ * the chunk carries go to a file-scope device array of SSM_NOALLOC_SCRATCH_BYTES bytes
+ * instead. The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).
+ *   - The first call on a device looks up that array's device address, with the device
+ *     current; make that first call before any stream capture.
+ *   - With chunk_len = 0 the scan uses as many chunks as fit the array (one chunk needs
+ *     none). An explicit chunk_len whose carries need more than SSM_NOALLOC_SCRATCH_BYTES
+ *     (see ssm_scan_workspace_bytes) returns SSM_ERR_UNSUPPORTED before anything runs.
+ *   - Every call shares the one array and it keeps the last call's contents. Nothing in it
+ *     needs clearing: each call's carry kernel writes every entry its main kernel reads.
+ *     Calls that overlap on the GPU (different streams, or different host threads without
+ *     ordering) race on the array and give wrong results; serialise them.
+ */
+SSM_API ssm_status ssm_selective_scan_fwd_noalloc(const void* x, const void* delta, const float* A, const void* B,
+                                                  const void* C, const float* D, const void* z,
+                                                  const float* delta_bias, int delta_softplus, const float* conv_w,
+                                                  const float* conv_b, int d_conv, const void* conv_init,
+                                                  const float* h0, void* out, float* h_last, void* conv_state_out,
+                                                  int batch, int dim, int seqlen, int dstate, ssm_dtype io,
+                                                  int chunk_len, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

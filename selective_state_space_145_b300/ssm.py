@@ -27,7 +27,11 @@ _lib = None
 
 # Exported C symbols, as declared in include/ssm.h.
 EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_scan_default_chunk_len",
-           "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update")
+           "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update",
+           "ssm_selective_scan_fwd_noalloc")
+
+# Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 
 class SSMError(RuntimeError):
@@ -60,6 +64,9 @@ def lib() -> ctypes.CDLL:
         L.ssm_selective_scan_fwd.restype = i
         L.ssm_selective_scan_fwd.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, vp, fp, vp]
                                              + [i] * 6 + [vp, sz, vp])
+        L.ssm_selective_scan_fwd_noalloc.restype = i
+        L.ssm_selective_scan_fwd_noalloc.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, vp, fp, vp]
+                                                     + [i] * 6 + [vp])
         L.ssm_selective_state_update.restype = i
         L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
                                                  i, i, i, i, vp]
