@@ -292,9 +292,10 @@ def run_gpu(args, w):
         launches_per_step = w.steps
         kernels = ["decode_kernel"]
     else:
-        cl = ssm.ssm_scan_default_chunk_len(w.batch, w.dim, w.seqlen, w.dstate, g["x"].dtype)
+        cl = args.chunk_len or ssm.ssm_scan_default_chunk_len(w.batch, w.dim, w.seqlen, w.dstate, g["x"].dtype)
+        cl = (cl + 63) // 64 * 64
         nchunks = (w.seqlen + cl - 1) // cl
-        ws_bytes = ssm.ssm_scan_workspace_bytes(w.batch, w.dim, w.seqlen, w.dstate, 0, g["x"].dtype)
+        ws_bytes = ssm.ssm_scan_workspace_bytes(w.batch, w.dim, w.seqlen, w.dstate, args.chunk_len, g["x"].dtype)
         ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
         out = torch.empty_like(g["x"])
         h_last = torch.empty(w.batch, w.dim, w.dstate, dtype=torch.float32, device=dev)
@@ -302,7 +303,7 @@ def run_gpu(args, w):
         def step():
             ssm.ssm_selective_scan_fwd(g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"],
                                        True, g["conv_w"], g["conv_b"], None, None, workspace=ws, out=out,
-                                       h_last=h_last)
+                                       h_last=h_last, chunk_len=args.chunk_len)
 
         launches_per_step = 2 if nchunks > 1 else 1
         kernels = ["scan_kernel<carry>", "scan_kernel<main>"] if nchunks > 1 else ["scan_kernel<main>"]
@@ -368,7 +369,8 @@ def run_gpu(args, w):
                         dev_in[k].copy_(v, non_blocking=True)
                 ssm.ssm_selective_scan_fwd(dev_in["x"], dev_in["delta"], dev_in["A"], dev_in["B"], dev_in["C"],
                                            dev_in["D"], dev_in["z"], dev_in["delta_bias"], True, dev_in["conv_w"],
-                                           dev_in["conv_b"], None, None, workspace=ws, out=out, h_last=h_last)
+                                           dev_in["conv_b"], None, None, workspace=ws, out=out, h_last=h_last,
+                                           chunk_len=args.chunk_len)
                 out_host.copy_(out, non_blocking=True)
                 hl_host.copy_(h_last, non_blocking=True)
 
@@ -436,6 +438,8 @@ def main(argv=None):
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override the workload's sequence length (smaller cases for profiling)")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
+    ap.add_argument("--chunk-len", type=int, default=0,
+                    help="scan chunk length (0 = the library's default policy)")
     args = ap.parse_args(argv)
     import dataclasses
 

@@ -46,18 +46,24 @@ static_assert(kTPC * kNPT == kMaxDstate, "four threads x four states cover N = 1
 static_assert(kDT * kTPC == kThreads, "one thread group per channel");
 static_assert(kSeg == 8, "element-wise segment of 8 steps");
 
-// Depth of the raw-tile ring: 3 tiles of 8 KB (bf16) or 2 of 16 KB (fp32) per CTA, which
-// keeps four (bf16) or three (fp32) CTAs resident per SM.
+// Depth of the raw-tile ring: two tiles per CTA, which keeps four (bf16) or three (fp32)
+// CTAs resident per SM.
 template <typename T>
-constexpr int stages() { return sizeof(T) == 2 ? 3 : 2; }
+constexpr int stages() { return 2; }
+
+// Raw rows are padded (80-byte bf16 / 144-byte fp32 rows) so that the 32 threads of a warp,
+// each reading its own channel's row, hit distinct banks within every quarter-warp.
+template <typename T>
+constexpr int row_stride() { return sizeof(T) == 2 ? kTT + 8 : kTT + 4; }
 
 template <typename T>
 struct __align__(16) Smem {
   static constexpr int S = stages<T>();
-  T raw[S][kRows][kTT];          // rows 0..31 x, 32..63 delta, 64..95 z, 96..111 B, 112..127 C
+  static constexpr int RS = row_stride<T>();
+  T raw[S][kRows][RS];           // rows 0..31 x, 32..63 delta, 64..95 z, 96..111 B, 112..127 C
   float s_dl[kDT][kTP];          // Delta
   float s_du[kDT][kTP];          // Delta * u
-  float s_y[kDT][kTPC][kTP];     // partial C.h of each thread, per step
+  float s_y[kTPC][kDT][kTP];     // partial C.h of each state group, per channel and step
   float s_B[kTT][kMaxDstate];    // B, fp32, t-major
   float s_C[kTT][kMaxDstate];
   float s_halo[2][kDT][4];       // the 3 raw inputs before the tile (ping-pong by tile parity)
@@ -71,8 +77,11 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   Smem<T>& S = *reinterpret_cast<Smem<T>*>(smem_raw);
 
   const int tid = threadIdx.x;
-  const int c = tid / kTPC;          // channel within the CTA
-  const int g = tid % kTPC;          // state group: n = 4g .. 4g+3; element-wise steps 8g .. 8g+7
+  // A warp is one state group g (states 4g .. 4g+3) of all 32 channels, so every B / C
+  // read of the scan is a warp-wide broadcast; thread (c, g) also owns the element-wise
+  // work and the epilogue of steps 8g .. 8g+7 of channel c.
+  const int c = tid % kDT;           // channel within the CTA
+  const int g = tid / kDT;           // state group
   const int d0 = blockIdx.x * kDT;
   const int q = blockIdx.y;
   const int b = blockIdx.z;
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
 #pragma unroll
     for (int k = 0; k < kCopies; ++k) {
       const bool ok = row_ok[k] && tin;
-      cp_async16(dst + k * kRowStep * kTT, ok ? (const void*)(src_row[k] + t0) : (const void*)gx, ok ? 16u : 0u);
+      cp_async16(dst + k * kRowStep * Smem<T>::RS, ok ? (const void*)(src_row[k] + t0) : (const void*)gx, ok ? 16u : 0u);
     }
   };
 
@@ -245,13 +254,13 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       if (nt < ntiles) issue_tile_async(nt, nt % kS);
       cp_async_commit();
     }
-    const T (*raw)[kTT] = S.raw[bf];
+    const T (*raw)[Smem<T>::RS] = S.raw[bf];
 
     // ---- B, C -> fp32 t-major, in 4x4 blocks (rows past N / steps past the end are zero)
     if (tid < (CARRY ? 32 : 64)) {
       const int blk = tid & 31;
       const int n0 = (blk & 3) * 4, s0 = (blk >> 2) * 4;
-      const T (*src)[kTT] = raw + 3 * kDT + (tid >= 32 ? kMaxDstate : 0);
+      const T (*src)[Smem<T>::RS] = raw + 3 * kDT + (tid >= 32 ? kMaxDstate : 0);
       float (*dst)[kMaxDstate] = tid >= 32 ? S.s_C : S.s_B;
       float v[4][4];
 #pragma unroll
@@ -357,19 +366,19 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
             dsum += dl[j];
           }
         }
-        if (!CARRY) store4(&S.s_y[c][g][t], yv);
+        if (!CARRY) store4(&S.s_y[g][c][t], yv);
       }
     }
 
     if (!CARRY) {
-      __syncwarp();  // the four partials of channel c come from this thread's own warp
+      __syncthreads();  // (C) the four partials of channel c come from the four warps
       // ---- epilogue: y = sum of the four partials + D u, gate, store steps tt .. tt+7
       if (valid && tt < tl) {
         float y0[kSeg], y1[kSeg], y2[kSeg], y3[kSeg];
-        load8(&S.s_y[c][0][tt], y0);
-        load8(&S.s_y[c][1][tt], y1);
-        load8(&S.s_y[c][2][tt], y2);
-        load8(&S.s_y[c][3][tt], y3);
+        load8(&S.s_y[0][c][tt], y0);
+        load8(&S.s_y[1][c][tt], y1);
+        load8(&S.s_y[2][c][tt], y2);
+        load8(&S.s_y[3][c][tt], y3);
         float o[kSeg];
 #pragma unroll
         for (int j = 0; j < kSeg; j += 2) {
