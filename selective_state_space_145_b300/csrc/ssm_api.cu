@@ -35,15 +35,16 @@ int sm_count() {
 long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 
 // Time-chunk length. Chunking costs a carry pass over all but the last chunk, so the scan
-// runs as one chunk whenever the channels alone give every SM at least two CTAs; otherwise
-// it takes the fewest chunks that give four CTAs per SM, keeping chunks >= 256 steps.
+// runs as one chunk whenever the channels alone give every SM a CTA. Otherwise each chunk's
+// CTAs walk their steps sequentially, and short chains of many CTAs beat long chains of few:
+// take up to 16 CTAs per SM, keeping chunks at least 256 steps long.
 int default_chunk_len_impl(int batch, int dim, int seqlen) {
   const int dt = ssm::scan_channels_per_cta();
   const long long ctas = ((dim + dt - 1) / dt) * (long long)batch;
   const long long sms = sm_count();
-  const long long target = sms * 4;
+  const long long target = sms * 16;
   const long long whole = round_up(seqlen > 0 ? seqlen : 1, kChunkQuantum);
-  if (ctas >= sms * 2 || seqlen <= 512) return (int)whole;
+  if (ctas >= sms || seqlen <= 512) return (int)whole;
   long long q = (target + ctas - 1) / ctas;
   const long long qmax = (seqlen + 255) / 256;
   if (q > qmax) q = qmax;

@@ -1,0 +1,72 @@
+"""Host logic of the multi-rank benchmark on CPU with two gloo ranks: every rank runs its own
+copy of the workload (no collective on the data path); the step time reported is the max over
+ranks, and the reference arm runs on rank 0 only."""
+
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        got = bench.reduce_max(float(rank + 1) * 1.5, world)
+        w, r, local = bench._dist()
+        q.put((rank, got, w, r, local))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_rank_env():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(world))
+    for rank, got, w, r, local in res:
+        assert got == pytest.approx(3.0)      # max of 1.5 and 3.0 on every rank
+        assert (w, r, local) == (world, rank, rank)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    import bench
+
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    assert bench.main(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_algorithmic_bytes_match_the_stated_formula():
+    import bench
+    from selective_state_space_145_b300 import inputs
+
+    w = inputs.WORKLOADS["block_bf16_b8_d2048_l2048_n16_k4"]
+    assert bench.algorithmic_bytes(w) == 270_721_024
+    w = inputs.WORKLOADS["longscan_bf16_b1_d1536_l131072_n16"]
+    assert bench.algorithmic_bytes(w) == 1_619_210_240
+    w = inputs.WORKLOADS["decode_bf16_b256_d5120_n16_k4_x64"]
+    assert bench.algorithmic_bytes(w) == 194_473_984 * 64
