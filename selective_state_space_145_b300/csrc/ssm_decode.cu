@@ -9,10 +9,9 @@
 // state[n] = exp(Delta A[d,n]) state[n] + Delta B[b,n] u, y = (C.state + D u) silu(z).
 //
 // HBM-bound: the fp32 state is read and written once (128 of the ~150 bytes a channel moves).
-// Four adjacent threads own one channel, four states each, so a warp moves 8 channels x 64 B
-// of state per access with 16-byte loads and stores; C.state is reduced over the four
-// threads with two shuffles. Tiles of 64 channels never cross a sequence, so no index needs
-// a division, and the conv width is a compile-time constant.
+// The fast kernel gives one thread a whole channel (16 states) and keeps the channel's
+// parameters in registers across sequences; the general kernel (any N, any alignment) gives
+// four threads a channel. The conv width is a compile-time constant in both.
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -115,132 +114,203 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a)
   }
 }
 
-// ---------------------------------------------------------------- streaming kernel (N = 16)
+// ---------------------------------------------------------------- channel-tile kernel (N = 16)
 //
-// Persistent CTAs walk tiles of 64 channels of one sequence. A 4-stage cp.async ring stages
-// each tile's fp32 state (4 KB) and its x, delta, z and conv-window bytes in shared memory,
-// so a CTA keeps three tiles on their way from HBM without holding registers for them; the
-// new state goes back with coalesced 16-byte stores. Needs dim * element size a multiple of
-// 16 bytes (every tile then starts 16-byte aligned) and 16-byte aligned pointers.
-constexpr int kStrThreads = 256;
-constexpr int kStrCh = kStrThreads / 4;
-constexpr int kStrStages = 4;
+// One thread owns one channel (all 16 states); a CTA owns a tile of 256 channels and walks
+// a set of sequences for that tile, so the channel's parameters (A, D, delta_bias, conv
+// taps) are loaded into registers once and reused. Each (tile, sequence) item is staged by
+// a 3-stage cp.async ring: the tile's fp32 state (16 KB, rows padded to 80 bytes so that the
+// per-thread row reads are bank-conflict free), x, delta, z, the conv window and that
+// sequence's B, C. The new state and window are written back into the staged rows and then
+// copied out in contiguous 16-byte chunks: whole-sector stores, which HBM takes at copy
+// speed (per-thread row stores leave half-written sectors).
+constexpr int kTileCh = 256;          // channels per CTA = threads per CTA
+constexpr int kTileStages = 3;
+constexpr int kStRow = kMaxDstate + 4;  // padded fp32 state row
 
 template <typename T>
-struct __align__(16) StrSmem {
-  float st[kStrStages][kStrCh * kMaxDstate];
-  T x[kStrStages][kStrCh];
-  T dl[kStrStages][kStrCh];
-  T z[kStrStages][kStrCh];
-  T win[kStrStages][kStrCh * (kMaxConv - 1)];
+struct __align__(16) TileSmem {
+  float st[kTileStages][kTileCh][kStRow];
+  T x[kTileStages][kTileCh];
+  T dl[kTileStages][kTileCh];
+  T z[kTileStages][kTileCh];
+  T win[kTileStages][kTileCh * (kMaxConv - 1)];
+  T bc[kTileStages][2 * kMaxDstate];   // B then C of the item's sequence (raw I/O dtype)
+  float bcf[2 * kMaxDstate];           // the current item's B, C in fp32
 };
 
 template <typename T, int KC>
-__global__ void __launch_bounds__(kStrThreads) decode_stream_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a, int n_ctiles, int row_groups) {
+  constexpr bool PRECISE = IoTraits<T>::kPrecise;
   constexpr int K1 = KC > 0 ? KC - 1 : 0;
   constexpr int ES = (int)sizeof(T);
-  constexpr int EPC = 16 / ES;             // I/O elements per 16-byte chunk
-  constexpr int kCpa = kStrCh / EPC;       // chunks of one per-channel I/O array per tile
-  __shared__ StrSmem<T> S;
+  constexpr int EPC = 16 / ES;
+  constexpr int kCpa = kTileCh / EPC;  // 16-byte chunks of one per-channel I/O array per tile
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TileSmem<T>& S = *reinterpret_cast<TileSmem<T>*>(smem_raw);
   const int tid = threadIdx.x;
-  const int c = tid / 4, g = tid % 4;
   const int dim = a.dim;
-  const int tiles_per_row = (dim + kStrCh - 1) / kStrCh;
+  const int ct = blockIdx.x % n_ctiles;         // channel tile
+  const int rg = blockIdx.x / n_ctiles;         // first sequence; then every row_groups-th
+  const int d0 = ct * kTileCh;
+  const int nvalid = min(kTileCh, dim - d0);
+  const int d = d0 + tid;
+  const bool valid = tid < nvalid;
+
+  // ---- this channel's parameters, once
+  float a2[kMaxDstate];
+  float bias = 0.f, Dd = 0.f, cb = 0.f, w[KC > 0 ? KC : 1];
+#pragma unroll
+  for (int k = 0; k < (KC > 0 ? KC : 1); ++k) w[k] = 0.f;
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < kMaxDstate; i += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(a.A + (long long)d * kMaxDstate + i);
+      a2[i] = q.x * kLog2e; a2[i + 1] = q.y * kLog2e; a2[i + 2] = q.z * kLog2e; a2[i + 3] = q.w * kLog2e;
+    }
+    bias = a.delta_bias ? a.delta_bias[d] : 0.f;
+    Dd = a.D ? a.D[d] : 0.f;
+    if (KC > 0) {
+#pragma unroll
+      for (int k = 0; k < KC; ++k) w[k] = a.conv_w[(long long)d * KC + k];
+      cb = a.conv_b ? a.conv_b[d] : 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kMaxDstate; ++i) a2[i] = 0.f;
+  }
+
   const T* gx = static_cast<const T*>(a.x);
   const T* gd = static_cast<const T*>(a.delta);
   const T* gz = static_cast<const T*>(a.z);
   const T* gw = static_cast<const T*>(a.conv_state);
+  const T* gB = static_cast<const T*>(a.B);
+  const T* gC = static_cast<const T*>(a.C);
 
-  // Tiles are visited as tile = blockIdx.x + i * gridDim.x; (sequence, tile-in-row) pairs are
-  // advanced incrementally so that no index needs a division inside the loop.
-  struct Pos {
-    int b, t;  // sequence, tile within the sequence
-  };
-  const int step_b = (int)(gridDim.x / (unsigned)tiles_per_row);
-  const int step_t = (int)(gridDim.x % (unsigned)tiles_per_row);
-  auto advance = [&](Pos p) {
-    p.b += step_b;
-    p.t += step_t;
-    if (p.t >= tiles_per_row) {
-      p.t -= tiles_per_row;
-      ++p.b;
-    }
-    return p;
-  };
-  auto issue_tile = [&](Pos p, int slot) {
-    const int b = p.b;
-    const int d0 = p.t * kStrCh;
+  auto issue_item = [&](int b, int slot) {
     const long long c0 = (long long)b * dim + d0;
-    const int nvalid = min(kStrCh, dim - d0);  // channels of this tile inside the sequence
-    {  // state: one 16-byte chunk (4 states) per thread
-      const bool ok = c < nvalid;
-      cp_async16(&S.st[slot][tid * 4], ok ? (const void*)(a.state + c0 * kMaxDstate + tid * 4) : (const void*)a.state,
-                 ok ? 16u : 0u);
+    // state: 128 channels x 4 chunks; chunk e -> channel e / 4, quarter e % 4 (coalesced in global)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = tid + k * kTileCh;
+      const int ch = e >> 2, part = e & 3;
+      const bool ok = ch < nvalid;
+      cp_async16(&S.st[slot][ch][4 * part], ok ? (const void*)(a.state + (c0 + ch) * kMaxDstate + 4 * part)
+                                                : (const void*)a.state, ok ? 16u : 0u);
     }
-    for (int e = tid; e < (3 + K1) * kCpa; e += kStrThreads) {
-      const int arr = e / kCpa, ch = e % kCpa;
-      if (arr < 3) {
+    // x, delta, z, window, B, C
+    constexpr int kBC = 2 * kMaxDstate * ES / 16;  // chunks of B and C together
+    for (int e = tid; e < (3 + K1) * kCpa + kBC; e += kTileCh) {
+      if (e < 3 * kCpa) {
+        const int arr = e / kCpa, first = (e % kCpa) * EPC;
         const T* base = arr == 0 ? gx : (arr == 1 ? gd : gz);
         T* dst = arr == 0 ? S.x[slot] : (arr == 1 ? S.dl[slot] : S.z[slot]);
-        const int first = ch * EPC;
         const int n = nvalid - first;
         const unsigned bytes = (base == nullptr || n <= 0) ? 0u : (n >= EPC ? 16u : (unsigned)(n * ES));
         cp_async16(dst + first, bytes ? (const void*)(base + c0 + first) : (const void*)a.state, bytes);
-      } else {
-        const int first = (e - 3 * kCpa) * EPC;  // element within this tile's window block
+      } else if (e < (3 + K1) * kCpa) {
+        const int first = (e - 3 * kCpa) * EPC;
         const int n = nvalid * K1 - first;
         const unsigned bytes = n <= 0 ? 0u : (n >= EPC ? 16u : (unsigned)(n * ES));
         cp_async16(S.win[slot] + first, bytes ? (const void*)(gw + c0 * K1 + first) : (const void*)a.state, bytes);
+      } else {
+        const int q = e - (3 + K1) * kCpa;               // 0 .. kBC-1
+        const int half = kBC / 2;
+        const T* src = q < half ? gB + (long long)b * kMaxDstate + q * EPC
+                                : gC + (long long)b * kMaxDstate + (q - half) * EPC;
+        cp_async16(S.bc[slot] + q * EPC, src, 16u);
       }
     }
   };
 
-  Pos cur{(int)(blockIdx.x / (unsigned)tiles_per_row), (int)(blockIdx.x % (unsigned)tiles_per_row)};
-  Pos ahead = cur;  // the tile kStrStages-1 visits ahead of `cur`
+  int b_ahead = rg;
 #pragma unroll 1
-  for (int st = 0; st < kStrStages - 1; ++st) {
-    if (ahead.b < a.batch) issue_tile(ahead, st);
+  for (int st = 0; st < kTileStages - 1; ++st) {
+    if (b_ahead < a.batch) issue_item(b_ahead, st);
     cp_async_commit();
-    ahead = advance(ahead);
+    b_ahead += row_groups;
   }
 
 #pragma unroll 1
-  for (int i = 0; cur.b < a.batch; ++i, cur = advance(cur)) {
-    const int slot = i % kStrStages;
-    cp_async_wait<kStrStages - 2>();
-    __syncthreads();  // tile i visible; every thread is done with tile i-1, whose slot is refilled next
-    if (ahead.b < a.batch) issue_tile(ahead, (i + kStrStages - 1) % kStrStages);
+  for (int i = 0, b = rg; b < a.batch; ++i, b += row_groups) {
+    const int slot = i % kTileStages;
+    cp_async_wait<kTileStages - 2>();
+    __syncthreads();  // (A) item i visible; every thread is done with item i-1 and its B/C copy
+    if (b_ahead < a.batch) issue_item(b_ahead, (i + kTileStages - 1) % kTileStages);
     cp_async_commit();
-    ahead = advance(ahead);
-    const int b = cur.b;
-    const int d = cur.t * kStrCh + c;
-    const bool valid = d < dim;
+    b_ahead += row_groups;
+    if (tid < 2 * kMaxDstate) S.bcf[tid] = to_f32(S.bc[slot][tid]);
+    __syncthreads();  // (B) this item's B, C in fp32
+
     const long long cc = (long long)b * dim + d;
-    float av[4] = {0.f, 0.f, 0.f, 0.f}, bv[4], cv[4];
-    if (valid) {
-      const float4 a4 = *reinterpret_cast<const float4*>(a.A + (long long)d * kMaxDstate + 4 * g);
-      av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+    float h[kMaxDstate];
+#pragma unroll
+    for (int i4 = 0; i4 < kMaxDstate; i4 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(&S.st[slot][tid][i4]);
+      h[i4] = q.x; h[i4 + 1] = q.y; h[i4 + 2] = q.z; h[i4 + 3] = q.w;
     }
-    load4(static_cast<const T*>(a.B) + (long long)b * kMaxDstate + 4 * g, bv);
-    load4(static_cast<const T*>(a.C) + (long long)b * kMaxDstate + 4 * g, cv);
-    const float4 h4 = *reinterpret_cast<const float4*>(&S.st[slot][c * kMaxDstate + 4 * g]);
-    float h[4] = {h4.x, h4.y, h4.z, h4.w};
-    float u = 0.f;
-    const T* win = &S.win[slot][c * K1];
-    float part = channel_step<T, KC>(a, valid ? d : 0, to_f32(S.x[slot][c]), to_f32(S.dl[slot][c]), win, h, av,
-                                     bv, cv, u);
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    const float xv = to_f32(S.x[slot][tid]);
+    float u = xv;
+    if (KC > 0) {
+      float acc = cb;
+#pragma unroll
+      for (int k = 0; k < K1; ++k) acc = fmaf(w[k], to_f32(S.win[slot][tid * K1 + k]), acc);
+      acc = fmaf(w[K1], xv, acc);
+      u = silu_f(acc);
+    }
+    const float v = to_f32(S.dl[slot][tid]) + bias;
+    const float Delta = a.delta_softplus ? softplus_f<PRECISE>(v) : v;
+    const float du = Delta * u;
+    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < kMaxDstate; n += 2) {
+      const float2 bq = *reinterpret_cast<const float2*>(&S.bcf[n]);
+      const float2 cq = *reinterpret_cast<const float2*>(&S.bcf[kMaxDstate + n]);
+      h[n] = fmaf(ex2_approx(Delta * a2[n]), h[n], du * bq.x);
+      h[n + 1] = fmaf(ex2_approx(Delta * a2[n + 1]), h[n + 1], du * bq.y);
+      y0 = fmaf(cq.x, h[n], y0);
+      y1 = fmaf(cq.y, h[n + 1], y1);
+    }
+    // new state and window back into this thread's own staged rows
+#pragma unroll
+    for (int i4 = 0; i4 < kMaxDstate; i4 += 4)
+      *reinterpret_cast<float4*>(&S.st[slot][tid][i4]) = make_float4(h[i4], h[i4 + 1], h[i4 + 2], h[i4 + 3]);
+    if (K1 > 0) {
+      // the window shifts one place towards the old end; the newest slot takes x
+      T nw[K1 > 0 ? K1 : 1];
+#pragma unroll
+      for (int k = 0; k + 1 < K1; ++k) nw[k] = S.win[slot][tid * K1 + k + 1];
+      nw[K1 - 1] = S.x[slot][tid];
+#pragma unroll
+      for (int k = 0; k < K1; ++k) S.win[slot][tid * K1 + k] = nw[k];
+    }
     if (valid) {
-      *reinterpret_cast<float4*>(a.state + cc * kMaxDstate + 4 * g) = make_float4(h[0], h[1], h[2], h[3]);
-      if (g == 0) {
-        float y = fmaf(a.D ? a.D[d] : 0.f, u, part);
-        if (gz) y *= silu_f(to_f32(S.z[slot][c]));
-        static_cast<T*>(a.y)[cc] = from_f32<T>(y);
+      float y = fmaf(Dd, u, y0 + y1);
+      if (gz) y *= silu_f(to_f32(S.z[slot][tid]));
+      static_cast<T*>(a.y)[cc] = from_f32<T>(y);
+    }
+    __syncthreads();  // (C) the tile's new rows are complete
+    {
+      const long long c0 = (long long)b * dim + d0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // state: chunk e -> channel e / 4, quarter e % 4
+        const int e = tid + k * kTileCh;
+        const int ch = e >> 2, part = e & 3;
+        if (ch < nvalid)
+          *reinterpret_cast<float4*>(a.state + (c0 + ch) * kMaxDstate + 4 * part) =
+              *reinterpret_cast<const float4*>(&S.st[slot][ch][4 * part]);
       }
-      if (g < K1) {
-        // the window shifts one place towards the old end; the newest slot takes x
-        static_cast<T*>(a.conv_state)[cc * K1 + g] = (g + 1 < K1) ? win[g + 1] : S.x[slot][c];
+      if (K1 > 0) {  // window: the tile's K1 * nvalid elements are contiguous in global memory
+        T* cs = static_cast<T*>(a.conv_state) + c0 * K1;
+        const int nel = nvalid * K1;
+        for (int e = tid; e * EPC < nel; e += kTileCh) {
+          const int first = e * EPC;
+          if (first + EPC <= nel) {
+            *reinterpret_cast<uint4*>(cs + first) = *reinterpret_cast<const uint4*>(S.win[slot] + first);
+          } else {
+            for (int j = first; j < nel; ++j) cs[j] = S.win[slot][j];
+          }
+        }
       }
     }
   }
@@ -254,24 +324,30 @@ cudaError_t launch_general(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 template <typename T, int KC>
-cudaError_t launch_stream(const DecodeArgs& a, cudaStream_t stream) {
-  // persistent grid: exactly the CTAs that are resident at once, so no CTA waits for a slot
+cudaError_t launch_tile(const DecodeArgs& a, cudaStream_t stream) {
+  // enough CTAs to fill the SMs at full occupancy; each walks several sequences of one tile
   static int resident[64] = {0};
+  const size_t smem = sizeof(TileSmem<T>);
+  auto kern = decode_tile_kernel<T, KC>;
   int dev = 0, sms = 148;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int per_sm = (dev >= 0 && dev < 64) ? resident[dev] : 0;
   if (per_sm == 0) {
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stream_kernel<T, KC>, kStrThreads, 0);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTileCh, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) per_sm = 1;
     if (dev >= 0 && dev < 64) resident[dev] = per_sm;
   }
-  const long long ntiles = (long long)a.batch * ((a.dim + kStrCh - 1) / kStrCh);
-  long long grid = (long long)sms * per_sm;
-  if (grid > ntiles) grid = ntiles;
-  decode_stream_kernel<T, KC><<<(unsigned)grid, kStrThreads, 0, stream>>>(a);
+  const int n_ctiles = (a.dim + kTileCh - 1) / kTileCh;
+  long long want = (long long)sms * per_sm;
+  int row_groups = (int)((want + n_ctiles - 1) / n_ctiles);
+  if (row_groups > a.batch) row_groups = a.batch;
+  if (row_groups < 1) row_groups = 1;
+  kern<<<(unsigned)(n_ctiles * row_groups), kTileCh, smem, stream>>>(a, n_ctiles, row_groups);
   return cudaGetLastError();
 }
 
@@ -280,11 +356,11 @@ cudaError_t dispatch_k(const DecodeArgs& a, bool stream_ok, cudaStream_t s) {
   const int KC = a.conv_w ? a.d_conv : 0;
   if (stream_ok) {
     switch (KC) {
-      case 0: return launch_stream<T, 0>(a, s);
-      case 1: return launch_stream<T, 1>(a, s);
-      case 2: return launch_stream<T, 2>(a, s);
-      case 3: return launch_stream<T, 3>(a, s);
-      default: return launch_stream<T, 4>(a, s);
+      case 0: return launch_tile<T, 0>(a, s);
+      case 1: return launch_tile<T, 1>(a, s);
+      case 2: return launch_tile<T, 2>(a, s);
+      case 3: return launch_tile<T, 3>(a, s);
+      default: return launch_tile<T, 4>(a, s);
     }
   }
   switch (KC) {
