@@ -69,15 +69,23 @@ def algorithmic_bytes(w) -> int:
     return b
 
 
-def kernel_source_hash() -> str:
+# The sources each kind of workload's kernels are built from: a traffic figure stays valid
+# while these files are unchanged.
+_KERNEL_SOURCES = {
+    "scan": ("ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
+    "decode": ("ssm_decode.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
+}
+
+
+def kernel_source_hash(kind: str = "scan") -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_145_b300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    for name in _KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "selective_state_space_145_b300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(workload: str):
+def traffic_from_profiles(workload: str, kind: str = "scan"):
     """DRAM bytes per step from a committed ncu summary, if its kernel-source hash is current."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -85,7 +93,7 @@ def traffic_from_profiles(workload: str):
     with open(path) as f:
         t = json.load(f)
     e = t.get(workload)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(kind):
         return None
     return e.get("dram_bytes_per_step")
 
@@ -409,7 +417,7 @@ def run_gpu(args, w):
         "config": config_of(w),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic_from_profiles(w.name), "peak_source": peak_kind,
+                     "traffic": traffic_from_profiles(w.name, w.kind), "peak_source": peak_kind,
                      "algorithmic_bytes_per_step": bytes_step,
                      "timed": "whole step (" + " + ".join(kernels) + "), CUDA events on the launching stream"},
         "cpu_baseline": cpu,

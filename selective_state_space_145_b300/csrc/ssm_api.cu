@@ -38,19 +38,22 @@ long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 // runs as one chunk whenever the channels alone give every SM a CTA. Otherwise each chunk's
 // CTAs walk their steps sequentially, and short chains of many CTAs beat long chains of few:
 // take up to 16 CTAs per SM, keeping chunks at least 256 steps long.
-int default_chunk_len_impl(int batch, int dim, int seqlen) {
+// Chunk length of the default policy. The scan is sequential in t within a CTA, so a
+// problem with few channels leaves most SMs idle unless the sequence is split into chunks.
+// The policy splits only as far as the main pass still fits in one wave of resident CTAs:
+// q chunks give q times the CTAs, each walking 1/q of the sequence, and a second wave
+// would cost as much as it saves.
+int default_chunk_len_impl(int batch, int dim, int seqlen, bool bf16) {
   const int dt = ssm::scan_channels_per_cta();
   const long long ctas = ((dim + dt - 1) / dt) * (long long)batch;
-  const long long sms = sm_count();
-  const long long target = sms * 16;
+  const long long resident = (long long)sm_count() * ssm::scan_resident_ctas_per_sm(bf16);
   const long long whole = round_up(seqlen > 0 ? seqlen : 1, kChunkQuantum);
-  if (ctas >= sms || seqlen <= 512) return (int)whole;
-  long long q = (target + ctas - 1) / ctas;
-  const long long qmax = (seqlen + 255) / 256;
+  if (ctas <= 0 || 2 * ctas > resident) return (int)whole;
+  long long q = resident / ctas;
+  const long long qmax = (seqlen + kChunkQuantum - 1) / kChunkQuantum;
   if (q > qmax) q = qmax;
-  if (q < 1) q = 1;
-  long long cl = round_up((seqlen + q - 1) / q, kChunkQuantum);
-  return (int)cl;
+  if (q <= 1) return (int)whole;
+  return (int)round_up((seqlen + q - 1) / q, kChunkQuantum);
 }
 
 int nchunks_for(int seqlen, int chunk_len) {
@@ -80,9 +83,8 @@ const char* ssm_status_string(int status) {
 
 int ssm_scan_default_chunk_len(int batch, int dim, int seqlen, int dstate, ssm_dtype io) {
   (void)dstate;
-  (void)io;
   if (batch <= 0 || dim <= 0 || seqlen < 0) return kChunkQuantum;
-  return default_chunk_len_impl(batch, dim, seqlen);
+  return default_chunk_len_impl(batch, dim, seqlen, io == SSM_BF16);
 }
 
 size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate, int chunk_len, ssm_dtype io) {
@@ -145,7 +147,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   // chunking
   int cl;
   if (chunk_len == 0) {
-    cl = default_chunk_len_impl(batch, dim, seqlen);
+    cl = default_chunk_len_impl(batch, dim, seqlen, io == SSM_BF16);
     // lower the chunk count until the given workspace suffices
     while (nchunks_for(seqlen, cl) > 1 &&
            ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl)) >

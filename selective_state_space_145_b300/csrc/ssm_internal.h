@@ -74,6 +74,8 @@ struct DecodeArgs {
 
 // Channels one scan CTA covers.
 int scan_channels_per_cta();
+// CTAs of the main scan kernel resident per SM (occupancy query; 4 without a device)
+int scan_resident_ctas_per_sm(bool bf16);
 
 // Workspace layout of the chunked scan.
 size_t scan_workspace_bytes(long long channels, int nchunks);

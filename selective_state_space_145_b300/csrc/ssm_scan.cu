@@ -12,8 +12,8 @@
 // per channel, each holding four of the (up to) 16 states in registers. Per time tile of
 // 32 steps:
 //  * the raw x / delta / z rows of the 32 channels and the 16 shared B / C rows are copied
-//    global->shared with 16-byte cp.async into a ring of 3-4 tiles, so several tiles are
-//    always in flight;
+//    global->shared with 16-byte cp.async into a two-slot ring, so the next tile is in
+//    flight while this one is processed;
 //  * element-wise phase: each thread turns 8 steps of its channel into Delta and Delta*u
 //    (conv, SiLU and softplus once per (t, d), never per state), keeps D*u and silu(z) for
 //    those steps in registers, and the block transposes B, C to fp32 [t][n];
@@ -41,13 +41,18 @@ constexpr int kDT = 32;        // channels per CTA
 constexpr int kTT = 32;        // time steps per tile
 constexpr int kTP = kTT + 4;   // padded row stride of the fp32 tile arrays (keeps float4 alignment)
 constexpr int kSeg = kTT / kTPC;  // steps per thread in the element-wise phase and the epilogue
-constexpr int kRows = 3 * kDT + 2 * kMaxDstate;  // staged rows per tile: x, delta, z, B, C
 static_assert(kTPC * kNPT == kMaxDstate, "four threads x four states cover N = 16");
 static_assert(kDT * kTPC == kThreads, "one thread group per channel");
 static_assert(kSeg == 8, "element-wise segment of 8 steps");
 
-// Depth of the raw-tile ring: two tiles per CTA, which keeps four (bf16) or three (fp32)
-// CTAs resident per SM.
+// Staged rows per tile. Main pass: x (rows 0..31), delta (32..63), z (64..95), B (96..111),
+// C (112..127). Carry pass (no readout, no gate): x, delta, B (64..79).
+template <bool CARRY>
+__host__ __device__ constexpr int rows_of() { return CARRY ? 2 * kDT + kMaxDstate : 3 * kDT + 2 * kMaxDstate; }
+template <bool CARRY>
+__host__ __device__ constexpr int row_B() { return CARRY ? 2 * kDT : 3 * kDT; }
+
+// Depth of the raw-tile ring: two tiles per CTA.
 template <typename T>
 constexpr int stages() { return 2; }
 
@@ -56,25 +61,52 @@ constexpr int stages() { return 2; }
 template <typename T>
 constexpr int row_stride() { return sizeof(T) == 2 ? kTT + 8 : kTT + 4; }
 
-template <typename T>
-struct __align__(16) Smem {
+constexpr size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+// Shared-memory layout (byte offsets into the dynamic allocation):
+//   ring  raw[S][R][RS]       staged raw rows
+//   dl    [kDT][kTP]          Delta
+//   du    [kDT][kTP]          Delta * u
+//   B, C  [kTT][16]           B, C as fp32, t-major (no C in the carry pass)
+//   halo  [2][kDT][4]         the 3 raw inputs before the tile (ping-pong by tile parity)
+//   y     [kTPC][kDT][kTP]    partial C.h of each state group, per channel and step
+// In the fp32 main pass y lives in the ring slot of the tile being processed: that slot is
+// dead once the element-wise phase and the B / C transpose have read it, and exactly as
+// large, which keeps the CTA at 51 KB (four CTAs per SM instead of three).
+template <typename T, bool CARRY>
+struct Layout {
   static constexpr int S = stages<T>();
   static constexpr int RS = row_stride<T>();
-  T raw[S][kRows][RS];           // rows 0..31 x, 32..63 delta, 64..95 z, 96..111 B, 112..127 C
-  float s_dl[kDT][kTP];          // Delta
-  float s_du[kDT][kTP];          // Delta * u
-  float s_y[kTPC][kDT][kTP];     // partial C.h of each state group, per channel and step
-  float s_B[kTT][kMaxDstate];    // B, fp32, t-major
-  float s_C[kTT][kMaxDstate];
-  float s_halo[2][kDT][4];       // the 3 raw inputs before the tile (ping-pong by tile parity)
+  static constexpr int R = rows_of<CARRY>();
+  static constexpr bool kYInRing = !CARRY && sizeof(T) == 4;
+  static constexpr size_t slot_bytes = sizeof(T) * (size_t)R * RS;
+  static constexpr size_t y_bytes = sizeof(float) * (size_t)kTPC * kDT * kTP;
+  static constexpr size_t ring = 0;
+  static constexpr size_t dl = align16(ring + slot_bytes * S);
+  static constexpr size_t du = dl + sizeof(float) * kDT * kTP;
+  static constexpr size_t Bt = du + sizeof(float) * kDT * kTP;
+  static constexpr size_t Ct = Bt + sizeof(float) * kTT * kMaxDstate;
+  static constexpr size_t halo = Ct + (CARRY ? 0 : sizeof(float) * kTT * kMaxDstate);
+  static constexpr size_t y = halo + sizeof(float) * 2 * kDT * 4;
+  static constexpr size_t bytes = y + ((CARRY || kYInRing) ? 0 : y_bytes);
+  static_assert(!kYInRing || y_bytes <= slot_bytes, "partials fit in one ring slot");
+  static_assert(slot_bytes % 16 == 0, "ring slots stay 16-byte aligned");
 };
 
 template <typename T, bool CONV, bool VEC, bool CARRY>
 __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
-  constexpr int kS = stages<T>();
+  using Lay = Layout<T, CARRY>;
+  constexpr int kS = Lay::S;
+  constexpr int RS = Lay::RS;
+  constexpr int kRows = Lay::R;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Smem<T>& S = *reinterpret_cast<Smem<T>*>(smem_raw);
+  T (*const ring)[kRows][RS] = reinterpret_cast<T (*)[kRows][RS]>(smem_raw + Lay::ring);
+  float (*const s_dl)[kTP] = reinterpret_cast<float (*)[kTP]>(smem_raw + Lay::dl);
+  float (*const s_du)[kTP] = reinterpret_cast<float (*)[kTP]>(smem_raw + Lay::du);
+  float (*const s_B)[kMaxDstate] = reinterpret_cast<float (*)[kMaxDstate]>(smem_raw + Lay::Bt);
+  float (*const s_C)[kMaxDstate] = reinterpret_cast<float (*)[kMaxDstate]>(smem_raw + Lay::Ct);
+  float (*const s_halo)[kDT][4] = reinterpret_cast<float (*)[kDT][4]>(smem_raw + Lay::halo);
 
   const int tid = threadIdx.x;
   // A warp is one state group g (states 4g .. 4g+3) of all 32 channels, so every B / C
@@ -83,8 +115,8 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   const int c = tid % kDT;           // channel within the CTA
   const int g = tid / kDT;           // state group
   const int d0 = blockIdx.x * kDT;
-  const int q = blockIdx.y;
-  const int b = blockIdx.z;
+  const int b = blockIdx.y;
+  const int q = blockIdx.z;  // chunk slowest: the chunk-0 CTAs, which need no carry, start first
   const int L = a.seqlen, N = a.dstate, dim = a.dim;
   const long long BD = (long long)a.batch * dim;
   const int t_begin = q * a.chunk_len;
@@ -94,9 +126,83 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   const bool valid = d < dim;
   const long long cc = (long long)b * dim + d;
 
+  if (CARRY) {
+    // let the main kernel's CTAs be scheduled as soon as every carry CTA is running: its
+    // chunk-0 CTAs need nothing from here, the others wait for this grid to complete
+    asm volatile("griddepcontrol.launch_dependents;");
+  }
+
   const T* __restrict__ gx = static_cast<const T*>(a.x);
   const T* __restrict__ gz = static_cast<const T*>(a.z);
   const bool has_z = (gz != nullptr) && !CARRY;
+
+  // ---- staging: every thread copies the same 16-byte column of a fixed set of rows for
+  // every tile, so the global row pointers are computed once. Rows past dim / N, z rows
+  // without a gate and steps past the chunk end are zero-filled.
+  constexpr int kEPC = 16 / (int)sizeof(T);        // elements per 16-byte chunk
+  constexpr int kCPR = kTT / kEPC;                 // chunks per row
+  constexpr int kRowStep = kThreads / kCPR;        // rows between one thread's chunks
+  constexpr int kCopies = (kRows + kRowStep - 1) / kRowStep;  // chunks per thread per tile
+  static_assert(kThreads % kCPR == 0, "copy tiling");
+  const int col = (tid % kCPR) * kEPC;             // this thread's column within a row
+  const T* src_row[kCopies];
+  bool row_ok[kCopies];
+#pragma unroll
+  for (int k = 0; k < kCopies; ++k) {
+    const int r = tid / kCPR + k * kRowStep;
+    const T* base = gx;
+    bool ok = false;
+    if (r < 2 * kDT || (!CARRY && r < 3 * kDT)) {
+      const int arr = r / kDT, rr = r % kDT;
+      const T* arrp = arr == 0 ? gx : (arr == 1 ? static_cast<const T*>(a.delta) : gz);
+      ok = d0 + rr < dim && (arr < 2 || has_z);
+      if (ok) base = arrp + ((long long)b * dim + d0 + rr) * L;
+    } else if (r < kRows) {
+      const int rr = r - row_B<CARRY>();
+      const int n = rr % kMaxDstate;
+      const bool isC = rr >= kMaxDstate;
+      ok = n < N;
+      if (ok) base = static_cast<const T*>(isC ? a.C : a.B) + ((long long)b * N + n) * L;
+    }
+    src_row[k] = base + col;
+    row_ok[k] = ok;
+  }
+  // whether copy k of this thread lands on a row of the layout (the last one may not)
+  auto row_in = [&](int k) { return kRows % kRowStep == 0 || tid / kCPR + k * kRowStep < kRows; };
+
+  auto issue_tile_async = [&](int it, int slot) {
+    const int t0 = t_begin + it * kTT;
+    const bool tin = col < t_end - t0;
+    T* dst = &ring[slot][tid / kCPR][col];
+#pragma unroll
+    for (int k = 0; k < kCopies; ++k) {
+      const bool ok = row_ok[k] && tin;
+      if (row_in(k))
+        cp_async16(dst + k * kRowStep * RS, ok ? (const void*)(src_row[k] + t0) : (const void*)gx, ok ? 16u : 0u);
+    }
+  };
+
+  auto load_tile_sync = [&](int it, int slot) {
+    const int t0 = t_begin + it * kTT;
+    const int tl = min(kTT, t_end - t0);
+#pragma unroll
+    for (int k = 0; k < kCopies; ++k) {
+      if (!row_in(k)) continue;
+      T* dst = &ring[slot][tid / kCPR + k * kRowStep][col];
+#pragma unroll
+      for (int e = 0; e < kEPC; ++e)
+        dst[e] = (row_ok[k] && col + e < tl) ? src_row[k][t0 + e] : from_f32<T>(0.f);
+    }
+  };
+
+  if (VEC) {
+    // prologue: tiles 0 .. kS-2 in flight (one commit group per tile, empty past the end)
+#pragma unroll 1
+    for (int st = 0; st < kS - 1; ++st) {
+      if (st < ntiles) issue_tile_async(st, st);
+      cp_async_commit();
+    }
+  }
 
   // ---- per-channel parameters, in registers; the conv filter is zero-padded to 4 taps
   float bias = 0.f, Dd = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f, cb = 0.f;
@@ -131,10 +237,10 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
         hv[2] = to_f32(gx[cc * L + (t_begin - 1)]);
       }
     }
-    S.s_halo[0][c][0] = hv[0];
-    S.s_halo[0][c][1] = hv[1];
-    S.s_halo[0][c][2] = hv[2];
-    S.s_halo[0][c][3] = 0.f;
+    s_halo[0][c][0] = hv[0];
+    s_halo[0][c][1] = hv[1];
+    s_halo[0][c][2] = hv[2];
+    s_halo[0][c][3] = 0.f;
   }
 
   // ---- states n = 4g .. 4g+3 and A * log2(e)
@@ -161,81 +267,33 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       h01 = make_float2(hv[0], hv[1]);
       h23 = make_float2(hv[2], hv[3]);
     }
-    // carry-in: compose the aggregates of chunks 0 .. q-1 onto h0
-    for (int j = 0; j < q; ++j) {
-      const float Sj = a.ws_S[(long long)j * BD + cc];
-      const float4 hb = *reinterpret_cast<const float4*>(a.ws_h + ((long long)j * BD + cc) * kMaxDstate + 4 * g);
-      const float2 x01 = fmul2(f2(Sj), a01), x23 = fmul2(f2(Sj), a23);
-      h01 = ffma2(make_float2(ex2_approx(x01.x), ex2_approx(x01.y)), h01, make_float2(hb.x, hb.y));
-      h23 = ffma2(make_float2(ex2_approx(x23.x), ex2_approx(x23.y)), h23, make_float2(hb.z, hb.w));
+    if (q > 0) {
+      // the chunk aggregates come from the carry kernel, which may still be running
+      // (this kernel can be launched as its programmatic dependent)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+    // carry-in: compose the aggregates of chunks 0 .. q-1 onto h0, four chunks' loads at a time
+    for (int j0 = 0; j0 < q; j0 += 4) {
+      float Sj[4];
+      float4 hb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool in = j0 + k < q;
+        const long long e = (long long)(in ? j0 + k : 0) * BD + cc;
+        Sj[k] = in ? a.ws_S[e] : 0.f;
+        hb[k] = in ? *reinterpret_cast<const float4*>(a.ws_h + e * kMaxDstate + 4 * g) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (j0 + k < q) {
+          const float2 x01 = fmul2(f2(Sj[k]), a01), x23 = fmul2(f2(Sj[k]), a23);
+          h01 = ffma2(make_float2(ex2_approx(x01.x), ex2_approx(x01.y)), h01, make_float2(hb[k].x, hb[k].y));
+          h23 = ffma2(make_float2(ex2_approx(x23.x), ex2_approx(x23.y)), h23, make_float2(hb[k].z, hb[k].w));
+        }
+      }
     }
   }
   float dsum = 0.f;  // CARRY: sum of Delta over the chunk
-
-  // ---- staging: every thread copies the same 16-byte column of a fixed set of rows for
-  // every tile, so the global row pointers are computed once. Row r of a slot is
-  // x (r < 32), delta, z, B (96..111) or C (112..127); rows past dim / N, z rows without a
-  // gate and steps past the chunk end are zero-filled.
-  constexpr int kEPC = 16 / (int)sizeof(T);        // elements per 16-byte chunk
-  constexpr int kCPR = kTT / kEPC;                 // chunks per row
-  constexpr int kRowStep = kThreads / kCPR;        // rows between one thread's chunks
-  constexpr int kCopies = kRows / kRowStep;        // chunks per thread per tile
-  static_assert(kThreads % kCPR == 0 && kRows % kRowStep == 0, "copy tiling");
-  const int col = (tid % kCPR) * kEPC;             // this thread's column within a row
-  const T* src_row[kCopies];
-  bool row_ok[kCopies];
-#pragma unroll
-  for (int k = 0; k < kCopies; ++k) {
-    const int r = tid / kCPR + k * kRowStep;
-    const T* base = gx;
-    bool ok = false;
-    if (r < 3 * kDT) {
-      const int arr = r / kDT, rr = r % kDT;
-      const T* arrp = arr == 0 ? gx : (arr == 1 ? static_cast<const T*>(a.delta) : gz);
-      ok = d0 + rr < dim && (arr < 2 || has_z);
-      if (ok) base = arrp + ((long long)b * dim + d0 + rr) * L;
-    } else {
-      const int rr = r - 3 * kDT;
-      const int n = rr % kMaxDstate;
-      const bool isC = rr >= kMaxDstate;
-      ok = n < N && !(CARRY && isC);
-      if (ok) base = static_cast<const T*>(isC ? a.C : a.B) + ((long long)b * N + n) * L;
-    }
-    src_row[k] = base + col;
-    row_ok[k] = ok;
-  }
-
-  auto issue_tile_async = [&](int it, int slot) {
-    const int t0 = t_begin + it * kTT;
-    const bool tin = col < t_end - t0;
-    T* dst = &S.raw[slot][tid / kCPR][col];
-#pragma unroll
-    for (int k = 0; k < kCopies; ++k) {
-      const bool ok = row_ok[k] && tin;
-      cp_async16(dst + k * kRowStep * Smem<T>::RS, ok ? (const void*)(src_row[k] + t0) : (const void*)gx, ok ? 16u : 0u);
-    }
-  };
-
-  auto load_tile_sync = [&](int it, int slot) {
-    const int t0 = t_begin + it * kTT;
-    const int tl = min(kTT, t_end - t0);
-#pragma unroll
-    for (int k = 0; k < kCopies; ++k) {
-      T* dst = &S.raw[slot][tid / kCPR + k * kRowStep][col];
-#pragma unroll
-      for (int e = 0; e < kEPC; ++e)
-        dst[e] = (row_ok[k] && col + e < tl) ? src_row[k][t0 + e] : from_f32<T>(0.f);
-    }
-  };
-
-  if (VEC) {
-    // prologue: tiles 0 .. kS-2 in flight (one commit group per tile, empty past the end)
-#pragma unroll 1
-    for (int st = 0; st < kS - 1; ++st) {
-      if (st < ntiles) issue_tile_async(st, st);
-      cp_async_commit();
-    }
-  }
 
   for (int it = 0; it < ntiles; ++it) {
     const int bf = it % kS;     // ring slot of tile `it`
@@ -254,14 +312,16 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       if (nt < ntiles) issue_tile_async(nt, nt % kS);
       cp_async_commit();
     }
-    const T (*raw)[Smem<T>::RS] = S.raw[bf];
+    const T (*raw)[RS] = ring[bf];
+    float (*const s_y)[kDT][kTP] =
+        reinterpret_cast<float (*)[kDT][kTP]>(smem_raw + (Lay::kYInRing ? Lay::ring + bf * Lay::slot_bytes : Lay::y));
 
     // ---- B, C -> fp32 t-major, in 4x4 blocks (rows past N / steps past the end are zero)
     if (tid < (CARRY ? 32 : 64)) {
       const int blk = tid & 31;
       const int n0 = (blk & 3) * 4, s0 = (blk >> 2) * 4;
-      const T (*src)[Smem<T>::RS] = raw + 3 * kDT + (tid >= 32 ? kMaxDstate : 0);
-      float (*dst)[kMaxDstate] = tid >= 32 ? S.s_C : S.s_B;
+      const T (*src)[RS] = raw + row_B<CARRY>() + (tid >= 32 ? kMaxDstate : 0);
+      float (*dst)[kMaxDstate] = tid >= 32 ? s_C : s_B;
       float v[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) load4(&src[n0 + i][s0], v[i]);
@@ -281,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       float p0 = 0.f, p1 = 0.f, p2 = 0.f;  // x[tt-3], x[tt-2], x[tt-1]
       if (CONV) {
         if (g == 0) {
-          p0 = S.s_halo[hb][c][0];
-          p1 = S.s_halo[hb][c][1];
-          p2 = S.s_halo[hb][c][2];
+          p0 = s_halo[hb][c][0];
+          p1 = s_halo[hb][c][1];
+          p2 = s_halo[hb][c][2];
         } else {
           float pv[4];
           load4(&raw[c][tt - 4], pv);
@@ -292,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           p2 = pv[3];
         }
         if (g == kTPC - 1) {
-          S.s_halo[hb ^ 1][c][0] = xv[kSeg - 3];
-          S.s_halo[hb ^ 1][c][1] = xv[kSeg - 2];
-          S.s_halo[hb ^ 1][c][2] = xv[kSeg - 1];
+          s_halo[hb ^ 1][c][0] = xv[kSeg - 3];
+          s_halo[hb ^ 1][c][1] = xv[kSeg - 2];
+          s_halo[hb ^ 1][c][2] = xv[kSeg - 1];
         }
       }
       float win[kSeg + 3];
@@ -334,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           gate[j / 2] = has_z ? silu2(make_float2(zv[j], zv[j + 1])) : f2(1.f);
         }
       }
-      store8(&S.s_dl[c][tt], dl);
-      store8(&S.s_du[c][tt], du);
+      store8(&s_dl[c][tt], dl);
+      store8(&s_du[c][tt], du);
     }
     __syncthreads();  // (B)
 
@@ -343,14 +403,14 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
     {
       const int tl4 = (tl + 3) & ~3;
       for (int t = 0; t < tl4; t += 4) {
-        const float4 dl4 = *reinterpret_cast<const float4*>(&S.s_dl[c][t]);
-        const float4 du4 = *reinterpret_cast<const float4*>(&S.s_du[c][t]);
+        const float4 dl4 = *reinterpret_cast<const float4*>(&s_dl[c][t]);
+        const float4 du4 = *reinterpret_cast<const float4*>(&s_du[c][t]);
         const float dl[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
         const float du[4] = {du4.x, du4.y, du4.z, du4.w};
         float yv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float4 bv = *reinterpret_cast<const float4*>(&S.s_B[t + j][4 * g]);
+          const float4 bv = *reinterpret_cast<const float4*>(&s_B[t + j][4 * g]);
           const float2 dd = f2(dl[j]);
           const float2 x01 = fmul2(dd, a01), x23 = fmul2(dd, a23);
           const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
@@ -359,14 +419,14 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           h01 = ffma2(e01, h01, fmul2(uu, make_float2(bv.x, bv.y)));
           h23 = ffma2(e23, h23, fmul2(uu, make_float2(bv.z, bv.w)));
           if (!CARRY) {
-            const float4 cv = *reinterpret_cast<const float4*>(&S.s_C[t + j][4 * g]);
+            const float4 cv = *reinterpret_cast<const float4*>(&s_C[t + j][4 * g]);
             const float2 p = ffma2(h23, make_float2(cv.z, cv.w), fmul2(h01, make_float2(cv.x, cv.y)));
             yv[j] = p.x + p.y;
           } else {
             dsum += dl[j];
           }
         }
-        if (!CARRY) store4(&S.s_y[g][c][t], yv);
+        if (!CARRY) store4(&s_y[g][c][t], yv);
       }
     }
 
@@ -375,10 +435,10 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       // ---- epilogue: y = sum of the four partials + D u, gate, store steps tt .. tt+7
       if (valid && tt < tl) {
         float y0[kSeg], y1[kSeg], y2[kSeg], y3[kSeg];
-        load8(&S.s_y[0][c][tt], y0);
-        load8(&S.s_y[1][c][tt], y1);
-        load8(&S.s_y[2][c][tt], y2);
-        load8(&S.s_y[3][c][tt], y3);
+        load8(&s_y[0][c][tt], y0);
+        load8(&s_y[1][c][tt], y1);
+        load8(&s_y[2][c][tt], y2);
+        load8(&s_y[3][c][tt], y3);
         float o[kSeg];
 #pragma unroll
         for (int j = 0; j < kSeg; j += 2) {
@@ -431,31 +491,59 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   }
 }
 
+// Opts the kernel into its dynamic shared memory once per device.
 template <typename T, bool CONV, bool VEC, bool CARRY>
-cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem<T>);
-  auto kern = scan_kernel<T, CONV, VEC, CARRY>;
+cudaError_t prepare() {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
+  err = cudaFuncSetAttribute(scan_kernel<T, CONV, VEC, CARRY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Layout<T, CARRY>::bytes);
+  if (err == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
+  return err;
+}
+
+// pdl: launch as the programmatic dependent of the kernel before it in the stream (which
+// must be this problem's carry kernel).
+template <typename T, bool CONV, bool VEC, bool CARRY>
+cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, bool pdl, cudaStream_t stream) {
+  cudaError_t err = prepare<T, CONV, VEC, CARRY>();
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.dim + kDT - 1) / kDT, a.batch, nchunks_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<T, CARRY>::bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, scan_kernel<T, CONV, VEC, CARRY>, a);
+}
+
+template <typename T>
+int resident_main_ctas() {
+  int n = 0;
+  if (prepare<T, true, true, false>() != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_kernel<T, true, true, false>, kThreads,
+                                                    Layout<T, false>::bytes) != cudaSuccess ||
+      n <= 0) {
+    cudaGetLastError();
+    return 4;  // no device to ask: the figure the kernel is built for
   }
-  dim3 grid((a.dim + kDT - 1) / kDT, nchunks_grid, a.batch);
-  kern<<<grid, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return n;
 }
 
 template <typename T, bool CONV, bool VEC>
 cudaError_t launch_pair(const ScanArgs& a, cudaStream_t stream) {
   if (a.nchunks > 1) {
-    cudaError_t err = launch_one<T, CONV, VEC, true>(a, a.nchunks - 1, stream);
+    cudaError_t err = launch_one<T, CONV, VEC, true>(a, a.nchunks - 1, false, stream);
     if (err != cudaSuccess) return err;
   }
-  return launch_one<T, CONV, VEC, false>(a, a.nchunks, stream);
+  return launch_one<T, CONV, VEC, false>(a, a.nchunks, a.nchunks > 1, stream);
 }
 
 template <typename T>
@@ -468,6 +556,10 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t s) {
 }  // namespace
 
 int scan_channels_per_cta() { return kDT; }
+
+int scan_resident_ctas_per_sm(bool bf16) {
+  return bf16 ? resident_main_ctas<__nv_bfloat16>() : resident_main_ctas<float>();
+}
 
 size_t scan_workspace_bytes(long long channels, int nchunks) {
   if (nchunks <= 1) return 0;
