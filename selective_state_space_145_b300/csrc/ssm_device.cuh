@@ -33,6 +33,13 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// tanh on the SFU; relative error about 2^-11 (used only by the bf16 tier).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- packed fp32 pairs (sm_100+ f32x2)
 // One instruction computes two fp32 lanes; the FMA pipe throughput per element is unchanged,
 // the issue slots are halved.
@@ -77,33 +84,69 @@ __device__ __forceinline__ float silu_f(float x) {
   return x * rcp_approx(1.0f + ex2_approx(-x * kLog2e));
 }
 
-// softplus(v) = log(1 + e^v); v itself above 20 (the remainder is below e^-20 relative).
-// PRECISE uses log1pf (accurate for the small step sizes, where 1 + e^v rounds);
-// the fast tier uses lg2(1 + e^v), whose relative error near Delta ~ 1e-3 is ~2e-4,
-// well inside the bf16 output tolerance.
-template <bool PRECISE>
-__device__ __forceinline__ float softplus_f(float v) {
-  if (v > 20.0f) return v;
-  float e = ex2_approx(v * kLog2e);
-  if (PRECISE) return log1pf(e);
-  return lg2_approx(1.0f + e) * kLn2;
+// log(1 + e) for e in [0, 1]: log(1 + e) = 2 atanh(s) with s = e / (2 + e) in [0, 1/3], summed
+// as s (1 + s^2/3 + s^4/5 + ... + s^12/13); the first omitted term is below 2e-8 relative, so
+// the result is good to a few ulp, including for tiny e where 1 + e rounds.
+__device__ __forceinline__ float log1p_unit(float e) {
+  const float s = e * rcp_approx(2.0f + e);
+  const float s2 = s * s;
+  float p = fmaf(s2, 1.0f / 13.0f, 1.0f / 11.0f);
+  p = fmaf(s2, p, 1.0f / 9.0f);
+  p = fmaf(s2, p, 1.0f / 7.0f);
+  p = fmaf(s2, p, 1.0f / 5.0f);
+  p = fmaf(s2, p, 1.0f / 3.0f);
+  p = fmaf(s2, p, 1.0f);
+  return 2.0f * s * p;
 }
 
-// Pairwise forms of the same functions: the FMA-pipe work packed two lanes per instruction,
-// the MUFU work per element unchanged.
+// softplus(v) = log(1 + e^v).
+// PRECISE: max(v, 0) + log(1 + e^-|v|), exact in form for every v, accurate to ~1e-6 relative.
+// Fast tier: lg2(1 + 2^(v log2 e)) ln 2, v itself above 20 (the remainder is below e^-20
+// relative); its relative error near Delta ~ 1e-3 is ~2e-4, inside the bf16 output tolerance.
+template <bool PRECISE>
+__device__ __forceinline__ float softplus_f(float v) {
+  if (PRECISE) return fmaxf(v, 0.0f) + log1p_unit(ex2_approx(-fabsf(v) * kLog2e));
+  if (v > 20.0f) return v;
+  return lg2_approx(1.0f + ex2_approx(v * kLog2e)) * kLn2;
+}
+
+// Pairwise forms: the FMA-pipe work packed two lanes per instruction, the SFU work per element.
+
+// silu, accurate tier: x / (1 + 2^(-x log2 e)).
 __device__ __forceinline__ float2 silu2(float2 x) {
   const float2 t = fmul2(x, f2(-kLog2e));
   const float2 den = fadd2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), f2(1.0f));
   return fmul2(x, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
 }
 
+// silu, fast tier: with h = x/2, silu(x) = h + h tanh(h); one SFU op per element.
+__device__ __forceinline__ float2 silu2_tanh(float2 x) {
+  const float2 h = fmul2(x, f2(0.5f));
+  return ffma2(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+}
+
 template <bool PRECISE>
-__device__ __forceinline__ float2 softplus2(float2 v) {
-  if (PRECISE) return make_float2(softplus_f<true>(v.x), softplus_f<true>(v.y));
-  const float2 t = fmul2(v, f2(kLog2e));
+__device__ __forceinline__ float2 silu2_tier(float2 x) {
+  if (PRECISE) return silu2(x);
+  return silu2_tanh(x);
+}
+
+// Delta log2(e) from the raw delta: Delta = softplus(delta + bias) (or delta + bias when
+// softplus is off). The scan keeps Delta in these log2 units, so exp(Delta A) = 2^(Delta' A)
+// needs no scaling of A; bias_l2 = bias log2(e).
+template <bool PRECISE>
+__device__ __forceinline__ float2 delta_log2(float2 dv, float bias, float bias_l2, bool softplus) {
+  if (PRECISE) {
+    float2 v = fadd2(dv, f2(bias));
+    if (softplus) v = make_float2(softplus_f<true>(v.x), softplus_f<true>(v.y));
+    return fmul2(v, f2(kLog2e));
+  }
+  const float2 t = ffma2(dv, f2(kLog2e), f2(bias_l2));
+  if (!softplus) return t;
+  // softplus(v) log2(e) = lg2(1 + 2^t), t = v log2(e); t itself above 20 log2(e)
   const float2 s = fadd2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), f2(1.0f));
-  const float2 r = fmul2(make_float2(lg2_approx(s.x), lg2_approx(s.y)), f2(kLn2));
-  return make_float2(v.x > 20.0f ? v.x : r.x, v.y > 20.0f ? v.y : r.y);
+  const float kT = 20.0f * kLog2e;
+  return make_float2(t.x > kT ? t.x : lg2_approx(s.x), t.y > kT ? t.y : lg2_approx(s.y));
 }
 
 // ---------------------------------------------------------------- I/O dtype

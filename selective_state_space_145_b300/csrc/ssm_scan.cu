@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       cb = a.conv_b ? a.conv_b[d] : 0.f;
     }
   }
+  const float bias_l2 = bias * kLog2e;
   if (CONV && g == 0) {
     // the 3 raw inputs before the chunk: conv_init (or zeros) for the first chunk, else x
     float hv[3] = {0.f, 0.f, 0.f};
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
     s_halo[0][c][3] = 0.f;
   }
 
-  // ---- states n = 4g .. 4g+3 and A * log2(e)
+  // ---- states n = 4g .. 4g+3 and A (Delta is kept in log2 units, so 2^(Delta' A) = exp(Delta A))
   float2 h01 = make_float2(0.f, 0.f), h23 = make_float2(0.f, 0.f);
   float2 a01, a23;
   {
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int n = 4 * g + k;
-      av[k] = (valid && n < N) ? a.A[(long long)d * N + n] * kLog2e : 0.f;
+      av[k] = (valid && n < N) ? a.A[(long long)d * N + n] : 0.f;
     }
     a01 = make_float2(av[0], av[1]);
     a23 = make_float2(av[2], av[3]);
@@ -325,9 +326,12 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       float v[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) load4(&src[n0 + i][s0], v[i]);
+      // B carries the ln 2 that turns Delta' (log2 units) back into Delta in Delta u B
+      const float sc = tid >= 32 ? 1.0f : kLn2;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<float4*>(&dst[s0 + j][n0]) = make_float4(v[0][j], v[1][j], v[2][j], v[3][j]);
+        *reinterpret_cast<float4*>(&dst[s0 + j][n0]) =
+            make_float4(v[0][j] * sc, v[1][j] * sc, v[2][j] * sc, v[3][j] * sc);
     }
 
     // ---- element-wise phase: steps tt .. tt+7 of channel c
@@ -369,16 +373,20 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       for (int j = 0; j < kSeg; j += 2) {
         float2 u;
         if (CONV) {
-          float2 acc = ffma2(f2(w0), make_float2(win[j], win[j + 1]), f2(cb));
-          acc = ffma2(f2(w1), make_float2(win[j + 1], win[j + 2]), acc);
-          acc = ffma2(f2(w2), make_float2(win[j + 2], win[j + 3]), acc);
-          acc = ffma2(f2(w3), make_float2(win[j + 3], win[j + 4]), acc);
-          u = silu2(acc);
+          // causal conv, taps w0..w3 on x[t-3..t], scalar FMAs (the odd-offset pairs of the
+          // window would need register moves to form f32x2 operands)
+          float c0 = fmaf(w0, win[j], cb), c1 = fmaf(w0, win[j + 1], cb);
+          c0 = fmaf(w1, win[j + 1], c0);
+          c1 = fmaf(w1, win[j + 2], c1);
+          c0 = fmaf(w2, win[j + 2], c0);
+          c1 = fmaf(w2, win[j + 3], c1);
+          c0 = fmaf(w3, win[j + 3], c0);
+          c1 = fmaf(w3, win[j + 4], c1);
+          u = silu2_tier<PRECISE>(make_float2(c0, c1));
         } else {
           u = make_float2(xv[j], xv[j + 1]);
         }
-        const float2 v = fadd2(make_float2(dv[j], dv[j + 1]), f2(bias));
-        float2 D2 = a.delta_softplus ? softplus2<PRECISE>(v) : v;
+        float2 D2 = delta_log2<PRECISE>(make_float2(dv[j], dv[j + 1]), bias, bias_l2, a.delta_softplus);
         if (!full) {  // steps past the tile end are identity updates: Delta = 0, u = 0
           const bool i0 = tt + j < tl, i1 = tt + j + 1 < tl;
           D2 = make_float2(i0 ? D2.x : 0.f, i1 ? D2.y : 0.f);
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
         du[j + 1] = du2.y;
         if (!CARRY) {
           skip[j / 2] = fmul2(f2(Dd), u);
-          gate[j / 2] = has_z ? silu2(make_float2(zv[j], zv[j + 1])) : f2(1.f);
+          gate[j / 2] = has_z ? silu2_tier<PRECISE>(make_float2(zv[j], zv[j + 1])) : f2(1.f);
         }
       }
       store8(&s_dl[c][tt], dl);
