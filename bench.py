@@ -44,6 +44,39 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _sm_max_mhz() -> float:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f).get("sm_max_mhz", 2032.0))
+    return 2032.0
+
+
+# Issue model of one state update on this part (probes: an ex2 occupies an SMSP's dispatch for
+# two cycles, an FFMA / FMUL lane-op for one cycle per 32 lanes): main pass ex2 + 4 FMA-pipe
+# ops (Delta*A, Delta*u*B, the recurrence, the readout) = 6 cycles per 32 updates per SMSP;
+# carry pass without the readout = 5.
+CYCLES_MAIN, CYCLES_CARRY = 6, 5
+
+
+def alu_roofline(w, seconds: float, chunk_len: int, sms: int):
+    """Scan step time against its issue floor: main + carry updates at the dispatch rate of
+    sms x 4 SMSPs x 32 lanes per clock at the maximum SM clock. The per-token element-wise work
+    (conv, SiLU, softplus, gate) is extra, so frac stays below 1 even for a perfect scan."""
+    if w.kind != "scan":
+        return None
+    per_t = w.batch * w.dim * w.dstate
+    nchunks = (w.seqlen + chunk_len - 1) // chunk_len if w.seqlen > 0 else 1
+    u_main = per_t * w.seqlen
+    u_carry = per_t * min(w.seqlen, (nchunks - 1) * chunk_len) if nchunks > 1 else 0
+    lane_clk = sms * 128 * _sm_max_mhz() * 1e6
+    floor_s = (CYCLES_MAIN * u_main + CYCLES_CARRY * u_carry) / lane_clk
+    return {"bound": "alu", "achieved": u_main / seconds / 1e9, "peak": u_main / floor_s / 1e9,
+            "unit": "Gupdates/s", "frac": floor_s / seconds, "carry_updates": u_carry,
+            "model": f"{CYCLES_MAIN} (main) / {CYCLES_CARRY} (carry) dispatch cycles per 32 updates per SMSP; "
+                     f"{sms} SMs x 4 SMSPs at {_sm_max_mhz():.0f} MHz"}
+
+
 def algorithmic_bytes(w) -> int:
     """Bytes every input read once / every output written once, per step (no per-step state)."""
     es = 2 if w.io == "bf16" else 4
@@ -297,6 +330,7 @@ def run_gpu(args, w):
                                                g["conv_w"], g["conv_b"], y=ybuf[t])
 
         ybuf = torch.empty(w.steps, w.batch, w.dim, dtype=g["x"].dtype, device=dev)
+        cl = 0
         launches_per_step = w.steps
         kernels = ["decode_kernel"]
     else:
@@ -420,6 +454,8 @@ def run_gpu(args, w):
                      "traffic": traffic_from_profiles(w.name, w.kind), "peak_source": peak_kind,
                      "algorithmic_bytes_per_step": bytes_step,
                      "timed": "whole step (" + " + ".join(kernels) + "), CUDA events on the launching stream"},
+        "roofline_alu": alu_roofline(w, ms * 1e-3, cl, torch.cuda.get_device_properties(dev).multi_processor_count)
+        if w.kind == "scan" else None,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
