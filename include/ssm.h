@@ -65,6 +65,9 @@ typedef enum {
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
 
+/* Scan option bits (the flags argument of the scan entry points). */
+#define SSM_SCAN_REVERSE 1u
+
 /* Library version (major * 10000 + minor * 100 + patch). */
 SSM_API int ssm_version(void);
 
@@ -138,13 +141,24 @@ SSM_API size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dsta
  *               or NULL/0 bytes. With chunk_len = 0 the library lowers the chunk count until the
  *               given workspace suffices (one chunk needs none); with an explicit chunk_len a
  *               too-small workspace is SSM_ERR_INVALID_ARG. Its contents need no initialisation.
+ *   flags       0, or SSM_SCAN_REVERSE; any other bit is SSM_ERR_INVALID_ARG.
+ *
+ * SSM_SCAN_REVERSE: the backward scan of a bidirectional layer ("Mamba", ozercemkelahmet.com,
+ * "Bidirectional and multi-directional scans": one scan forward, one backward, results merged
+ * by the caller). It is the same operation applied to the time-reversed stream:
+ *   out = flip(scan(flip(x), flip(delta), flip(B), flip(C), flip(z))),  flip: t -> L-1-t,
+ * so the recurrence runs from t = L-1 down to t = 0 and the conv looks at t .. t+K-1.
+ * h0 is the state before t = L-1, h_last the state after t = 0; conv_init holds the K-1 raw
+ * inputs that follow the sequence, in reversed order (conv_init[j] is x at L+K-2-j), and
+ * conv_state_out returns x at K-2, ..., 0, which is the conv_init of a backward call over the
+ * part of the sequence before this one.
  */
 SSM_API ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
                                   const float* D, const void* z, const float* delta_bias, int delta_softplus,
                                   const float* conv_w, const float* conv_b, int d_conv, const void* conv_init,
                                   const float* h0, void* out, float* h_last, void* conv_state_out, int batch,
                                   int dim, int seqlen, int dstate, ssm_dtype io, int chunk_len, void* workspace,
-                                  size_t workspace_bytes, void* stream);
+                                  size_t workspace_bytes, unsigned int flags, void* stream);
 
 /*
  * One recurrent (decode) step for every sequence b and channel d, state updated in place:
@@ -203,7 +217,7 @@ SSM_API ssm_status ssm_selective_scan_fwd_noalloc(const void* x, const void* del
                                                   const float* conv_b, int d_conv, const void* conv_init,
                                                   const float* h0, void* out, float* h_last, void* conv_state_out,
                                                   int batch, int dim, int seqlen, int dstate, ssm_dtype io,
-                                                  int chunk_len, void* stream);
+                                                  int chunk_len, unsigned int flags, void* stream);
 
 #ifdef __cplusplus
 }

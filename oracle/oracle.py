@@ -85,10 +85,21 @@ def causal_conv1d(x, w, bias=None, window=None, apply_silu: bool = True, nthread
 
 def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True,
                    conv_w=None, conv_b=None, conv_init=None, h0=None, want_conv_state: bool = False,
-                   want_trace: bool = False, nthreads: int = 1) -> Tuple[np.ndarray, ...]:
-    """Returns (out [b, d, L], h_last [b, d, N]) plus conv_state_out and/or h_trace [b, d, L, N] if asked."""
+                   want_trace: bool = False, nthreads: int = 1, reverse: bool = False) -> Tuple[np.ndarray, ...]:
+    """Returns (out [b, d, L], h_last [b, d, N]) plus conv_state_out and/or h_trace [b, d, L, N] if asked.
+
+    reverse: the backward scan of a bidirectional layer ("Mamba", ozercemkelahmet.com, "Bidirectional
+    and multi-directional scans": one scan runs forward, one backward). It is the forward scan of
+    the time-reversed stream, so it is computed as exactly that: the per-token inputs are re-indexed
+    t -> L-1-t, the forward routine runs, and out / h_trace are re-indexed back. h0, conv_init and
+    the returned h_last / conv_state_out belong to the reversed stream (conv_init[j] is the raw
+    input at L+K-2-j; conv_state_out[j] is x at K-2-j).
+    """
     x, delta, A, B, C = _f64(x), _f64(delta), _f64(A), _f64(B), _f64(C)
     D, z, delta_bias, conv_w, conv_b, conv_init, h0 = map(_f64, (D, z, delta_bias, conv_w, conv_b, conv_init, h0))
+    if reverse:
+        flip = lambda a: None if a is None else np.ascontiguousarray(a[..., ::-1])
+        x, delta, B, C, z = map(flip, (x, delta, B, C, z))
     batch, dim, L = x.shape
     N = A.shape[1]
     K = conv_w.shape[1] if conv_w is not None else 0
@@ -100,6 +111,9 @@ def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
                                   _ptr(delta_bias), int(delta_softplus), _ptr(conv_w), _ptr(conv_b), K,
                                   _ptr(conv_init), _ptr(h0), _ptr(out), _ptr(h_last), _ptr(cs), _ptr(tr),
                                   batch, dim, L, N, nthreads)
+    if reverse:
+        out = np.ascontiguousarray(out[..., ::-1])
+        tr = None if tr is None else np.ascontiguousarray(tr[:, :, ::-1, :])
     res = [out, h_last]
     if want_conv_state:
         res.append(cs)

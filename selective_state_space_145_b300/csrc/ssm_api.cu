@@ -121,8 +121,9 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
                                   const float* conv_w, const float* conv_b, int d_conv, const void* conv_init,
                                   const float* h0, void* out, float* h_last, void* conv_state_out, int batch,
                                   int dim, int seqlen, int dstate, ssm_dtype io, int chunk_len, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+                                  size_t workspace_bytes, unsigned int flags, void* stream) {
   if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (flags & ~SSM_SCAN_REVERSE) return SSM_ERR_INVALID_ARG;
   if (!dims_ok(batch, dim, seqlen, dstate)) return SSM_ERR_INVALID_ARG;
   if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
   if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
@@ -178,6 +179,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
           aligned(out, 16) && (!z || aligned(z, 16));
   a.chunk_len = cl;
   a.nchunks = nchunks;
+  a.reverse = (flags & SSM_SCAN_REVERSE) ? 1 : 0;
   ssm::scan_workspace_split(workspace, (long long)batch * dim, nchunks, &a.ws_S, &a.ws_h);
   return ssm::launch_scan(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

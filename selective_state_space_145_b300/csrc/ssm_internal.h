@@ -37,6 +37,7 @@ struct ScanArgs {
   int vec;               // 1: 16-byte vector path is legal for every per-token tensor
   int chunk_len;         // multiple of kChunkQuantum, >= 1 chunk
   int nchunks;
+  int reverse;           // 1: the scan runs from t = L-1 down to t = 0
   float* ws_S;           // [nchunks-1][batch*dim] sum of Delta per chunk
   float* ws_h;           // [nchunks-1][batch*dim][kMaxDstate] chunk end state from zero
 };

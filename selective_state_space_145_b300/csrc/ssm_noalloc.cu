@@ -47,7 +47,7 @@ extern "C" ssm_status ssm_selective_scan_fwd_noalloc(
     const void* x, const void* delta, const float* A, const void* B, const void* C, const float* D, const void* z,
     const float* delta_bias, int delta_softplus, const float* conv_w, const float* conv_b, int d_conv,
     const void* conv_init, const float* h0, void* out, float* h_last, void* conv_state_out, int batch, int dim,
-    int seqlen, int dstate, ssm_dtype io, int chunk_len, void* stream) {
+    int seqlen, int dstate, ssm_dtype io, int chunk_len, unsigned int flags, void* stream) {
   // An explicit chunk length whose carries do not fit the fixed scratch is refused before
   // anything runs; with chunk_len = 0 the scan lowers its chunk count to fit.
   if (chunk_len > 0 && batch > 0 && dim > 0 && seqlen > 0 &&
@@ -62,5 +62,5 @@ extern "C" ssm_status ssm_selective_scan_fwd_noalloc(
   }
   return ssm_selective_scan_fwd(x, delta, A, B, C, D, z, delta_bias, delta_softplus, conv_w, conv_b, d_conv,
                                 conv_init, h0, out, h_last, conv_state_out, batch, dim, seqlen, dstate, io,
-                                chunk_len, scratch, scratch ? (size_t)SSM_NOALLOC_SCRATCH_BYTES : 0, stream);
+                                chunk_len, scratch, scratch ? (size_t)SSM_NOALLOC_SCRATCH_BYTES : 0, flags, stream);
 }

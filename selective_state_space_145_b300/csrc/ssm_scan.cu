@@ -93,7 +93,9 @@ struct Layout {
   static_assert(slot_bytes % 16 == 0, "ring slots stay 16-byte aligned");
 };
 
-template <typename T, bool CONV, bool VEC, bool CARRY>
+// REV: the scan runs backward in time. The kernel walks virtual time tau = 0 .. L-1 and
+// touches real position L-1-tau; every other part of the method is unchanged.
+template <typename T, bool CONV, bool VEC, bool CARRY, bool REV>
 __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   using Lay = Layout<T, CARRY>;
@@ -125,6 +127,8 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   const int d = d0 + c;
   const bool valid = d < dim;
   const long long cc = (long long)b * dim + d;
+  // real position of virtual step tau
+  auto real_t = [&](int tau) { return REV ? L - 1 - tau : tau; };
 
   if (CARRY) {
     // let the main kernel's CTAs be scheduled as soon as every carry CTA is running: its
@@ -170,28 +174,35 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   // whether copy k of this thread lands on a row of the layout (the last one may not)
   auto row_in = [&](int k) { return kRows % kRowStep == 0 || tid / kCPR + k * kRowStep < kRows; };
 
+  // A staged row holds the tile's kTT steps in real order: forward, column p is virtual step
+  // t0 + p; backward, it is virtual step t0 + kTT-1-p, and the row starts at real L - t0 - kTT.
   auto issue_tile_async = [&](int it, int slot) {
     const int t0 = t_begin + it * kTT;
-    const bool tin = col < t_end - t0;
+    const int seg = REV ? L - t0 - kTT : t0;
+    // rows are a whole number of 16-byte chunks long, so a chunk is all in or all out
+    const bool tin = REV ? col >= kTT - (t_end - t0) : col < t_end - t0;
     T* dst = &ring[slot][tid / kCPR][col];
 #pragma unroll
     for (int k = 0; k < kCopies; ++k) {
       const bool ok = row_ok[k] && tin;
       if (row_in(k))
-        cp_async16(dst + k * kRowStep * RS, ok ? (const void*)(src_row[k] + t0) : (const void*)gx, ok ? 16u : 0u);
+        cp_async16(dst + k * kRowStep * RS, ok ? (const void*)(src_row[k] + seg) : (const void*)gx, ok ? 16u : 0u);
     }
   };
 
   auto load_tile_sync = [&](int it, int slot) {
     const int t0 = t_begin + it * kTT;
     const int tl = min(kTT, t_end - t0);
+    const int seg = REV ? L - t0 - kTT : t0;
 #pragma unroll
     for (int k = 0; k < kCopies; ++k) {
       if (!row_in(k)) continue;
       T* dst = &ring[slot][tid / kCPR + k * kRowStep][col];
 #pragma unroll
-      for (int e = 0; e < kEPC; ++e)
-        dst[e] = (row_ok[k] && col + e < tl) ? src_row[k][t0 + e] : from_f32<T>(0.f);
+      for (int e = 0; e < kEPC; ++e) {
+        const bool in = REV ? col + e >= kTT - tl : col + e < tl;
+        dst[e] = (row_ok[k] && in) ? src_row[k][seg + e] : from_f32<T>(0.f);
+      }
     }
   };
 
@@ -233,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           if (K >= 4) hv[0] = to_f32(ci[K - 4]);
         }
       } else {
-        hv[0] = to_f32(gx[cc * L + (t_begin - 3)]);
-        hv[1] = to_f32(gx[cc * L + (t_begin - 2)]);
-        hv[2] = to_f32(gx[cc * L + (t_begin - 1)]);
+        hv[0] = to_f32(gx[cc * L + real_t(t_begin - 3)]);
+        hv[1] = to_f32(gx[cc * L + real_t(t_begin - 2)]);
+        hv[2] = to_f32(gx[cc * L + real_t(t_begin - 1)]);
       }
     }
     s_halo[0][c][0] = hv[0];
@@ -325,7 +336,15 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       float (*dst)[kMaxDstate] = tid >= 32 ? s_C : s_B;
       float v[4][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) load4(&src[n0 + i][s0], v[i]);
+      for (int i = 0; i < 4; ++i) {
+        if (REV) {  // virtual steps s0 .. s0+3 are columns kTT-1-s0 down to kTT-4-s0
+          float r[4];
+          load4(&src[n0 + i][kTT - 4 - s0], r);
+          v[i][0] = r[3]; v[i][1] = r[2]; v[i][2] = r[1]; v[i][3] = r[0];
+        } else {
+          load4(&src[n0 + i][s0], v[i]);
+        }
+      }
       // B carries the ln 2 that turns Delta' (log2 units) back into Delta in Delta u B
       const float sc = tid >= 32 ? 1.0f : kLn2;
 #pragma unroll
@@ -339,9 +358,20 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
     float2 skip[kSeg / 2], gate[kSeg / 2];
     {
       float xv[kSeg], dv[kSeg], zv[kSeg];
-      load8(&raw[c][tt], xv);
-      load8(&raw[kDT + c][tt], dv);
-      if (has_z) load8(&raw[2 * kDT + c][tt], zv);
+      // virtual steps tt .. tt+7 of a row (backward: columns kTT-1-tt down to kTT-8-tt)
+      auto load_seg = [&](const T* row, float (&v)[kSeg]) {
+        if (REV) {
+          float r[kSeg];
+          load8(row + (kTT - kSeg - tt), r);
+#pragma unroll
+          for (int j = 0; j < kSeg; ++j) v[j] = r[kSeg - 1 - j];
+        } else {
+          load8(row + tt, v);
+        }
+      };
+      load_seg(raw[c], xv);
+      load_seg(raw[kDT + c], dv);
+      if (has_z) load_seg(raw[2 * kDT + c], zv);
       float p0 = 0.f, p1 = 0.f, p2 = 0.f;  // x[tt-3], x[tt-2], x[tt-1]
       if (CONV) {
         if (g == 0) {
@@ -350,10 +380,17 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           p2 = s_halo[hb][c][2];
         } else {
           float pv[4];
-          load4(&raw[c][tt - 4], pv);
-          p0 = pv[1];
-          p1 = pv[2];
-          p2 = pv[3];
+          if (REV) {  // virtual tt-1, tt-2, tt-3 are columns kTT-tt, +1, +2
+            load4(&raw[c][kTT - tt], pv);
+            p0 = pv[2];
+            p1 = pv[1];
+            p2 = pv[0];
+          } else {
+            load4(&raw[c][tt - 4], pv);
+            p0 = pv[1];
+            p1 = pv[2];
+            p2 = pv[3];
+          }
         }
         if (g == kTPC - 1) {
           s_halo[hb ^ 1][c][0] = xv[kSeg - 3];
@@ -456,16 +493,34 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           o[j] = y.x;
           o[j + 1] = y.y;
         }
-        T* dst = static_cast<T*>(a.out) + cc * L + t0 + tt;
-        if (VEC && tt + kSeg <= tl) {
-          store8(dst, o);
-        } else if (VEC && tt + 4 <= tl) {  // fp32 rows can end on a 4-step boundary
-          const float o4[4] = {o[0], o[1], o[2], o[3]};
-          store4(dst, o4);
-        } else {
+        T* orow = static_cast<T*>(a.out) + cc * L;
+        if (REV) {
+          // virtual tt+j is real L-1-(t0+tt+j): the segment is stored reversed
+          if (VEC && tt + kSeg <= tl) {
+            float r[kSeg];
 #pragma unroll
-          for (int j = 0; j < kSeg; ++j)
-            if (tt + j < tl) dst[j] = from_f32<T>(o[j]);
+            for (int j = 0; j < kSeg; ++j) r[j] = o[kSeg - 1 - j];
+            store8(orow + (L - t0 - tt - kSeg), r);
+          } else if (VEC && tt + 4 <= tl) {  // fp32 rows can end on a 4-step boundary
+            const float r4[4] = {o[3], o[2], o[1], o[0]};
+            store4(orow + (L - t0 - tt - 4), r4);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kSeg; ++j)
+              if (tt + j < tl) orow[L - 1 - (t0 + tt + j)] = from_f32<T>(o[j]);
+          }
+        } else {
+          T* dst = orow + t0 + tt;
+          if (VEC && tt + kSeg <= tl) {
+            store8(dst, o);
+          } else if (VEC && tt + 4 <= tl) {  // fp32 rows can end on a 4-step boundary
+            const float o4[4] = {o[0], o[1], o[2], o[3]};
+            store4(dst, o4);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kSeg; ++j)
+              if (tt + j < tl) dst[j] = from_f32<T>(o[j]);
+          }
         }
       }
     }
@@ -492,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
     for (int j = g; j < K1; j += kTPC) {
       const int s = L - K1 + j;
       T v;
-      if (s >= 0) v = gx[cc * L + s];
+      if (s >= 0) v = gx[cc * L + real_t(s)];
       else v = a.conv_init ? static_cast<const T*>(a.conv_init)[cc * K1 + (K1 + s)] : from_f32<T>(0.f);
       static_cast<T*>(a.conv_state_out)[cc * K1 + j] = v;
     }
@@ -500,14 +555,14 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
 }
 
 // Opts the kernel into its dynamic shared memory once per device.
-template <typename T, bool CONV, bool VEC, bool CARRY>
+template <typename T, bool CONV, bool VEC, bool CARRY, bool REV>
 cudaError_t prepare() {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(scan_kernel<T, CONV, VEC, CARRY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(scan_kernel<T, CONV, VEC, CARRY, REV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Layout<T, CARRY>::bytes);
   if (err == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
   return err;
@@ -515,9 +570,9 @@ cudaError_t prepare() {
 
 // pdl: launch as the programmatic dependent of the kernel before it in the stream (which
 // must be this problem's carry kernel).
-template <typename T, bool CONV, bool VEC, bool CARRY>
+template <typename T, bool CONV, bool VEC, bool CARRY, bool REV>
 cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, bool pdl, cudaStream_t stream) {
-  cudaError_t err = prepare<T, CONV, VEC, CARRY>();
+  cudaError_t err = prepare<T, CONV, VEC, CARRY, REV>();
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.dim + kDT - 1) / kDT, a.batch, nchunks_grid);
@@ -529,14 +584,14 @@ cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, bool pdl, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, scan_kernel<T, CONV, VEC, CARRY>, a);
+  return cudaLaunchKernelEx(&cfg, scan_kernel<T, CONV, VEC, CARRY, REV>, a);
 }
 
 template <typename T>
 int resident_main_ctas() {
   int n = 0;
-  if (prepare<T, true, true, false>() != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_kernel<T, true, true, false>, kThreads,
+  if (prepare<T, true, true, false, false>() != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_kernel<T, true, true, false, false>, kThreads,
                                                     Layout<T, false>::bytes) != cudaSuccess ||
       n <= 0) {
     cudaGetLastError();
@@ -545,20 +600,25 @@ int resident_main_ctas() {
   return n;
 }
 
-template <typename T, bool CONV, bool VEC>
+template <typename T, bool CONV, bool VEC, bool REV>
 cudaError_t launch_pair(const ScanArgs& a, cudaStream_t stream) {
   if (a.nchunks > 1) {
-    cudaError_t err = launch_one<T, CONV, VEC, true>(a, a.nchunks - 1, false, stream);
+    cudaError_t err = launch_one<T, CONV, VEC, true, REV>(a, a.nchunks - 1, false, stream);
     if (err != cudaSuccess) return err;
   }
-  return launch_one<T, CONV, VEC, false>(a, a.nchunks, a.nchunks > 1, stream);
+  return launch_one<T, CONV, VEC, false, REV>(a, a.nchunks, a.nchunks > 1, stream);
+}
+
+template <typename T, bool REV>
+cudaError_t dispatch_dir(const ScanArgs& a, cudaStream_t s) {
+  const bool conv = a.conv_w != nullptr;
+  if (conv) return a.vec ? launch_pair<T, true, true, REV>(a, s) : launch_pair<T, true, false, REV>(a, s);
+  return a.vec ? launch_pair<T, false, true, REV>(a, s) : launch_pair<T, false, false, REV>(a, s);
 }
 
 template <typename T>
 cudaError_t dispatch(const ScanArgs& a, cudaStream_t s) {
-  const bool conv = a.conv_w != nullptr;
-  if (conv) return a.vec ? launch_pair<T, true, true>(a, s) : launch_pair<T, true, false>(a, s);
-  return a.vec ? launch_pair<T, false, true>(a, s) : launch_pair<T, false, false>(a, s);
+  return a.reverse ? dispatch_dir<T, true>(a, s) : dispatch_dir<T, false>(a, s);
 }
 
 }  // namespace

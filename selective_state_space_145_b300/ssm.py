@@ -33,6 +33,9 @@ EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_sca
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
+# Scan option bits (include/ssm.h).
+SCAN_REVERSE = 1
+
 
 class SSMError(RuntimeError):
     """A libssm call returned a non-OK status."""
@@ -50,7 +53,7 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
                                "(python -m selective_state_space_145_b300.build)")
         L = ctypes.CDLL(LIB_PATH)
-        vp, fp, i, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        vp, fp, i, sz, u = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
         L.ssm_version.restype = i
         L.ssm_version.argtypes = []
         L.ssm_status_string.restype = ctypes.c_char_p
@@ -63,10 +66,10 @@ def lib() -> ctypes.CDLL:
         L.ssm_scan_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.ssm_selective_scan_fwd.restype = i
         L.ssm_selective_scan_fwd.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, vp, fp, vp]
-                                             + [i] * 6 + [vp, sz, vp])
+                                             + [i] * 6 + [vp, sz, u, vp])
         L.ssm_selective_scan_fwd_noalloc.restype = i
         L.ssm_selective_scan_fwd_noalloc.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, vp, fp, vp]
-                                                     + [i] * 6 + [vp])
+                                                     + [i] * 6 + [u, vp])
         L.ssm_selective_state_update.restype = i
         L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
                                                  i, i, i, i, vp]
@@ -154,12 +157,14 @@ def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor
                            d_conv: Optional[int] = None, chunk_len: int = 0,
                            workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                            h_last: Optional[torch.Tensor] = None,
-                           conv_state_out: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, ...]:
+                           conv_state_out: Optional[torch.Tensor] = None,
+                           reverse: bool = False) -> Tuple[torch.Tensor, ...]:
     """Selective scan forward. Returns (out, h_last) [+ conv_state_out when asked].
 
     x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (all float32 or bfloat16, one dtype);
     A [dim, dstate], D / delta_bias / conv_b [dim], conv_w [dim, K], h0 [batch, dim, dstate]: float32.
     The workspace (if the chosen chunking needs one) is allocated here unless passed in.
+    reverse: the backward scan (SSM_SCAN_REVERSE), the recurrence runs from t = L-1 to 0.
     """
     batch, dim, L = x.shape
     N = A.shape[1]
@@ -200,7 +205,8 @@ def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor
     st = lib().ssm_selective_scan_fwd(
         _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
         _ptr(conv_w), _ptr(conv_b), K, _ptr(conv_init), _ptr(h0), _ptr(out), _ptr(h_last), _ptr(conv_state_out),
-        batch, dim, L, N, io_code, int(chunk_len), _ptr(workspace), ws_bytes, _stream(dev))
+        batch, dim, L, N, io_code, int(chunk_len), _ptr(workspace), ws_bytes,
+        SCAN_REVERSE if reverse else 0, _stream(dev))
     _check("ssm_selective_scan_fwd", st)
     res = (out, h_last)
     if return_conv_state:

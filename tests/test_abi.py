@@ -60,12 +60,12 @@ FAKE = 0x10000
 def _scan(L, **kw):
     a = dict(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, delta_bias=None, sp=1, conv_w=None,
              conv_b=None, d_conv=0, conv_init=None, h0=None, out=FAKE, h_last=None, cs_out=None, batch=1, dim=4,
-             seqlen=8, dstate=16, io=0, chunk_len=0, ws=None, ws_bytes=0)
+             seqlen=8, dstate=16, io=0, chunk_len=0, ws=None, ws_bytes=0, flags=0)
     a.update(kw)
     return L.ssm_selective_scan_fwd(a["x"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["delta_bias"],
                                     a["sp"], a["conv_w"], a["conv_b"], a["d_conv"], a["conv_init"], a["h0"],
                                     a["out"], a["h_last"], a["cs_out"], a["batch"], a["dim"], a["seqlen"],
-                                    a["dstate"], a["io"], a["chunk_len"], a["ws"], a["ws_bytes"], None)
+                                    a["dstate"], a["io"], a["chunk_len"], a["ws"], a["ws_bytes"], a["flags"], None)
 
 
 def test_scan_argument_checks(L):
@@ -81,6 +81,8 @@ def test_scan_argument_checks(L):
     assert _scan(L, conv_b=FAKE) == 1              # conv bias without conv weight
     assert _scan(L, x=FAKE + 2) == 2               # misaligned fp32 pointer
     assert _scan(L, chunk_len=-5) == 1
+    assert _scan(L, flags=2) == 1                  # unknown option bit
+    assert _scan(L, flags=1, x=None) == 1          # reverse: same checks
     assert _scan(L, seqlen=1 << 20, chunk_len=64, batch=1, dim=4) == 1   # chunked: workspace missing
     # empty work: no launch, OK
     assert _scan(L, batch=0) == 0

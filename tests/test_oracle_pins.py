@@ -201,6 +201,65 @@ def test_brute_force_tiny():
     np.testing.assert_allclose(hL, refL, rtol=1e-13, atol=1e-13)
 
 
+def _brute_force_backward(x, delta, A, B, C, D, z, bias, w, cb, ahead, h0):
+    """The backward scan written directly, t = L-1 down to 0: the conv reads x at t .. t+K-1
+    (w[K-1] on x_t, w[0] on x_{t+K-1}; positions past the end come from `ahead`, ahead[j]
+    being the input at L+K-2-j), and h_t = exp(Delta_t A) h_{t+1} + Delta_t B_t u_t from
+    h_L = h0. Scalars only, no re-indexing of arrays."""
+    b, d, L = x.shape
+    N = A.shape[1]
+    K = w.shape[1]
+    out = np.zeros((b, d, L))
+    hL = np.zeros((b, d, N))
+    for bi in range(b):
+        for di in range(d):
+            def xs(s):
+                return x[bi, di, s] if s < L else ahead[bi, di, L + K - 2 - s]
+            h = [h0[bi, di, n] for n in range(N)]
+            for t in range(L - 1, -1, -1):
+                acc = sum(w[di, k] * xs(t + K - 1 - k) for k in range(K)) + cb[di]
+                u = acc / (1.0 + math.exp(-acc))
+                Dl = math.log1p(math.exp(delta[bi, di, t] + bias[di]))
+                y = 0.0
+                for n in range(N):
+                    h[n] = math.exp(Dl * A[di, n]) * h[n] + Dl * B[bi, n, t] * u
+                    y += C[bi, n, t] * h[n]
+                y += D[di] * u
+                out[bi, di, t] = y * z[bi, di, t] / (1.0 + math.exp(-z[bi, di, t]))
+            hL[bi, di] = h
+    return out, hL
+
+
+def test_backward_scan_brute_force():
+    b, d, L, N, K = 2, 3, 9, 3, 4
+    x, delta, z = _rand(b, d, L), 0.8 * _rand(b, d, L), _rand(b, d, L)
+    A, B, C, D, bias = _neg_A(d, N), _rand(b, N, L), _rand(b, N, L), _rand(d), _rand(d) - 1
+    w, cb, ahead, h0 = RNG.uniform(-0.5, 0.5, (d, K)), _rand(d), _rand(b, d, K - 1), _rand(b, d, N)
+    out, hL, cs = oracle.selective_scan(x, delta, A, B, C, D, z, bias, True, w, cb, conv_init=ahead, h0=h0,
+                                        want_conv_state=True, reverse=True)
+    ref, refL = _brute_force_backward(x, delta, A, B, C, D, z, bias, w, cb, ahead, h0)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(hL, refL, rtol=1e-13, atol=1e-13)
+    np.testing.assert_array_equal(cs, x[:, :, K - 2::-1])   # x at K-2, ..., 0
+
+
+def test_backward_scan_split_equals_whole():
+    """The backward scan over [0, L) equals the backward scan over [L1, L) followed by the one
+    over [0, L1) started from its end state and raw-input window."""
+    p = _problem()
+    L = p["x"].shape[-1]
+    full, hfull, csfull = oracle.selective_scan(**p, want_conv_state=True, reverse=True)
+    for L1 in (1, 5, 13, L - 1):
+        late = {k: (v[..., L1:] if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+        out2, h2, cs2 = oracle.selective_scan(**late, want_conv_state=True, reverse=True)
+        early = {k: (v[..., :L1] if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+        early["h0"], early["conv_init"] = h2, cs2
+        out1, h1, cs1 = oracle.selective_scan(**early, want_conv_state=True, reverse=True)
+        np.testing.assert_array_equal(np.concatenate([out1, out2], axis=-1), full)
+        np.testing.assert_array_equal(h1, hfull)
+        np.testing.assert_array_equal(cs1, csfull)
+
+
 # ---------------------------------------------------------------- invariants
 
 def _problem(b=2, d=3, L=21, N=4, K=4):

@@ -118,6 +118,68 @@ def test_empty_and_zero_length(cuda_device):
     assert out.shape == (0, 8, 16)
 
 
+# ---------------------------------------------------------------- backward scan (SSM_SCAN_REVERSE)
+
+REVERSE = [
+    # batch, dim, L, N, K, io, with_h0, with_init, chunk_len
+    (2, 37, 200, 16, 4, "f32", True, True, 0),       # ragged last tile, vector path, partial channel tile
+    (1, 40, 100, 16, 4, "f32", True, True, 0),       # fp32 rows ending on a 4-step boundary
+    (2, 40, 264, 16, 4, "bf16", True, True, 128),    # 3 chunks, ragged last chunk
+    (2, 33, 101, 7, 3, "f32", True, True, 64),       # element-wise path (row not a whole 16 bytes), chunks
+    (1, 70, 130, 16, 0, "bf16", True, False, 0),     # element-wise path, no conv
+    (2, 64, 196, 16, 4, "f32", False, False, 64),    # chunks of 64, last chunk 4 steps
+    (1, 8, 3, 16, 4, "bf16", False, True, 0),        # L < K-1: the window comes from conv_init
+]
+
+
+@pytest.mark.parametrize("case", REVERSE, ids=lambda c: "b{}_d{}_l{}_n{}_k{}_{}_h0{}_ci{}_cl{}".format(*c))
+def test_reverse_small_whole(cuda_device, case):
+    batch, dim, L, N, K, io, h0, ci, cl = case
+    p = inputs.scan_inputs(batch, dim, L, N, K, io, seed=3000 + dim + L, with_h0=h0, with_conv_init=ci,
+                           random_A=True)
+    g = to_dev(p, cuda_device)
+    if K > 0:
+        out, hL, cs = gpu_scan(g, chunk_len=cl, return_conv_state=True, d_conv=K, reverse=True)
+        ref, refL, refcs = oracle_scan(p, want_conv_state=True, reverse=True)
+    else:
+        out, hL = gpu_scan(g, chunk_len=cl, reverse=True)
+        ref, refL = oracle_scan(p, reverse=True)
+    assert_close(out, ref, io, "out")
+    assert_close(hL, refL, io, "h_last")
+    if K > 1:
+        np.testing.assert_array_equal(cs.float().cpu().numpy(), refcs)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_reverse_chunked_equals_unchunked(cuda_device, io):
+    p = inputs.scan_inputs(2, 48, 700, 16, 4, io, seed=78, with_h0=True, with_conv_init=True, salient_frac=0.02)
+    g = to_dev(p, cuda_device)
+    ref, refL = oracle_scan(p, reverse=True)
+    one, _ = gpu_scan(g, chunk_len=1 << 20, reverse=True)
+    for cl in (64, 192, 320):
+        out, hL = gpu_scan(g, chunk_len=cl, reverse=True)
+        assert_close(out, ref, io, f"out chunk_len={cl}")
+        assert_close(hL, refL, io, f"h_last chunk_len={cl}")
+        assert_close(out, one.float().cpu().double().numpy(), io, f"chunked vs whole cl={cl}")
+
+
+def test_reverse_split_on_gpu(cuda_device):
+    """Two backward GPU calls, the later part first, passing (h_last, conv window), equal one."""
+    p = inputs.scan_inputs(2, 50, 257, 16, 4, "f32", seed=10, with_h0=True, with_conv_init=True)
+    g = to_dev(p, cuda_device)
+    full, hfull, csfull = gpu_scan(g, return_conv_state=True, reverse=True)
+    L1 = 100
+    late = {k: (v[..., L1:].contiguous() if k in ("x", "delta", "z", "B", "C") else v) for k, v in g.items()}
+    o2, h2, cs2 = gpu_scan(late, return_conv_state=True, reverse=True)
+    early = {k: (v[..., :L1].contiguous() if k in ("x", "delta", "z", "B", "C") else v) for k, v in g.items()}
+    early["h0"], early["conv_init"] = h2, cs2
+    o1, h1, cs1 = gpu_scan(early, return_conv_state=True, reverse=True)
+    ref, refL = oracle_scan(p, reverse=True)
+    assert_close(torch.cat([o1, o2], dim=-1), ref, "f32", "two backward calls vs oracle")
+    assert_close(h1, refL, "f32", "h_last after two backward calls")
+    assert torch.equal(cs1, csfull)
+
+
 def test_deterministic(cuda_device):
     p = inputs.scan_inputs(2, 64, 512, 16, 4, "bf16", seed=21, with_h0=True)
     g = to_dev(p, cuda_device)

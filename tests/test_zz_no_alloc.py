@@ -32,7 +32,7 @@ def _call_noalloc(g, out, h_last, chunk_len):
     return L.ssm_selective_scan_fwd_noalloc(
         p(g["x"]), p(g["delta"]), p(g["A"]), p(g["B"]), p(g["C"]), p(g["D"]), p(g["z"]), p(g["delta_bias"]), 1,
         p(g.get("conv_w")), p(g.get("conv_b")), K, p(g.get("conv_init")), p(g.get("h0")), p(out), p(h_last), None,
-        batch, dim, seqlen, N, _io_code(g["x"]), chunk_len, stream)
+        batch, dim, seqlen, N, _io_code(g["x"]), chunk_len, 0, stream)
 
 
 @pytest.mark.parametrize("io,chunk_len", [("f32", 64), ("bf16", 128), ("bf16", 0)])
