@@ -209,7 +209,8 @@ def barrier(world: int):
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
-def oracle_sample_rate(w, target_s: float = 10.0, max_channels: int = 1024, reverse: bool = False):
+def oracle_sample_rate(w, target_s: float = 10.0, max_channels: int = 1024, reverse: bool = False,
+                       zoh: bool = False):
     """Time the fp64 oracle, as it stands, on a bounded sample of the workload's channels.
 
     Returns (updates/s, cores, sample description)."""
@@ -228,7 +229,7 @@ def oracle_sample_rate(w, target_s: float = 10.0, max_channels: int = 1024, reve
         while time.perf_counter() - t0 < target_s:
             _, state, win = oracle.state_update(state, win, q["x"][0], q["delta"][0], q["A"], q["B"][0], q["C"][0],
                                                 q["D"], q["z"][0], q["delta_bias"], True, q["conv_w"], q["conv_b"],
-                                                nthreads=cores)
+                                                nthreads=cores, zoh=zoh)
             ups += state.size
             reps += 1
         dt = time.perf_counter() - t0
@@ -244,7 +245,7 @@ def oracle_sample_rate(w, target_s: float = 10.0, max_channels: int = 1024, reve
     t0 = time.perf_counter()
     oracle.selective_scan(p["x"][..., :probe_len], p["delta"][..., :probe_len], p["A"], p["B"][..., :probe_len],
                           p["C"][..., :probe_len], p["D"], p["z"][..., :probe_len], p["delta_bias"], True,
-                          p["conv_w"], p["conv_b"], nthreads=cores, reverse=reverse)
+                          p["conv_w"], p["conv_b"], nthreads=cores, reverse=reverse, zoh=zoh)
     per_step = (time.perf_counter() - t0) / probe_len
     use_len = int(max(probe_len, min(L, target_s / max(per_step, 1e-9))))
     sub = {k: (v[..., :use_len] if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
@@ -253,7 +254,7 @@ def oracle_sample_rate(w, target_s: float = 10.0, max_channels: int = 1024, reve
     while True:
         oracle.selective_scan(sub["x"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"], sub["z"],
                               sub["delta_bias"], True, sub["conv_w"], sub["conv_b"], nthreads=cores,
-                              reverse=reverse)
+                              reverse=reverse, zoh=zoh)
         reps += 1
         if time.perf_counter() - t0 >= target_s or reps >= 10000:
             break
@@ -271,25 +272,27 @@ def run_reference(args, w):
     desc, cores = "", 1
     budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
     for i in range(args.warmup + args.steps):
-        r, cores, desc = oracle_sample_rate(w, target_s=budget, reverse=args.reverse)
+        r, cores, desc = oracle_sample_rate(w, target_s=budget, reverse=args.reverse, zoh=args.zoh)
         if i >= args.warmup:
             rates.append(r)
     value = statistics.mean(rates)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, args.reverse),
+            "config": config_of(w, args.reverse, args.zoh),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def config_of(w, reverse: bool = False):
+def config_of(w, reverse: bool = False, zoh: bool = False):
     c = {"workload": w.name, "kind": w.kind, "io": w.io, "batch": w.batch, "d_inner": w.dim, "seqlen": w.seqlen,
          "d_state": w.dstate, "d_conv": w.d_conv, "l2": "flushed before every timed step (256 MiB write)"}
     if reverse:
         c["direction"] = "backward (SSM_SCAN_REVERSE)"
+    if zoh:
+        c["discretisation"] = "zero-order hold (SSM_SCAN_ZOH)"
     if w.d_model:
         c.update({"d_model": w.d_model, "expand": w.expand})
     if w.kind == "decode":
@@ -330,7 +333,7 @@ def run_gpu(args, w):
             for t in range(w.steps):
                 ssm.ssm_selective_state_update(g["state"], g["conv_state"], g["x"][t], g["delta"][t], g["A"],
                                                g["B"][t], g["C"][t], g["D"], g["z"][t], g["delta_bias"], True,
-                                               g["conv_w"], g["conv_b"], y=ybuf[t])
+                                               g["conv_w"], g["conv_b"], y=ybuf[t], zoh=args.zoh)
 
         ybuf = torch.empty(w.steps, w.batch, w.dim, dtype=g["x"].dtype, device=dev)
         cl = 0
@@ -348,7 +351,8 @@ def run_gpu(args, w):
         def step():
             ssm.ssm_selective_scan_fwd(g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"],
                                        True, g["conv_w"], g["conv_b"], None, None, workspace=ws, out=out,
-                                       h_last=h_last, chunk_len=args.chunk_len, reverse=args.reverse)
+                                       h_last=h_last, chunk_len=args.chunk_len, reverse=args.reverse,
+                                       zoh=args.zoh)
 
         launches_per_step = 2 if nchunks > 1 else 1
         kernels = ["scan_kernel<carry>", "scan_kernel<main>"] if nchunks > 1 else ["scan_kernel<main>"]
@@ -399,7 +403,7 @@ def run_gpu(args, w):
                     ssm.ssm_selective_state_update(dev_in["state"], dev_in["conv_state"], dev_in["x"][t],
                                                    dev_in["delta"][t], dev_in["A"], dev_in["B"][t], dev_in["C"][t],
                                                    dev_in["D"], dev_in["z"][t], dev_in["delta_bias"], True,
-                                                   dev_in["conv_w"], dev_in["conv_b"], y=ybuf[t])
+                                                   dev_in["conv_w"], dev_in["conv_b"], y=ybuf[t], zoh=args.zoh)
                 res_host.copy_(ybuf, non_blocking=True)
                 st_host.copy_(dev_in["state"], non_blocking=True)
 
@@ -415,7 +419,7 @@ def run_gpu(args, w):
                 ssm.ssm_selective_scan_fwd(dev_in["x"], dev_in["delta"], dev_in["A"], dev_in["B"], dev_in["C"],
                                            dev_in["D"], dev_in["z"], dev_in["delta_bias"], True, dev_in["conv_w"],
                                            dev_in["conv_b"], None, None, workspace=ws, out=out, h_last=h_last,
-                                           chunk_len=args.chunk_len, reverse=args.reverse)
+                                           chunk_len=args.chunk_len, reverse=args.reverse, zoh=args.zoh)
                 out_host.copy_(out, non_blocking=True)
                 hl_host.copy_(h_last, non_blocking=True)
 
@@ -444,14 +448,14 @@ def run_gpu(args, w):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        r, cores, desc = oracle_sample_rate(w, target_s=args.cpu_seconds, reverse=args.reverse)
+        r, cores, desc = oracle_sample_rate(w, target_s=args.cpu_seconds, reverse=args.reverse, zoh=args.zoh)
         cpu = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": config_of(w, args.reverse),
+        "config": config_of(w, args.reverse, args.zoh),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profiles(w.name, w.kind), "peak_source": peak_kind,
@@ -488,6 +492,7 @@ def main(argv=None):
     ap.add_argument("--chunk-len", type=int, default=0,
                     help="scan chunk length (0 = the library's default policy)")
     ap.add_argument("--reverse", action="store_true", help="time the backward scan (SSM_SCAN_REVERSE)")
+    ap.add_argument("--zoh", action="store_true", help="zero-order-hold discretisation (SSM_SCAN_ZOH)")
     args = ap.parse_args(argv)
     import dataclasses
 

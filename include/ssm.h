@@ -65,8 +65,9 @@ typedef enum {
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
 
-/* Scan option bits (the flags argument of the scan entry points). */
+/* Option bits of the flags argument. SSM_SCAN_REVERSE: the scan entry points only. */
 #define SSM_SCAN_REVERSE 1u
+#define SSM_SCAN_ZOH 2u
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 SSM_API int ssm_version(void);
@@ -141,7 +142,14 @@ SSM_API size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dsta
  *               or NULL/0 bytes. With chunk_len = 0 the library lowers the chunk count until the
  *               given workspace suffices (one chunk needs none); with an explicit chunk_len a
  *               too-small workspace is SSM_ERR_INVALID_ARG. Its contents need no initialisation.
- *   flags       0, or SSM_SCAN_REVERSE; any other bit is SSM_ERR_INVALID_ARG.
+ *   flags       0, or SSM_SCAN_REVERSE and / or SSM_SCAN_ZOH; any other bit is SSM_ERR_INVALID_ARG.
+ *
+ * SSM_SCAN_ZOH: zero-order-hold discretisation of the input term,
+ *   h_t[n] = exp(Delta_t A[d,n]) h_{t-1}[n] + expm1(Delta_t A[d,n]) / A[d,n] * B[b,n,t] u_t
+ * ("Mamba", ai360xpert.com, "Show Me the Code": B_bar = (1 - A_bar)/(-A) B; "Mamba",
+ * inferensys.com: the continuous system is discretized by a zero-order hold), instead of the
+ * default Euler term Delta_t B u_t. Where A[d,n] = 0 the factor is its limit Delta_t; near it
+ * the factor is taken from its series, so it stays accurate as Delta A -> 0.
  *
  * SSM_SCAN_REVERSE: the backward scan of a bidirectional layer ("Mamba", ozercemkelahmet.com,
  * "Bidirectional and multi-directional scans": one scan forward, one backward, results merged
@@ -167,6 +175,7 @@ SSM_API ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, cons
  *              (u = x[b,d] when conv_w == NULL; conv_state is then unused and may be NULL)
  *   Delta    = softplus(delta[b,d] + delta_bias[d])
  *   state[n] = exp(Delta A[d,n]) state[n] + Delta B[b,n] u
+ *              (with SSM_SCAN_ZOH: + expm1(Delta A[d,n]) / A[d,n] B[b,n] u, as for the scan)
  *   y[b,d]   = (sum_n C[b,n] state[n] + D[d] u) * silu(z[b,d])
  * ("Mamba" ozercemkelahmet.com, step 5 and deployment notes: a fixed-size state per sequence
  *  updated once per token; "Mamba (Selective State-Space Model)", constant inference state.)
@@ -177,12 +186,13 @@ SSM_API ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, cons
  *   A           [dim, dstate] float32;   B, C [batch, dstate] io
  *   D, delta_bias, conv_w, conv_b as for the scan
  *   y           [batch, dim] io output
+ *   flags       0 or SSM_SCAN_ZOH; any other bit is SSM_ERR_INVALID_ARG
  */
 SSM_API ssm_status ssm_selective_state_update(float* state, void* conv_state, const void* x, const void* delta,
                                       const float* A, const void* B, const void* C, const float* D, const void* z,
                                       const float* delta_bias, int delta_softplus, const float* conv_w,
                                       const float* conv_b, int d_conv, void* y, int batch, int dim, int dstate,
-                                      ssm_dtype io, void* stream);
+                                      ssm_dtype io, unsigned int flags, void* stream);
 
 /*
  * Size in bytes of the fixed device array that ssm_selective_scan_fwd_noalloc uses as its

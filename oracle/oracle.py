@@ -30,11 +30,11 @@ def _load():
         lib.oracle_silu.argtypes = [_P, _P, L]
         lib.oracle_causal_conv1d.argtypes = [_P, _P, _P, _P, _P, L, L, L, I, I, I]
         lib.oracle_selective_scan.argtypes = ([_P] * 8 + [I] + [_P, _P, I] + [_P, _P, _P, _P, _P, _P]
-                                              + [L, L, L, L, I])
+                                              + [L, L, L, L, I, I])
         lib.oracle_compose.argtypes = [_P, _P, _P, _P, _P, _P, L]
         lib.oracle_chunk_aggregates.argtypes = ([_P] * 5 + [I] + [_P, _P, I, _P, L, _P, _P]
-                                                + [L, L, L, L, I])
-        lib.oracle_state_update.argtypes = ([_P, _P] + [_P] * 8 + [I] + [_P, _P, I, _P] + [L, L, L, I])
+                                                + [L, L, L, L, I, I])
+        lib.oracle_state_update.argtypes = ([_P, _P] + [_P] * 8 + [I] + [_P, _P, I, _P] + [L, L, L, I, I])
         for f in ("oracle_softplus", "oracle_silu", "oracle_causal_conv1d", "oracle_selective_scan",
                   "oracle_compose", "oracle_chunk_aggregates", "oracle_state_update"):
             getattr(lib, f).restype = None
@@ -85,7 +85,8 @@ def causal_conv1d(x, w, bias=None, window=None, apply_silu: bool = True, nthread
 
 def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True,
                    conv_w=None, conv_b=None, conv_init=None, h0=None, want_conv_state: bool = False,
-                   want_trace: bool = False, nthreads: int = 1, reverse: bool = False) -> Tuple[np.ndarray, ...]:
+                   want_trace: bool = False, nthreads: int = 1, reverse: bool = False,
+                   zoh: bool = False) -> Tuple[np.ndarray, ...]:
     """Returns (out [b, d, L], h_last [b, d, N]) plus conv_state_out and/or h_trace [b, d, L, N] if asked.
 
     reverse: the backward scan of a bidirectional layer ("Mamba", ozercemkelahmet.com, "Bidirectional
@@ -94,6 +95,8 @@ def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
     t -> L-1-t, the forward routine runs, and out / h_trace are re-indexed back. h0, conv_init and
     the returned h_last / conv_state_out belong to the reversed stream (conv_init[j] is the raw
     input at L+K-2-j; conv_state_out[j] is x at K-2-j).
+
+    zoh: zero-order-hold input factor, Bbar = expm1(Delta A)/A * B, instead of Euler's Delta * B.
     """
     x, delta, A, B, C = _f64(x), _f64(delta), _f64(A), _f64(B), _f64(C)
     D, z, delta_bias, conv_w, conv_b, conv_init, h0 = map(_f64, (D, z, delta_bias, conv_w, conv_b, conv_init, h0))
@@ -110,7 +113,7 @@ def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
     _load().oracle_selective_scan(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                   _ptr(delta_bias), int(delta_softplus), _ptr(conv_w), _ptr(conv_b), K,
                                   _ptr(conv_init), _ptr(h0), _ptr(out), _ptr(h_last), _ptr(cs), _ptr(tr),
-                                  batch, dim, L, N, nthreads)
+                                  batch, dim, L, N, nthreads, int(zoh))
     if reverse:
         out = np.ascontiguousarray(out[..., ::-1])
         tr = None if tr is None else np.ascontiguousarray(tr[:, :, ::-1, :])
@@ -132,7 +135,8 @@ def compose(a1, b1, a2, b2) -> Tuple[np.ndarray, np.ndarray]:
 
 
 def chunk_aggregates(x, delta, A, B, delta_bias=None, delta_softplus: bool = True, conv_w=None, conv_b=None,
-                     conv_init=None, chunk_len: int = 64, nthreads: int = 1) -> Tuple[np.ndarray, np.ndarray]:
+                     conv_init=None, chunk_len: int = 64, nthreads: int = 1,
+                     zoh: bool = False) -> Tuple[np.ndarray, np.ndarray]:
     """Per-chunk aggregates (a, b), each [batch, dim, nchunks, N]."""
     x, delta, A, B = _f64(x), _f64(delta), _f64(A), _f64(B)
     delta_bias, conv_w, conv_b, conv_init = map(_f64, (delta_bias, conv_w, conv_b, conv_init))
@@ -144,13 +148,14 @@ def chunk_aggregates(x, delta, A, B, delta_bias=None, delta_softplus: bool = Tru
     agg_b = np.empty((batch, dim, q, N))
     _load().oracle_chunk_aggregates(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(delta_bias),
                                     int(delta_softplus), _ptr(conv_w), _ptr(conv_b), K, _ptr(conv_init),
-                                    chunk_len, _ptr(agg_a), _ptr(agg_b), batch, dim, L, N, nthreads)
+                                    chunk_len, _ptr(agg_a), _ptr(agg_b), batch, dim, L, N, nthreads, int(zoh))
     return agg_a, agg_b
 
 
 def state_update(state, conv_state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
-                 delta_softplus: bool = True, conv_w=None, conv_b=None, nthreads: int = 1):
-    """One decode step. Returns (y [batch, dim], new state, new conv_state); the inputs are not modified."""
+                 delta_softplus: bool = True, conv_w=None, conv_b=None, nthreads: int = 1, zoh: bool = False):
+    """One decode step. Returns (y [batch, dim], new state, new conv_state); the inputs are not modified.
+    zoh: zero-order-hold input factor expm1(Delta A)/A instead of Delta."""
     state = _f64(state).copy()
     conv_state = _f64(conv_state).copy() if conv_state is not None else None
     x, delta, A, B, C = _f64(x), _f64(delta), _f64(A), _f64(B), _f64(C)
@@ -161,5 +166,5 @@ def state_update(state, conv_state, x, delta, A, B, C, D=None, z=None, delta_bia
     y = np.empty((batch, dim))
     _load().oracle_state_update(_ptr(state), _ptr(conv_state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                                 _ptr(D), _ptr(z), _ptr(delta_bias), int(delta_softplus), _ptr(conv_w),
-                                _ptr(conv_b), K, _ptr(y), batch, dim, N, nthreads)
+                                _ptr(conv_b), K, _ptr(y), batch, dim, N, nthreads, int(zoh))
     return y, state, conv_state

@@ -29,7 +29,10 @@
  * this library (y_t = C_t . h_t + D_d u_t, gated by silu(z_t)).
  *
  * Readings taken where the pages are silent (stated once here, used throughout):
- *  - Bbar is the Euler form Delta*B (not zero-order hold).
+ *  - Bbar is the Euler form Delta*B by default. With the zoh flag it is the zero-order-hold
+ *    form (Abar - 1)/A * B = expm1(Delta A)/A * B ("Mamba", ai360xpert.com, "Show Me the
+ *    Code": B_bar = (1 - A_bar)/(-A) B; "Mamba", inferensys.com: a zero-order hold rule
+ *    discretizes the continuous system), whose limit as A -> 0 is the Euler form.
  *  - Delta, B and C are per token; A is a fixed parameter A[d, n].
  *  - B and C are shared by every channel: B[b, n, t], C[b, n, t].
  *  - The conv is a cross-correlation with K-1 zeros (or a supplied window) on
@@ -49,6 +52,13 @@
 
 /* softplus(x) = log(1 + e^x), written in the overflow-free form max(x,0) + log1p(e^-|x|). */
 static double softplus(double x) { return fmax(x, 0.0) + log1p(exp(-fabs(x))); }
+
+/* Input factor of Bbar = factor * B: Delta (Euler), or expm1(Delta A) / A (zero-order hold;
+ * Delta when A = 0, its limit). */
+static double bbar_factor(double Delta, double A, int zoh) {
+  if (!zoh) return Delta;
+  return A != 0.0 ? expm1(Delta * A) / A : Delta;
+}
 
 /* silu(x) = x * sigmoid(x) = x / (1 + e^-x). */
 static double silu(double x) { return x / (1.0 + exp(-x)); }
@@ -109,7 +119,7 @@ void oracle_selective_scan(const double* x, const double* delta, const double* A
                            int delta_softplus, const double* conv_w, const double* conv_b, int d_conv,
                            const double* conv_init, const double* h0, double* out, double* h_last,
                            double* conv_state_out, double* h_trace, long batch, long dim, long seqlen,
-                           long dstate, int nthreads) {
+                           long dstate, int nthreads, int zoh) {
   long nch = batch * dim;
 #pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 1)
   for (long c = 0; c < nch; ++c) {
@@ -129,7 +139,7 @@ void oracle_selective_scan(const double* x, const double* delta, const double* A
       double Delta = delta_softplus ? softplus(v) : v;
       for (long n = 0; n < dstate; ++n) {
         double Abar = exp(Delta * A[d * dstate + n]);
-        double Bbar = Delta * Bm[(b * dstate + n) * seqlen + t];
+        double Bbar = bbar_factor(Delta, A[d * dstate + n], zoh) * Bm[(b * dstate + n) * seqlen + t];
         h[n] = Abar * h[n] + Bbar * u[t];
         if (h_trace) h_trace[(c * seqlen + t) * dstate + n] = h[n];
       }
@@ -185,7 +195,7 @@ void oracle_chunk_aggregates(const double* x, const double* delta, const double*
                              const double* delta_bias, int delta_softplus, const double* conv_w,
                              const double* conv_b, int d_conv, const double* conv_init, long chunk_len,
                              double* agg_a, double* agg_b, long batch, long dim, long seqlen, long dstate,
-                             int nthreads) {
+                             int nthreads, int zoh) {
   long nchunks = (seqlen + chunk_len - 1) / chunk_len;
   long nch = batch * dim;
 #pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 1)
@@ -207,7 +217,7 @@ void oracle_chunk_aggregates(const double* x, const double* delta, const double*
           double v = delta[c * seqlen + t] + (delta_bias ? delta_bias[d] : 0.0);
           double Delta = delta_softplus ? softplus(v) : v;
           double step_a = exp(Delta * A[d * dstate + n]);
-          double step_b = Delta * Bm[(b * dstate + n) * seqlen + t] * u[t];
+          double step_b = bbar_factor(Delta, A[d * dstate + n], zoh) * Bm[(b * dstate + n) * seqlen + t] * u[t];
           double na, nb;
           oracle_compose(&a, &bb, &step_a, &step_b, &na, &nb, 1);
           a = na;
@@ -235,7 +245,7 @@ void oracle_state_update(double* state, double* conv_state, const double* x, con
                          const double* A, const double* Bm, const double* Cm, const double* Dskip,
                          const double* z, const double* delta_bias, int delta_softplus, const double* conv_w,
                          const double* conv_b, int d_conv, double* y, long batch, long dim, long dstate,
-                         int nthreads) {
+                         int nthreads, int zoh) {
   long nch = batch * dim;
 #pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(static)
   for (long c = 0; c < nch; ++c) {
@@ -262,7 +272,7 @@ void oracle_state_update(double* state, double* conv_state, const double* x, con
     double yy = 0.0;
     for (long n = 0; n < dstate; ++n) {
       double Abar = exp(Delta * A[d * dstate + n]);
-      double Bbar = Delta * Bm[b * dstate + n];
+      double Bbar = bbar_factor(Delta, A[d * dstate + n], zoh) * Bm[b * dstate + n];
       state[c * dstate + n] = Abar * state[c * dstate + n] + Bbar * u;
     }
     for (long n = 0; n < dstate; ++n) yy += Cm[b * dstate + n] * state[c * dstate + n];

@@ -123,7 +123,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
                                   int dim, int seqlen, int dstate, ssm_dtype io, int chunk_len, void* workspace,
                                   size_t workspace_bytes, unsigned int flags, void* stream) {
   if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
-  if (flags & ~SSM_SCAN_REVERSE) return SSM_ERR_INVALID_ARG;
+  if (flags & ~(SSM_SCAN_REVERSE | SSM_SCAN_ZOH)) return SSM_ERR_INVALID_ARG;
   if (!dims_ok(batch, dim, seqlen, dstate)) return SSM_ERR_INVALID_ARG;
   if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
   if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
@@ -180,6 +180,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   a.chunk_len = cl;
   a.nchunks = nchunks;
   a.reverse = (flags & SSM_SCAN_REVERSE) ? 1 : 0;
+  a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
   ssm::scan_workspace_split(workspace, (long long)batch * dim, nchunks, &a.ws_S, &a.ws_h);
   return ssm::launch_scan(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -188,8 +189,9 @@ ssm_status ssm_selective_state_update(float* state, void* conv_state, const void
                                       const float* A, const void* B, const void* C, const float* D, const void* z,
                                       const float* delta_bias, int delta_softplus, const float* conv_w,
                                       const float* conv_b, int d_conv, void* y, int batch, int dim, int dstate,
-                                      ssm_dtype io, void* stream) {
+                                      ssm_dtype io, unsigned int flags, void* stream) {
   if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (flags & ~SSM_SCAN_ZOH) return SSM_ERR_INVALID_ARG;
   if (batch < 0 || dim < 0 || dstate < 1) return SSM_ERR_INVALID_ARG;
   if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
   if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
@@ -215,6 +217,7 @@ ssm_status ssm_selective_state_update(float* state, void* conv_state, const void
   a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias; a.delta_softplus = delta_softplus;
   a.conv_w = conv_w; a.conv_b = conv_b; a.d_conv = conv ? d_conv : 0; a.y = y;
   a.batch = batch; a.dim = dim; a.dstate = dstate; a.bf16 = io == SSM_BF16;
+  a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
   return ssm::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

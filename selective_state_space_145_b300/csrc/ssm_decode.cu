@@ -22,7 +22,7 @@ namespace {
 // For the four threads that own a channel (this thread holds states 4g .. 4g+3).
 // KC = d_conv (0: no conv); the window holds K1 = KC - 1 raw inputs. Returns this thread's
 // part of C.h.
-template <typename T, int KC>
+template <typename T, int KC, bool ZOH>
 __device__ __forceinline__ float channel_step(const DecodeArgs& a, int d, float xv, float dv, const T* win,
                                               float (&h)[4], const float (&av)[4], const float (&bv)[4],
                                               const float (&cv)[4], float& u) {
@@ -44,7 +44,11 @@ __device__ __forceinline__ float channel_step(const DecodeArgs& a, int d, float 
   float part = 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    h[j] = fmaf(ex2_approx(dl2 * av[j]), h[j], du * bv[j]);
+    const float x = dl2 * av[j];
+    const float e = ex2_approx(x);
+    // input term: Euler Delta B u, or zero-order hold expm1(Delta A)/A B u
+    const float in = ZOH ? zoh_factor(x, e, dl2, av[j] != 0.f ? 1.0f / av[j] : 0.f) * u * bv[j] : du * bv[j];
+    h[j] = fmaf(e, h[j], in);
     part = fmaf(cv[j], h[j], part);
   }
   return part;
@@ -56,7 +60,7 @@ __device__ __forceinline__ float channel_step(const DecodeArgs& a, int d, float 
 constexpr int kDecThreads = 256;
 constexpr int kDecCh = kDecThreads / 4;
 
-template <typename T, int KC>
+template <typename T, int KC, bool ZOH>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a) {
   constexpr int K1 = KC > 0 ? KC - 1 : 0;
   const int c = threadIdx.x / 4, g = threadIdx.x % 4;
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a)
   // window before any of them overwrites a slot
   __syncwarp();
   float u = 0.f;
-  float part = valid ? channel_step<T, KC>(a, d, xv, dv, win, h, av, bv, cv, u) : 0.f;
+  float part = valid ? channel_step<T, KC, ZOH>(a, d, xv, dv, win, h, av, bv, cv, u) : 0.f;
   part += __shfl_xor_sync(0xffffffffu, part, 1);
   part += __shfl_xor_sync(0xffffffffu, part, 2);
   if (!valid) return;
@@ -139,7 +143,7 @@ struct __align__(16) TileSmem {
   float bcf[2 * kMaxDstate];           // the current item's B, C in fp32
 };
 
-template <typename T, int KC>
+template <typename T, int KC, bool ZOH>
 __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a, int n_ctiles, int row_groups) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   constexpr int K1 = KC > 0 ? KC - 1 : 0;
@@ -262,14 +266,32 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
     const float Delta = a.delta_softplus ? softplus_f<PRECISE>(v) : v;
     const float du = Delta * u;
     float y0 = 0.f, y1 = 0.f;
+    if (ZOH) {
+      // zero-order hold: input term expm1(Delta A)/A B u; a2 = A log2(e), so 1/A = log2(e)/a2
+      const float dlog2 = Delta * kLog2e;
 #pragma unroll
-    for (int n = 0; n < kMaxDstate; n += 2) {
-      const float2 bq = *reinterpret_cast<const float2*>(&S.bcf[n]);
-      const float2 cq = *reinterpret_cast<const float2*>(&S.bcf[kMaxDstate + n]);
-      h[n] = fmaf(ex2_approx(Delta * a2[n]), h[n], du * bq.x);
-      h[n + 1] = fmaf(ex2_approx(Delta * a2[n + 1]), h[n + 1], du * bq.y);
-      y0 = fmaf(cq.x, h[n], y0);
-      y1 = fmaf(cq.y, h[n + 1], y1);
+      for (int n = 0; n < kMaxDstate; n += 2) {
+        const float2 bq = *reinterpret_cast<const float2*>(&S.bcf[n]);
+        const float2 cq = *reinterpret_cast<const float2*>(&S.bcf[kMaxDstate + n]);
+        const float x0 = Delta * a2[n], x1 = Delta * a2[n + 1];
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+        const float m0 = zoh_factor(x0, e0, dlog2, a2[n] != 0.f ? kLog2e / a2[n] : 0.f);
+        const float m1 = zoh_factor(x1, e1, dlog2, a2[n + 1] != 0.f ? kLog2e / a2[n + 1] : 0.f);
+        h[n] = fmaf(e0, h[n], m0 * u * bq.x);
+        h[n + 1] = fmaf(e1, h[n + 1], m1 * u * bq.y);
+        y0 = fmaf(cq.x, h[n], y0);
+        y1 = fmaf(cq.y, h[n + 1], y1);
+      }
+    } else {
+#pragma unroll
+      for (int n = 0; n < kMaxDstate; n += 2) {
+        const float2 bq = *reinterpret_cast<const float2*>(&S.bcf[n]);
+        const float2 cq = *reinterpret_cast<const float2*>(&S.bcf[kMaxDstate + n]);
+        h[n] = fmaf(ex2_approx(Delta * a2[n]), h[n], du * bq.x);
+        h[n + 1] = fmaf(ex2_approx(Delta * a2[n + 1]), h[n + 1], du * bq.y);
+        y0 = fmaf(cq.x, h[n], y0);
+        y1 = fmaf(cq.y, h[n + 1], y1);
+      }
     }
     // new state and window back into this thread's own staged rows
 #pragma unroll
@@ -316,19 +338,19 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
   }
 }
 
-template <typename T, int KC>
+template <typename T, int KC, bool ZOH>
 cudaError_t launch_general(const DecodeArgs& a, cudaStream_t stream) {
   dim3 grid((a.dim + kDecCh - 1) / kDecCh, a.batch);
-  decode_kernel<T, KC><<<grid, kDecThreads, 0, stream>>>(a);
+  decode_kernel<T, KC, ZOH><<<grid, kDecThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <typename T, int KC>
+template <typename T, int KC, bool ZOH>
 cudaError_t launch_tile(const DecodeArgs& a, cudaStream_t stream) {
   // enough CTAs to fill the SMs at full occupancy; each walks several sequences of one tile
   static int resident[64] = {0};
   const size_t smem = sizeof(TileSmem<T>);
-  auto kern = decode_tile_kernel<T, KC>;
+  auto kern = decode_tile_kernel<T, KC, ZOH>;
   int dev = 0, sms = 148;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -351,25 +373,30 @@ cudaError_t launch_tile(const DecodeArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool ZOH>
 cudaError_t dispatch_k(const DecodeArgs& a, bool stream_ok, cudaStream_t s) {
   const int KC = a.conv_w ? a.d_conv : 0;
   if (stream_ok) {
     switch (KC) {
-      case 0: return launch_tile<T, 0>(a, s);
-      case 1: return launch_tile<T, 1>(a, s);
-      case 2: return launch_tile<T, 2>(a, s);
-      case 3: return launch_tile<T, 3>(a, s);
-      default: return launch_tile<T, 4>(a, s);
+      case 0: return launch_tile<T, 0, ZOH>(a, s);
+      case 1: return launch_tile<T, 1, ZOH>(a, s);
+      case 2: return launch_tile<T, 2, ZOH>(a, s);
+      case 3: return launch_tile<T, 3, ZOH>(a, s);
+      default: return launch_tile<T, 4, ZOH>(a, s);
     }
   }
   switch (KC) {
-    case 0: return launch_general<T, 0>(a, s);
-    case 1: return launch_general<T, 1>(a, s);
-    case 2: return launch_general<T, 2>(a, s);
-    case 3: return launch_general<T, 3>(a, s);
-    default: return launch_general<T, 4>(a, s);
+    case 0: return launch_general<T, 0, ZOH>(a, s);
+    case 1: return launch_general<T, 1, ZOH>(a, s);
+    case 2: return launch_general<T, 2, ZOH>(a, s);
+    case 3: return launch_general<T, 3, ZOH>(a, s);
+    default: return launch_general<T, 4, ZOH>(a, s);
   }
+}
+
+template <typename T>
+cudaError_t dispatch_t(const DecodeArgs& a, bool stream_ok, cudaStream_t s) {
+  return a.zoh ? dispatch_k<T, true>(a, stream_ok, s) : dispatch_k<T, false>(a, stream_ok, s);
 }
 
 }  // namespace
@@ -380,7 +407,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const bool stream_ok = a.dstate == kMaxDstate && (a.dim * es) % 16 == 0 && al(a.state, 16) && al(a.A, 16) &&
                          al(a.B, 16) && al(a.C, 16) && al(a.x, 16) && al(a.delta, 16) && al(a.z, 16) &&
                          (a.conv_w == nullptr || al(a.conv_state, 16));
-  return a.bf16 ? dispatch_k<__nv_bfloat16>(a, stream_ok, stream) : dispatch_k<float>(a, stream_ok, stream);
+  return a.bf16 ? dispatch_t<__nv_bfloat16>(a, stream_ok, stream) : dispatch_t<float>(a, stream_ok, stream);
 }
 
 }  // namespace ssm

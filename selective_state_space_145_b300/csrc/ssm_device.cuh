@@ -149,6 +149,37 @@ __device__ __forceinline__ float2 delta_log2(float2 dv, float bias, float bias_l
   return make_float2(t.x > kT ? t.x : lg2_approx(s.x), t.y > kT ? t.y : lg2_approx(s.y));
 }
 
+// Zero-order-hold input factor expm1(Delta A) / A (so that Bbar = factor * B), from
+// x = Delta' A (Delta' = Delta log2 e, so Delta A = x ln 2), e = 2^x, Delta' and 1/A (0 for A = 0):
+//   |Delta A| < 1/16: Delta expm1(y)/y = Delta' (ln2 + x ln2^2/2 + x^2 ln2^3/6 + x^3 ln2^4/24
+//                     + x^4 ln2^5/120), the series truncated after y^4 (next term below 2e-9
+//                     relative); this also covers A = 0, where the factor is Delta;
+//   otherwise:        (e - 1) / A, where e's 2^-22 error is at most 3e-6 of e - 1.
+constexpr float kZohC1 = 0.6931471805599453f;   // ln2
+constexpr float kZohC2 = 0.2402265069591007f;   // ln2^2 / 2
+constexpr float kZohC3 = 0.0555041086648216f;   // ln2^3 / 6
+constexpr float kZohC4 = 0.0096181291076285f;   // ln2^4 / 24
+constexpr float kZohC5 = 0.0013333558146428f;   // ln2^5 / 120
+constexpr float kZohSmall = 0.0901684400555602f;  // 1 / (16 ln2): |x| below it means |Delta A| < 1/16
+
+__device__ __forceinline__ float zoh_factor(float x, float e, float dlog2, float invA) {
+  float p = fmaf(x, kZohC5, kZohC4);
+  p = fmaf(x, p, kZohC3);
+  p = fmaf(x, p, kZohC2);
+  p = fmaf(x, p, kZohC1);
+  return fabsf(x) < kZohSmall ? dlog2 * p : (e - 1.0f) * invA;
+}
+
+__device__ __forceinline__ float2 zoh_factor2(float2 x, float2 e, float2 dlog2, float2 invA) {
+  float2 p = ffma2(x, f2(kZohC5), f2(kZohC4));
+  p = ffma2(x, p, f2(kZohC3));
+  p = ffma2(x, p, f2(kZohC2));
+  p = ffma2(x, p, f2(kZohC1));
+  const float2 small = fmul2(dlog2, p);
+  const float2 large = fmul2(fadd2(e, f2(-1.0f)), invA);
+  return make_float2(fabsf(x.x) < kZohSmall ? small.x : large.x, fabsf(x.y) < kZohSmall ? small.y : large.y);
+}
+
 // ---------------------------------------------------------------- I/O dtype
 
 template <typename T> struct IoTraits;

@@ -38,6 +38,7 @@ struct ScanArgs {
   int chunk_len;         // multiple of kChunkQuantum, >= 1 chunk
   int nchunks;
   int reverse;           // 1: the scan runs from t = L-1 down to t = 0
+  int zoh;               // 1: zero-order-hold input term expm1(Delta A)/A B u
   float* ws_S;           // [nchunks-1][batch*dim] sum of Delta per chunk
   float* ws_h;           // [nchunks-1][batch*dim][kMaxDstate] chunk end state from zero
 };
@@ -71,6 +72,7 @@ struct DecodeArgs {
   void* y;
   int batch, dim, dstate;
   int bf16;
+  int zoh;               // 1: zero-order-hold input term expm1(Delta A)/A B u
 };
 
 // Channels one scan CTA covers.

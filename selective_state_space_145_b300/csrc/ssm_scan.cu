@@ -21,6 +21,8 @@
 //    exp2 per state update, and leaves its partial C.h per step in shared memory;
 //  * epilogue: the same thread sums the four partials of its 8 steps (written by its own
 //    warp), adds D*u, applies the gate and stores straight to global memory.
+//  Options (template parameters): REV walks time backward (the backward scan of a
+//  bidirectional layer); ZOH uses the zero-order-hold input term expm1(Delta A)/A B u.
 //  The per-step state never leaves registers. With more than one chunk, a carry kernel
 //  (same code, CARRY = true: no C, no gate, no output) first writes every chunk's sum of
 //  Delta and its end state from zero; the main kernel starts chunk q from h0 composed with
@@ -95,7 +97,8 @@ struct Layout {
 
 // REV: the scan runs backward in time. The kernel walks virtual time tau = 0 .. L-1 and
 // touches real position L-1-tau; every other part of the method is unchanged.
-template <typename T, bool CONV, bool VEC, bool CARRY, bool REV>
+// ZOH: zero-order-hold input term expm1(Delta A)/A * B u instead of Euler's Delta B u.
+template <typename T, bool CONV, bool VEC, bool CARRY, bool REV, bool ZOH>
 __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   using Lay = Layout<T, CARRY>;
@@ -268,6 +271,12 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
     a01 = make_float2(av[0], av[1]);
     a23 = make_float2(av[2], av[3]);
   }
+  float2 ia01 = f2(0.f), ia23 = f2(0.f);  // ZOH: 1/A (0 where A = 0)
+  if (ZOH) {
+    auto inv = [](float v) { return v != 0.f ? 1.0f / v : 0.f; };
+    ia01 = make_float2(inv(a01.x), inv(a01.y));
+    ia23 = make_float2(inv(a23.x), inv(a23.y));
+  }
   if (!CARRY && valid) {
     if (a.h0) {
       float hv[4];
@@ -345,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           load4(&src[n0 + i][s0], v[i]);
         }
       }
-      // B carries the ln 2 that turns Delta' (log2 units) back into Delta in Delta u B
-      const float sc = tid >= 32 ? 1.0f : kLn2;
+      // Euler: B carries the ln 2 that turns Delta' (log2 units) back into Delta in Delta u B
+      const float sc = (tid >= 32 || ZOH) ? 1.0f : kLn2;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         *reinterpret_cast<float4*>(&dst[s0 + j][n0]) =
@@ -429,7 +438,8 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           D2 = make_float2(i0 ? D2.x : 0.f, i1 ? D2.y : 0.f);
           u = make_float2(i0 ? u.x : 0.f, i1 ? u.y : 0.f);
         }
-        const float2 du2 = fmul2(D2, u);
+        // the scan's per-step input: Delta' u (Euler) or u (ZOH, whose factor is per state)
+        const float2 du2 = ZOH ? u : fmul2(D2, u);
         dl[j] = D2.x;
         dl[j + 1] = D2.y;
         du[j] = du2.x;
@@ -461,8 +471,13 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
           const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
           const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
           const float2 uu = f2(du[j]);
-          h01 = ffma2(e01, h01, fmul2(uu, make_float2(bv.x, bv.y)));
-          h23 = ffma2(e23, h23, fmul2(uu, make_float2(bv.z, bv.w)));
+          float2 in01 = fmul2(uu, make_float2(bv.x, bv.y)), in23 = fmul2(uu, make_float2(bv.z, bv.w));
+          if (ZOH) {
+            in01 = fmul2(in01, zoh_factor2(x01, e01, dd, ia01));
+            in23 = fmul2(in23, zoh_factor2(x23, e23, dd, ia23));
+          }
+          h01 = ffma2(e01, h01, in01);
+          h23 = ffma2(e23, h23, in23);
           if (!CARRY) {
             const float4 cv = *reinterpret_cast<const float4*>(&s_C[t + j][4 * g]);
             const float2 p = ffma2(h23, make_float2(cv.z, cv.w), fmul2(h01, make_float2(cv.x, cv.y)));
@@ -555,24 +570,24 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
 }
 
 // Opts the kernel into its dynamic shared memory once per device.
-template <typename T, bool CONV, bool VEC, bool CARRY, bool REV>
+template <typename T, bool CONV, bool VEC, bool CARRY, bool REV, bool ZOH>
 cudaError_t prepare() {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(scan_kernel<T, CONV, VEC, CARRY, REV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<T, CARRY>::bytes);
+  err = cudaFuncSetAttribute(scan_kernel<T, CONV, VEC, CARRY, REV, ZOH>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<T, CARRY>::bytes);
   if (err == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
   return err;
 }
 
 // pdl: launch as the programmatic dependent of the kernel before it in the stream (which
 // must be this problem's carry kernel).
-template <typename T, bool CONV, bool VEC, bool CARRY, bool REV>
+template <typename T, bool CONV, bool VEC, bool CARRY, bool REV, bool ZOH>
 cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, bool pdl, cudaStream_t stream) {
-  cudaError_t err = prepare<T, CONV, VEC, CARRY, REV>();
+  cudaError_t err = prepare<T, CONV, VEC, CARRY, REV, ZOH>();
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.dim + kDT - 1) / kDT, a.batch, nchunks_grid);
@@ -584,14 +599,14 @@ cudaError_t launch_one(const ScanArgs& a, int nchunks_grid, bool pdl, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, scan_kernel<T, CONV, VEC, CARRY, REV>, a);
+  return cudaLaunchKernelEx(&cfg, scan_kernel<T, CONV, VEC, CARRY, REV, ZOH>, a);
 }
 
 template <typename T>
 int resident_main_ctas() {
   int n = 0;
-  if (prepare<T, true, true, false, false>() != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_kernel<T, true, true, false, false>, kThreads,
+  if (prepare<T, true, true, false, false, false>() != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_kernel<T, true, true, false, false, false>, kThreads,
                                                     Layout<T, false>::bytes) != cudaSuccess ||
       n <= 0) {
     cudaGetLastError();
@@ -600,25 +615,27 @@ int resident_main_ctas() {
   return n;
 }
 
-template <typename T, bool CONV, bool VEC, bool REV>
+template <typename T, bool CONV, bool VEC, bool REV, bool ZOH>
 cudaError_t launch_pair(const ScanArgs& a, cudaStream_t stream) {
   if (a.nchunks > 1) {
-    cudaError_t err = launch_one<T, CONV, VEC, true, REV>(a, a.nchunks - 1, false, stream);
+    cudaError_t err = launch_one<T, CONV, VEC, true, REV, ZOH>(a, a.nchunks - 1, false, stream);
     if (err != cudaSuccess) return err;
   }
-  return launch_one<T, CONV, VEC, false, REV>(a, a.nchunks, a.nchunks > 1, stream);
+  return launch_one<T, CONV, VEC, false, REV, ZOH>(a, a.nchunks, a.nchunks > 1, stream);
 }
 
-template <typename T, bool REV>
-cudaError_t dispatch_dir(const ScanArgs& a, cudaStream_t s) {
+template <typename T, bool REV, bool ZOH>
+cudaError_t dispatch_opts(const ScanArgs& a, cudaStream_t s) {
   const bool conv = a.conv_w != nullptr;
-  if (conv) return a.vec ? launch_pair<T, true, true, REV>(a, s) : launch_pair<T, true, false, REV>(a, s);
-  return a.vec ? launch_pair<T, false, true, REV>(a, s) : launch_pair<T, false, false, REV>(a, s);
+  if (conv)
+    return a.vec ? launch_pair<T, true, true, REV, ZOH>(a, s) : launch_pair<T, true, false, REV, ZOH>(a, s);
+  return a.vec ? launch_pair<T, false, true, REV, ZOH>(a, s) : launch_pair<T, false, false, REV, ZOH>(a, s);
 }
 
 template <typename T>
 cudaError_t dispatch(const ScanArgs& a, cudaStream_t s) {
-  return a.reverse ? dispatch_dir<T, true>(a, s) : dispatch_dir<T, false>(a, s);
+  if (a.zoh) return a.reverse ? dispatch_opts<T, true, true>(a, s) : dispatch_opts<T, false, true>(a, s);
+  return a.reverse ? dispatch_opts<T, true, false>(a, s) : dispatch_opts<T, false, false>(a, s);
 }
 
 }  // namespace

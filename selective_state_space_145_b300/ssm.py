@@ -33,8 +33,9 @@ EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_sca
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
-# Scan option bits (include/ssm.h).
+# Option bits (include/ssm.h).
 SCAN_REVERSE = 1
+SCAN_ZOH = 2
 
 
 class SSMError(RuntimeError):
@@ -72,7 +73,7 @@ def lib() -> ctypes.CDLL:
                                                      + [i] * 6 + [u, vp])
         L.ssm_selective_state_update.restype = i
         L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
-                                                 i, i, i, i, vp]
+                                                 i, i, i, i, u, vp]
         _lib = L
     return _lib
 
@@ -158,13 +159,14 @@ def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor
                            workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                            h_last: Optional[torch.Tensor] = None,
                            conv_state_out: Optional[torch.Tensor] = None,
-                           reverse: bool = False) -> Tuple[torch.Tensor, ...]:
+                           reverse: bool = False, zoh: bool = False) -> Tuple[torch.Tensor, ...]:
     """Selective scan forward. Returns (out, h_last) [+ conv_state_out when asked].
 
     x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (all float32 or bfloat16, one dtype);
     A [dim, dstate], D / delta_bias / conv_b [dim], conv_w [dim, K], h0 [batch, dim, dstate]: float32.
     The workspace (if the chosen chunking needs one) is allocated here unless passed in.
     reverse: the backward scan (SSM_SCAN_REVERSE), the recurrence runs from t = L-1 to 0.
+    zoh: zero-order-hold input term expm1(Delta A)/A B u (SSM_SCAN_ZOH) instead of Delta B u.
     """
     batch, dim, L = x.shape
     N = A.shape[1]
@@ -206,7 +208,7 @@ def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor
         _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
         _ptr(conv_w), _ptr(conv_b), K, _ptr(conv_init), _ptr(h0), _ptr(out), _ptr(h_last), _ptr(conv_state_out),
         batch, dim, L, N, io_code, int(chunk_len), _ptr(workspace), ws_bytes,
-        SCAN_REVERSE if reverse else 0, _stream(dev))
+        (SCAN_REVERSE if reverse else 0) | (SCAN_ZOH if zoh else 0), _stream(dev))
     _check("ssm_selective_scan_fwd", st)
     res = (out, h_last)
     if return_conv_state:
@@ -219,7 +221,7 @@ def ssm_selective_state_update(state: torch.Tensor, conv_state: Optional[torch.T
                                D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
                                delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
                                conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
-                               y: Optional[torch.Tensor] = None) -> torch.Tensor:
+                               y: Optional[torch.Tensor] = None, zoh: bool = False) -> torch.Tensor:
     """One decode step; updates ``state`` [batch, dim, N] f32 and ``conv_state`` [batch, dim, K-1] in place.
 
     x, delta, z: [batch, dim]; B, C: [batch, N]. Returns y [batch, dim].
@@ -247,6 +249,6 @@ def ssm_selective_state_update(state: torch.Tensor, conv_state: Optional[torch.T
     st = lib().ssm_selective_state_update(
         _ptr(state), _ptr(conv_state if conv_w is not None else None), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
         _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(conv_w), _ptr(conv_b), K, _ptr(y),
-        batch, dim, N, _io_code(x), _stream(dev))
+        batch, dim, N, _io_code(x), SCAN_ZOH if zoh else 0, _stream(dev))
     _check("ssm_selective_state_update", st)
     return y

@@ -50,13 +50,13 @@ def gpu_scan(g: dict, chunk_len: int = 0, use_conv: bool = True, use_h0: bool = 
 
 def oracle_scan(p: dict, use_conv: bool = True, use_h0: bool = True, use_init: bool = True,
                 want_conv_state: bool = False, delta_softplus: bool = True, nthreads: int = 0,
-                reverse: bool = False):
+                reverse: bool = False, zoh: bool = False):
     nthreads = nthreads or oracle.oracle.default_threads()
     return oracle.selective_scan(
         p["x"], p["delta"], p["A"], p["B"], p["C"], p.get("D"), p.get("z"), p.get("delta_bias"), delta_softplus,
         p.get("conv_w") if use_conv else None, p.get("conv_b") if use_conv else None,
         p.get("conv_init") if (use_conv and use_init) else None, p.get("h0") if use_h0 else None,
-        want_conv_state=want_conv_state, nthreads=nthreads, reverse=reverse)
+        want_conv_state=want_conv_state, nthreads=nthreads, reverse=reverse, zoh=zoh)
 
 
 def channel_slice(p: dict, b: int, d: int) -> dict:

@@ -81,7 +81,7 @@ def test_scan_argument_checks(L):
     assert _scan(L, conv_b=FAKE) == 1              # conv bias without conv weight
     assert _scan(L, x=FAKE + 2) == 2               # misaligned fp32 pointer
     assert _scan(L, chunk_len=-5) == 1
-    assert _scan(L, flags=2) == 1                  # unknown option bit
+    assert _scan(L, flags=4) == 1                  # unknown option bit
     assert _scan(L, flags=1, x=None) == 1          # reverse: same checks
     assert _scan(L, seqlen=1 << 20, chunk_len=64, batch=1, dim=4) == 1   # chunked: workspace missing
     # empty work: no launch, OK
@@ -104,7 +104,7 @@ def test_workspace_query(L):
 
 def test_decode_and_conv_argument_checks(L):
     f = L.ssm_selective_state_update
-    base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, FAKE, None, 4, FAKE, 2, 8, 16, 1, None]
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, FAKE, None, 4, FAKE, 2, 8, 16, 1, 0, None]
     bad = list(base)
     bad[0] = None
     assert f(*bad) == 1                            # state missing
@@ -117,6 +117,10 @@ def test_decode_and_conv_argument_checks(L):
     bad = list(base)
     bad[13] = 6
     assert f(*bad) == 2                            # d_conv > 4
+    for flags in (1, 4):                           # reverse has no decode form; unknown bit
+        bad = list(base)
+        bad[19] = flags
+        assert f(*bad) == 1
     c = L.ssm_causal_conv1d_fwd
     assert c(None, FAKE, None, None, FAKE, 1, 4, 8, 4, 1, 0, None) == 1
     assert c(FAKE, FAKE, None, None, FAKE, 1, 4, 8, 0, 1, 0, None) == 1

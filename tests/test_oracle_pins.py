@@ -260,6 +260,76 @@ def test_backward_scan_split_equals_whole():
         np.testing.assert_array_equal(cs1, csfull)
 
 
+# ---------------------------------------------------------------- zero-order hold (zoh=True)
+
+def test_zoh_is_exact_for_piecewise_constant_input():
+    """With a constant input u, B, A and h(0) = h0, the continuous system h' = A h + B u has
+    h(T) = e^{A T} h0 + (B u / -A)(1 - e^{A T}). Zero-order hold is exact for inputs held
+    constant over each step, so after steps of any lengths Delta_t the discrete state equals
+    the solution at T = sum of Delta_t ("Mamba", ai360xpert.com, "Show Me the Code")."""
+    b, d, L, N = 1, 3, 40, 5
+    A = _neg_A(d, N, 0.05, 3.0)
+    uval, Bval, h0 = 0.7, RNG.standard_normal(N), RNG.standard_normal((b, d, N))
+    x = np.full((b, d, L), uval)
+    B = np.repeat(Bval[None, :, None], L, axis=2).reshape(b, N, L)
+    delta = RNG.uniform(0.01, 0.6, (b, d, L))                  # softplus off: Delta = delta
+    C = np.zeros((b, N, L))
+    _, hL, tr = oracle.selective_scan(x, delta, A, B, C, h0=h0, delta_softplus=False, want_trace=True, zoh=True)
+    T = np.cumsum(delta, axis=-1)                             # [b, d, L]
+    for t in (0, 7, L - 1):
+        eAT = np.exp(A[None] * T[:, :, t:t + 1])              # [b, d, N]
+        ref = eAT * h0 + (Bval[None, None, :] * uval / -A[None]) * (1.0 - eAT)
+        np.testing.assert_allclose(tr[:, :, t, :], ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hL, tr[:, :, -1, :], rtol=0, atol=0)
+
+
+def test_zoh_tends_to_euler_as_A_vanishes():
+    """expm1(Delta A)/A -> Delta as A -> 0: with A = -1e-9 both rules agree to ~1e-9 relative,
+    and A = 0 exactly takes the limit."""
+    p = _problem(L=30)
+    for a in (-1e-9, 0.0):
+        q = dict(p, A=np.full_like(p["A"], a))
+        e_out, e_h = oracle.selective_scan(**q)
+        z_out, z_h = oracle.selective_scan(**q, zoh=True)
+        np.testing.assert_allclose(z_out, e_out, rtol=1e-7, atol=1e-9)
+        np.testing.assert_allclose(z_h, e_h, rtol=1e-7, atol=1e-9)
+
+
+def test_zoh_brute_force_tiny():
+    """Scalar loop with Bbar = (1 - exp(Delta A)) / (-A) B written as the pages print it."""
+    b, d, L, N = 1, 2, 6, 3
+    x, delta, z = _rand(b, d, L), 0.8 * _rand(b, d, L), _rand(b, d, L)
+    A, B, C, D, bias = _neg_A(d, N), _rand(b, N, L), _rand(b, N, L), _rand(d), _rand(d) - 1
+    out, hL = oracle.selective_scan(x, delta, A, B, C, D, z, bias, True, zoh=True)
+    for di in range(d):
+        h = [0.0] * N
+        for t in range(L):
+            Dl = math.log1p(math.exp(delta[0, di, t] + bias[di]))
+            y = 0.0
+            for n in range(N):
+                Ab = math.exp(Dl * A[di, n])
+                h[n] = Ab * h[n] + (1.0 - Ab) / (-A[di, n]) * B[0, n, t] * x[0, di, t]
+                y += C[0, n, t] * h[n]
+            y += D[di] * x[0, di, t]
+            ref = y * z[0, di, t] / (1.0 + math.exp(-z[0, di, t]))
+            assert abs(out[0, di, t] - ref) <= 1e-12 * (1 + abs(ref))
+        np.testing.assert_allclose(hL[0, di], h, rtol=1e-12, atol=1e-13)
+
+
+def test_zoh_decode_equals_scan():
+    """One ZOH decode step per token equals the ZOH scan over the same tokens."""
+    p = _problem(L=6)
+    out, hL, cs = oracle.selective_scan(**p, want_conv_state=True, zoh=True)
+    state, win = p["h0"], p["conv_init"]
+    for t in range(6):
+        y, state, win = oracle.state_update(state, win, p["x"][..., t], p["delta"][..., t], p["A"], p["B"][..., t],
+                                            p["C"][..., t], p["D"], p["z"][..., t], p["delta_bias"], True,
+                                            p["conv_w"], p["conv_b"], zoh=True)
+        np.testing.assert_allclose(y, out[..., t], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(state, hL, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(win, cs)
+
+
 # ---------------------------------------------------------------- invariants
 
 def _problem(b=2, d=3, L=21, N=4, K=4):

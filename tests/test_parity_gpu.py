@@ -259,6 +259,70 @@ def test_recurrent_equals_parallel_on_gpu(cuda_device, io):
     assert torch.equal(win, cs)
 
 
+# ---------------------------------------------------------------- zero-order hold (SSM_SCAN_ZOH)
+
+def _zoh_edge_A(A: torch.Tensor) -> torch.Tensor:
+    """A with exact zeros and tiny magnitudes in some states, so the expm1 series branch,
+    its boundary and the A = 0 limit are all exercised."""
+    A = A.clone()
+    N = A.shape[1]
+    if N > 3:
+        A[:, 0] = 0.0
+        A[:, 1] = -1e-6
+        A[:, 2] = -0.02
+        A[:, 3] = 0.3   # a growing mode
+    return A
+
+
+ZOH = [
+    # batch, dim, L, N, K, io, chunk_len, reverse
+    (2, 37, 200, 16, 4, "f32", 0, False),
+    (2, 40, 264, 16, 4, "bf16", 128, False),
+    (2, 33, 101, 7, 3, "f32", 64, False),        # element-wise path, chunks, N < 16
+    (2, 48, 300, 16, 4, "f32", 64, True),        # backward + ZOH, chunked
+    (1, 70, 130, 16, 0, "bf16", 0, True),
+]
+
+
+@pytest.mark.parametrize("case", ZOH, ids=lambda c: "b{}_d{}_l{}_n{}_k{}_{}_cl{}_rev{}".format(*c))
+def test_zoh_small_whole(cuda_device, case):
+    batch, dim, L, N, K, io, cl, rev = case
+    p = inputs.scan_inputs(batch, dim, L, N, K, io, seed=4000 + dim + L, with_h0=True, with_conv_init=K > 1,
+                           random_A=True)
+    p["A"] = _zoh_edge_A(p["A"])
+    g = to_dev(p, cuda_device)
+    out, hL = gpu_scan(g, chunk_len=cl, reverse=rev, zoh=True)
+    ref, refL = oracle_scan(p, reverse=rev, zoh=True)
+    assert_close(out, ref, io, "out")
+    assert_close(hL, refL, io, "h_last")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_zoh_decode_matches_oracle_and_scan(cuda_device, io):
+    """ZOH decode steps against the oracle, and against the ZOH scan over the same tokens."""
+    ssm = _ssm()
+    batch, dim, N, K, T = 2, 300, 16, 4, 6
+    p = inputs.scan_inputs(batch, dim, T, N, K, io, seed=41, with_h0=True, with_conv_init=True, random_A=True)
+    p["A"] = _zoh_edge_A(p["A"])
+    g = to_dev(p, cuda_device)
+    out, hL, cs = gpu_scan(g, return_conv_state=True, zoh=True)
+    state, win = g["h0"].clone(), g["conv_init"].clone()
+    ostate, owin = p["h0"].double().numpy(), p["conv_init"].double().numpy()
+    ys = []
+    for t in range(T):
+        cols = {k: g[k][..., t].contiguous() for k in ("x", "delta", "B", "C", "z")}
+        ys.append(ssm.ssm_selective_state_update(state, win, cols["x"], cols["delta"], g["A"], cols["B"], cols["C"],
+                                                 g["D"], cols["z"], g["delta_bias"], True, g["conv_w"], g["conv_b"],
+                                                 zoh=True))
+        yr, ostate, owin = oracle.state_update(ostate, owin, p["x"][..., t], p["delta"][..., t], p["A"],
+                                               p["B"][..., t], p["C"][..., t], p["D"], p["z"][..., t],
+                                               p["delta_bias"], True, p["conv_w"], p["conv_b"], zoh=True)
+        assert_close(ys[-1], yr, io, f"decode y step {t}")
+        assert_close(state, ostate, io, f"decode state step {t}")
+    assert_close(torch.stack(ys, dim=-1), out.float().cpu().double().numpy(), io, "ZOH decode vs ZOH scan")
+    assert torch.equal(win, cs)
+
+
 # ---------------------------------------------------------------- the five workloads, full size
 
 def _workload_scan(name, n_sample, cuda_device, seed):
