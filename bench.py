@@ -102,11 +102,23 @@ def algorithmic_bytes(w) -> int:
     return b
 
 
+def bwd_algorithmic_bytes(w) -> int:
+    """Bytes of one backward step, every input read once and every output written once: u,
+    delta, z, dout in and du, ddelta, dz out (io dtype); B, C in (io) and dB, dC out (fp32);
+    h0, dh_last in and dh0 out; A, D, bias in and dA, dD, dbias out (fp32)."""
+    es = 2 if w.io == "bf16" else 4
+    tok = w.batch * w.dim * w.seqlen
+    bnl = w.batch * w.dstate * w.seqlen
+    return (tok * es * 7 + bnl * (2 * es + 2 * 4) + w.batch * w.dim * w.dstate * 4 * 3
+            + w.dim * w.dstate * 4 * 2 + w.dim * 4 * 4)
+
+
 # The sources each kind of workload's kernels are built from: a traffic figure stays valid
 # while these files are unchanged.
 _KERNEL_SOURCES = {
     "scan": ("ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
     "decode": ("ssm_decode.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
+    "backward": ("ssm_scan_bwd.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
 }
 
 
@@ -503,6 +515,107 @@ def run_gpu(args, w):
     return 0
 
 
+def run_gpu_bwd(args, w):
+    """The scan's backward pass on the workload's shapes (x taken as the scan input u): one
+    ssm_selective_scan_bwd call per step, CUDA events on the launching stream, L2 flushed
+    before every step outside the events."""
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import dataclasses
+
+    import selective_state_space_145_b300 as ssm
+    from selective_state_space_145_b300 import inputs
+
+    p = inputs.workload_inputs(w if world == 1 else dataclasses.replace(w, seed=w.seed + 1000 * rank))
+    gen = torch.Generator().manual_seed(w.seed + 7)
+    dout = torch.randn(w.batch, w.dim, w.seqlen, generator=gen).to(p["x"].dtype)
+    dhl = torch.randn(w.batch, w.dim, w.dstate, generator=gen)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    dout_d, dhl_d = dout.to(dev), dhl.to(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(max(1, ssm.ssm_scan_bwd_workspace_bytes(w.batch, w.dim, w.seqlen, w.dstate, g["x"].dtype)),
+                     dtype=torch.uint8, device=dev)
+    args_bwd = (g["x"], g["delta"], g["A"], g["B"], g["C"], dout_d, g["D"], g["z"], g["delta_bias"], True, g["h0"],
+                dhl_d)
+    grads = ssm.ssm_selective_scan_bwd(*args_bwd, workspace=ws)
+
+    def step():
+        ssm.ssm_selective_scan_bwd(*args_bwd, workspace=ws, grads=grads)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    ms = reduce_max(statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)), world, dev)
+    updates = w.updates
+    bytes_step = bwd_algorithmic_bytes(w)
+    peak, peak_kind = _peaks()
+    achieved = bytes_step / (ms * 1e-3) / 1e9
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        nch = min(w.dim, 64)
+        sub = inputs.scan_inputs(1, nch, w.seqlen, w.dstate, 0, w.io, w.seed, with_h0=True)
+        sd = torch.randn(1, nch, w.seqlen, generator=gen).to(sub["x"].dtype)
+        cores = oracle.oracle.default_threads()
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds and reps < 1000:
+            oracle.selective_scan_bwd(sub["x"], sub["delta"], sub["A"], sub["B"], sub["C"], sd, sub["D"], sub["z"],
+                                      sub["delta_bias"], True, sub["h0"], None, nthreads=cores)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps * nch * w.seqlen * w.dstate / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{reps} backward pass(es) over {nch} channels x {w.seqlen} steps x N={w.dstate} (fp64)"}
+    cfg = config_of(w)
+    cfg["pass"] = "backward (ssm_selective_scan_bwd; x taken as the scan input u)"
+    line = {
+        "metric": METRIC, "value": updates * world / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic_from_profiles(w.name + "#backward", "backward"), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_step": bytes_step,
+                     "timed": "whole step (scan_bwd_kernel + scan_bwd_reduce_kernel)"},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -519,6 +632,7 @@ def main(argv=None):
                     help="scan chunk length (0 = the library's default policy)")
     ap.add_argument("--reverse", action="store_true", help="time the backward scan (SSM_SCAN_REVERSE)")
     ap.add_argument("--zoh", action="store_true", help="zero-order-hold discretisation (SSM_SCAN_ZOH)")
+    ap.add_argument("--backward", action="store_true", help="time the scan's backward pass")
     args = ap.parse_args(argv)
     import dataclasses
 
@@ -534,6 +648,10 @@ def main(argv=None):
         w = dataclasses.replace(w, name=f"{w.name}[batch={w.batch},seqlen={w.seqlen}]")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.backward:
+        if w.kind != "scan" or args.impl != "ours":
+            ap.error("--backward times this library's backward pass on a scan workload")
+        return run_gpu_bwd(args, w)
     return run_gpu(args, w)
 
 

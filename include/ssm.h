@@ -1,11 +1,12 @@
 /*
  * ssm.h -- C ABI of the B300 selective state-space (S6) library, libssm.so.
  *
- * Three operations, each on the caller's CUDA stream:
+ * Four operations, each on the caller's CUDA stream:
  *   ssm_causal_conv1d_fwd       depthwise causal conv1d (+ SiLU), the block's short conv
  *   ssm_selective_scan_fwd      selective scan forward (optionally with the conv fused in
  *                               front), returning y and the final state h_L
  *   ssm_selective_state_update  one recurrent (decode) step for a batch of sequences
+ *   ssm_selective_scan_bwd      the scan's backward pass (training)
  *
  * Sources (page title, section):
  *   "Mamba" (ai360xpert.com, core ML), "The selection mechanism":
@@ -167,6 +168,48 @@ SSM_API ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, cons
                                   const float* h0, void* out, float* h_last, void* conv_state_out, int batch,
                                   int dim, int seqlen, int dstate, ssm_dtype io, int chunk_len, void* workspace,
                                   size_t workspace_bytes, unsigned int flags, void* stream);
+
+/*
+ * Workspace bytes ssm_selective_scan_bwd needs (about 4 bytes per (b, d, t) for the state
+ * checkpoints plus the per-channel-tile partial sums of dB, dC).
+ */
+SSM_API size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int dstate, ssm_dtype io);
+
+/*
+ * Backward pass of ssm_selective_scan_fwd (training) for the forward-time Euler scan with the
+ * scan input u given directly (conv_w = NULL in the forward call): the gradients of a scalar
+ * loss L from dout = dL/dout and dh_last = dL/dh_last, through the adjoint recurrence
+ *   g_t[n] = dL/dh_t[n] = exp(Delta_{t+1} A[d,n]) g_{t+1}[n] + C[b,n,t] dy_t,   g_{L-1} starts at dh_last
+ *   dy_t  = dout_t silu(z_t)          dz_t = dout_t y_t silu'(z_t)
+ *   du_t  = D[d] dy_t + sum_n g_t[n] Delta_t B[b,n,t]
+ *   ddelta_t = sigmoid(delta_t + bias) sum_n g_t[n] (A[d,n] Abar_t[n] h_{t-1}[n] + B[b,n,t] u_t)
+ *   dA[d,n] = sum_{b,t} g_t[n] Delta_t Abar_t[n] h_{t-1}[n]      dB[b,n,t] = sum_d g_t[n] Delta_t u_t
+ *   dC[b,n,t] = sum_d dy_t h_t[n]     dD[d] = sum_{b,t} dy_t u_t     ddelta_bias[d] = sum_{b,t} ddelta_t
+ *   dh0[b,d,n] = Abar_0[n] g_0[n]
+ * (the chain rule on the forward definition; "Mamba (Selective State-Space Model)",
+ * gunjandhanuka.github.io, "Cost of selectivity": training runs through the parallel scan). Without
+ * softplus the sigmoid factor is 1.
+ *
+ * Inputs as for the forward call (u in place of x); dout [batch, dim, seqlen] io; dh_last
+ * [batch, dim, dstate] float32 or NULL (= 0).
+ * Outputs (all written, none accumulated into):
+ *   du, ddelta [batch, dim, seqlen] io;  dz [batch, dim, seqlen] io, required when z != NULL;
+ *   dA [dim, dstate], dB, dC [batch, dstate, seqlen], dD [dim], ddelta_bias [dim],
+ *   dh0 [batch, dim, dstate], all float32; dD, ddelta_bias and dh0 may be NULL (not computed).
+ * The intermediate states are recomputed from checkpoints the call writes to the workspace
+ * (ssm_scan_bwd_workspace_bytes, 256-byte aligned, no initialisation needed). Channel and
+ * sequence sums are formed in a fixed order, so the results are deterministic.
+ *   flags  must be 0: SSM_SCAN_REVERSE and SSM_SCAN_ZOH have no backward pass here
+ *          (SSM_ERR_UNSUPPORTED); unknown bits are SSM_ERR_INVALID_ARG.
+ */
+SSM_API ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                                          const void* C, const float* D, const void* z, const float* delta_bias,
+                                          int delta_softplus, const float* h0, const void* dout,
+                                          const float* dh_last, void* du, void* ddelta, void* dz, float* dA,
+                                          float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                                          int batch, int dim, int seqlen, int dstate, ssm_dtype io,
+                                          void* workspace, size_t workspace_bytes, unsigned int flags,
+                                          void* stream);
 
 /*
  * One recurrent (decode) step for every sequence b and channel d, state updated in place:

@@ -10,6 +10,7 @@ from .oracle import (  # noqa: F401
     chunk_aggregates,
     compose,
     selective_scan,
+    selective_scan_bwd,
     silu,
     softplus,
     state_update,

@@ -35,8 +35,9 @@ def _load():
         lib.oracle_chunk_aggregates.argtypes = ([_P] * 5 + [I] + [_P, _P, I, _P, L, _P, _P]
                                                 + [L, L, L, L, I, I])
         lib.oracle_state_update.argtypes = ([_P, _P] + [_P] * 8 + [I] + [_P, _P, I, _P] + [L, L, L, I, I])
+        lib.oracle_selective_scan_bwd.argtypes = ([_P] * 8 + [I] + [_P] * 3 + [_P] * 9 + [L, L, L, L, I])
         for f in ("oracle_softplus", "oracle_silu", "oracle_causal_conv1d", "oracle_selective_scan",
-                  "oracle_compose", "oracle_chunk_aggregates", "oracle_state_update"):
+                  "oracle_compose", "oracle_chunk_aggregates", "oracle_state_update", "oracle_selective_scan_bwd"):
             getattr(lib, f).restype = None
         _lib = lib
     return _lib
@@ -123,6 +124,29 @@ def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_sof
     if want_trace:
         res.append(tr)
     return tuple(res)
+
+
+def selective_scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, delta_softplus: bool = True,
+                       h0=None, dh_last=None, nthreads: int = 1) -> dict:
+    """Gradients of a scalar loss through selective_scan (u given directly, Euler, forward in
+    time) from dout = dL/dout and dh_last = dL/dh_last. Returns a dict with du, ddelta, dz (or
+    None), dA [d, N], dB, dC [b, N, L], dD, ddelta_bias [d] (None when D / delta_bias are None)
+    and dh0 [b, d, N]."""
+    u, delta, A, B, C, dout = _f64(u), _f64(delta), _f64(A), _f64(B), _f64(C), _f64(dout)
+    D, z, delta_bias, h0, dh_last = map(_f64, (D, z, delta_bias, h0, dh_last))
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    g = {"du": np.empty((batch, dim, L)), "ddelta": np.empty((batch, dim, L)),
+         "dz": np.empty((batch, dim, L)) if z is not None else None, "dA": np.empty((dim, N)),
+         "dB": np.empty((batch, N, L)), "dC": np.empty((batch, N, L)),
+         "dD": np.empty(dim) if D is not None else None,
+         "ddelta_bias": np.empty(dim) if delta_bias is not None else None, "dh0": np.empty((batch, dim, N))}
+    _load().oracle_selective_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                      _ptr(delta_bias), int(delta_softplus), _ptr(h0), _ptr(dout), _ptr(dh_last),
+                                      _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                                      _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
+                                      batch, dim, L, N, nthreads)
+    return g
 
 
 def compose(a1, b1, a2, b2) -> Tuple[np.ndarray, np.ndarray]:

@@ -282,4 +282,131 @@ void oracle_state_update(double* state, double* conv_state, const double* x, con
   }
 }
 
+/*
+ * Backward pass of the selective scan (training): the gradients of a scalar loss L through
+ * oracle_selective_scan with the scan input u given directly (no conv) and the Euler rule,
+ * given dout = dL/dout [b,d,t] and dh_last = dL/dh_last [b,d,n] (NULL: 0). The backward pass
+ * is the adjoint of the recurrence ("Mamba (Selective State-Space Model)",
+ * gunjandhanuka.github.io, "Cost of selectivity": training runs through the parallel scan); every line
+ * below is the chain rule applied to one line of the forward definition.
+ *   forward:  Delta_t = softplus(v_t), v_t = delta_t + bias;  Abar_t[n] = exp(Delta_t A[n]);
+ *             h_t[n] = Abar_t[n] h_{t-1}[n] + Delta_t B_t[n] u_t;  y_t = sum_n C_t[n] h_t[n] + D u_t;
+ *             out_t = y_t silu(z_t)
+ *   adjoint:  g_t[n] = dL/dh_t[n] = Abar_{t+1}[n] g_{t+1}[n] + C_t[n] dy_t,  g_L = dh_last
+ *   dy_t = dout_t silu(z_t);  dz_t = dout_t y_t silu'(z_t),  silu'(z) = s(z) (1 + z (1 - s(z)))
+ *   dC_t[n] += dy_t h_t[n];  dB_t[n] += g_t[n] Delta_t u_t      (summed over channels d)
+ *   du_t = D dy_t + sum_n g_t[n] Delta_t B_t[n]
+ *   dDelta_t = sum_n g_t[n] (A[n] Abar_t[n] h_{t-1}[n] + B_t[n] u_t)
+ *   dA[n] += g_t[n] Delta_t Abar_t[n] h_{t-1}[n];  dD += dy_t u_t   (summed over b and t)
+ *   ddelta_t = dDelta_t sigmoid(v_t) (softplus on) or dDelta_t;  ddelta_bias += ddelta_t
+ *   dh0[n] = Abar_0[n] g_0[n]
+ * Outputs: du, ddelta [b,d,t]; dz [b,d,t] (when z is given); dA [d,n]; dB, dC [b,n,t];
+ * dD, ddelta_bias [d]; dh0 [b,d,n]. All are written (not accumulated into).
+ */
+void oracle_selective_scan_bwd(const double* u, const double* delta, const double* A, const double* Bm,
+                               const double* Cm, const double* Dskip, const double* z, const double* delta_bias,
+                               int delta_softplus, const double* h0, const double* dout, const double* dh_last,
+                               double* du, double* ddelta, double* dz, double* dA, double* dB, double* dC,
+                               double* dD, double* ddelta_bias, double* dh0, long batch, long dim, long seqlen,
+                               long dstate, int nthreads) {
+  long nch = batch * dim;
+  long NL = dstate * seqlen;
+  /* per-channel contributions, summed below in a fixed order */
+  double* cA = (double*)calloc((size_t)(nch * dstate), sizeof(double));
+  double* cD = (double*)calloc((size_t)nch, sizeof(double));
+  double* cbias = (double*)calloc((size_t)nch, sizeof(double));
+  double* cB = (double*)calloc((size_t)(nch * NL > 0 ? nch * NL : 1), sizeof(double));
+  double* cC = (double*)calloc((size_t)(nch * NL > 0 ? nch * NL : 1), sizeof(double));
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 1)
+  for (long c = 0; c < nch; ++c) {
+    long b = c / dim, d = c % dim;
+    const double* uc = u + c * seqlen;
+    double* hs = (double*)malloc(sizeof(double) * (size_t)((seqlen + 1) * dstate)); /* h_{-1} .. h_{L-1} */
+    double* Dl = (double*)malloc(sizeof(double) * (size_t)(seqlen > 0 ? seqlen : 1));
+    double* sg = (double*)malloc(sizeof(double) * (size_t)(seqlen > 0 ? seqlen : 1));
+    double* g = (double*)malloc(sizeof(double) * (size_t)dstate);
+    /* forward, keeping every state */
+    for (long n = 0; n < dstate; ++n) hs[n] = h0 ? h0[c * dstate + n] : 0.0;
+    for (long t = 0; t < seqlen; ++t) {
+      double v = delta[c * seqlen + t] + (delta_bias ? delta_bias[d] : 0.0);
+      Dl[t] = delta_softplus ? softplus(v) : v;
+      sg[t] = delta_softplus ? 1.0 / (1.0 + exp(-v)) : 1.0; /* dDelta/dv */
+      for (long n = 0; n < dstate; ++n) {
+        double Abar = exp(Dl[t] * A[d * dstate + n]);
+        hs[(t + 1) * dstate + n] = Abar * hs[t * dstate + n] + Dl[t] * Bm[(b * dstate + n) * seqlen + t] * uc[t];
+      }
+    }
+    /* backward */
+    for (long n = 0; n < dstate; ++n) g[n] = dh_last ? dh_last[c * dstate + n] : 0.0;
+    for (long t = seqlen - 1; t >= 0; --t) {
+      const double* ht = hs + (t + 1) * dstate;
+      const double* hp = hs + t * dstate;
+      double y = 0.0;
+      for (long n = 0; n < dstate; ++n) y += Cm[(b * dstate + n) * seqlen + t] * ht[n];
+      if (Dskip) y += Dskip[d] * uc[t];
+      double dy = dout[c * seqlen + t];
+      if (z) {
+        double zz = z[c * seqlen + t];
+        double s = 1.0 / (1.0 + exp(-zz));
+        dz[c * seqlen + t] = dout[c * seqlen + t] * y * s * (1.0 + zz * (1.0 - s));
+        dy = dout[c * seqlen + t] * zz * s;
+      }
+      double dut = Dskip ? Dskip[d] * dy : 0.0;
+      double dDel = 0.0;
+      for (long n = 0; n < dstate; ++n) {
+        double Bt = Bm[(b * dstate + n) * seqlen + t];
+        double Ct = Cm[(b * dstate + n) * seqlen + t];
+        double An = A[d * dstate + n];
+        double Abar = exp(Dl[t] * An);
+        g[n] += Ct * dy;
+        cC[c * NL + n * seqlen + t] = dy * ht[n];
+        cB[c * NL + n * seqlen + t] = g[n] * Dl[t] * uc[t];
+        dut += g[n] * Dl[t] * Bt;
+        dDel += g[n] * (An * Abar * hp[n] + Bt * uc[t]);
+        cA[c * dstate + n] += g[n] * Dl[t] * Abar * hp[n];
+        g[n] = Abar * g[n];
+      }
+      du[c * seqlen + t] = dut;
+      ddelta[c * seqlen + t] = dDel * sg[t];
+      cbias[c] += dDel * sg[t];
+      if (Dskip) cD[c] += dy * uc[t];
+    }
+    for (long n = 0; n < dstate; ++n) dh0[c * dstate + n] = g[n];
+    free(hs);
+    free(Dl);
+    free(sg);
+    free(g);
+  }
+  /* reductions: over b for the per-channel parameters, over d for B and C */
+  for (long d = 0; d < dim; ++d) {
+    double sD = 0.0, sb = 0.0;
+    for (long b = 0; b < batch; ++b) {
+      sD += cD[b * dim + d];
+      sb += cbias[b * dim + d];
+    }
+    if (dD) dD[d] = sD;
+    if (ddelta_bias) ddelta_bias[d] = sb;
+    for (long n = 0; n < dstate; ++n) {
+      double sA = 0.0;
+      for (long b = 0; b < batch; ++b) sA += cA[(b * dim + d) * dstate + n];
+      dA[d * dstate + n] = sA;
+    }
+  }
+  for (long b = 0; b < batch; ++b)
+    for (long i = 0; i < NL; ++i) {
+      double sB = 0.0, sC = 0.0;
+      for (long d = 0; d < dim; ++d) {
+        sB += cB[(b * dim + d) * NL + i];
+        sC += cC[(b * dim + d) * NL + i];
+      }
+      dB[b * NL + i] = sB;
+      dC[b * NL + i] = sC;
+    }
+  free(cA);
+  free(cD);
+  free(cbias);
+  free(cB);
+  free(cC);
+}
+
 int oracle_version(void) { return 1; }

@@ -1,5 +1,5 @@
 """B300-native selective state-space (S6) hot path: causal conv prologue, selective scan
-forward and the decode state update, as hand-written sm_103a CUDA behind a C ABI
+forward (and its backward pass) and the decode state update, as hand-written sm_103a CUDA behind a C ABI
 (``libssm.so``, declared in ``include/ssm.h``) with a thin ctypes binding.
 
 The binding loads the library on first use and raises if it is missing.
@@ -11,8 +11,10 @@ from .ssm import (  # noqa: F401
     SSMError,
     lib,
     ssm_causal_conv1d_fwd,
+    ssm_scan_bwd_workspace_bytes,
     ssm_scan_default_chunk_len,
     ssm_scan_workspace_bytes,
+    ssm_selective_scan_bwd,
     ssm_selective_scan_fwd,
     ssm_selective_state_update,
     status_string,
@@ -23,6 +25,8 @@ __all__ = [
     "ssm_causal_conv1d_fwd",
     "ssm_selective_scan_fwd",
     "ssm_selective_state_update",
+    "ssm_selective_scan_bwd",
+    "ssm_scan_bwd_workspace_bytes",
     "ssm_scan_default_chunk_len",
     "ssm_scan_workspace_bytes",
     "version",

@@ -221,4 +221,48 @@ ssm_status ssm_selective_state_update(float* state, void* conv_state, const void
   return ssm::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int dstate, ssm_dtype io) {
+  (void)dstate;
+  (void)io;
+  if (batch <= 0 || dim <= 0 || seqlen < 0) return 0;
+  return ssm::scan_bwd_workspace_bytes(batch, dim, seqlen);
+}
+
+ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                  const float* D, const void* z, const float* delta_bias, int delta_softplus,
+                                  const float* h0, const void* dout, const float* dh_last, void* du, void* ddelta,
+                                  void* dz, float* dA, float* dB, float* dC, float* dD, float* ddelta_bias,
+                                  float* dh0, int batch, int dim, int seqlen, int dstate, ssm_dtype io,
+                                  void* workspace, size_t workspace_bytes, unsigned int flags, void* stream) {
+  if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (flags & ~(SSM_SCAN_REVERSE | SSM_SCAN_ZOH)) return SSM_ERR_INVALID_ARG;
+  if (flags) return SSM_ERR_UNSUPPORTED;  // the backward pass covers the forward-time Euler scan
+  if (!dims_ok(batch, dim, seqlen, dstate)) return SSM_ERR_INVALID_ARG;
+  if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
+  if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+  if ((long long)batch * dim == 0) return SSM_OK;
+  if (!A || !dA) return SSM_ERR_INVALID_ARG;
+  if (seqlen > 0 && (!u || !delta || !B || !C || !dout || !du || !ddelta || !dB || !dC))
+    return SSM_ERR_INVALID_ARG;
+  if (z && seqlen > 0 && !dz) return SSM_ERR_INVALID_ARG;
+  const size_t es = io_bytes(io);
+  const void* io_ptrs[] = {u, delta, B, C, z, dout, du, ddelta, dz};
+  for (const void* p : io_ptrs)
+    if (p && !aligned(p, es)) return SSM_ERR_UNSUPPORTED;
+  const void* f_ptrs[] = {A, D, delta_bias, h0, dh_last, dA, dB, dC, dD, ddelta_bias, dh0};
+  for (const void* p : f_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_UNSUPPORTED;
+  const size_t need = ssm::scan_bwd_workspace_bytes(batch, dim, seqlen);
+  if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return SSM_ERR_UNSUPPORTED;
+  ssm::ScanBwdArgs a;
+  a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
+  a.delta_softplus = delta_softplus; a.h0 = h0; a.dout = dout; a.dh_last = dh_last;
+  a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD;
+  a.ddelta_bias = ddelta_bias; a.dh0 = dh0;
+  a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.dstate = dstate; a.bf16 = io == SSM_BF16;
+  ssm::scan_bwd_workspace_split(workspace, batch, dim, seqlen, a);
+  return ssm::launch_scan_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -75,6 +75,38 @@ struct DecodeArgs {
   int zoh;               // 1: zero-order-hold input term expm1(Delta A)/A B u
 };
 
+struct ScanBwdArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* delta_bias;
+  int delta_softplus;
+  const float* h0;
+  const void* dout;
+  const float* dh_last;
+  void* du;
+  void* ddelta;
+  void* dz;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;
+  float* ddelta_bias;
+  float* dh0;
+  int batch, dim, seqlen, dstate;
+  int bf16;
+  float* ws_ckpt;        // [batch][channel tiles][tiles][128 threads] float4: state before each tile
+  float* ws_dB;          // [batch][channel tiles][16][seqlen] per-CTA channel sums
+  float* ws_dC;
+  float* ws_dA;          // [batch][dim][16]
+  float* ws_dD;          // [batch][dim]
+  float* ws_dbias;       // [batch][dim]
+};
+
 // Channels one scan CTA covers.
 int scan_channels_per_cta();
 // CTAs of the main scan kernel resident per SM (occupancy query; 4 without a device)
@@ -85,6 +117,9 @@ size_t scan_workspace_bytes(long long channels, int nchunks);
 void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, float** h);
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
+size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen);
+void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, ScanBwdArgs& a);
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

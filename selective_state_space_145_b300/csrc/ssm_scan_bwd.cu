@@ -1,0 +1,382 @@
+// ssm_scan_bwd.cu -- backward pass of the selective scan (training), Euler rule, forward time,
+// scan input u given directly (no fused conv).
+//
+// What it computes: the gradients of a scalar loss through
+//   Delta_t = softplus(delta_t + bias_d),  h_t[n] = exp(Delta_t A[d,n]) h_{t-1}[n] + Delta_t B[b,n,t] u_t,
+//   y_t = sum_n C[b,n,t] h_t[n] + D_d u_t,  out_t = y_t silu(z_t)
+// from dout = dL/dout and dh_last = dL/dh_{L-1}. The adjoint g_t[n] = dL/dh_t[n] obeys the
+// same recurrence run backward, g_t = exp(Delta_{t+1} A) g_{t+1} + C_t dy_t ("Mamba (Selective
+// State-Space Model)", gunjandhanuka.github.io, "Cost of selectivity": training runs through
+// the parallel scan), and
+//   dy_t = dout_t silu(z_t),  dz_t = dout_t y_t silu'(z_t),  du_t = D dy_t + sum_n g_t Delta_t B_t,
+//   dDelta_t = sum_n g_t (A Abar_t h_{t-1} + B_t u_t),  ddelta_t = dDelta_t sigmoid(delta_t + bias),
+//   dA += g_t Delta_t Abar_t h_{t-1},  dB_t += g_t Delta_t u_t,  dC_t += dy_t h_t,  dD += dy_t u_t,
+//   dh0 = Abar_0 g_0.
+//
+// Design. One CTA = 32 channels of one sequence, the whole sequence, 128 threads; thread
+// (c, g) holds states 4g .. 4g+3 of channel c, as in the forward kernel.
+//  * Checkpoint pass: the forward recurrence (no readout) over the sequence, writing the state
+//    before every 16-step tile to the workspace.
+//  * Reverse pass, tile by tile from the end: stage the tile's u, delta, z, dout rows and B, C;
+//    recompute h_t of the 16 steps from the tile's checkpoint into shared memory, with the
+//    readout partials that give y_t; then dy, dz; the channel sums of dC_t over the CTA's 32
+//    channels; the adjoint walk (16 steps backward, four states per thread in registers),
+//    which leaves g_t in the slot of h_t; the channel sums of dB_t; and du, ddelta.
+//  * dA, dD and dbias accumulate per channel in registers. dB, dC, dA, dD, dbias are written as
+//    per-CTA partials and summed over channel tiles / sequences by a second kernel in a fixed
+//    order (deterministic, no atomics).
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kBThreads = 128;
+constexpr int kBDT = 32;        // channels per CTA
+constexpr int kBT = 16;         // steps per tile
+constexpr int kBTP = kBT + 1;   // padded row of the per-(channel, step) arrays
+static_assert(kBThreads == kBDT * 4, "four threads per channel");
+
+struct BwdSmem {
+  float4 hist[kBT][kBThreads];        // h_t of the tile, then the adjoint g_t
+  float Bt[kBT][kMaxDstate];          // B, C of the tile, fp32, t-major
+  float Ct[kBT][kMaxDstate];
+  float dl[kBDT][kBTP];               // Delta' = Delta log2(e)
+  float Dl[kBDT][kBTP];               // Delta
+  float uu[kBDT][kBTP];               // u
+  float du[kBDT][kBTP];               // Delta u
+  float sg[kBDT][kBTP];               // dDelta / d(delta)
+  float dy[kBDT][kBTP];               // dL/dy
+  float dout[kBDT][kBTP];
+  float zz[kBDT][kBTP];
+  float p0[4][kBDT][kBTP];            // per-state-group partials: readout, then du
+  float p1[4][kBDT][kBTP];            // per-state-group partials of dDelta
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArgs a) {
+  constexpr bool PRECISE = IoTraits<T>::kPrecise;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BwdSmem& S = *reinterpret_cast<BwdSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int c = tid % kBDT, g = tid / kBDT;
+  const int dtile = blockIdx.x, b = blockIdx.y;
+  const int d0 = dtile * kBDT, d = d0 + c;
+  const int L = a.seqlen, N = a.dstate, dim = a.dim;
+  const bool valid = d < dim;
+  const long long cc = (long long)b * dim + d;
+  const int ntiles = (L + kBT - 1) / kBT;
+  const long long cta = (long long)b * gridDim.x + dtile;
+  float4* ckpt = reinterpret_cast<float4*>(a.ws_ckpt) + cta * (long long)ntiles * kBThreads;
+
+  const T* gu = static_cast<const T*>(a.u);
+  const T* gdel = static_cast<const T*>(a.delta);
+  const T* gz = static_cast<const T*>(a.z);
+  const T* gdo = static_cast<const T*>(a.dout);
+  const T* gB = static_cast<const T*>(a.B);
+  const T* gC = static_cast<const T*>(a.C);
+
+  const float Dd = (valid && a.D) ? a.D[d] : 0.f;
+  float An[4];  // A of this thread's states (Delta is staged in log2 units)
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int n = 4 * g + k;
+    An[k] = (valid && n < N) ? a.A[(long long)d * N + n] : 0.f;
+  }
+
+  // ---- stage tile `it`: per-(channel, step) inputs and B, C (zeros past L / dim / N)
+  auto stage = [&](int it, bool need_all) {
+    const int t0 = it * kBT;
+    for (int e = tid; e < kBDT * kBT; e += kBThreads) {
+      const int ch = e / kBT, s = e % kBT, t = t0 + s;
+      const bool in = d0 + ch < dim && t < L;
+      const long long idx = ((long long)b * dim + d0 + ch) * L + t;
+      float uv = 0.f, dv = 0.f, zv = 0.f, dov = 0.f;
+      if (in) {
+        uv = to_f32(gu[idx]);
+        dv = to_f32(gdel[idx]);
+        if (need_all) {
+          if (gz) zv = to_f32(gz[idx]);
+          dov = to_f32(gdo[idx]);
+        }
+      }
+      float D = 0.f, sgv = 0.f;
+      if (in) {
+        const float v = dv + ((a.delta_bias) ? a.delta_bias[d0 + ch] : 0.f);
+        if (a.delta_softplus) {
+          D = softplus_f<PRECISE>(v);
+          sgv = 1.0f / (1.0f + ex2_approx(-v * kLog2e));
+        } else {
+          D = v;
+          sgv = 1.0f;
+        }
+      } else {
+        uv = 0.f;  // identity step: Delta = 0, u = 0
+      }
+      S.Dl[ch][s] = D;
+      S.dl[ch][s] = D * kLog2e;
+      S.uu[ch][s] = uv;
+      S.du[ch][s] = D * uv;
+      S.sg[ch][s] = sgv;
+      S.zz[ch][s] = zv;
+      S.dout[ch][s] = dov;
+    }
+    for (int e = tid; e < kBT * kMaxDstate; e += kBThreads) {
+      const int n = e / kBT, s = e % kBT, t = t0 + s;
+      const bool in = n < N && t < L;
+      const long long idx = ((long long)b * N + n) * L + t;
+      S.Bt[s][n] = in ? to_f32(gB[idx]) : 0.f;
+      S.Ct[s][n] = (in && need_all) ? to_f32(gC[idx]) : 0.f;
+    }
+  };
+
+  // ---- checkpoint pass: the state before every tile
+  float h[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = (valid && a.h0 && 4 * g + k < N) ? a.h0[cc * N + 4 * g + k] : 0.f;
+  for (int it = 0; it < ntiles; ++it) {
+    ckpt[(long long)it * kBThreads + tid] = make_float4(h[0], h[1], h[2], h[3]);
+    __syncthreads();  // previous tile's smem reads are done
+    stage(it, false);
+    __syncthreads();
+    for (int s = 0; s < kBT; ++s) {
+      const float x = S.dl[c][s], w = S.du[c][s];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = fmaf(ex2_approx(x * An[k]), h[k], w * S.Bt[s][4 * g + k]);
+    }
+  }
+
+  // ---- reverse pass
+  float gad[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) gad[k] = (valid && a.dh_last && 4 * g + k < N) ? a.dh_last[cc * N + 4 * g + k] : 0.f;
+  float dA_acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float dD_acc = 0.f, dbias_acc = 0.f;
+  const int ng = kBThreads / kBT;  // threads per step in the channel reductions (8)
+  for (int it = ntiles - 1; it >= 0; --it) {
+    const int t0 = it * kBT;
+    const int tl = min(kBT, L - t0);
+    __syncthreads();  // the previous tile is done with shared memory
+    stage(it, true);
+    const float4 hs = ckpt[(long long)it * kBThreads + tid];
+    __syncthreads();
+    // recompute h_t of the tile, with this group's readout partial
+    {
+      float hh[4] = {hs.x, hs.y, hs.z, hs.w};
+      for (int s = 0; s < kBT; ++s) {
+        const float x = S.dl[c][s], w = S.du[c][s];
+        float p = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          hh[k] = fmaf(ex2_approx(x * An[k]), hh[k], w * S.Bt[s][4 * g + k]);
+          p = fmaf(S.Ct[s][4 * g + k], hh[k], p);
+        }
+        S.hist[s][tid] = make_float4(hh[0], hh[1], hh[2], hh[3]);
+        S.p0[g][c][s] = p;
+      }
+    }
+    __syncthreads();
+    // y, dy, dz for steps 4g .. 4g+3 of channel c
+    for (int s = 4 * g; s < 4 * g + 4; ++s) {
+      const float y = S.p0[0][c][s] + S.p0[1][c][s] + S.p0[2][c][s] + S.p0[3][c][s] + Dd * S.uu[c][s];
+      const float dov = S.dout[c][s];
+      float dyv = dov;
+      if (gz) {
+        const float zv = S.zz[c][s];
+        const float sz = 1.0f / (1.0f + ex2_approx(-zv * kLog2e));
+        dyv = dov * zv * sz;
+        if (valid && s < tl)
+          static_cast<T*>(a.dz)[cc * L + t0 + s] = from_f32<T>(dov * y * sz * (1.0f + zv * (1.0f - sz)));
+      }
+      S.dy[c][s] = dyv;
+      dD_acc = fmaf(dyv, S.uu[c][s], dD_acc);
+    }
+    __syncthreads();
+    // dC_t[n] over the CTA's channels: thread -> (step s, states n, n+1)
+    {
+      const int s = tid / ng, n = 2 * (tid % ng), gg = n / 4, kk = n % 4;
+      float s0 = 0.f, s1 = 0.f;
+      for (int j = 0; j < kBDT; ++j) {
+        const int ch = (j + tid) % kBDT;
+        const float4 hv = S.hist[s][gg * kBDT + ch];
+        const float dyv = S.dy[ch][s];
+        s0 = fmaf(dyv, kk == 0 ? hv.x : hv.z, s0);
+        s1 = fmaf(dyv, kk == 0 ? hv.y : hv.w, s1);
+      }
+      if (s < tl) {
+        float* out = a.ws_dC + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
+        if (n < N) out[(long long)n * L + t0 + s] = s0;
+        if (n + 1 < N) out[(long long)(n + 1) * L + t0 + s] = s1;
+      }
+    }
+    __syncthreads();  // dC has read every h_t; the adjoint walk overwrites them
+    // adjoint walk: steps kBT-1 .. 0 of the tile
+    for (int s = kBT - 1; s >= 0; --s) {
+      const float dyv = S.dy[c][s], x = S.dl[c][s], Dl = S.Dl[c][s], uv = S.uu[c][s];
+      const float4 hp4 = s > 0 ? S.hist[s - 1][tid] : hs;
+      const float hp[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
+      float dup = 0.f, ddp = 0.f, gt[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int n = 4 * g + k;
+        const float Bv = S.Bt[s][n], Cv = S.Ct[s][n];
+        const float e = ex2_approx(x * An[k]);
+        gad[k] = fmaf(Cv, dyv, gad[k]);
+        gt[k] = gad[k];
+        dup = fmaf(gad[k] * Dl, Bv, dup);
+        ddp = fmaf(gad[k], fmaf(An[k] * e, hp[k], Bv * uv), ddp);
+        dA_acc[k] = fmaf(gad[k] * Dl * e, hp[k], dA_acc[k]);
+        gad[k] *= e;
+      }
+      S.hist[s][tid] = make_float4(gt[0], gt[1], gt[2], gt[3]);
+      S.p0[g][c][s] = dup;
+      S.p1[g][c][s] = ddp;
+    }
+    __syncthreads();
+    // dB_t[n] over the CTA's channels from g_t and Delta u
+    {
+      const int s = tid / ng, n = 2 * (tid % ng), gg = n / 4, kk = n % 4;
+      float s0 = 0.f, s1 = 0.f;
+      for (int j = 0; j < kBDT; ++j) {
+        const int ch = (j + tid) % kBDT;
+        const float4 gv = S.hist[s][gg * kBDT + ch];
+        const float w = S.du[ch][s];
+        s0 = fmaf(w, kk == 0 ? gv.x : gv.z, s0);
+        s1 = fmaf(w, kk == 0 ? gv.y : gv.w, s1);
+      }
+      if (s < tl) {
+        float* out = a.ws_dB + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
+        if (n < N) out[(long long)n * L + t0 + s] = s0;
+        if (n + 1 < N) out[(long long)(n + 1) * L + t0 + s] = s1;
+      }
+    }
+    // du, ddelta for steps 4g .. 4g+3 of channel c
+    for (int s = 4 * g; s < 4 * g + 4; ++s) {
+      if (!valid || s >= tl) continue;
+      const float duv = Dd * S.dy[c][s] + S.p0[0][c][s] + S.p0[1][c][s] + S.p0[2][c][s] + S.p0[3][c][s];
+      const float dD = (S.p1[0][c][s] + S.p1[1][c][s] + S.p1[2][c][s] + S.p1[3][c][s]) * S.sg[c][s];
+      static_cast<T*>(a.du)[cc * L + t0 + s] = from_f32<T>(duv);
+      static_cast<T*>(a.ddelta)[cc * L + t0 + s] = from_f32<T>(dD);
+      dbias_acc += dD;
+    }
+  }
+
+  // ---- per-channel results
+  if (valid) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int n = 4 * g + k;
+      if (n < N) {
+        if (a.dh0) a.dh0[cc * N + n] = gad[k];
+        a.ws_dA[cc * N + n] = dA_acc[k];
+      }
+    }
+  }
+  // dD and dbias: the four threads of a channel hold steps 4g .. 4g+3 of every tile
+  __syncthreads();
+  S.p0[g][c][0] = dD_acc;
+  S.p1[g][c][0] = dbias_acc;
+  __syncthreads();
+  if (g == 0 && valid) {
+    a.ws_dD[cc] = S.p0[0][c][0] + S.p0[1][c][0] + S.p0[2][c][0] + S.p0[3][c][0];
+    a.ws_dbias[cc] = S.p1[0][c][0] + S.p1[1][c][0] + S.p1[2][c][0] + S.p1[3][c][0];
+  }
+}
+
+// Sums of the per-CTA partials, in a fixed order:
+//   dB, dC [b, n, t] over the channel tiles of sequence b; dA [d, n], dD, dbias [d] over b.
+__global__ void scan_bwd_reduce_kernel(const ScanBwdArgs a, int ndt) {
+  const long long L = a.seqlen, N = a.dstate;
+  const long long nBC = (long long)a.batch * N * L;
+  const long long nA = (long long)a.dim * N;
+  const long long total = 2 * nBC + nA + 2LL * a.dim;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    if (i < 2 * nBC) {
+      const bool isC = i >= nBC;
+      const long long j = isC ? i - nBC : i;
+      const long long b = j / (N * L), r = j % (N * L);
+      const float* src = isC ? a.ws_dC : a.ws_dB;
+      float s = 0.f;
+      for (int dt = 0; dt < ndt; ++dt) s += src[((b * ndt + dt) * kMaxDstate) * L + r];
+      (isC ? a.dC : a.dB)[j] = s;
+    } else if (i < 2 * nBC + nA) {
+      const long long j = i - 2 * nBC;  // d * N + n
+      float s = 0.f;
+      for (int b = 0; b < a.batch; ++b) s += a.ws_dA[(long long)b * nA + j];
+      a.dA[j] = s;
+    } else {
+      const long long j = i - 2 * nBC - nA;
+      const bool isBias = j >= a.dim;
+      const long long dd = isBias ? j - a.dim : j;
+      const float* src = isBias ? a.ws_dbias : a.ws_dD;
+      float s = 0.f;
+      for (int b = 0; b < a.batch; ++b) s += src[(long long)b * a.dim + dd];
+      float* dst = isBias ? a.ddelta_bias : a.dD;
+      if (dst) dst[dd] = s;
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_bwd_t(const ScanBwdArgs& a, cudaStream_t stream) {
+  const size_t smem = sizeof(BwdSmem);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    err = cudaFuncSetAttribute(scan_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  const int ndt = (a.dim + kBDT - 1) / kBDT;
+  scan_bwd_kernel<T><<<dim3(ndt, a.batch), kBThreads, smem, stream>>>(a);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const long long total = 2LL * a.batch * a.dstate * a.seqlen + (long long)a.dim * a.dstate + 2LL * a.dim;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 148 * 16) blocks = 148 * 16;
+  if (blocks < 1) blocks = 1;
+  scan_bwd_reduce_kernel<<<(unsigned)blocks, threads, 0, stream>>>(a, ndt);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen) {
+  const long long ndt = (dim + kBDT - 1) / kBDT;
+  const long long ntiles = (seqlen + kBT - 1) / kBT;
+  auto up = [](long long v) { return (size_t)((v + 255) & ~255LL); };
+  size_t s = up(batch * ndt * ntiles * kBThreads * 16LL);                 // checkpoints
+  s += 2 * up(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);        // dB, dC partials
+  s += up((long long)batch * dim * kMaxDstate * 4LL);                     // dA partials
+  s += 2 * up((long long)batch * dim * 4LL);                              // dD, dbias partials
+  return s;
+}
+
+void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, ScanBwdArgs& a) {
+  const long long ndt = (dim + kBDT - 1) / kBDT;
+  const long long ntiles = (seqlen + kBT - 1) / kBT;
+  auto up = [](long long v) { return (size_t)((v + 255) & ~255LL); };
+  char* p = static_cast<char*>(ws);
+  a.ws_ckpt = reinterpret_cast<float*>(p);
+  p += up(batch * ndt * ntiles * kBThreads * 16LL);
+  a.ws_dB = reinterpret_cast<float*>(p);
+  p += up(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);
+  a.ws_dC = reinterpret_cast<float*>(p);
+  p += up(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);
+  a.ws_dA = reinterpret_cast<float*>(p);
+  p += up((long long)batch * dim * kMaxDstate * 4LL);
+  a.ws_dD = reinterpret_cast<float*>(p);
+  p += up((long long)batch * dim * 4LL);
+  a.ws_dbias = reinterpret_cast<float*>(p);
+}
+
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream) {
+  if (a.bf16) return launch_bwd_t<__nv_bfloat16>(a, stream);
+  return launch_bwd_t<float>(a, stream);
+}
+
+}  // namespace ssm

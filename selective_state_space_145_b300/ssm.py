@@ -28,7 +28,7 @@ _lib = None
 # Exported C symbols, as declared in include/ssm.h.
 EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_scan_default_chunk_len",
            "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update",
-           "ssm_selective_scan_fwd_noalloc")
+           "ssm_selective_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_selective_scan_bwd")
 
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -71,6 +71,11 @@ def lib() -> ctypes.CDLL:
         L.ssm_selective_scan_fwd_noalloc.restype = i
         L.ssm_selective_scan_fwd_noalloc.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, vp, fp, vp]
                                                      + [i] * 6 + [u, vp])
+        L.ssm_scan_bwd_workspace_bytes.restype = sz
+        L.ssm_scan_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.ssm_selective_scan_bwd.restype = i
+        L.ssm_selective_scan_bwd.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, vp, fp]
+                                             + [vp, vp, vp, fp, fp, fp, fp, fp, fp] + [i] * 5 + [vp, sz, u, vp])
         L.ssm_selective_state_update.restype = i
         L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
                                                  i, i, i, i, u, vp]
@@ -214,6 +219,56 @@ def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor
     if return_conv_state:
         res = res + (conv_state_out,)
     return res
+
+
+def ssm_scan_bwd_workspace_bytes(batch: int, dim: int, seqlen: int, dstate: int, io) -> int:
+    return int(lib().ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate, _DTYPE_CODE[io]))
+
+
+def ssm_selective_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                           C: torch.Tensor, dout: torch.Tensor, D: Optional[torch.Tensor] = None,
+                           z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+                           delta_softplus: bool = True, h0: Optional[torch.Tensor] = None,
+                           dh_last: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, grads: Optional[dict] = None) -> dict:
+    """Backward pass of the forward-time Euler scan with u given directly. Returns a dict with
+    du, ddelta, dz (None without z) in the io dtype and dA, dB, dC, dD, ddelta_bias, dh0 in
+    float32 (dD / ddelta_bias None when D / delta_bias are None). ``grads``: a dict of the same
+    keys to write into instead of allocating (a previous call's result)."""
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev, io = u.device, u.dtype
+    for t, name, shape, dt in ((u, "u", (batch, dim, L), io), (delta, "delta", (batch, dim, L), io),
+                               (A, "A", (dim, N), torch.float32), (B, "B", (batch, N, L), io),
+                               (C, "C", (batch, N, L), io), (dout, "dout", (batch, dim, L), io)):
+        _need(t, name, shape, dt, dev)
+    _need(D, "D", (dim,), torch.float32, dev, optional=True)
+    _need(z, "z", (batch, dim, L), io, dev, optional=True)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    _need(h0, "h0", (batch, dim, N), torch.float32, dev, optional=True)
+    _need(dh_last, "dh_last", (batch, dim, N), torch.float32, dev, optional=True)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = grads if grads is not None else {"du": torch.empty_like(u), "ddelta": torch.empty_like(u), "dz": torch.empty_like(u) if z is not None else None,
+         "dA": torch.empty(dim, N, **f32), "dB": torch.empty(batch, N, L, **f32), "dC": torch.empty(batch, N, L, **f32),
+         "dD": torch.empty(dim, **f32) if D is not None else None,
+         "ddelta_bias": torch.empty(dim, **f32) if delta_bias is not None else None,
+         "dh0": torch.empty(batch, dim, N, **f32)}
+    for name, shape, dt in (("du", (batch, dim, L), io), ("ddelta", (batch, dim, L), io),
+                            ("dA", (dim, N), torch.float32), ("dB", (batch, N, L), torch.float32),
+                            ("dC", (batch, N, L), torch.float32), ("dh0", (batch, dim, N), torch.float32)):
+        _need(g[name], name, shape, dt, dev)
+    _need(g["dz"], "dz", (batch, dim, L), io, dev, optional=z is None)
+    need = ssm_scan_bwd_workspace_bytes(batch, dim, L, N, io)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().ssm_selective_scan_bwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)),
+        _ptr(h0), _ptr(dout), _ptr(dh_last), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dz"]), _ptr(g["dA"]),
+        _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
+        batch, dim, L, N, _io_code(u), _ptr(workspace), ws_bytes, 0, _stream(dev))
+    _check("ssm_selective_scan_bwd", st)
+    return g
 
 
 def ssm_selective_state_update(state: torch.Tensor, conv_state: Optional[torch.Tensor], x: torch.Tensor,

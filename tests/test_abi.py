@@ -102,6 +102,19 @@ def test_workspace_query(L):
     assert cl % 64 == 0 and 256 <= cl <= 131072
 
 
+def test_backward_argument_checks(L):
+    f = L.ssm_selective_scan_bwd
+    # u, delta, A, B, C, D, z, bias, sp, h0, dout, dh_last, du, ddelta, dz, dA, dB, dC, dD, dbias, dh0,
+    # batch, dim, seqlen, dstate, io, ws, ws_bytes, flags, stream
+    base = [FAKE] * 5 + [None, None, None, 1, None, FAKE, None] + [FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None,
+                                                                     None] + [1, 4, 8, 16, 0, FAKE, 1 << 30, 0, None]
+    for i, v, want in ((0, None, 1), (15, None, 1), (24, 17, 2), (25, 7, 2), (28, 1, 2), (28, 2, 2), (28, 4, 1),
+                       (6, FAKE, 1), (27, 0, 1), (0, FAKE + 2, 2)):
+        bad = list(base)
+        bad[i] = v
+        assert f(*bad) == want, (i, v)
+
+
 def test_decode_and_conv_argument_checks(L):
     f = L.ssm_selective_state_update
     base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, FAKE, None, 4, FAKE, 2, 8, 16, 1, 0, None]

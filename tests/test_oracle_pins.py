@@ -330,6 +330,69 @@ def test_zoh_decode_equals_scan():
     np.testing.assert_array_equal(win, cs)
 
 
+# ---------------------------------------------------------------- backward pass
+
+def _bwd_problem(b=2, d=3, L=9, N=3):
+    return dict(u=_rand(b, d, L), delta=0.7 * _rand(b, d, L), A=_neg_A(d, N), B=_rand(b, N, L),
+                C=_rand(b, N, L), D=_rand(d), z=_rand(b, d, L), delta_bias=_rand(d) - 1.0, h0=_rand(b, d, N))
+
+
+def _loss(p, dout, dhl):
+    out, hL = oracle.selective_scan(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
+                                    True, h0=p["h0"])
+    return float(np.sum(dout * out) + np.sum(dhl * hL))
+
+
+def test_backward_matches_finite_differences():
+    """Every gradient of L = sum(dout * out) + sum(dh_last * h_last) against central differences
+    of the forward oracle, element by element."""
+    p = _bwd_problem()
+    dout, dhl = _rand(*p["u"].shape), _rand(*p["h0"].shape)
+    g = oracle.selective_scan_bwd(p["u"], p["delta"], p["A"], p["B"], p["C"], dout, p["D"], p["z"],
+                                  p["delta_bias"], True, p["h0"], dhl)
+    names = {"u": "du", "delta": "ddelta", "z": "dz", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "delta_bias": "ddelta_bias", "h0": "dh0"}
+    eps = 1e-6
+    for key, gk in names.items():
+        num = np.empty_like(p[key])
+        for idx in np.ndindex(p[key].shape):
+            q = {k: v.copy() for k, v in p.items()}
+            q[key][idx] += eps
+            lp = _loss(q, dout, dhl)
+            q[key][idx] -= 2 * eps
+            lm = _loss(q, dout, dhl)
+            num[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[gk], num, rtol=1e-6, atol=1e-7, err_msg=key)
+
+
+def _torch_scan(u, delta, A, B, C, D, z, bias, h0):
+    """The forward as tensor algebra over all channels at once (independent of the C oracle)."""
+    Dl = F.softplus(delta + bias[None, :, None])                  # [b, d, L]
+    h = h0
+    ys = []
+    for t in range(u.shape[-1]):
+        Ab = torch.exp(Dl[:, :, t, None] * A[None])               # [b, d, N]
+        h = Ab * h + Dl[:, :, t, None] * B[:, None, :, t] * u[:, :, t, None]
+        ys.append((h * C[:, None, :, t]).sum(-1) + D[None] * u[:, :, t])
+    y = torch.stack(ys, dim=-1)
+    return y * F.silu(z), h
+
+
+def test_backward_matches_autograd():
+    """The oracle's gradients equal torch autograd through an independent fp64 forward."""
+    p = _bwd_problem(b=2, d=4, L=17, N=5)
+    dout, dhl = _rand(*p["u"].shape), _rand(*p["h0"].shape)
+    tp = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in p.items()}
+    out, hL = _torch_scan(tp["u"], tp["delta"], tp["A"], tp["B"], tp["C"], tp["D"], tp["z"], tp["delta_bias"],
+                          tp["h0"])
+    ((out * torch.tensor(dout)).sum() + (hL * torch.tensor(dhl)).sum()).backward()
+    g = oracle.selective_scan_bwd(p["u"], p["delta"], p["A"], p["B"], p["C"], dout, p["D"], p["z"],
+                                  p["delta_bias"], True, p["h0"], dhl)
+    for key, gk in {"u": "du", "delta": "ddelta", "z": "dz", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+                    "delta_bias": "ddelta_bias", "h0": "dh0"}.items():
+        np.testing.assert_allclose(g[gk], tp[key].grad.numpy(), rtol=1e-11, atol=1e-12, err_msg=key)
+
+
 # ---------------------------------------------------------------- invariants
 
 def _problem(b=2, d=3, L=21, N=4, K=4):
