@@ -364,9 +364,11 @@ cudaError_t launch_tile(const DecodeArgs& a, cudaStream_t stream) {
     if (per_sm < 1) per_sm = 1;
     if (dev >= 0 && dev < 64) resident[dev] = per_sm;
   }
+  // as many sequence groups per channel tile as keep every CTA resident in one wave (a
+  // rounded-up count would leave a few CTAs for a second wave)
   const int n_ctiles = (a.dim + kTileCh - 1) / kTileCh;
   long long want = (long long)sms * per_sm;
-  int row_groups = (int)((want + n_ctiles - 1) / n_ctiles);
+  int row_groups = (int)(want / n_ctiles);
   if (row_groups > a.batch) row_groups = a.batch;
   if (row_groups < 1) row_groups = 1;
   kern<<<(unsigned)(n_ctiles * row_groups), kTileCh, smem, stream>>>(a, n_ctiles, row_groups);
