@@ -16,11 +16,12 @@
 // Design. One CTA = 32 channels of one sequence, the whole sequence, 128 threads; thread
 // (c, g) holds states 4g .. 4g+3 of channel c, as in the forward kernel.
 //  * Checkpoint pass: the forward recurrence (no readout) over the sequence, writing the state
-//    before every 16-step tile to the workspace.
+//    before every 16-step tile to the workspace. Each tile's global loads are issued into
+//    registers one tile ahead, so they complete while the previous tile computes.
 //  * Reverse pass, tile by tile from the end: stage the tile's u, delta, z, dout rows and B, C;
-//    recompute h_t of the 16 steps from the tile's checkpoint into shared memory, with the
+//    recompute h_t of the tile's steps from its checkpoint into shared memory, with the
 //    readout partials that give y_t; then dy, dz; the channel sums of dC_t over the CTA's 32
-//    channels; the adjoint walk (16 steps backward, four states per thread in registers),
+//    channels; the adjoint walk (backward over the tile, four states per thread in registers),
 //    which leaves g_t in the slot of h_t; the channel sums of dB_t; and du, ddelta.
 //  * dA, dD and dbias accumulate per channel in registers. dB, dC, dA, dD, dbias are written as
 //    per-CTA partials and summed over channel tiles / sequences by a second kernel in a fixed
@@ -36,6 +37,8 @@ constexpr int kBDT = 32;        // channels per CTA
 constexpr int kBT = 16;         // steps per tile
 constexpr int kBTP = kBT + 1;   // padded row of the per-(channel, step) arrays
 static_assert(kBThreads == kBDT * 4, "four threads per channel");
+constexpr int kOut = kBT * kMaxDstate / kBThreads;  // (step, state) channel sums per thread
+static_assert(kOut >= 1 && kMaxDstate % kOut == 0 && 4 % kOut == 0, "channel-sum mapping");
 
 struct BwdSmem {
   float4 hist[kBT][kBThreads];        // h_t of the tile, then the adjoint g_t
@@ -84,60 +87,84 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
     An[k] = (valid && n < N) ? a.A[(long long)d * N + n] : 0.f;
   }
 
-  // ---- stage tile `it`: per-(channel, step) inputs and B, C (zeros past L / dim / N)
-  auto stage = [&](int it, bool need_all) {
+  // ---- staging of tile `it`, in two halves: fetch() issues the global loads into registers
+  // (so the next tile's loads are in flight while this tile computes); put() derives Delta,
+  // its softplus derivative and Delta u and stores everything to shared memory (zeros past
+  // L / dim / N: identity steps with Delta = 0 and u = 0).
+  constexpr int kPE = kBDT * kBT / kBThreads;           // per-(channel, step) elements per thread
+  constexpr int kPB = kBT * kMaxDstate / kBThreads;     // B / C elements per thread
+  struct Fetched {
+    float u[kPE], dv[kPE], z[kPE], dout[kPE], B[kPB], C[kPB];
+  };
+  auto fetch = [&](int it, bool need_all, Fetched& f) {
     const int t0 = it * kBT;
-    for (int e = tid; e < kBDT * kBT; e += kBThreads) {
+#pragma unroll
+    for (int k = 0; k < kPE; ++k) {
+      const int e = tid + k * kBThreads;
       const int ch = e / kBT, s = e % kBT, t = t0 + s;
       const bool in = d0 + ch < dim && t < L;
       const long long idx = ((long long)b * dim + d0 + ch) * L + t;
-      float uv = 0.f, dv = 0.f, zv = 0.f, dov = 0.f;
-      if (in) {
-        uv = to_f32(gu[idx]);
-        dv = to_f32(gdel[idx]);
-        if (need_all) {
-          if (gz) zv = to_f32(gz[idx]);
-          dov = to_f32(gdo[idx]);
-        }
-      }
+      f.u[k] = in ? to_f32(gu[idx]) : 0.f;
+      f.dv[k] = in ? to_f32(gdel[idx]) : 0.f;
+      f.z[k] = (in && need_all && gz) ? to_f32(gz[idx]) : 0.f;
+      f.dout[k] = (in && need_all) ? to_f32(gdo[idx]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kPB; ++k) {
+      const int e = tid + k * kBThreads;
+      const int n = e / kBT, s = e % kBT, t = t0 + s;
+      const bool in = n < N && t < L;
+      const long long idx = ((long long)b * N + n) * L + t;
+      f.B[k] = in ? to_f32(gB[idx]) : 0.f;
+      f.C[k] = (in && need_all) ? to_f32(gC[idx]) : 0.f;
+    }
+  };
+  auto put = [&](int it, const Fetched& f) {
+    const int t0 = it * kBT;
+#pragma unroll
+    for (int k = 0; k < kPE; ++k) {
+      const int e = tid + k * kBThreads;
+      const int ch = e / kBT, s = e % kBT, t = t0 + s;
+      const bool in = d0 + ch < dim && t < L;
       float D = 0.f, sgv = 0.f;
       if (in) {
-        const float v = dv + ((a.delta_bias) ? a.delta_bias[d0 + ch] : 0.f);
+        const float v = f.dv[k] + ((a.delta_bias) ? a.delta_bias[d0 + ch] : 0.f);
         if (a.delta_softplus) {
           D = softplus_f<PRECISE>(v);
-          sgv = 1.0f / (1.0f + ex2_approx(-v * kLog2e));
+          sgv = rcp_approx(1.0f + ex2_approx(-v * kLog2e));
         } else {
           D = v;
           sgv = 1.0f;
         }
-      } else {
-        uv = 0.f;  // identity step: Delta = 0, u = 0
       }
       S.Dl[ch][s] = D;
       S.dl[ch][s] = D * kLog2e;
-      S.uu[ch][s] = uv;
-      S.du[ch][s] = D * uv;
+      S.uu[ch][s] = f.u[k];
+      S.du[ch][s] = D * f.u[k];
       S.sg[ch][s] = sgv;
-      S.zz[ch][s] = zv;
-      S.dout[ch][s] = dov;
+      S.zz[ch][s] = f.z[k];
+      S.dout[ch][s] = f.dout[k];
     }
-    for (int e = tid; e < kBT * kMaxDstate; e += kBThreads) {
-      const int n = e / kBT, s = e % kBT, t = t0 + s;
-      const bool in = n < N && t < L;
-      const long long idx = ((long long)b * N + n) * L + t;
-      S.Bt[s][n] = in ? to_f32(gB[idx]) : 0.f;
-      S.Ct[s][n] = (in && need_all) ? to_f32(gC[idx]) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kPB; ++k) {
+      const int e = tid + k * kBThreads;
+      const int n = e / kBT, s = e % kBT;
+      S.Bt[s][n] = f.B[k];
+      S.Ct[s][n] = f.C[k];
     }
   };
+  Fetched fb;
 
   // ---- checkpoint pass: the state before every tile
   float h[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) h[k] = (valid && a.h0 && 4 * g + k < N) ? a.h0[cc * N + 4 * g + k] : 0.f;
+  if (ntiles > 0) fetch(0, false, fb);
   for (int it = 0; it < ntiles; ++it) {
     ckpt[(long long)it * kBThreads + tid] = make_float4(h[0], h[1], h[2], h[3]);
     __syncthreads();  // previous tile's smem reads are done
-    stage(it, false);
+    put(it, fb);
+    if (it + 1 < ntiles) fetch(it + 1, false, fb);
     __syncthreads();
     for (int s = 0; s < kBT; ++s) {
       const float x = S.dl[c][s], w = S.du[c][s];
@@ -152,13 +179,18 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
   for (int k = 0; k < 4; ++k) gad[k] = (valid && a.dh_last && 4 * g + k < N) ? a.dh_last[cc * N + 4 * g + k] : 0.f;
   float dA_acc[4] = {0.f, 0.f, 0.f, 0.f};
   float dD_acc = 0.f, dbias_acc = 0.f;
-  const int ng = kBThreads / kBT;  // threads per step in the channel reductions (8)
+  // channel sums: thread -> step tid / (16 / kOut), states n0 .. n0 + kOut - 1 of one group
+  const int rs = tid / (kMaxDstate / kOut), rn0 = kOut * (tid % (kMaxDstate / kOut));
+  const int rg = rn0 / 4, rk = rn0 % 4;
+  auto comp = [](const float4& v, int k) { return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w)); };
+  if (ntiles > 0) fetch(ntiles - 1, true, fb);
   for (int it = ntiles - 1; it >= 0; --it) {
     const int t0 = it * kBT;
     const int tl = min(kBT, L - t0);
     __syncthreads();  // the previous tile is done with shared memory
-    stage(it, true);
+    put(it, fb);
     const float4 hs = ckpt[(long long)it * kBThreads + tid];
+    if (it > 0) fetch(it - 1, true, fb);
     __syncthreads();
     // recompute h_t of the tile, with this group's readout partial
     {
@@ -176,14 +208,15 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
       }
     }
     __syncthreads();
-    // y, dy, dz for steps 4g .. 4g+3 of channel c
-    for (int s = 4 * g; s < 4 * g + 4; ++s) {
+    // y, dy, dz for this thread's steps of channel c
+    constexpr int kSPT = kBT / 4;  // steps per thread
+    for (int s = kSPT * g; s < kSPT * g + kSPT; ++s) {
       const float y = S.p0[0][c][s] + S.p0[1][c][s] + S.p0[2][c][s] + S.p0[3][c][s] + Dd * S.uu[c][s];
       const float dov = S.dout[c][s];
       float dyv = dov;
       if (gz) {
         const float zv = S.zz[c][s];
-        const float sz = 1.0f / (1.0f + ex2_approx(-zv * kLog2e));
+        const float sz = rcp_approx(1.0f + ex2_approx(-zv * kLog2e));
         dyv = dov * zv * sz;
         if (valid && s < tl)
           static_cast<T*>(a.dz)[cc * L + t0 + s] = from_f32<T>(dov * y * sz * (1.0f + zv * (1.0f - sz)));
@@ -192,21 +225,23 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
       dD_acc = fmaf(dyv, S.uu[c][s], dD_acc);
     }
     __syncthreads();
-    // dC_t[n] over the CTA's channels: thread -> (step s, states n, n+1)
+    // dC_t[n] over the CTA's channels
     {
-      const int s = tid / ng, n = 2 * (tid % ng), gg = n / 4, kk = n % 4;
-      float s0 = 0.f, s1 = 0.f;
+      float acc[kOut];
+#pragma unroll
+      for (int o = 0; o < kOut; ++o) acc[o] = 0.f;
       for (int j = 0; j < kBDT; ++j) {
         const int ch = (j + tid) % kBDT;
-        const float4 hv = S.hist[s][gg * kBDT + ch];
-        const float dyv = S.dy[ch][s];
-        s0 = fmaf(dyv, kk == 0 ? hv.x : hv.z, s0);
-        s1 = fmaf(dyv, kk == 0 ? hv.y : hv.w, s1);
+        const float4 hv = S.hist[rs][rg * kBDT + ch];
+        const float dyv = S.dy[ch][rs];
+#pragma unroll
+        for (int o = 0; o < kOut; ++o) acc[o] = fmaf(dyv, comp(hv, rk + o), acc[o]);
       }
-      if (s < tl) {
+      if (rs < tl) {
         float* out = a.ws_dC + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
-        if (n < N) out[(long long)n * L + t0 + s] = s0;
-        if (n + 1 < N) out[(long long)(n + 1) * L + t0 + s] = s1;
+#pragma unroll
+        for (int o = 0; o < kOut; ++o)
+          if (rn0 + o < N) out[(long long)(rn0 + o) * L + t0 + rs] = acc[o];
       }
     }
     __syncthreads();  // dC has read every h_t; the adjoint walk overwrites them
@@ -235,23 +270,25 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
     __syncthreads();
     // dB_t[n] over the CTA's channels from g_t and Delta u
     {
-      const int s = tid / ng, n = 2 * (tid % ng), gg = n / 4, kk = n % 4;
-      float s0 = 0.f, s1 = 0.f;
+      float acc[kOut];
+#pragma unroll
+      for (int o = 0; o < kOut; ++o) acc[o] = 0.f;
       for (int j = 0; j < kBDT; ++j) {
         const int ch = (j + tid) % kBDT;
-        const float4 gv = S.hist[s][gg * kBDT + ch];
-        const float w = S.du[ch][s];
-        s0 = fmaf(w, kk == 0 ? gv.x : gv.z, s0);
-        s1 = fmaf(w, kk == 0 ? gv.y : gv.w, s1);
+        const float4 gv = S.hist[rs][rg * kBDT + ch];
+        const float w = S.du[ch][rs];
+#pragma unroll
+        for (int o = 0; o < kOut; ++o) acc[o] = fmaf(w, comp(gv, rk + o), acc[o]);
       }
-      if (s < tl) {
+      if (rs < tl) {
         float* out = a.ws_dB + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
-        if (n < N) out[(long long)n * L + t0 + s] = s0;
-        if (n + 1 < N) out[(long long)(n + 1) * L + t0 + s] = s1;
+#pragma unroll
+        for (int o = 0; o < kOut; ++o)
+          if (rn0 + o < N) out[(long long)(rn0 + o) * L + t0 + rs] = acc[o];
       }
     }
-    // du, ddelta for steps 4g .. 4g+3 of channel c
-    for (int s = 4 * g; s < 4 * g + 4; ++s) {
+    // du, ddelta for this thread's steps of channel c
+    for (int s = kSPT * g; s < kSPT * g + kSPT; ++s) {
       if (!valid || s >= tl) continue;
       const float duv = Dd * S.dy[c][s] + S.p0[0][c][s] + S.p0[1][c][s] + S.p0[2][c][s] + S.p0[3][c][s];
       const float dD = (S.p1[0][c][s] + S.p1[1][c][s] + S.p1[2][c][s] + S.p1[3][c][s]) * S.sg[c][s];
@@ -272,7 +309,7 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
       }
     }
   }
-  // dD and dbias: the four threads of a channel hold steps 4g .. 4g+3 of every tile
+  // dD and dbias: the four threads of a channel each hold a quarter of every tile's steps
   __syncthreads();
   S.p0[g][c][0] = dD_acc;
   S.p1[g][c][0] = dbias_acc;
