@@ -56,6 +56,19 @@ int default_chunk_len_impl(int batch, int dim, int seqlen, bool bf16) {
   return (int)round_up((seqlen + q - 1) / q, kChunkQuantum);
 }
 
+// Chunk length of the backward pass: the same one-wave rule, with the backward kernel's occupancy.
+int bwd_chunk_len(int batch, int dim, int seqlen, bool bf16) {
+  const long long ctas = ((dim + 31) / 32) * (long long)batch;
+  const long long resident = (long long)sm_count() * ssm::scan_bwd_resident_ctas_per_sm(bf16);
+  const long long whole = round_up(seqlen > 0 ? seqlen : 1, kChunkQuantum);
+  if (ctas <= 0 || 2 * ctas > resident) return (int)whole;
+  long long q = resident / ctas;
+  const long long qmax = (seqlen + kChunkQuantum - 1) / kChunkQuantum;
+  if (q > qmax) q = qmax;
+  if (q <= 1) return (int)whole;
+  return (int)round_up((seqlen + q - 1) / q, kChunkQuantum);
+}
+
 int nchunks_for(int seqlen, int chunk_len) {
   if (seqlen <= 0) return 1;
   return (int)((seqlen + (long long)chunk_len - 1) / chunk_len);
@@ -223,9 +236,9 @@ ssm_status ssm_selective_state_update(float* state, void* conv_state, const void
 
 size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int dstate, ssm_dtype io) {
   (void)dstate;
-  (void)io;
   if (batch <= 0 || dim <= 0 || seqlen < 0) return 0;
-  return ssm::scan_bwd_workspace_bytes(batch, dim, seqlen);
+  const int cl = bwd_chunk_len(batch, dim, seqlen, io == SSM_BF16);
+  return ssm::scan_bwd_workspace_bytes(batch, dim, seqlen, nchunks_for(seqlen, cl));
 }
 
 ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
@@ -252,7 +265,10 @@ ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float*
   const void* f_ptrs[] = {A, D, delta_bias, h0, dh_last, dA, dB, dC, dD, ddelta_bias, dh0};
   for (const void* p : f_ptrs)
     if (p && !aligned(p, 4)) return SSM_ERR_UNSUPPORTED;
-  const size_t need = ssm::scan_bwd_workspace_bytes(batch, dim, seqlen);
+  // time is cut into chunks when the channels alone leave SMs idle (as in the forward pass)
+  const int cl = bwd_chunk_len(batch, dim, seqlen, io == SSM_BF16);
+  const int nchunks = nchunks_for(seqlen, cl);
+  const size_t need = ssm::scan_bwd_workspace_bytes(batch, dim, seqlen, nchunks);
   if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return SSM_ERR_UNSUPPORTED;
   ssm::ScanBwdArgs a;
@@ -261,8 +277,24 @@ ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float*
   a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD;
   a.ddelta_bias = ddelta_bias; a.dh0 = dh0;
   a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.dstate = dstate; a.bf16 = io == SSM_BF16;
-  ssm::scan_bwd_workspace_split(workspace, batch, dim, seqlen, a);
-  return ssm::launch_scan_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  a.chunk_len = cl;
+  a.nchunks = nchunks;
+  ssm::scan_bwd_workspace_split(workspace, batch, dim, seqlen, nchunks, a);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (nchunks > 1) {
+    // forward carries of chunks 0 .. nchunks-2: the chunk-start states of the checkpoint pass
+    ssm::ScanArgs f;
+    f.x = u; f.delta = delta; f.A = A; f.B = B; f.C = C; f.D = nullptr; f.z = nullptr; f.delta_bias = delta_bias;
+    f.delta_softplus = delta_softplus; f.conv_w = nullptr; f.conv_b = nullptr; f.d_conv = 0; f.conv_init = nullptr;
+    f.h0 = nullptr; f.out = nullptr; f.h_last = nullptr; f.conv_state_out = nullptr;
+    f.batch = batch; f.dim = dim; f.seqlen = seqlen; f.dstate = dstate; f.bf16 = io == SSM_BF16;
+    f.vec = ((long long)seqlen * (long long)es) % 16 == 0 && aligned(u, 16) && aligned(delta, 16) &&
+            aligned(B, 16) && aligned(C, 16);
+    f.chunk_len = cl; f.nchunks = nchunks; f.reverse = 0; f.zoh = 0;
+    f.ws_S = const_cast<float*>(a.fS); f.ws_h = const_cast<float*>(a.fh);
+    if (ssm::launch_scan_carry(f, st) != cudaSuccess) return SSM_ERR_CUDA;
+  }
+  return ssm::launch_scan_bwd(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // extern "C"

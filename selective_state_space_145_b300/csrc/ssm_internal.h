@@ -99,12 +99,18 @@ struct ScanBwdArgs {
   float* dh0;
   int batch, dim, seqlen, dstate;
   int bf16;
+  int chunk_len;         // multiple of 64; the sequence is cut into nchunks chunks
+  int nchunks;
+  const float* fS;       // forward carries [nchunks-1][batch*dim]: sum of Delta' per chunk
+  const float* fh;       // [nchunks-1][batch*dim][16]: chunk end state from zero
+  float* bS;             // backward carries [nchunks][batch*dim] (chunk 0 unused): sum of Delta'
+  float* bh;             // [nchunks][batch*dim][16]: adjoint leaving the chunk's start, from zero
   float* ws_ckpt;        // [batch][channel tiles][tiles][128 threads] float4: state before each tile
   float* ws_dB;          // [batch][channel tiles][16][seqlen] per-CTA channel sums
   float* ws_dC;
-  float* ws_dA;          // [batch][dim][16]
-  float* ws_dD;          // [batch][dim]
-  float* ws_dbias;       // [batch][dim]
+  float* ws_dA;          // [nchunks][batch][dim][16]
+  float* ws_dD;          // [nchunks][batch][dim]
+  float* ws_dbias;       // [nchunks][batch][dim]
 };
 
 // Channels one scan CTA covers.
@@ -117,8 +123,11 @@ size_t scan_workspace_bytes(long long channels, int nchunks);
 void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, float** h);
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
-size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen);
-void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, ScanBwdArgs& a);
+// the forward chunk carries only (ws_S, ws_h for chunks 0 .. nchunks-2; no conv, forward time)
+cudaError_t launch_scan_carry(const ScanArgs& a, cudaStream_t stream);
+size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int nchunks);
+void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, int nchunks, ScanBwdArgs& a);
+int scan_bwd_resident_ctas_per_sm(bool bf16);
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -665,6 +665,16 @@ void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, 
   *h = reinterpret_cast<float*>(static_cast<char*>(ws) + s_bytes);
 }
 
+cudaError_t launch_scan_carry(const ScanArgs& a, cudaStream_t stream) {
+  // the forward carries alone (chunks 0 .. nchunks-2), forward time, Euler, no conv
+  if (a.nchunks <= 1) return cudaSuccess;
+  if (a.bf16)
+    return a.vec ? launch_one<__nv_bfloat16, false, true, true, false, false>(a, a.nchunks - 1, false, stream)
+                 : launch_one<__nv_bfloat16, false, false, true, false, false>(a, a.nchunks - 1, false, stream);
+  return a.vec ? launch_one<float, false, true, true, false, false>(a, a.nchunks - 1, false, stream)
+               : launch_one<float, false, false, true, false, false>(a, a.nchunks - 1, false, stream);
+}
+
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
   if (a.bf16) return dispatch<__nv_bfloat16>(a, stream);
   return dispatch<float>(a, stream);

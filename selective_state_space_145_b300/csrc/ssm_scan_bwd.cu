@@ -56,8 +56,11 @@ struct BwdSmem {
   float p1[4][kBDT][kBTP];            // per-state-group partials of dDelta
 };
 
-template <typename T>
-__global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArgs a) {
+// ADJ: the adjoint carry of one chunk (chunks 1 .. nchunks-1): the adjoint walked backward over
+// the chunk from zero with its own dy_t C_t inputs, and the chunk's sum of Delta', so that every
+// chunk can start from the composed adjoint of the chunks after it.
+template <typename T, bool ADJ>
+__global__ void __launch_bounds__(kBThreads, 3) scan_bwd_kernel(const ScanBwdArgs a) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem& S = *reinterpret_cast<BwdSmem*>(smem_raw);
@@ -69,6 +72,11 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
   const bool valid = d < dim;
   const long long cc = (long long)b * dim + d;
   const int ntiles = (L + kBT - 1) / kBT;
+  const int Q = a.nchunks;
+  const int q = ADJ ? blockIdx.z + 1 : blockIdx.z;   // chunk; chunk boundaries are tile boundaries
+  const int it_begin = q * (a.chunk_len / kBT);
+  const int it_end = min(ntiles, it_begin + a.chunk_len / kBT);
+  const long long BD = (long long)a.batch * dim;
   const long long cta = (long long)b * gridDim.x + dtile;
   float4* ckpt = reinterpret_cast<float4*>(a.ws_ckpt) + cta * (long long)ntiles * kBThreads;
 
@@ -155,16 +163,26 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
   };
   Fetched fb;
 
-  // ---- checkpoint pass: the state before every tile
+  // ---- checkpoint pass: the state before every tile of the chunk, from the chunk's start
+  // state h0 o carry_0 o ... o carry_{q-1} (forward carries: a = 2^(A sum Delta'), b = end state)
   float h[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) h[k] = (valid && a.h0 && 4 * g + k < N) ? a.h0[cc * N + 4 * g + k] : 0.f;
-  if (ntiles > 0) fetch(0, false, fb);
-  for (int it = 0; it < ntiles; ++it) {
+  if (!ADJ && valid) {
+    for (int j = 0; j < q; ++j) {
+      const float Sj = a.fS[(long long)j * BD + cc];
+      const float4 hb = *reinterpret_cast<const float4*>(a.fh + ((long long)j * BD + cc) * kMaxDstate + 4 * g);
+      const float hbv[4] = {hb.x, hb.y, hb.z, hb.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = fmaf(ex2_approx(Sj * An[k]), h[k], hbv[k]);
+    }
+  }
+  if (!ADJ && it_begin < it_end) fetch(it_begin, false, fb);
+  for (int it = it_begin; it < (ADJ ? it_begin : it_end); ++it) {
     ckpt[(long long)it * kBThreads + tid] = make_float4(h[0], h[1], h[2], h[3]);
     __syncthreads();  // previous tile's smem reads are done
     put(it, fb);
-    if (it + 1 < ntiles) fetch(it + 1, false, fb);
+    if (it + 1 < it_end) fetch(it + 1, false, fb);
     __syncthreads();
     for (int s = 0; s < kBT; ++s) {
       const float x = S.dl[c][s], w = S.du[c][s];
@@ -173,25 +191,59 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
     }
   }
 
-  // ---- reverse pass
-  float gad[4];
+  // ---- reverse pass. The adjoint entering the chunk's end: dh_last composed with the adjoint
+  // carries of chunks nchunks-1 .. q+1 (ADJ: zero)
+  float gad[4] = {0.f, 0.f, 0.f, 0.f};
+  if (!ADJ) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) gad[k] = (valid && a.dh_last && 4 * g + k < N) ? a.dh_last[cc * N + 4 * g + k] : 0.f;
+    for (int k = 0; k < 4; ++k) gad[k] = (valid && a.dh_last && 4 * g + k < N) ? a.dh_last[cc * N + 4 * g + k] : 0.f;
+    if (valid) {
+      for (int j = Q - 1; j > q; --j) {
+        const float Sj = a.bS[(long long)j * BD + cc];
+        const float4 gb = *reinterpret_cast<const float4*>(a.bh + ((long long)j * BD + cc) * kMaxDstate + 4 * g);
+        const float gbv[4] = {gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) gad[k] = fmaf(ex2_approx(Sj * An[k]), gad[k], gbv[k]);
+      }
+    }
+  }
+  float dsum = 0.f;  // ADJ: the chunk's sum of Delta (log2 units)
   float dA_acc[4] = {0.f, 0.f, 0.f, 0.f};
   float dD_acc = 0.f, dbias_acc = 0.f;
   // channel sums: thread -> step tid / (16 / kOut), states n0 .. n0 + kOut - 1 of one group
   const int rs = tid / (kMaxDstate / kOut), rn0 = kOut * (tid % (kMaxDstate / kOut));
   const int rg = rn0 / 4, rk = rn0 % 4;
   auto comp = [](const float4& v, int k) { return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w)); };
-  if (ntiles > 0) fetch(ntiles - 1, true, fb);
-  for (int it = ntiles - 1; it >= 0; --it) {
+  if (it_begin < it_end) fetch(it_end - 1, true, fb);
+  for (int it = it_end - 1; it >= it_begin; --it) {
     const int t0 = it * kBT;
     const int tl = min(kBT, L - t0);
     __syncthreads();  // the previous tile is done with shared memory
     put(it, fb);
-    const float4 hs = ckpt[(long long)it * kBThreads + tid];
-    if (it > 0) fetch(it - 1, true, fb);
+    const float4 hs = ADJ ? make_float4(0.f, 0.f, 0.f, 0.f) : ckpt[(long long)it * kBThreads + tid];
+    if (it > it_begin) fetch(it - 1, true, fb);
     __syncthreads();
+    if (ADJ) {
+      // dy only (no y needed), then the adjoint from zero over the tile
+      constexpr int kSPT0 = kBT / 4;
+      for (int s = kSPT0 * g; s < kSPT0 * g + kSPT0; ++s) {
+        const float dov = S.dout[c][s];
+        float dyv = dov;
+        if (gz) {
+          const float zv = S.zz[c][s];
+          dyv = dov * zv * rcp_approx(1.0f + ex2_approx(-zv * kLog2e));
+        }
+        S.dy[c][s] = dyv;
+      }
+      __syncthreads();
+      for (int s = kBT - 1; s >= 0; --s) {
+        const float dyv = S.dy[c][s], x = S.dl[c][s];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) gad[k] = ex2_approx(x * An[k]) * fmaf(S.Ct[s][4 * g + k], dyv, gad[k]);
+        dsum += x;
+      }
+      continue;
+    }
     // recompute h_t of the tile, with this group's readout partial
     {
       float hh[4] = {hs.x, hs.y, hs.z, hs.w};
@@ -299,13 +351,21 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
   }
 
   // ---- per-channel results
+  if (ADJ) {
+    if (valid) {
+      *reinterpret_cast<float4*>(a.bh + ((long long)q * BD + cc) * kMaxDstate + 4 * g) =
+          make_float4(gad[0], gad[1], gad[2], gad[3]);
+      if (g == 0) a.bS[(long long)q * BD + cc] = dsum;
+    }
+    return;
+  }
   if (valid) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int n = 4 * g + k;
       if (n < N) {
-        if (a.dh0) a.dh0[cc * N + n] = gad[k];
-        a.ws_dA[cc * N + n] = dA_acc[k];
+        if (a.dh0 && q == 0) a.dh0[cc * N + n] = gad[k];
+        a.ws_dA[((long long)q * BD + cc) * N + n] = dA_acc[k];
       }
     }
   }
@@ -315,8 +375,8 @@ __global__ void __launch_bounds__(kBThreads, 2) scan_bwd_kernel(const ScanBwdArg
   S.p1[g][c][0] = dbias_acc;
   __syncthreads();
   if (g == 0 && valid) {
-    a.ws_dD[cc] = S.p0[0][c][0] + S.p0[1][c][0] + S.p0[2][c][0] + S.p0[3][c][0];
-    a.ws_dbias[cc] = S.p1[0][c][0] + S.p1[1][c][0] + S.p1[2][c][0] + S.p1[3][c][0];
+    a.ws_dD[(long long)q * BD + cc] = S.p0[0][c][0] + S.p0[1][c][0] + S.p0[2][c][0] + S.p0[3][c][0];
+    a.ws_dbias[(long long)q * BD + cc] = S.p1[0][c][0] + S.p1[1][c][0] + S.p1[2][c][0] + S.p1[3][c][0];
   }
 }
 
@@ -340,7 +400,7 @@ __global__ void scan_bwd_reduce_kernel(const ScanBwdArgs a, int ndt) {
     } else if (i < 2 * nBC + nA) {
       const long long j = i - 2 * nBC;  // d * N + n
       float s = 0.f;
-      for (int b = 0; b < a.batch; ++b) s += a.ws_dA[(long long)b * nA + j];
+      for (int qb = 0; qb < a.nchunks * a.batch; ++qb) s += a.ws_dA[(long long)qb * nA + j];
       a.dA[j] = s;
     } else {
       const long long j = i - 2 * nBC - nA;
@@ -348,27 +408,41 @@ __global__ void scan_bwd_reduce_kernel(const ScanBwdArgs a, int ndt) {
       const long long dd = isBias ? j - a.dim : j;
       const float* src = isBias ? a.ws_dbias : a.ws_dD;
       float s = 0.f;
-      for (int b = 0; b < a.batch; ++b) s += src[(long long)b * a.dim + dd];
+      for (int qb = 0; qb < a.nchunks * a.batch; ++qb) s += src[(long long)qb * a.dim + dd];
       float* dst = isBias ? a.ddelta_bias : a.dD;
       if (dst) dst[dd] = s;
     }
   }
 }
 
-template <typename T>
-cudaError_t launch_bwd_t(const ScanBwdArgs& a, cudaStream_t stream) {
-  const size_t smem = sizeof(BwdSmem);
+template <typename T, bool ADJ>
+cudaError_t prepare_bwd() {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(scan_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
-  }
+  if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
+  err = cudaFuncSetAttribute(scan_bwd_kernel<T, ADJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(BwdSmem));
+  if (err == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
+  return err;
+}
+
+template <typename T>
+cudaError_t launch_bwd_t(const ScanBwdArgs& a, cudaStream_t stream) {
+  const size_t smem = sizeof(BwdSmem);
+  cudaError_t err = prepare_bwd<T, false>();
+  if (err != cudaSuccess) return err;
   const int ndt = (a.dim + kBDT - 1) / kBDT;
-  scan_bwd_kernel<T><<<dim3(ndt, a.batch), kBThreads, smem, stream>>>(a);
+  if (a.nchunks > 1) {
+    // adjoint carries of chunks 1 .. nchunks-1 (the forward carries are already on the stream)
+    err = prepare_bwd<T, true>();
+    if (err != cudaSuccess) return err;
+    scan_bwd_kernel<T, true><<<dim3(ndt, a.batch, a.nchunks - 1), kBThreads, smem, stream>>>(a);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  scan_bwd_kernel<T, false><<<dim3(ndt, a.batch, a.nchunks), kBThreads, smem, stream>>>(a);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const long long total = 2LL * a.batch * a.dstate * a.seqlen + (long long)a.dim * a.dstate + 2LL * a.dim;
@@ -380,35 +454,60 @@ cudaError_t launch_bwd_t(const ScanBwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <typename T>
+int bwd_resident() {
+  int n = 0;
+  if (prepare_bwd<T, false>() != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_bwd_kernel<T, false>, kBThreads, sizeof(BwdSmem)) !=
+          cudaSuccess ||
+      n <= 0) {
+    cudaGetLastError();
+    return 3;  // no device to ask: the figure the kernel is built for
+  }
+  return n;
+}
+
+auto up256 = [](long long v) { return (size_t)((v + 255) & ~255LL); };
+
 }  // namespace
 
-size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen) {
+int scan_bwd_resident_ctas_per_sm(bool bf16) { return bf16 ? bwd_resident<__nv_bfloat16>() : bwd_resident<float>(); }
+
+int scan_bwd_channels_per_cta() { return kBDT; }
+
+size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int nchunks) {
   const long long ndt = (dim + kBDT - 1) / kBDT;
   const long long ntiles = (seqlen + kBT - 1) / kBT;
-  auto up = [](long long v) { return (size_t)((v + 255) & ~255LL); };
-  size_t s = up(batch * ndt * ntiles * kBThreads * 16LL);                 // checkpoints
-  s += 2 * up(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);        // dB, dC partials
-  s += up((long long)batch * dim * kMaxDstate * 4LL);                     // dA partials
-  s += 2 * up((long long)batch * dim * 4LL);                              // dD, dbias partials
+  const long long BD = (long long)batch * dim;
+  const long long Q = nchunks < 1 ? 1 : nchunks;
+  size_t s = up256(batch * ndt * ntiles * kBThreads * 16LL);             // checkpoints
+  s += 2 * up256(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);     // dB, dC partials
+  s += up256(Q * BD * kMaxDstate * 4LL);                                  // dA partials
+  s += 2 * up256(Q * BD * 4LL);                                           // dD, dbias partials
+  s += up256((Q - 1) * BD * 4LL) + up256((Q - 1) * BD * kMaxDstate * 4LL); // forward carries
+  s += up256(Q * BD * 4LL) + up256(Q * BD * kMaxDstate * 4LL);             // adjoint carries
   return s;
 }
 
-void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, ScanBwdArgs& a) {
+void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, int nchunks, ScanBwdArgs& a) {
   const long long ndt = (dim + kBDT - 1) / kBDT;
   const long long ntiles = (seqlen + kBT - 1) / kBT;
-  auto up = [](long long v) { return (size_t)((v + 255) & ~255LL); };
+  const long long BD = (long long)batch * dim;
+  const long long Q = nchunks < 1 ? 1 : nchunks;
   char* p = static_cast<char*>(ws);
-  a.ws_ckpt = reinterpret_cast<float*>(p);
-  p += up(batch * ndt * ntiles * kBThreads * 16LL);
-  a.ws_dB = reinterpret_cast<float*>(p);
-  p += up(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);
-  a.ws_dC = reinterpret_cast<float*>(p);
-  p += up(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);
-  a.ws_dA = reinterpret_cast<float*>(p);
-  p += up((long long)batch * dim * kMaxDstate * 4LL);
-  a.ws_dD = reinterpret_cast<float*>(p);
-  p += up((long long)batch * dim * 4LL);
-  a.ws_dbias = reinterpret_cast<float*>(p);
+  auto take = [&](size_t bytes) { char* r = p; p += bytes; return reinterpret_cast<float*>(r); };
+  a.ws_ckpt = take(up256(batch * ndt * ntiles * kBThreads * 16LL));
+  a.ws_dB = take(up256(batch * ndt * (long long)kMaxDstate * seqlen * 4LL));
+  a.ws_dC = take(up256(batch * ndt * (long long)kMaxDstate * seqlen * 4LL));
+  a.ws_dA = take(up256(Q * BD * kMaxDstate * 4LL));
+  a.ws_dD = take(up256(Q * BD * 4LL));
+  a.ws_dbias = take(up256(Q * BD * 4LL));
+  float* fS = take(up256((Q - 1) * BD * 4LL));
+  float* fh = take(up256((Q - 1) * BD * kMaxDstate * 4LL));
+  a.fS = fS;
+  a.fh = fh;
+  a.bS = take(up256(Q * BD * 4LL));
+  a.bh = take(up256(Q * BD * kMaxDstate * 4LL));
 }
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream) {

@@ -77,6 +77,22 @@ def test_backward_matches_oracle(cuda_device, case):
         _assert_grad(got[k], ref[k], io, k)
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_backward_chunked_long(cuda_device, io):
+    """Few channels and a long sequence: the backward pass cuts time into chunks (forward carries
+    for the chunk-start states, adjoint carries for the chunk-end adjoints)."""
+    import selective_state_space_145_b300 as ssm
+
+    p, dout, dhl = _problem(2, 48, 700, 16, io, seed=77)
+    g = to_dev(p, cuda_device)
+    got = ssm.ssm_selective_scan_bwd(g["x"], g["delta"], g["A"], g["B"], g["C"], dout.to(cuda_device), g["D"], g["z"],
+                                     g["delta_bias"], True, g["h0"], dhl.to(cuda_device))
+    ref = oracle.selective_scan_bwd(p["x"], p["delta"], p["A"], p["B"], p["C"], dout, p["D"], p["z"],
+                                    p["delta_bias"], True, p["h0"], dhl, nthreads=oracle.oracle.default_threads())
+    for k in GRADS:
+        _assert_grad(got[k], ref[k], io, k)
+
+
 def test_backward_softplus_off_and_deterministic(cuda_device):
     import selective_state_space_145_b300 as ssm
 
