@@ -118,7 +118,7 @@ def bwd_algorithmic_bytes(w) -> int:
 _KERNEL_SOURCES = {
     "scan": ("ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
     "decode": ("ssm_decode.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
-    "backward": ("ssm_scan_bwd.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
+    "backward": ("ssm_scan_bwd.cu", "ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
 }
 
 
