@@ -38,7 +38,7 @@ constexpr int kBT = 16;         // steps per tile
 constexpr int kBTP = kBT + 1;   // padded row of the per-(channel, step) arrays
 static_assert(kBThreads == kBDT * 4, "four threads per channel");
 constexpr int kOut = kBT * kMaxDstate / kBThreads;  // (step, state) channel sums per thread
-static_assert(kOut >= 1 && kMaxDstate % kOut == 0 && 4 % kOut == 0, "channel-sum mapping");
+static_assert(kOut == 2, "channel sums: two states (one 8-byte load) per thread");
 
 struct BwdSmem {
   float4 hist[kBT][kBThreads];        // h_t of the tile, then the adjoint g_t
@@ -186,8 +186,10 @@ __global__ void __launch_bounds__(kBThreads, 3) scan_bwd_kernel(const ScanBwdArg
     __syncthreads();
     for (int s = 0; s < kBT; ++s) {
       const float x = S.dl[c][s], w = S.du[c][s];
+      const float4 B4 = *reinterpret_cast<const float4*>(&S.Bt[s][4 * g]);
+      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) h[k] = fmaf(ex2_approx(x * An[k]), h[k], w * S.Bt[s][4 * g + k]);
+      for (int k = 0; k < 4; ++k) h[k] = fmaf(ex2_approx(x * An[k]), h[k], w * Bv[k]);
     }
   }
 
@@ -213,7 +215,6 @@ __global__ void __launch_bounds__(kBThreads, 3) scan_bwd_kernel(const ScanBwdArg
   // channel sums: thread -> step tid / (16 / kOut), states n0 .. n0 + kOut - 1 of one group
   const int rs = tid / (kMaxDstate / kOut), rn0 = kOut * (tid % (kMaxDstate / kOut));
   const int rg = rn0 / 4, rk = rn0 % 4;
-  auto comp = [](const float4& v, int k) { return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w)); };
   if (it_begin < it_end) fetch(it_end - 1, true, fb);
   for (int it = it_end - 1; it >= it_begin; --it) {
     const int t0 = it * kBT;
@@ -249,11 +250,14 @@ __global__ void __launch_bounds__(kBThreads, 3) scan_bwd_kernel(const ScanBwdArg
       float hh[4] = {hs.x, hs.y, hs.z, hs.w};
       for (int s = 0; s < kBT; ++s) {
         const float x = S.dl[c][s], w = S.du[c][s];
+        const float4 B4 = *reinterpret_cast<const float4*>(&S.Bt[s][4 * g]);
+        const float4 C4 = *reinterpret_cast<const float4*>(&S.Ct[s][4 * g]);
+        const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
         float p = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          hh[k] = fmaf(ex2_approx(x * An[k]), hh[k], w * S.Bt[s][4 * g + k]);
-          p = fmaf(S.Ct[s][4 * g + k], hh[k], p);
+          hh[k] = fmaf(ex2_approx(x * An[k]), hh[k], w * Bv[k]);
+          p = fmaf(Cv[k], hh[k], p);
         }
         S.hist[s][tid] = make_float4(hh[0], hh[1], hh[2], hh[3]);
         S.p0[g][c][s] = p;
@@ -277,66 +281,63 @@ __global__ void __launch_bounds__(kBThreads, 3) scan_bwd_kernel(const ScanBwdArg
       dD_acc = fmaf(dyv, S.uu[c][s], dD_acc);
     }
     __syncthreads();
-    // dC_t[n] over the CTA's channels
+    // dC_t[n] over the CTA's channels (this thread: step rs, states rn0, rn0 + 1)
     {
-      float acc[kOut];
-#pragma unroll
-      for (int o = 0; o < kOut; ++o) acc[o] = 0.f;
+      float acc0 = 0.f, acc1 = 0.f;
       for (int j = 0; j < kBDT; ++j) {
         const int ch = (j + tid) % kBDT;
-        const float4 hv = S.hist[rs][rg * kBDT + ch];
+        const float2 hv = reinterpret_cast<const float2*>(&S.hist[rs][rg * kBDT + ch])[rk / 2];
         const float dyv = S.dy[ch][rs];
-#pragma unroll
-        for (int o = 0; o < kOut; ++o) acc[o] = fmaf(dyv, comp(hv, rk + o), acc[o]);
+        acc0 = fmaf(dyv, hv.x, acc0);
+        acc1 = fmaf(dyv, hv.y, acc1);
       }
       if (rs < tl) {
         float* out = a.ws_dC + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
-#pragma unroll
-        for (int o = 0; o < kOut; ++o)
-          if (rn0 + o < N) out[(long long)(rn0 + o) * L + t0 + rs] = acc[o];
+        if (rn0 < N) out[(long long)rn0 * L + t0 + rs] = acc0;
+        if (rn0 + 1 < N) out[(long long)(rn0 + 1) * L + t0 + rs] = acc1;
       }
     }
     __syncthreads();  // dC has read every h_t; the adjoint walk overwrites them
     // adjoint walk: steps kBT-1 .. 0 of the tile
+    // per state: g_t = g + C dy; with gB = g_t B and t1 = g_t Abar h_{t-1},
+    //   du part = Delta sum gB,  dDelta part = sum A t1 + u sum gB,  dA += Delta t1,  g <- Abar g_t
     for (int s = kBT - 1; s >= 0; --s) {
       const float dyv = S.dy[c][s], x = S.dl[c][s], Dl = S.Dl[c][s], uv = S.uu[c][s];
       const float4 hp4 = s > 0 ? S.hist[s - 1][tid] : hs;
+      const float4 B4 = *reinterpret_cast<const float4*>(&S.Bt[s][4 * g]);
+      const float4 C4 = *reinterpret_cast<const float4*>(&S.Ct[s][4 * g]);
       const float hp[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
-      float dup = 0.f, ddp = 0.f, gt[4];
+      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
+      float sgb = 0.f, sat = 0.f, gt[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int n = 4 * g + k;
-        const float Bv = S.Bt[s][n], Cv = S.Ct[s][n];
         const float e = ex2_approx(x * An[k]);
-        gad[k] = fmaf(Cv, dyv, gad[k]);
-        gt[k] = gad[k];
-        dup = fmaf(gad[k] * Dl, Bv, dup);
-        ddp = fmaf(gad[k], fmaf(An[k] * e, hp[k], Bv * uv), ddp);
-        dA_acc[k] = fmaf(gad[k] * Dl * e, hp[k], dA_acc[k]);
-        gad[k] *= e;
+        gt[k] = fmaf(Cv[k], dyv, gad[k]);
+        sgb = fmaf(gt[k], Bv[k], sgb);
+        const float t1 = gt[k] * (e * hp[k]);
+        sat = fmaf(An[k], t1, sat);
+        dA_acc[k] = fmaf(Dl, t1, dA_acc[k]);
+        gad[k] = e * gt[k];
       }
       S.hist[s][tid] = make_float4(gt[0], gt[1], gt[2], gt[3]);
-      S.p0[g][c][s] = dup;
-      S.p1[g][c][s] = ddp;
+      S.p0[g][c][s] = Dl * sgb;
+      S.p1[g][c][s] = fmaf(uv, sgb, sat);
     }
     __syncthreads();
     // dB_t[n] over the CTA's channels from g_t and Delta u
     {
-      float acc[kOut];
-#pragma unroll
-      for (int o = 0; o < kOut; ++o) acc[o] = 0.f;
+      float acc0 = 0.f, acc1 = 0.f;
       for (int j = 0; j < kBDT; ++j) {
         const int ch = (j + tid) % kBDT;
-        const float4 gv = S.hist[rs][rg * kBDT + ch];
+        const float2 gv = reinterpret_cast<const float2*>(&S.hist[rs][rg * kBDT + ch])[rk / 2];
         const float w = S.du[ch][rs];
-#pragma unroll
-        for (int o = 0; o < kOut; ++o) acc[o] = fmaf(w, comp(gv, rk + o), acc[o]);
+        acc0 = fmaf(w, gv.x, acc0);
+        acc1 = fmaf(w, gv.y, acc1);
       }
       if (rs < tl) {
         float* out = a.ws_dB + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
-#pragma unroll
-        for (int o = 0; o < kOut; ++o)
-          if (rn0 + o < N) out[(long long)(rn0 + o) * L + t0 + rs] = acc[o];
+        if (rn0 < N) out[(long long)rn0 * L + t0 + rs] = acc0;
+        if (rn0 + 1 < N) out[(long long)(rn0 + 1) * L + t0 + rs] = acc1;
       }
     }
     // du, ddelta for this thread's steps of channel c
