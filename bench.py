@@ -59,6 +59,24 @@ def _sm_max_mhz() -> float:
 CYCLES_MAIN, CYCLES_CARRY = 6, 5
 
 
+def _as_graph(fn, dev):
+    """Capture fn (library calls on the current stream) once into a CUDA graph; return a
+    function that replays it on the current stream."""
+    import torch
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn()  # one eager call: kernel attributes are set outside the capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            fn()
+    torch.cuda.synchronize(dev)
+    return graph.replay
+
+
 def alu_roofline(w, seconds: float, chunk_len: int, sms: int):
     """Scan step time against its issue floor: main + carry updates at the dispatch rate of
     sms x 4 SMSPs x 32 lanes per clock at the maximum SM clock. The per-token element-wise work
@@ -309,6 +327,7 @@ def config_of(w, reverse: bool = False, zoh: bool = False):
         c.update({"d_model": w.d_model, "expand": w.expand})
     if w.kind == "decode":
         c["decode_steps_per_step"] = w.steps
+        c["launch"] = "the token steps replayed from one CUDA graph"
     if w.salient_frac:
         c["salient_frac"] = w.salient_frac
     return c
@@ -351,6 +370,8 @@ def run_gpu(args, w):
         cl = 0
         launches_per_step = w.steps
         kernels = ["decode_kernel"]
+        # the 64 token steps are replayed from one CUDA graph, as a serving loop would run them
+        step = _as_graph(step, dev)
     else:
         cl = args.chunk_len or ssm.ssm_scan_default_chunk_len(w.batch, w.dim, w.seqlen, w.dstate, g["x"].dtype)
         cl = (cl + 63) // 64 * 64
@@ -368,6 +389,8 @@ def run_gpu(args, w):
 
         launches_per_step = 2 if nchunks > 1 else 1
         kernels = ["scan_kernel<carry>", "scan_kernel<main>"] if nchunks > 1 else ["scan_kernel<main>"]
+        if args.graph:
+            step = _as_graph(step, dev)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -418,11 +441,16 @@ def run_gpu(args, w):
             host_out = [{"y": torch.empty(w.steps, w.batch, w.dim, dtype=host["x"].dtype).pin_memory(),
                          "state": torch.empty_like(host["state"]).pin_memory()} for _ in range(nbuf)]
 
-            def call(d, o):
+            def eager(d, o):
                 for t in range(w.steps):
                     ssm.ssm_selective_state_update(d["state"], d["conv_state"], d["x"][t], d["delta"][t], d["A"],
                                                    d["B"][t], d["C"][t], d["D"], d["z"][t], d["delta_bias"], True,
                                                    d["conv_w"], d["conv_b"], y=o["y"][t], zoh=args.zoh)
+
+            replays = [_as_graph(lambda d=d, o=o: eager(d, o), dev) for d, o in zip(bufs, outs)]
+
+            def call(d, o):
+                replays[next(i for i, bb in enumerate(bufs) if bb is d)]()
 
             def results(d, o):
                 return {"y": o["y"], "state": d["state"]}
@@ -633,6 +661,7 @@ def main(argv=None):
     ap.add_argument("--reverse", action="store_true", help="time the backward scan (SSM_SCAN_REVERSE)")
     ap.add_argument("--zoh", action="store_true", help="zero-order-hold discretisation (SSM_SCAN_ZOH)")
     ap.add_argument("--backward", action="store_true", help="time the scan's backward pass")
+    ap.add_argument("--graph", action="store_true", help="replay the scan step from a CUDA graph")
     args = ap.parse_args(argv)
     import dataclasses
 
