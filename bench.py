@@ -33,6 +33,7 @@ DEFAULT_WORKLOAD = "block_f32_b2_d1024_l1024_n16_k4"
 METRIC = "selective-scan state updates/s (B*L*D*N) and HBM GB/s vs B300 peak"
 UNIT = "updates/s"
 FALLBACK_HBM_GBS = 6400.0
+SPEC_HBM_GBS = 8000.0  # the part's nominal HBM3e bandwidth, reported beside the measured copy peak
 
 
 def _peaks():
@@ -525,6 +526,7 @@ def run_gpu(args, w):
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profiles(w.name, w.kind), "peak_source": peak_kind,
+                     "spec_gbs": SPEC_HBM_GBS, "frac_of_spec": achieved / SPEC_HBM_GBS,
                      "algorithmic_bytes_per_step": bytes_step,
                      "timed": "whole step (" + " + ".join(kernels) + "), CUDA events on the launching stream"},
         "roofline_alu": alu_roofline(w, ms * 1e-3, cl, torch.cuda.get_device_properties(dev).multi_processor_count)

@@ -65,11 +65,16 @@ constexpr int row_stride() { return sizeof(T) == 2 ? kTT + 8 : kTT + 4; }
 
 constexpr size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
+// Row stride of the fp32 t-major B / C arrays: 20 floats, so that the transpose's 16-byte
+// stores from threads four steps apart fall on different banks (a 16-float row put them on
+// the same ones); 80-byte rows keep the scan's float4 reads aligned.
+constexpr int kBCS = kMaxDstate + 4;
+
 // Shared-memory layout (byte offsets into the dynamic allocation):
 //   ring  raw[S][R][RS]       staged raw rows
 //   dl    [kDT][kTP]          Delta
 //   du    [kDT][kTP]          Delta * u
-//   B, C  [kTT][16]           B, C as fp32, t-major (no C in the carry pass)
+//   B, C  [kTT][20]           B, C as fp32, t-major, rows padded (no C in the carry pass)
 //   halo  [2][kDT][4]         the 3 raw inputs before the tile (ping-pong by tile parity)
 //   y     [kTPC][kDT][kTP]    partial C.h of each state group, per channel and step
 // In the fp32 main pass y lives in the ring slot of the tile being processed: that slot is
@@ -87,8 +92,8 @@ struct Layout {
   static constexpr size_t dl = align16(ring + slot_bytes * S);
   static constexpr size_t du = dl + sizeof(float) * kDT * kTP;
   static constexpr size_t Bt = du + sizeof(float) * kDT * kTP;
-  static constexpr size_t Ct = Bt + sizeof(float) * kTT * kMaxDstate;
-  static constexpr size_t halo = Ct + (CARRY ? 0 : sizeof(float) * kTT * kMaxDstate);
+  static constexpr size_t Ct = Bt + sizeof(float) * kTT * kBCS;
+  static constexpr size_t halo = Ct + (CARRY ? 0 : sizeof(float) * kTT * kBCS);
   static constexpr size_t y = halo + sizeof(float) * 2 * kDT * 4;
   static constexpr size_t bytes = y + ((CARRY || kYInRing) ? 0 : y_bytes);
   static_assert(!kYInRing || y_bytes <= slot_bytes, "partials fit in one ring slot");
@@ -109,8 +114,8 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
   T (*const ring)[kRows][RS] = reinterpret_cast<T (*)[kRows][RS]>(smem_raw + Lay::ring);
   float (*const s_dl)[kTP] = reinterpret_cast<float (*)[kTP]>(smem_raw + Lay::dl);
   float (*const s_du)[kTP] = reinterpret_cast<float (*)[kTP]>(smem_raw + Lay::du);
-  float (*const s_B)[kMaxDstate] = reinterpret_cast<float (*)[kMaxDstate]>(smem_raw + Lay::Bt);
-  float (*const s_C)[kMaxDstate] = reinterpret_cast<float (*)[kMaxDstate]>(smem_raw + Lay::Ct);
+  float (*const s_B)[kBCS] = reinterpret_cast<float (*)[kBCS]>(smem_raw + Lay::Bt);
+  float (*const s_C)[kBCS] = reinterpret_cast<float (*)[kBCS]>(smem_raw + Lay::Ct);
   float (*const s_halo)[kDT][4] = reinterpret_cast<float (*)[kDT][4]>(smem_raw + Lay::halo);
 
   const int tid = threadIdx.x;
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
       const int blk = tid & 31;
       const int n0 = (blk & 3) * 4, s0 = (blk >> 2) * 4;
       const T (*src)[RS] = raw + row_B<CARRY>() + (tid >= 32 ? kMaxDstate : 0);
-      float (*dst)[kMaxDstate] = tid >= 32 ? s_C : s_B;
+      float (*dst)[kBCS] = tid >= 32 ? s_C : s_B;
       float v[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
