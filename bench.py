@@ -317,9 +317,10 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w, reverse: bool = False, zoh: bool = False):
+def config_of(w, reverse: bool = False, zoh: bool = False, eager: bool = False):
     c = {"workload": w.name, "kind": w.kind, "io": w.io, "batch": w.batch, "d_inner": w.dim, "seqlen": w.seqlen,
-         "d_state": w.dstate, "d_conv": w.d_conv, "l2": "flushed before every timed step (256 MiB write)"}
+         "d_state": w.dstate, "d_conv": w.d_conv, "l2": "flushed before every timed step (256 MiB write)",
+         "launch": "direct library calls" if eager else "the step's library calls replayed from one CUDA graph"}
     if reverse:
         c["direction"] = "backward (SSM_SCAN_REVERSE)"
     if zoh:
@@ -328,7 +329,6 @@ def config_of(w, reverse: bool = False, zoh: bool = False):
         c.update({"d_model": w.d_model, "expand": w.expand})
     if w.kind == "decode":
         c["decode_steps_per_step"] = w.steps
-        c["launch"] = "the token steps replayed from one CUDA graph"
     if w.salient_frac:
         c["salient_frac"] = w.salient_frac
     return c
@@ -372,7 +372,8 @@ def run_gpu(args, w):
         launches_per_step = w.steps
         kernels = ["decode_kernel"]
         # the 64 token steps are replayed from one CUDA graph, as a serving loop would run them
-        step = _as_graph(step, dev)
+        if not args.eager:
+            step = _as_graph(step, dev)
     else:
         cl = args.chunk_len or ssm.ssm_scan_default_chunk_len(w.batch, w.dim, w.seqlen, w.dstate, g["x"].dtype)
         cl = (cl + 63) // 64 * 64
@@ -390,7 +391,7 @@ def run_gpu(args, w):
 
         launches_per_step = 2 if nchunks > 1 else 1
         kernels = ["scan_kernel<carry>", "scan_kernel<main>"] if nchunks > 1 else ["scan_kernel<main>"]
-        if args.graph:
+        if not args.eager:
             step = _as_graph(step, dev)
 
     for _ in range(args.warmup):
@@ -522,7 +523,7 @@ def run_gpu(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": config_of(w, args.reverse, args.zoh),
+        "config": config_of(w, args.reverse, args.zoh, args.eager),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profiles(w.name, w.kind), "peak_source": peak_kind,
@@ -663,7 +664,8 @@ def main(argv=None):
     ap.add_argument("--reverse", action="store_true", help="time the backward scan (SSM_SCAN_REVERSE)")
     ap.add_argument("--zoh", action="store_true", help="zero-order-hold discretisation (SSM_SCAN_ZOH)")
     ap.add_argument("--backward", action="store_true", help="time the scan's backward pass")
-    ap.add_argument("--graph", action="store_true", help="replay the scan step from a CUDA graph")
+    ap.add_argument("--eager", action="store_true",
+                    help="time direct library calls instead of replaying the step from a CUDA graph")
     args = ap.parse_args(argv)
     import dataclasses
 

@@ -14,20 +14,22 @@
 //  * the raw x / delta / z rows of the 32 channels and the 16 shared B / C rows are copied
 //    global->shared with 16-byte cp.async into a two-slot ring, so the next tile is in
 //    flight while this one is processed;
-//  * element-wise phase: each thread turns 8 steps of its channel into Delta and Delta*u
-//    (conv, SiLU and softplus once per (t, d), never per state), keeps D*u and silu(z) for
-//    those steps in registers, and the block transposes B, C to fp32 [t][n];
+//  * element-wise phase: each thread turns 8 steps of its channel into Delta' = Delta log2(e)
+//    and Delta' u (conv, SiLU and softplus once per (t, d), never per state), keeps D*u and
+//    silu(z) for those steps in registers, and the block transposes B, C to fp32 [t][n];
 //  * scan phase: each thread walks the 32 steps sequentially with packed f32x2 math, one
-//    exp2 per state update, and leaves its partial C.h per step in shared memory;
-//  * epilogue: the same thread sums the four partials of its 8 steps (written by its own
-//    warp), adds D*u, applies the gate and stores straight to global memory.
+//    exp2 per state update (2^(Delta' A) = exp(Delta A)), and leaves its partial C.h per
+//    step in shared memory;
+//  * epilogue: the same thread sums the four partials of its 8 steps (one from each warp,
+//    i.e. each state group), adds D*u, applies the gate and stores straight to global memory.
 //  Options (template parameters): REV walks time backward (the backward scan of a
 //  bidirectional layer); ZOH uses the zero-order-hold input term expm1(Delta A)/A B u.
 //  The per-step state never leaves registers. With more than one chunk, a carry kernel
 //  (same code, CARRY = true: no C, no gate, no output) first writes every chunk's sum of
-//  Delta and its end state from zero; the main kernel starts chunk q from h0 composed with
+//  Delta' and its end state from zero; the main kernel starts chunk q from h0 composed with
 //  the carries of chunks 0..q-1 through (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) with
-//  a = exp(A sum Delta).
+//  a = 2^(A sum Delta') = exp(A sum Delta). The main kernel is launched as the carry
+//  kernel's programmatic dependent, so its chunk-0 CTAs run beside the carry kernel.
 #include <algorithm>
 
 #include "ssm_device.cuh"

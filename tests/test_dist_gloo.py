@@ -70,3 +70,21 @@ def test_algorithmic_bytes_match_the_stated_formula():
     assert bench.algorithmic_bytes(w) == 1_619_210_240
     w = inputs.WORKLOADS["decode_bf16_b256_d5120_n16_k4_x64"]
     assert bench.algorithmic_bytes(w) == 194_473_984 * 64
+
+
+def test_issue_floor_and_backward_bytes():
+    """The issue-floor model and the backward's algorithmic bytes, spelled out for one shape."""
+    import bench
+    from selective_state_space_145_b300 import inputs
+
+    w = inputs.WORKLOADS["block_f32_b2_d1024_l1024_n16_k4"]
+    per_t = 2 * 1024 * 16
+    # 8 chunks of 128: main 1024 steps, carry 7 * 128 steps; 148 SMs x 128 lanes at 2032 MHz
+    r = bench.alu_roofline(w, 1e-3, 128, 148)
+    floor = (6 * per_t * 1024 + 5 * per_t * 7 * 128) / (148 * 128 * bench._sm_max_mhz() * 1e6)
+    assert r["frac"] == pytest.approx(floor / 1e-3)
+    assert r["carry_updates"] == per_t * 7 * 128
+    assert bench.alu_roofline(inputs.WORKLOADS["decode_bf16_b256_d5120_n16_k4_x64"], 1e-3, 0, 148) is None
+    tok, bnl = 2 * 1024 * 1024, 2 * 16 * 1024
+    assert bench.bwd_algorithmic_bytes(w) == (tok * 4 * 7 + bnl * (2 * 4 + 8) + 2 * 1024 * 16 * 4 * 3
+                                              + 1024 * 16 * 4 * 2 + 1024 * 4 * 4)
