@@ -601,6 +601,24 @@ def run_gpu_bwd(args, w):
         torch.cuda.synchronize(dev)
         barrier(world)
     ms = reduce_max(statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)), world, dev)
+    # the conv prologue's backward (block workloads): du -> dx, dconv_w, dconv_b, timed alone
+    conv_ms = None
+    if w.d_conv:
+        cws = torch.empty(max(1, int(ssm.lib().ssm_conv_bwd_workspace_bytes(w.batch, w.dim, w.seqlen, w.d_conv,
+                                                                            1 if w.io == "bf16" else 0))),
+                          dtype=torch.uint8, device=dev)
+        cargs = (g["x"], g["conv_w"], grads["du"], g["conv_b"])
+        for _ in range(3):
+            ssm.ssm_causal_conv1d_bwd(*cargs, workspace=cws)
+        cs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ce = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            cs[i].record(stream)
+            ssm.ssm_causal_conv1d_bwd(*cargs, workspace=cws)
+            ce[i].record(stream)
+        torch.cuda.synchronize(dev)
+        conv_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(cs, ce))
     updates = w.updates
     bytes_step = bwd_algorithmic_bytes(w)
     peak, peak_kind = _peaks()
@@ -638,6 +656,9 @@ def run_gpu_bwd(args, w):
                      "algorithmic_bytes_per_step": bytes_step,
                      "timed": "whole step (scan_bwd_kernel + scan_bwd_reduce_kernel)"},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+        "conv_backward_ms": conv_ms,
+        "conv_backward_gbs": (None if conv_ms is None else
+                              w.batch * w.dim * w.seqlen * (2 if w.io == "bf16" else 4) * 3 / (conv_ms * 1e-3) / 1e9),
     }
     print(json.dumps(line), flush=True)
     if world > 1:

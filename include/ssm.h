@@ -1,12 +1,13 @@
 /*
  * ssm.h -- C ABI of the B300 selective state-space (S6) library, libssm.so.
  *
- * Four operations, each on the caller's CUDA stream:
+ * Five operations, each on the caller's CUDA stream:
  *   ssm_causal_conv1d_fwd       depthwise causal conv1d (+ SiLU), the block's short conv
  *   ssm_selective_scan_fwd      selective scan forward (optionally with the conv fused in
  *                               front), returning y and the final state h_L
  *   ssm_selective_state_update  one recurrent (decode) step for a batch of sequences
  *   ssm_selective_scan_bwd      the scan's backward pass (training)
+ *   ssm_causal_conv1d_bwd       the conv prologue's backward pass (training)
  *
  * Sources (page title, section):
  *   "Mamba" (ai360xpert.com, core ML), "The selection mechanism":
@@ -210,6 +211,31 @@ SSM_API ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, cons
                                           int batch, int dim, int seqlen, int dstate, ssm_dtype io,
                                           void* workspace, size_t workspace_bytes, unsigned int flags,
                                           void* stream);
+
+/*
+ * Workspace bytes ssm_causal_conv1d_bwd needs (20 bytes per 1024 steps of every row).
+ */
+SSM_API size_t ssm_conv_bwd_workspace_bytes(int batch, int dim, int seqlen, int d_conv, ssm_dtype io);
+
+/*
+ * Backward of ssm_causal_conv1d_fwd (training): with acc_t = sum_k w[d,k] xs(t-(K-1)+k) + bias[d]
+ * and out_t = silu(acc_t) (apply_silu) or acc_t, where xs(s) is x for s >= 0 and conv_init for
+ * s < 0, the chain rule gives from dout = dL/dout
+ *   dacc_t = dout_t silu'(acc_t)        dx[s] = sum_k w[d,k] dacc_{s+(K-1)-k}
+ *   dconv_init: the same sum at the window positions s = -(K-1) .. -1
+ *   dw[d,k] = sum_{b,t} dacc_t xs(t-(K-1)+k)      dbias[d] = sum_{b,t} dacc_t
+ * ("Overview of Mamba (SSM) Model", "How the Mamba Block Works": the conv and SiLU in front of
+ * the SSM; with ssm_selective_scan_bwd, whose du is this call's dout, it completes the
+ * gradient of the fused block.)
+ *   x, dout, dx  [batch, dim, seqlen] io;  conv_init, dconv_init [batch, dim, d_conv-1] io or NULL
+ *   w [dim, d_conv], bias [dim] or NULL: float32;  dw [dim, d_conv], dbias [dim] or NULL: float32
+ *   workspace    ssm_conv_bwd_workspace_bytes(...) bytes, 16-byte aligned, no initialisation
+ * All outputs are written, not accumulated into; sums are formed in a fixed order.
+ */
+SSM_API ssm_status ssm_causal_conv1d_bwd(const void* x, const float* w, const float* bias, const void* conv_init,
+                                         const void* dout, int apply_silu, void* dx, float* dw, float* dbias,
+                                         void* dconv_init, int batch, int dim, int seqlen, int d_conv, ssm_dtype io,
+                                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * One recurrent (decode) step for every sequence b and channel d, state updated in place:

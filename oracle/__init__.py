@@ -7,6 +7,7 @@ never does, and this package never imports it.
 
 from .oracle import (  # noqa: F401
     causal_conv1d,
+    causal_conv1d_bwd,
     chunk_aggregates,
     compose,
     selective_scan,

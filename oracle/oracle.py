@@ -36,8 +36,10 @@ def _load():
                                                 + [L, L, L, L, I, I])
         lib.oracle_state_update.argtypes = ([_P, _P] + [_P] * 8 + [I] + [_P, _P, I, _P] + [L, L, L, I, I])
         lib.oracle_selective_scan_bwd.argtypes = ([_P] * 8 + [I] + [_P] * 3 + [_P] * 9 + [L, L, L, L, I])
+        lib.oracle_causal_conv1d_bwd.argtypes = [_P] * 9 + [L, L, L, I, I, I]
         for f in ("oracle_softplus", "oracle_silu", "oracle_causal_conv1d", "oracle_selective_scan",
-                  "oracle_compose", "oracle_chunk_aggregates", "oracle_state_update", "oracle_selective_scan_bwd"):
+                  "oracle_compose", "oracle_chunk_aggregates", "oracle_state_update", "oracle_selective_scan_bwd",
+                  "oracle_causal_conv1d_bwd"):
             getattr(lib, f).restype = None
         _lib = lib
     return _lib
@@ -82,6 +84,20 @@ def causal_conv1d(x, w, bias=None, window=None, apply_silu: bool = True, nthread
     _load().oracle_causal_conv1d(_ptr(x), _ptr(w), _ptr(bias), _ptr(window), _ptr(out), batch, dim, L, K,
                                  int(apply_silu), nthreads)
     return out
+
+
+def causal_conv1d_bwd(x, w, dout, bias=None, window=None, apply_silu: bool = True, nthreads: int = 1) -> dict:
+    """Gradients through causal_conv1d from dout = dL/dout: dict with dx [b, d, L], dw [d, K],
+    dbias [d] (None without bias) and dwindow [b, d, K-1] (None without a window)."""
+    x, w, dout, bias, window = _f64(x), _f64(w), _f64(dout), _f64(bias), _f64(window)
+    batch, dim, L = x.shape
+    K = w.shape[1]
+    g = {"dx": np.empty_like(x), "dw": np.empty((dim, K)), "dbias": np.empty(dim) if bias is not None else None,
+         "dwindow": np.empty((batch, dim, K - 1)) if (window is not None and K > 1) else None}
+    _load().oracle_causal_conv1d_bwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(window), _ptr(dout), _ptr(g["dx"]),
+                                     _ptr(g["dwindow"]), _ptr(g["dw"]), _ptr(g["dbias"]), batch, dim, L, K,
+                                     int(apply_silu), nthreads)
+    return g
 
 
 def selective_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus: bool = True,

@@ -168,6 +168,79 @@ void oracle_selective_scan(const double* x, const double* delta, const double* A
 }
 
 /*
+ * Backward of oracle_causal_conv1d: given dout = dL/dout [b,d,t], the chain rule on
+ *   acc_t = sum_k w[k] xs(t - (K-1) + k) + bias,  out_t = silu(acc_t) (or acc_t),
+ * where xs(s) = x[s] for s >= 0 and window[K-1+s] for s < 0, gives
+ *   dacc_t = dout_t silu'(acc_t) (or dout_t),  silu'(a) = s(a) (1 + a (1 - s(a)))
+ *   dx[s] = sum_k w[k] dacc_{s + (K-1) - k} over t = s + (K-1) - k in [0, L)
+ *   dwindow[j] (position s = j - (K-1)) likewise;  dw[d,k] = sum_{b,t} dacc_t xs(t - (K-1) + k)
+ *   dbias[d] = sum_{b,t} dacc_t
+ * Outputs: dx [b,d,L]; dwindow [b,d,K-1] (NULL: not wanted); dw [d,K]; dbias [d] (NULL: not
+ * wanted). All are written, not accumulated into.
+ */
+void oracle_causal_conv1d_bwd(const double* x, const double* w, const double* bias, const double* window,
+                              const double* dout, double* dx, double* dwindow, double* dw, double* dbias,
+                              long batch, long dim, long seqlen, int d_conv, int apply_silu, int nthreads) {
+  long nch = batch * dim;
+  int K = d_conv;
+  double* cw = (double*)calloc((size_t)(nch * K), sizeof(double));
+  double* cb = (double*)calloc((size_t)nch, sizeof(double));
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 1)
+  for (long c = 0; c < nch; ++c) {
+    long d = c % dim;
+    const double* xc = x + c * seqlen;
+    const double* wc = w + d * K;
+    const double* win = window ? window + c * (K - 1) : NULL;
+    double* dacc = (double*)malloc(sizeof(double) * (size_t)(seqlen > 0 ? seqlen : 1));
+    for (long t = 0; t < seqlen; ++t) {
+      double acc = bias ? bias[d] : 0.0;
+      for (int k = 0; k < K; ++k) {
+        long s = t - (K - 1) + k;
+        double xs = s >= 0 ? xc[s] : (win ? win[(K - 1) + s] : 0.0);
+        acc += wc[k] * xs;
+      }
+      double g = dout[c * seqlen + t];
+      if (apply_silu) {
+        double sg = 1.0 / (1.0 + exp(-acc));
+        g *= sg * (1.0 + acc * (1.0 - sg));
+      }
+      dacc[t] = g;
+      cb[c] += g;
+      for (int k = 0; k < K; ++k) {
+        long s = t - (K - 1) + k;
+        double xs = s >= 0 ? xc[s] : (win ? win[(K - 1) + s] : 0.0);
+        cw[c * K + k] += g * xs;
+      }
+    }
+    /* dx[s] and dwindow: every (t, k) with t - (K-1) + k = s */
+    for (long s = -(K - 1); s < seqlen; ++s) {
+      double v = 0.0;
+      for (int k = 0; k < K; ++k) {
+        long t = s + (K - 1) - k;
+        if (t >= 0 && t < seqlen) v += wc[k] * dacc[t];
+      }
+      if (s >= 0) dx[c * seqlen + s] = v;
+      else if (dwindow) dwindow[c * (K - 1) + (K - 1) + s] = v;
+    }
+    free(dacc);
+  }
+  for (long d = 0; d < dim; ++d) {
+    for (int k = 0; k < K; ++k) {
+      double sw = 0.0;
+      for (long b = 0; b < batch; ++b) sw += cw[(b * dim + d) * K + k];
+      dw[d * K + k] = sw;
+    }
+    if (dbias) {
+      double sb = 0.0;
+      for (long b = 0; b < batch; ++b) sb += cb[b * dim + d];
+      dbias[d] = sb;
+    }
+  }
+  free(cw);
+  free(cb);
+}
+
+/*
  * Composition of two affine maps h -> a*h + b (first (a1,b1), then (a2,b2)):
  *   (a1, b1) o (a2, b2) = (a1*a2, a2*b1 + b2).
  * This is the associative operator of the parallel scan ("Mamba", ai360xpert.com,

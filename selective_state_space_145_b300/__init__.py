@@ -10,6 +10,7 @@ from .ssm import (  # noqa: F401
     LIB_PATH,
     SSMError,
     lib,
+    ssm_causal_conv1d_bwd,
     ssm_causal_conv1d_fwd,
     ssm_scan_bwd_workspace_bytes,
     ssm_scan_default_chunk_len,
@@ -23,6 +24,7 @@ from .ssm import (  # noqa: F401
 
 __all__ = [
     "ssm_causal_conv1d_fwd",
+    "ssm_causal_conv1d_bwd",
     "ssm_selective_scan_fwd",
     "ssm_selective_state_update",
     "ssm_selective_scan_bwd",

@@ -297,4 +297,48 @@ ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float*
   return ssm::launch_scan_bwd(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+size_t ssm_conv_bwd_workspace_bytes(int batch, int dim, int seqlen, int d_conv, ssm_dtype io) {
+  (void)d_conv;
+  (void)io;
+  if (batch <= 0 || dim <= 0 || seqlen < 0) return 0;
+  return ssm::conv_bwd_workspace_bytes(batch, dim, seqlen);
+}
+
+ssm_status ssm_causal_conv1d_bwd(const void* x, const float* w, const float* bias, const void* conv_init,
+                                 const void* dout, int apply_silu, void* dx, float* dw, float* dbias,
+                                 void* dconv_init, int batch, int dim, int seqlen, int d_conv, ssm_dtype io,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (batch < 0 || dim < 0 || seqlen < 0) return SSM_ERR_INVALID_ARG;
+  if (d_conv < 1) return SSM_ERR_INVALID_ARG;
+  if (d_conv > kMaxConv) return SSM_ERR_UNSUPPORTED;
+  if (apply_silu != 0 && apply_silu != 1) return SSM_ERR_INVALID_ARG;
+  if ((long long)batch * dim == 0) return SSM_OK;
+  if (!w || !dw) return SSM_ERR_INVALID_ARG;
+  if (seqlen > 0 && (!x || !dout || !dx)) return SSM_ERR_INVALID_ARG;
+  const size_t es = io_bytes(io);
+  const void* io_ptrs[] = {x, conv_init, dout, dx, dconv_init};
+  for (const void* p : io_ptrs)
+    if (p && !aligned(p, es)) return SSM_ERR_UNSUPPORTED;
+  const void* f_ptrs[] = {w, bias, dw, dbias};
+  for (const void* p : f_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_UNSUPPORTED;
+  const size_t need = ssm::conv_bwd_workspace_bytes(batch, dim, seqlen);
+  if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return SSM_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (seqlen == 0 && dconv_init && d_conv > 1) {
+    // no step reaches the window: its gradient is zero
+    if (cudaMemsetAsync(dconv_init, 0, (size_t)batch * dim * (d_conv - 1) * es, st) != cudaSuccess)
+      return SSM_ERR_CUDA;
+  }
+  ssm::ConvBwdArgs a;
+  a.x = x; a.w = w; a.bias = bias; a.conv_init = conv_init; a.dout = dout; a.dx = dx; a.dw = dw; a.dbias = dbias;
+  a.dconv_init = d_conv > 1 ? dconv_init : nullptr;
+  a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.d_conv = d_conv; a.apply_silu = apply_silu;
+  a.bf16 = io == SSM_BF16;
+  a.ws_part = static_cast<float*>(workspace);
+  return ssm::launch_conv_bwd(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // extern "C"

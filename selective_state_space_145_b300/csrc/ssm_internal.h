@@ -54,6 +54,21 @@ struct ConvArgs {
   int vec;
 };
 
+struct ConvBwdArgs {
+  const void* x;
+  const float* w;
+  const float* bias;
+  const void* conv_init;
+  const void* dout;
+  void* dx;
+  float* dw;
+  float* dbias;          // NULL: not computed
+  void* dconv_init;      // NULL: not computed
+  int batch, dim, seqlen, d_conv, apply_silu;
+  int bf16;
+  float* ws_part;        // [batch*dim][segments][5] per-block dw (padded taps) and dbias sums
+};
+
 struct DecodeArgs {
   float* state;
   void* conv_state;
@@ -130,6 +145,8 @@ void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, int nchu
 int scan_bwd_resident_ctas_per_sm(bool bf16);
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
+size_t conv_bwd_workspace_bytes(int batch, int dim, int seqlen);
+cudaError_t launch_conv_bwd(const ConvBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace ssm

@@ -28,7 +28,8 @@ _lib = None
 # Exported C symbols, as declared in include/ssm.h.
 EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_scan_default_chunk_len",
            "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update",
-           "ssm_selective_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_selective_scan_bwd")
+           "ssm_selective_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_selective_scan_bwd",
+           "ssm_conv_bwd_workspace_bytes", "ssm_causal_conv1d_bwd")
 
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -71,6 +72,10 @@ def lib() -> ctypes.CDLL:
         L.ssm_selective_scan_fwd_noalloc.restype = i
         L.ssm_selective_scan_fwd_noalloc.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, vp, fp, vp]
                                                      + [i] * 6 + [u, vp])
+        L.ssm_conv_bwd_workspace_bytes.restype = sz
+        L.ssm_conv_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.ssm_causal_conv1d_bwd.restype = i
+        L.ssm_causal_conv1d_bwd.argtypes = [vp, fp, fp, vp, vp, i, vp, fp, fp, vp, i, i, i, i, i, vp, sz, vp]
         L.ssm_scan_bwd_workspace_bytes.restype = sz
         L.ssm_scan_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
         L.ssm_selective_scan_bwd.restype = i
@@ -143,6 +148,35 @@ def ssm_causal_conv1d_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch
                                      int(bool(apply_silu)), _io_code(x), _stream(dev))
     _check("ssm_causal_conv1d_fwd", st)
     return out
+
+
+def ssm_causal_conv1d_bwd(x: torch.Tensor, w: torch.Tensor, dout: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                          conv_init: Optional[torch.Tensor] = None, apply_silu: bool = True,
+                          workspace: Optional[torch.Tensor] = None) -> dict:
+    """Backward of ssm_causal_conv1d_fwd. Returns a dict with dx [batch, dim, L] (io dtype),
+    dw [dim, K] and dbias [dim] (float32), and dconv_init [batch, dim, K-1] (io dtype; None
+    without conv_init or for K = 1)."""
+    batch, dim, L = x.shape
+    K = w.shape[1]
+    dev, io = x.device, x.dtype
+    _need(x, "x", (batch, dim, L), io, dev)
+    _need(w, "w", (dim, K), torch.float32, dev)
+    _need(dout, "dout", (batch, dim, L), io, dev)
+    _need(bias, "bias", (dim,), torch.float32, dev, optional=True)
+    _need(conv_init, "conv_init", (batch, dim, K - 1), io, dev, optional=True)
+    g = {"dx": torch.empty_like(x), "dw": torch.empty(dim, K, dtype=torch.float32, device=dev),
+         "dbias": torch.empty(dim, dtype=torch.float32, device=dev),
+         "dconv_init": torch.empty(batch, dim, K - 1, dtype=io, device=dev) if (conv_init is not None and K > 1)
+         else None}
+    need = int(lib().ssm_conv_bwd_workspace_bytes(batch, dim, L, K, _io_code(x)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib().ssm_causal_conv1d_bwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(conv_init), _ptr(dout), int(bool(apply_silu)),
+                                     _ptr(g["dx"]), _ptr(g["dw"]), _ptr(g["dbias"]), _ptr(g["dconv_init"]),
+                                     batch, dim, L, K, _io_code(x), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(dev))
+    _check("ssm_causal_conv1d_bwd", st)
+    return g
 
 
 def ssm_scan_default_chunk_len(batch: int, dim: int, seqlen: int, dstate: int, io: torch.dtype) -> int:

@@ -115,6 +115,17 @@ def test_backward_argument_checks(L):
         assert f(*bad) == want, (i, v)
 
 
+def test_conv_backward_argument_checks(L):
+    f = L.ssm_causal_conv1d_bwd
+    # x, w, bias, conv_init, dout, silu, dx, dw, dbias, dconv_init, batch, dim, L, K, io, ws, ws_bytes, stream
+    base = [FAKE, FAKE, None, None, FAKE, 1, FAKE, FAKE, None, None, 1, 4, 8, 4, 0, FAKE, 1 << 20, None]
+    for i, v, want in ((0, None, 1), (7, None, 1), (13, 5, 2), (13, 0, 1), (5, 2, 1), (14, 9, 2), (16, 0, 1),
+                       (0, FAKE + 2, 2)):
+        bad = list(base)
+        bad[i] = v
+        assert f(*bad) == want, (i, v)
+
+
 def test_decode_and_conv_argument_checks(L):
     f = L.ssm_selective_state_update
     base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, FAKE, None, 4, FAKE, 2, 8, 16, 1, 0, None]

@@ -393,6 +393,42 @@ def test_backward_matches_autograd():
         np.testing.assert_allclose(g[gk], tp[key].grad.numpy(), rtol=1e-11, atol=1e-12, err_msg=key)
 
 
+def test_conv_backward_matches_autograd_conv1d():
+    """The conv backward against torch autograd through F.conv1d (groups = channels, left
+    padding supplied by the window), with and without SiLU."""
+    b, d, L, K = 2, 5, 13, 4
+    x, w, bias, win, dout = _rand(b, d, L), RNG.uniform(-0.5, 0.5, (d, K)), _rand(d), _rand(b, d, K - 1), _rand(b, d, L)
+    for act in (True, False):
+        g = oracle.causal_conv1d_bwd(x, w, dout, bias, win, apply_silu=act)
+        tx, tw, tb, twin = (torch.tensor(v, requires_grad=True) for v in (x, w, bias, win))
+        y = F.conv1d(torch.cat([twin, tx], dim=-1), tw[:, None, :], tb, groups=d)
+        if act:
+            y = F.silu(y)
+        (y * torch.tensor(dout)).sum().backward()
+        np.testing.assert_allclose(g["dx"], tx.grad.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g["dw"], tw.grad.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g["dbias"], tb.grad.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g["dwindow"], twin.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_conv_backward_matches_finite_differences():
+    b, d, L, K = 1, 3, 7, 3
+    x, w, bias, win, dout = _rand(b, d, L), RNG.uniform(-0.5, 0.5, (d, K)), _rand(d), _rand(b, d, K - 1), _rand(b, d, L)
+    g = oracle.causal_conv1d_bwd(x, w, dout, bias, win)
+    p = {"x": x, "w": w, "bias": bias, "window": win}
+    eps = 1e-6
+    for key, gk in (("x", "dx"), ("w", "dw"), ("bias", "dbias"), ("window", "dwindow")):
+        num = np.empty_like(p[key])
+        for idx in np.ndindex(p[key].shape):
+            q = {k: v.copy() for k, v in p.items()}
+            q[key][idx] += eps
+            lp = float(np.sum(dout * oracle.causal_conv1d(q["x"], q["w"], q["bias"], q["window"])))
+            q[key][idx] -= 2 * eps
+            lm = float(np.sum(dout * oracle.causal_conv1d(q["x"], q["w"], q["bias"], q["window"])))
+            num[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[gk], num, rtol=1e-6, atol=1e-8, err_msg=key)
+
+
 # ---------------------------------------------------------------- invariants
 
 def _problem(b=2, d=3, L=21, N=4, K=4):
