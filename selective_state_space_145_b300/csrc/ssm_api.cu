@@ -82,7 +82,7 @@ bool dims_ok(int batch, int dim, int seqlen, int dstate) {
 
 extern "C" {
 
-int ssm_version(void) { return 100; }
+int ssm_version(void) { return 200; }  // 0.2.0: reverse and ZOH flags, backward passes
 
 const char* ssm_status_string(int status) {
   switch (status) {
