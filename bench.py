@@ -583,6 +583,9 @@ def run_gpu_bwd(args, w):
     def step():
         ssm.ssm_selective_scan_bwd(*args_bwd, workspace=ws, grads=grads)
 
+    if not args.eager:
+        step = _as_graph(step, dev)
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -608,14 +611,20 @@ def run_gpu_bwd(args, w):
                                                                             1 if w.io == "bf16" else 0))),
                           dtype=torch.uint8, device=dev)
         cargs = (g["x"], g["conv_w"], grads["du"], g["conv_b"])
-        for _ in range(3):
+
+        def conv_step():
             ssm.ssm_causal_conv1d_bwd(*cargs, workspace=cws)
+
+        if not args.eager:
+            conv_step = _as_graph(conv_step, dev)
+        for _ in range(3):
+            conv_step()
         cs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ce = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for i in range(args.steps):
             flush.zero_()
             cs[i].record(stream)
-            ssm.ssm_causal_conv1d_bwd(*cargs, workspace=cws)
+            conv_step()
             ce[i].record(stream)
         torch.cuda.synchronize(dev)
         conv_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(cs, ce))
