@@ -1,4 +1,5 @@
-"""fp64 CPU oracle of the selective-scan (S6) hot path.
+"""fp64 CPU oracle of the selective-scan (S6) hot path and of the multi-head SSM with one decay
+per head (the state-space-duality layer).
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
 baseline may import this package; the library in ``selective_state_space_145_b300``
@@ -14,5 +15,6 @@ from .oracle import (  # noqa: F401
     selective_scan_bwd,
     silu,
     softplus,
+    ssd,
     state_update,
 )

@@ -37,7 +37,8 @@ def _load():
         lib.oracle_state_update.argtypes = ([_P, _P] + [_P] * 8 + [I] + [_P, _P, I, _P] + [L, L, L, I, I])
         lib.oracle_selective_scan_bwd.argtypes = ([_P] * 8 + [I] + [_P] * 3 + [_P] * 9 + [L, L, L, L, I])
         lib.oracle_causal_conv1d_bwd.argtypes = [_P] * 9 + [L, L, L, I, I, I]
-        for f in ("oracle_softplus", "oracle_silu", "oracle_causal_conv1d", "oracle_selective_scan",
+        lib.oracle_ssd.argtypes = [_P] * 7 + [I, _P, _P, _P] + [L] * 5 + [I]
+        for f in ("oracle_softplus", "oracle_silu", "oracle_causal_conv1d", "oracle_selective_scan", "oracle_ssd",
                   "oracle_compose", "oracle_chunk_aggregates", "oracle_state_update", "oracle_selective_scan_bwd",
                   "oracle_causal_conv1d_bwd"):
             getattr(lib, f).restype = None
@@ -208,3 +209,20 @@ def state_update(state, conv_state, x, delta, A, B, C, D=None, z=None, delta_bia
                                 _ptr(D), _ptr(z), _ptr(delta_bias), int(delta_softplus), _ptr(conv_w),
                                 _ptr(conv_b), K, _ptr(y), batch, dim, N, nthreads, int(zoh))
     return y, state, conv_state
+
+
+def ssd(x, dt, A, B, C, D=None, dt_bias=None, dt_softplus: bool = True, h0=None,
+        nthreads: int = 1) -> Tuple[np.ndarray, np.ndarray]:
+    """Multi-head SSM with one scalar decay per head (the layer of the state-space duality).
+
+    x [batch, L, H, P], dt [batch, L, H], A [H], B, C [batch, L, N], D and dt_bias [H],
+    h0 [batch, H, P, N]. Returns (y [batch, L, H, P], h_last [batch, H, P, N])."""
+    x, dt, A, B, C = _f64(x), _f64(dt), _f64(A), _f64(B), _f64(C)
+    D, dt_bias, h0 = map(_f64, (D, dt_bias, h0))
+    batch, L, H, P = x.shape
+    N = B.shape[2]
+    y = np.empty((batch, L, H, P))
+    h_last = np.empty((batch, H, P, N))
+    _load().oracle_ssd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias), int(dt_softplus),
+                       _ptr(h0), _ptr(y), _ptr(h_last), batch, L, H, P, N, nthreads)
+    return y, h_last

@@ -482,4 +482,53 @@ void oracle_selective_scan_bwd(const double* u, const double* delta, const doubl
   free(cC);
 }
 
+/*
+ * Multi-head selective SSM with one scalar decay per head: the layer of the structured
+ * state-space duality ("Mamba" (inferensys.com / ai360xpert.com pages), "Mamba-2 introduces the
+ * Structured State Space Duality": multi-head SSM, every head with its own selective parameters;
+ * the state dimension treated like a head dimension; "Mamba" (ozercemkelahmet.com), "Mamba-2 and
+ * the dual view": the same layer written as a masked matrix product with a decaying mask). A
+ * single decay per head and step is what makes that mask one matrix per head. For every batch
+ * element b and head h, with a state H of P x N (head dim x state dim):
+ *   Delta_t   = softplus(dt[b,t,h] + dt_bias[h])       (the raw sum when dt_softplus == 0)
+ *   H_t[p][n] = exp(Delta_t A[h]) H_{t-1}[p][n] + Delta_t x[b,t,h,p] B[b,t,n],   H_{-1} = h0 or 0
+ *   y[b,t,h,p] = sum_n C[b,t,n] H_t[p][n] + D[h] x[b,t,h,p]
+ * B and C are shared by all heads (one group). Layouts: x, y [batch, L, H, P]; dt [batch, L, H];
+ * B, C [batch, L, N]; A, D, dt_bias [H]; h0, h_last [batch, H, P, N]. With d = h*P + p this is the
+ * selective scan above with A[d,n] = A[h], delta[b,d,t] = dt[b,t,h] and B, C transposed.
+ */
+void oracle_ssd(const double* x, const double* dt, const double* A, const double* Bm, const double* Cm,
+                const double* Dskip, const double* dt_bias, int dt_softplus, const double* h0, double* y,
+                double* h_last, long batch, long seqlen, long nheads, long headdim, long dstate, int nthreads) {
+  long npairs = batch * nheads;
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 1)
+  for (long c = 0; c < npairs; ++c) {
+    long b = c / nheads, h = c % nheads;
+    double* H = (double*)malloc(sizeof(double) * (size_t)(headdim * dstate));
+    for (long i = 0; i < headdim * dstate; ++i) H[i] = h0 ? h0[c * headdim * dstate + i] : 0.0;
+    for (long t = 0; t < seqlen; ++t) {
+      double v = dt[(b * seqlen + t) * nheads + h] + (dt_bias ? dt_bias[h] : 0.0);
+      double Delta = dt_softplus ? softplus(v) : v;
+      double a = exp(Delta * A[h]);
+      const double* xt = x + ((b * seqlen + t) * nheads + h) * headdim;
+      const double* Bt = Bm + (b * seqlen + t) * dstate;
+      const double* Ct = Cm + (b * seqlen + t) * dstate;
+      double* yt = y + ((b * seqlen + t) * nheads + h) * headdim;
+      for (long p = 0; p < headdim; ++p) {
+        double acc = 0.0;
+        for (long n = 0; n < dstate; ++n) {
+          double* hp = H + p * dstate + n;
+          *hp = a * (*hp) + Delta * xt[p] * Bt[n];
+          acc += Ct[n] * (*hp);
+        }
+        if (Dskip) acc += Dskip[h] * xt[p];
+        yt[p] = acc;
+      }
+    }
+    if (h_last)
+      for (long i = 0; i < headdim * dstate; ++i) h_last[c * headdim * dstate + i] = H[i];
+    free(H);
+  }
+}
+
 int oracle_version(void) { return 1; }
