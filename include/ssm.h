@@ -298,6 +298,40 @@ SSM_API ssm_status ssm_selective_scan_fwd_noalloc(const void* x, const void* del
                                                   int batch, int dim, int seqlen, int dstate, ssm_dtype io,
                                                   int chunk_len, unsigned int flags, void* stream);
 
+/*
+ * Multi-head selective SSM with one decay per head: the layer of the structured state-space
+ * duality ("Mamba" (ai360xpert.com / inferensys.com pages), "Mamba-2 introduces the Structured
+ * State Space Duality": multi-head SSM with selective parameters per head, the state dimension
+ * used like a head dimension, the computation mapped to structured matrix products that run on
+ * tensor cores; "Mamba" (ozercemkelahmet.com), "Mamba-2 and the dual view": the layer as a
+ * masked matrix product with a decaying mask). For every batch element b and head h, with a
+ * state H of headdim x dstate:
+ *   Delta_t   = softplus(dt[b,t,h] + dt_bias[h])        (the raw sum when dt_softplus == 0)
+ *   H_t[p][n] = exp(Delta_t A[h]) H_{t-1}[p][n] + Delta_t x[b,t,h,p] B[b,t,n],   H_{-1} = h0 or 0
+ *   y[b,t,h,p] = sum_n C[b,t,n] H_t[p][n] + D[h] x[b,t,h,p]
+ * B and C are shared by all heads. The GPU evaluates the chunked dual form: per chunk of 128
+ * steps the masked product (C B^T masked and decayed) X and the chunk state B^T (decayed X) on
+ * the tensor cores (tcgen05, bf16 operands, fp32 accumulation), a carry pass over chunks in
+ * fp32, and C H_in for the state entering the chunk.
+ *
+ *   x       [batch, seqlen, nheads, headdim] bf16      y [batch, seqlen, nheads, headdim] bf16
+ *   dt      [batch, seqlen, nheads] bf16               B, C [batch, seqlen, dstate] bf16
+ *   A, D, dt_bias [nheads] float32 (D, dt_bias may be NULL)
+ *   h0, h_last [batch, nheads, headdim, dstate] float32 or NULL (h_last = h0 or 0 when seqlen == 0)
+ *   io      SSM_BF16 only (SSM_F32 returns SSM_ERR_UNSUPPORTED); headdim must be 64 and dstate
+ *           128, else SSM_ERR_UNSUPPORTED
+ *   workspace  device buffer of ssm_ssd_workspace_bytes(...) bytes, 256-byte aligned; its
+ *           contents need no initialisation. After the call its first 4 bytes hold a status
+ *           word: nonzero if a wait on the tensor cores ran out (results then invalid).
+ * x, B, C and y must be 16-byte aligned; dt 2-byte aligned. The call allocates nothing and
+ * runs three kernels on `stream`.
+ */
+SSM_API size_t ssm_ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, ssm_dtype io);
+SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                               const float* D, const float* dt_bias, int dt_softplus, const float* h0, void* y,
+                               float* h_last, int batch, int seqlen, int nheads, int headdim, int dstate,
+                               ssm_dtype io, void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

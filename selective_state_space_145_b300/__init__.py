@@ -1,5 +1,6 @@
 """B300-native selective state-space (S6) hot path: causal conv prologue, selective scan
-forward (and its backward pass) and the decode state update, as hand-written sm_103a CUDA behind a C ABI
+forward (and its backward pass), the decode state update and the multi-head SSM with one decay
+per head (state-space-duality layer) on the tensor cores, as hand-written sm_103a CUDA behind a C ABI
 (``libssm.so``, declared in ``include/ssm.h``) with a thin ctypes binding.
 
 The binding loads the library on first use and raises if it is missing.
@@ -18,6 +19,8 @@ from .ssm import (  # noqa: F401
     ssm_selective_scan_bwd,
     ssm_selective_scan_fwd,
     ssm_selective_state_update,
+    ssm_ssd_fwd,
+    ssm_ssd_workspace_bytes,
     status_string,
     version,
 )
@@ -31,6 +34,8 @@ __all__ = [
     "ssm_scan_bwd_workspace_bytes",
     "ssm_scan_default_chunk_len",
     "ssm_scan_workspace_bytes",
+    "ssm_ssd_fwd",
+    "ssm_ssd_workspace_bytes",
     "version",
     "status_string",
     "SSMError",

@@ -341,4 +341,47 @@ ssm_status ssm_causal_conv1d_bwd(const void* x, const float* w, const float* bia
   return ssm::launch_conv_bwd(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+size_t ssm_ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, ssm_dtype io) {
+  if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim != 64 || dstate != 128 || io != SSM_BF16) return 0;
+  const int q = ssm::ssd_chunk_len();
+  return ssm::ssd_workspace_bytes(batch, nheads, (int)(((long long)seqlen + q - 1) / q));
+}
+
+ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+                       const float* dt_bias, int dt_softplus, const float* h0, void* y, float* h_last, int batch,
+                       int seqlen, int nheads, int headdim, int dstate, ssm_dtype io, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (batch < 0 || seqlen < 0 || nheads < 0 || headdim < 1 || dstate < 1) return SSM_ERR_INVALID_ARG;
+  if (dt_softplus != 0 && dt_softplus != 1) return SSM_ERR_INVALID_ARG;
+  if (io != SSM_BF16 || headdim != 64 || dstate != 128) return SSM_ERR_UNSUPPORTED;
+  if (batch > 65535 || nheads > 65535) return SSM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((long long)batch * nheads == 0) return SSM_OK;
+  const size_t state_bytes = (size_t)batch * nheads * headdim * dstate * sizeof(float);
+  if (seqlen == 0) {  // no tokens: the final state is the initial one
+    if (!h_last) return SSM_OK;
+    const cudaError_t e = h0 ? cudaMemcpyAsync(h_last, h0, state_bytes, cudaMemcpyDeviceToDevice, st)
+                             : cudaMemsetAsync(h_last, 0, state_bytes, st);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  }
+  if (!x || !dt || !A || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) || !aligned(dt, 2) ||
+      !aligned(A, 4) || (D && !aligned(D, 4)) || (dt_bias && !aligned(dt_bias, 4)) || (h0 && !aligned(h0, 4)) ||
+      (h_last && !aligned(h_last, 4)))
+    return SSM_ERR_UNSUPPORTED;
+  const int q = ssm::ssd_chunk_len();
+  const long long nchunks = ((long long)seqlen + q - 1) / q;
+  if (nchunks > (1LL << 30)) return SSM_ERR_INVALID_ARG;
+  const size_t need = ssm::ssd_workspace_bytes(batch, nheads, (int)nchunks);
+  if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return SSM_ERR_UNSUPPORTED;
+  ssm::SsdArgs a;
+  a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.dt_bias = dt_bias; a.dt_softplus = dt_softplus;
+  a.h0 = h0; a.y = y; a.h_last = h_last;
+  a.batch = batch; a.seqlen = seqlen; a.nheads = nheads; a.nchunks = (int)nchunks;
+  ssm::ssd_workspace_split(workspace, batch, nheads, (int)nchunks, a);
+  return ssm::launch_ssd(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -54,6 +54,28 @@ struct ConvArgs {
   int vec;
 };
 
+// Multi-head SSM with one decay per head (state-space-duality layer), bf16 I/O, head dim 64,
+// state dim 128, chunks of 128 steps.
+struct SsdArgs {
+  const void* x;         // [batch, seqlen, nheads, 64] bf16
+  const void* dt;        // [batch, seqlen, nheads] bf16
+  const float* A;        // [nheads]
+  const void* B;         // [batch, seqlen, 128] bf16
+  const void* C;
+  const float* D;        // [nheads] or NULL
+  const float* dt_bias;  // [nheads] or NULL
+  int dt_softplus;
+  const float* h0;       // [batch, nheads, 64, 128] or NULL
+  void* y;               // [batch, seqlen, nheads, 64] bf16
+  float* h_last;         // [batch, nheads, 64, 128] or NULL
+  int batch, seqlen, nheads, nchunks;
+  int* ws_status;        // nonzero after the call: a tensor-core wait ran out
+  float* ws_cs;          // [batch][nheads][nchunks] sum of Delta A log2(e) over the chunk
+  float* ws_S;           // [batch][nheads][nchunks][128][64] chunk states from zero (fp32)
+  void* ws_Sin;          // [batch][nheads][nchunks][128][64] state entering each chunk, bf16(v)
+  void* ws_Sin_lo;       // the same, bf16(v - bf16(v))
+};
+
 struct ConvBwdArgs {
   const void* x;
   const float* w;
@@ -138,6 +160,12 @@ size_t scan_workspace_bytes(long long channels, int nchunks);
 void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, float** h);
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
+
+// State-space-duality layer: chunk length, workspace layout and launch.
+int ssd_chunk_len();
+size_t ssd_workspace_bytes(int batch, int nheads, int nchunks);
+void ssd_workspace_split(void* ws, int batch, int nheads, int nchunks, SsdArgs& a);
+cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t stream);
 // the forward chunk carries only (ws_S, ws_h for chunks 0 .. nchunks-2; no conv, forward time)
 cudaError_t launch_scan_carry(const ScanArgs& a, cudaStream_t stream);
 size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int nchunks);

@@ -193,3 +193,66 @@ def workload_inputs(w: Workload) -> Dict[str, Optional[torch.Tensor]]:
         return decode_inputs(w.batch, w.dim, w.dstate, w.d_conv, w.io, w.seed, steps=w.steps)
     return scan_inputs(w.batch, w.dim, w.seqlen, w.dstate, w.d_conv, w.io, w.seed,
                        salient_frac=w.salient_frac)
+
+
+# ---- multi-head SSM with one decay per head (the state-space-duality layer)
+#
+# Recipe, one seeded CPU generator per call, float32 draws in this order, then the per-token
+# tensors cast to bf16 once:
+#   x ~ N(0, 1) [batch, L, nheads, headdim]; dt (step pre-activation) ~ N(0, 0.5^2) [batch, L, nheads];
+#   B, C ~ N(0, 1) [batch, L, dstate] (one group: shared by every head); D ~ N(0, 1) [nheads];
+#   per-head step dt0 log-uniform in [1e-3, 0.1] with dt_bias = dt0 + log(-expm1(-dt0));
+#   A[h] = -U(1, 16) (one decay rate per head); optionally h0 ~ N(0, 1) [batch, nheads, headdim, dstate].
+# The pages give no sizes for this layer; the workload below takes the bf16 block workload's model
+# (d_model 1024, expand 2, so 2048 channels = 32 heads of 64) with a state of 128 per head.
+
+@dataclasses.dataclass(frozen=True)
+class SsdWorkload:
+    """A named synthetic workload of the state-space-duality layer."""
+
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    dstate: int
+    seed: int
+    d_model: Optional[int] = None
+    expand: Optional[int] = None
+    kind: str = "ssd"
+    io: str = "bf16"
+
+    @property
+    def updates(self) -> int:
+        """State updates (b, t, h, p, n) of one pass."""
+        return self.batch * self.seqlen * self.nheads * self.headdim * self.dstate
+
+
+SSD_WORKLOADS: Dict[str, SsdWorkload] = {w.name: w for w in [
+    SsdWorkload("ssd_bf16_b8_l2048_h32_p64_n128", 8, 2048, 32, 64, 128, seed=145005, d_model=1024, expand=2),
+]}
+
+
+def ssd_inputs(batch: int, seqlen: int, nheads: int, headdim: int = 64, dstate: int = 128, seed: int = 0,
+               with_h0: bool = False, with_D: bool = True) -> Dict[str, Optional[torch.Tensor]]:
+    """Draw one problem of the state-space-duality layer. Keys: x, dt, B, C (bf16), A, D, dt_bias, h0."""
+    g = _gen(seed)
+    x = torch.randn(batch, seqlen, nheads, headdim, generator=g)
+    dt = 0.5 * torch.randn(batch, seqlen, nheads, generator=g)
+    Bm = torch.randn(batch, seqlen, dstate, generator=g)
+    Cm = torch.randn(batch, seqlen, dstate, generator=g)
+    D = torch.randn(nheads, generator=g)
+    dt0 = _log_uniform(g, nheads, 1e-3, 0.1)
+    dt_bias = (dt0 + torch.log(-torch.expm1(-dt0))).to(torch.float32)
+    A = -(1.0 + 15.0 * torch.rand(nheads, generator=g))
+    h0 = torch.randn(batch, nheads, headdim, dstate, generator=g) if with_h0 else None
+    bf = torch.bfloat16
+    return {
+        "x": x.to(bf).contiguous(), "dt": dt.to(bf).contiguous(), "B": Bm.to(bf).contiguous(),
+        "C": Cm.to(bf).contiguous(), "A": A.contiguous(), "D": D.contiguous() if with_D else None,
+        "dt_bias": dt_bias.contiguous(), "h0": h0.contiguous() if h0 is not None else None,
+    }
+
+
+def ssd_workload_inputs(w: SsdWorkload) -> Dict[str, Optional[torch.Tensor]]:
+    return ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.seed)

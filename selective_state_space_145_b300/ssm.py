@@ -29,7 +29,7 @@ _lib = None
 EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_scan_default_chunk_len",
            "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update",
            "ssm_selective_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_selective_scan_bwd",
-           "ssm_conv_bwd_workspace_bytes", "ssm_causal_conv1d_bwd")
+           "ssm_conv_bwd_workspace_bytes", "ssm_causal_conv1d_bwd", "ssm_ssd_workspace_bytes", "ssm_ssd_fwd")
 
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -81,6 +81,10 @@ def lib() -> ctypes.CDLL:
         L.ssm_selective_scan_bwd.restype = i
         L.ssm_selective_scan_bwd.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, vp, fp]
                                              + [vp, vp, vp, fp, fp, fp, fp, fp, fp] + [i] * 5 + [vp, sz, u, vp])
+        L.ssm_ssd_workspace_bytes.restype = sz
+        L.ssm_ssd_workspace_bytes.argtypes = [i] * 6
+        L.ssm_ssd_fwd.restype = i
+        L.ssm_ssd_fwd.argtypes = [vp, vp, fp, vp, vp, fp, fp, i, fp, vp, fp] + [i] * 6 + [vp, sz, vp]
         L.ssm_selective_state_update.restype = i
         L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
                                                  i, i, i, i, u, vp]
@@ -253,6 +257,47 @@ def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor
     if return_conv_state:
         res = res + (conv_state_out,)
     return res
+
+
+def ssm_ssd_workspace_bytes(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int, io) -> int:
+    return int(lib().ssm_ssd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, _DTYPE_CODE[io]))
+
+
+def ssm_ssd_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                D: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = True,
+                h0: Optional[torch.Tensor] = None, return_last_state: bool = True,
+                workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                h_last: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Multi-head SSM with one decay per head (the state-space-duality layer). Returns (y, h_last).
+
+    x [batch, L, nheads, headdim], dt [batch, L, nheads], B, C [batch, L, dstate] (bfloat16);
+    A, D, dt_bias [nheads] and h0 [batch, nheads, headdim, dstate] float32. headdim 64, dstate 128.
+    The workspace is allocated here unless passed in."""
+    batch, L, H, P = x.shape
+    N = B.shape[2]
+    dev, io = x.device, x.dtype
+    _need(x, "x", (batch, L, H, P), io, dev)
+    _need(dt, "dt", (batch, L, H), io, dev)
+    _need(A, "A", (H,), torch.float32, dev)
+    _need(B, "B", (batch, L, N), io, dev)
+    _need(C, "C", (batch, L, N), io, dev)
+    _need(D, "D", (H,), torch.float32, dev, optional=True)
+    _need(dt_bias, "dt_bias", (H,), torch.float32, dev, optional=True)
+    _need(h0, "h0", (batch, H, P, N), torch.float32, dev, optional=True)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", (batch, L, H, P), io, dev)
+    if return_last_state and h_last is None:
+        h_last = torch.empty(batch, H, P, N, dtype=torch.float32, device=dev)
+    _need(h_last, "h_last", (batch, H, P, N), torch.float32, dev, optional=True)
+    need = ssm_ssd_workspace_bytes(batch, L, H, P, N, io)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib().ssm_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                           int(bool(dt_softplus)), _ptr(h0), _ptr(out), _ptr(h_last), batch, L, H, P, N,
+                           _io_code(x), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev))
+    _check("ssm_ssd_fwd", st)
+    return out, h_last
 
 
 def ssm_scan_bwd_workspace_bytes(batch: int, dim: int, seqlen: int, dstate: int, io) -> int:

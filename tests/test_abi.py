@@ -152,6 +152,31 @@ def test_decode_and_conv_argument_checks(L):
     assert c(FAKE, FAKE, None, None, FAKE, 0, 4, 8, 4, 1, 0, None) == 0
 
 
+def test_ssd_argument_checks_and_workspace(L):
+    f = L.ssm_ssd_fwd
+    # x, dt, A, B, C, D, dt_bias, softplus, h0, y, h_last, batch, L, H, P, N, io, ws, ws_bytes, stream
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 1, None, FAKE, None, 2, 300, 4, 64, 128, 1, FAKE, 1 << 40, None]
+    for i, v, want in ((16, 0, 2),        # fp32 I/O: the tensor-core path is bf16
+                       (14, 32, 2),       # head dim other than 64
+                       (15, 64, 2),       # state dim other than 128
+                       (0, None, 1),      # x missing
+                       (7, 2, 1),         # softplus flag not 0/1
+                       (18, 1024, 1),     # workspace too small
+                       (17, None, 1),     # workspace missing
+                       (0, FAKE + 2, 2),  # x not 16-byte aligned
+                       (17, FAKE + 16, 2),  # workspace not 256-byte aligned
+                       (11, 0, 0),        # no sequences: nothing to do
+                       (13, 0, 0)):
+        bad = list(base)
+        bad[i] = v
+        assert f(*bad) == want, (i, v)
+    ws = L.ssm_ssd_workspace_bytes
+    q = (300 + 127) // 128
+    pairs = 2 * 4 * q
+    assert ws(2, 300, 4, 64, 128, 1) == 256 + (pairs * 4 + 255) // 256 * 256 + pairs * 128 * 64 * 8
+    assert ws(2, 300, 4, 64, 128, 0) == 0 and ws(2, 300, 4, 32, 128, 1) == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import selective_state_space_145_b300.ssm as s
 

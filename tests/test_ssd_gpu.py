@@ -1,0 +1,116 @@
+"""GPU parity of the multi-head SSM with one decay per head (the state-space-duality layer, run on
+the tcgen05 tensor cores), called through the C ABI, against the fp64 oracle on the same seeded
+inputs: whole small problems (one chunk, several chunks, a ragged last chunk, one step, with and
+without an initial state or softplus) and sampled heads of the full-size workload. Tolerance is
+the bf16-I/O bound: |gpu - oracle| <= 1e-2 + 2e-2 |oracle| on y and on the final state.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_145_b300 import inputs
+from ssm_testutil import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _ssm():
+    import selective_state_space_145_b300 as ssm
+
+    return ssm
+
+
+def _dev(p, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+
+
+def _run(g, softplus=True, workspace=None):
+    ssm = _ssm()
+    batch, L, H, P = g["x"].shape
+    N = g["B"].shape[2]
+    if workspace is None:
+        workspace = torch.zeros(max(1, ssm.ssm_ssd_workspace_bytes(batch, L, H, P, N, torch.bfloat16)),
+                                dtype=torch.uint8, device=g["x"].device)
+    y, hl = ssm.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["dt_bias"], softplus, g["h0"],
+                            workspace=workspace)
+    torch.cuda.synchronize()
+    if L > 0:
+        assert int(workspace[:4].view(torch.int32).item()) == 0, "tensor-core wait ran out"
+    return y, hl
+
+
+CASES = [
+    # batch, L, heads, with_h0
+    (1, 128, 2, False),     # exactly one chunk
+    (2, 300, 3, True),      # three chunks, ragged last chunk, initial state
+    (1, 1, 1, True),        # one step
+    (2, 1000, 2, False),    # eight chunks, ragged
+    (3, 256, 5, True),      # two full chunks, odd head count
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}_l{}_h{}_h0{}".format(*c))
+def test_ssd_matches_oracle(cuda_device, case):
+    batch, L, H, with_h0 = case
+    p = inputs.ssd_inputs(batch, L, H, seed=11 + L + H, with_h0=with_h0)
+    y, hl = _run(_dev(p, cuda_device))
+    ref, ref_h = oracle.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["dt_bias"], True, p["h0"],
+                            nthreads=oracle.oracle.default_threads())
+    assert_close(y, ref, "bf16", "y")
+    assert_close(hl, ref_h, "bf16", "h_last")
+
+
+def test_ssd_softplus_off_and_no_skip(cuda_device):
+    p = inputs.ssd_inputs(2, 260, 2, seed=5, with_h0=True, with_D=False)
+    p["dt"] = (p["dt"].float().abs() * 0.05).to(torch.bfloat16)
+    p["dt_bias"] = torch.full((2,), 0.01)
+    y, hl = _run(_dev(p, cuda_device), softplus=False)
+    ref, ref_h = oracle.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], None, p["dt_bias"], False, p["h0"])
+    assert_close(y, ref, "bf16", "y")
+    assert_close(hl, ref_h, "bf16", "h_last")
+
+
+def test_ssd_deterministic_and_two_calls(cuda_device):
+    p = inputs.ssd_inputs(2, 512, 2, seed=8, with_h0=True)
+    g = _dev(p, cuda_device)
+    y1, h1 = _run(g)
+    y2, h2 = _run(g)
+    assert torch.equal(y1, y2) and torch.equal(h1, h2)
+    # two calls passing the state equal one call (the state is fp32 between calls)
+    L1 = 200
+    cut = lambda sl: {k: (v[:, sl].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in g.items()}
+    ya, ha = _run(cut(slice(0, L1)))
+    gb = cut(slice(L1, None))
+    gb["h0"] = ha
+    yb, hb = _run(gb)
+    assert_close(torch.cat([ya, yb], dim=1), y1.float().cpu().double().numpy(), "bf16", "two calls")
+    assert_close(hb, h1.cpu().double().numpy(), "bf16", "state after two calls")
+
+
+def test_ssd_empty(cuda_device):
+    ssm = _ssm()
+    p = _dev(inputs.ssd_inputs(2, 0, 3, seed=1, with_h0=True), cuda_device)
+    y, hl = ssm.ssm_ssd_fwd(p["x"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["dt_bias"], True, p["h0"])
+    torch.cuda.synchronize()
+    assert y.numel() == 0 and torch.equal(hl, p["h0"])
+    p["h0"] = None
+    y, hl = ssm.ssm_ssd_fwd(p["x"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["dt_bias"], True, None)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(hl) == 0
+
+
+def test_ssd_workload_sampled_heads(cuda_device):
+    """The full-size workload in the benchmark's launch configuration; two (batch, head) pairs
+    are recomputed by the oracle (heads are independent, so a head's slice is exact)."""
+    w = inputs.SSD_WORKLOADS["ssd_bf16_b8_l2048_h32_p64_n128"]
+    p = inputs.ssd_workload_inputs(w)
+    y, hl = _run(_dev(p, cuda_device))
+    y, hl = y.cpu(), hl.cpu()
+    for b, h in ((0, 0), (w.batch - 1, w.nheads - 1)):
+        sl = slice(h, h + 1)
+        ref, ref_h = oracle.ssd(p["x"][b:b + 1, :, sl], p["dt"][b:b + 1, :, sl], p["A"][sl], p["B"][b:b + 1],
+                                p["C"][b:b + 1], p["D"][sl], p["dt_bias"][sl], True, None)
+        assert_close(y[b:b + 1, :, sl], ref, "bf16", f"y b{b} h{h}")
+        assert_close(hl[b:b + 1, sl], ref_h, "bf16", f"h_last b{b} h{h}")
