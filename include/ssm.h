@@ -309,10 +309,10 @@ SSM_API ssm_status ssm_selective_scan_fwd_noalloc(const void* x, const void* del
  *   Delta_t   = softplus(dt[b,t,h] + dt_bias[h])        (the raw sum when dt_softplus == 0)
  *   H_t[p][n] = exp(Delta_t A[h]) H_{t-1}[p][n] + Delta_t x[b,t,h,p] B[b,t,n],   H_{-1} = h0 or 0
  *   y[b,t,h,p] = sum_n C[b,t,n] H_t[p][n] + D[h] x[b,t,h,p]
- * B and C are shared by all heads. The GPU evaluates the chunked dual form: per chunk of 128
- * steps the masked product (C B^T masked and decayed) X and the chunk state B^T (decayed X) on
- * the tensor cores (tcgen05, bf16 operands, fp32 accumulation), a carry pass over chunks in
- * fp32, and C H_in for the state entering the chunk.
+ * B and C are shared by all heads. The GPU evaluates the chunked dual form in one kernel: one
+ * CTA per (batch, head) walks chunks of 128 steps with the running state on the chip, and per
+ * chunk computes the masked product (C B^T masked and decayed) X, C H_in and the chunk's state
+ * increment B^T (decayed X) on the tensor cores (tcgen05, bf16 operands, fp32 accumulation).
  *
  *   x       [batch, seqlen, nheads, headdim] bf16      y [batch, seqlen, nheads, headdim] bf16
  *   dt      [batch, seqlen, nheads] bf16               B, C [batch, seqlen, dstate] bf16
@@ -320,11 +320,11 @@ SSM_API ssm_status ssm_selective_scan_fwd_noalloc(const void* x, const void* del
  *   h0, h_last [batch, nheads, headdim, dstate] float32 or NULL (h_last = h0 or 0 when seqlen == 0)
  *   io      SSM_BF16 only (SSM_F32 returns SSM_ERR_UNSUPPORTED); headdim must be 64 and dstate
  *           128, else SSM_ERR_UNSUPPORTED
- *   workspace  device buffer of ssm_ssd_workspace_bytes(...) bytes, 256-byte aligned; its
- *           contents need no initialisation. After the call its first 4 bytes hold a status
+ *   workspace  device buffer of ssm_ssd_workspace_bytes(...) bytes (256), 256-byte aligned;
+ *           its contents need no initialisation. After the call its first 4 bytes hold a status
  *           word: nonzero if a wait on the tensor cores ran out (results then invalid).
  * x, B, C and y must be 16-byte aligned; dt 2-byte aligned. The call allocates nothing and
- * runs three kernels on `stream`.
+ * runs one kernel (after clearing the status word) on `stream`.
  */
 SSM_API size_t ssm_ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, ssm_dtype io);
 SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,

@@ -70,10 +70,6 @@ struct SsdArgs {
   float* h_last;         // [batch, nheads, 64, 128] or NULL
   int batch, seqlen, nheads, nchunks;
   int* ws_status;        // nonzero after the call: a tensor-core wait ran out
-  float* ws_cs;          // [batch][nheads][nchunks] sum of Delta A log2(e) over the chunk
-  float* ws_S;           // [batch][nheads][nchunks][128][64] chunk states from zero (fp32)
-  void* ws_Sin;          // [batch][nheads][nchunks][128][64] state entering each chunk, bf16(v)
-  void* ws_Sin_lo;       // the same, bf16(v - bf16(v))
 };
 
 struct ConvBwdArgs {

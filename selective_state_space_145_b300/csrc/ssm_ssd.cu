@@ -5,22 +5,38 @@
 // Structured State Space Duality": multi-head SSM, the state dimension used like a head
 // dimension, the computation mapped to structured matrix products; "Mamba" (ozercemkelahmet.com),
 // "Mamba-2 and the dual view": the layer as a masked matrix product with a decaying mask). Per
-// batch element b and head h, state H [P x N]:
+// batch element b and head h, state H [N x P] (stored transposed to the public [P x N]):
 //   Delta_t = softplus(dt[b,t,h] + dt_bias[h]),  a_t = exp(Delta_t A[h])
-//   H_t = a_t H_{t-1} + Delta_t x_t B_t^T,  y_t = H_t C_t + D[h] x_t
-// Chunked form (chunk of Q = 128 steps, c_t = sum of Delta A over the chunk up to t):
-//   intra-chunk:  y_t += sum_{s<=t} (C_t . B_s) exp(c_t - c_s) Delta_s x_s     (masked G = C B^T)
-//   chunk state:  S = sum_s exp(c_end - c_s) Delta_s B_s x_s^T                  ([N x P], from zero)
-//   carry-in:     H_in(chunk q+1) = exp(c_end(q)) H_in(q) + S(q)                 (sequential, cheap)
-//   inter-chunk:  y_t += exp(c_t) C_t . H_in
-// Three launches: chunk states (one tcgen05 GEMM per chunk), the carry pass (CUDA cores), chunk
-// outputs (tcgen05 GEMMs per chunk: G = C B^T, G' X, C H_in). Every GEMM is bf16 x bf16 into fp32
-// tensor memory; operands are staged into shared memory with 16-byte cp.async copies in the
-// no-swizzle core-matrix layout; the masked decay of G is applied in registers between GEMMs.
-// Operands the kernels compute (G' and H_in) are carried as two bf16 terms, hi = bf16(v) and
-// lo = bf16(v - hi), multiplied in two GEMMs into one accumulator: a single bf16 rounding of them
-// costs up to 2^-9 of each summand, which for sums of 128 products of O(1) terms that cancel
-// exceeds the bf16-I/O tolerance on a fraction of a percent of the outputs.
+//   H_t = a_t H_{t-1} + Delta_t B_t x_t^T,  y_t = H_t^T C_t + D[h] x_t
+// Chunked form (chunks of Q = 128 steps; c_t = sum of Delta A over the chunk up to t):
+//   y_t   = sum_{s<=t} (C_t . B_s) exp(c_t - c_s) Delta_s x_s  +  exp(c_t) C_t . H_in  +  D x_t
+//   H_out = exp(c_end) H_in + sum_s exp(c_end - c_s) Delta_s B_s x_s^T
+//
+// Design. One CTA of 256 threads per (batch, head) walks the chunks in order and keeps the
+// running state on the chip: fp32 in registers (row n of H is held by threads n and n + 128,
+// 32 columns each), and as the bf16 operand of the next chunk's GEMM in shared memory. Rows of
+// the tensor-memory accumulators map to threads; the two warps that share a row split its
+// columns. Per chunk, two rounds of tcgen05 GEMMs
+// (bf16 operands, fp32 accumulators in tensor memory, issued by one thread, completion through an
+// mbarrier):
+//   round A:  G = C B^T [Q x Q] and Y_off = C H_in [Q x P];
+//   (threads) G' = G masked to s <= t and scaled by exp(c_t - c_s) Delta_s; B~ = B scaled per row
+//             by Delta_s exp(c_end - c_s);
+//   round B:  Y_diag = G' X [Q x P] and S = B~^T X [N x P];
+//   (threads) y = Y_diag + exp(c_t) Y_off + D x; H <- exp(c_end) H + S.
+// The next chunk's C, B and X are copied in while the epilogue and the state update of the current
+// one run: when the sequence length is a multiple of the chunk, by three TMA bulk-tensor copies
+// issued by one thread, whose 4-D / 5-D boxes (8 elements, 8 rows, column groups, row groups)
+// land directly in the no-swizzle core-matrix layout; otherwise by 16-byte cp.async copies with
+// zero fill past the end. The B tile serves as
+// the K-major B operand of G and, scaled, as the MN-major A operand of S: the two layouts are the
+// same bytes. Operands the kernel computes (G' and H_in) are carried as two bf16 terms,
+// hi = bf16(v) and lo = bf16(v - hi), multiplied in two GEMMs into one accumulator: a single bf16
+// rounding of them costs up to 2^-9 of each summand, which for sums of 128 products of O(1)
+// terms that cancel exceeds the bf16-I/O tolerance on a fraction of a percent of the outputs.
+#include <cstring>
+
+#include <cuda.h>  // CUtensorMap and its encoder's signature (resolved at run time, not linked)
 #include <cuda_bf16.h>
 
 #include "ssm_device.cuh"
@@ -30,64 +46,32 @@
 namespace ssm {
 namespace {
 
-constexpr int kQ = 128;  // chunk length; one thread (and one TMEM lane) per step
+constexpr int kQ = 128;  // chunk length; one TMEM lane per step
 constexpr int kP = 64;   // head dim
 constexpr int kN = 128;  // state dim
-constexpr int kThreads = 128;
-static_assert(kQ == kN, "the masked G' [Q x Q] reuses the B tile [Q x N]");
-static_assert(kQ == kThreads, "one thread per step");
+constexpr int kThreads = 256;  // two threads per row (step or state row), each with half the columns
+constexpr int kHalfP = kP / 2;
+static_assert(kQ == kN && 2 * kQ == kThreads, "two threads per step and per state row");
 
 using bf16 = __nv_bfloat16;
 
-// Shared-memory layout of the chunk-state kernel (byte offsets).
-struct StateSmem {
-  static constexpr int B = 0;                    // B^T [N x Q], MN-major: A operand (M = n, K = s)
-  static constexpr int X = B + kQ * kN * 2;      // X [Q x P] scaled rows, MN-major: B operand (N = p, K = s)
-  static constexpr int bytes = X + kQ * kP * 2;  // 48 KB
+// Shared-memory layout (byte offsets); 112 KB, so two CTAs fit an SM.
+struct Smem {
+  static constexpr int C = 0;                    // C [Q x N], K-major: A operand of G and Y_off (M = t,
+                                                 // K = n); after round A, G'_hi [Q x Q], K-major
+  static constexpr int B = C + kQ * kN * 2;      // B [Q x N]: K-major B operand of G (N = s, K = n); scaled,
+                                                 // the MN-major A operand of S (M = n, K = s)
+  static constexpr int X = B + kQ * kN * 2;      // X [Q x P], MN-major: B operand of Y_diag and S (N = p, K = s)
+  static constexpr int H = X + kQ * kP * 2;      // H_in hi, lo [N x P] each, MN-major: B operand of Y_off
+                                                 // (N = p, K = n); after round A, G'_lo [Q x Q], K-major
+  static constexpr int HL = H + kN * kP * 2;
+  static constexpr int bytes = HL + kN * kP * 2;
 };
 
-// Shared-memory layout of the chunk-output kernel.
-struct ScanSmem {
-  static constexpr int C = 0;                    // C [Q x N], K-major: A operand (M = t, K = n); then
-                                                 // G'_lo [Q x Q], K-major
-  static constexpr int BG = C + kQ * kN * 2;     // B [Q x N], K-major: B operand (N = s, K = n); then
-                                                 // G'_hi [Q x Q], K-major: A operand (M = t, K = s)
-  static constexpr int X = BG + kQ * kN * 2;     // X [Q x P], MN-major: B operand (N = p, K = s)
-  static constexpr int S = X + kQ * kP * 2;      // H_in hi [N x P], MN-major: B operand (N = p, K = n);
-                                                 // then c_t and Delta_t of the chunk (1 KB)
-  static constexpr int SL = S + kN * kP * 2;     // H_in lo [N x P]
-  static constexpr int bytes = SL + kN * kP * 2; // 112 KB: two CTAs per SM, 2 x 256 TMEM columns
-};
+// TMEM columns: G [128 x 128] (Y_diag [128 x 64] after it), Y_off [128 x 64], S [128 x 64].
+constexpr uint32_t kColG = 0, kColDiag = 0, kColOff = 128, kColS = 192, kCols = 256;
 
-// TMEM columns of the chunk-output kernel: G [128 x 128], C H_in [128 x 64], G' X [128 x 64].
-constexpr uint32_t kColG = 0, kColOff = 128, kColDiag = 192, kScanCols = 256;
-constexpr uint32_t kStateCols = 64;
-
-// Delta_t of this thread's step and the inclusive prefix over the chunk of Delta A log2(e).
-__device__ __forceinline__ void chunk_decay(const SsdArgs& a, int b, int h, int t0, int len, float* s_wsum,
-                                            float& Delta, float& cs) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  Delta = 0.f;
-  if (t < len) {
-    const float v = to_f32(static_cast<const bf16*>(a.dt)[((long long)b * a.seqlen + t0 + t) * a.nheads + h]) +
-                    (a.dt_bias ? a.dt_bias[h] : 0.f);
-    Delta = a.dt_softplus ? softplus_f<true>(v) : v;
-  }
-  float v = Delta * a.A[h] * kLog2e;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) s_wsum[warp] = v;
-  __syncthreads();
-  float off = 0.f;
-  for (int w = 0; w < warp; ++w) off += s_wsum[w];
-  cs = v + off;
-}
-
-// 8 bf16 of a 16-byte shared-memory chunk to fp32
-__device__ __forceinline__ void unpack8(const unsigned char* p, float (&f)[8]) {
+__device__ __forceinline__ void unpack8(const unsigned char* p, float* f) {
   const uint4 v = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -104,297 +88,332 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   for (int k = 0; k < 4; ++k) e[k] = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
   return v;
 }
-
-// ---- launch 1: S(q) = sum_s exp(c_end - c_s) Delta_s B_s x_s^T for every chunk q, as
-// D[n][p] = sum_s B[s][n] * (w_s x[s][p]); one CTA per (chunk, head, batch).
-__global__ void __launch_bounds__(kThreads) ssd_chunk_state_kernel(const SsdArgs a) {
-  extern __shared__ __align__(128) unsigned char sm[];
-  __shared__ uint64_t mbar;
-  __shared__ uint32_t tslot;
-  __shared__ float s_wsum[4];
-  __shared__ float s_cs_end;
-  const int t = threadIdx.x, warp = t >> 5;
-  const int q = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int L = a.seqlen, H = a.nheads;
-  const int t0 = q * kQ, len = min(kQ, L - t0);
-  const bf16* gB = static_cast<const bf16*>(a.B);
-  const bf16* gx = static_cast<const bf16*>(a.x);
-  unsigned char* sB = sm + StateSmem::B;
-  unsigned char* sX = sm + StateSmem::X;
-
-  // stage: a 16-byte chunk of row s holds 8 consecutive n (or p) at step s; rows past the
-  // sequence end are zero-filled
-  for (int i = t; i < kQ * kN / 8; i += kThreads) {
-    const int s = i / (kN / 8), n0 = (i % (kN / 8)) * 8;
-    const bool ok = s < len;
-    cp_async16(sB + umma::mnmajor_off(n0, s, kN), ok ? (const void*)(gB + ((long long)b * L + t0 + s) * kN + n0)
-                                                     : (const void*)gB, ok ? 16u : 0u);
-  }
-  for (int i = t; i < kQ * kP / 8; i += kThreads) {
-    const int s = i / (kP / 8), p0 = (i % (kP / 8)) * 8;
-    const bool ok = s < len;
-    cp_async16(sX + umma::mnmajor_off(p0, s, kP),
-               ok ? (const void*)(gx + (((long long)b * L + t0 + s) * H + h) * kP + p0) : (const void*)gx,
-               ok ? 16u : 0u);
-  }
-  cp_async_commit();
-  float Delta, cs;
-  chunk_decay(a, b, h, t0, len, s_wsum, Delta, cs);
-  if (t == kQ - 1) s_cs_end = cs;  // steps past the end add nothing, so the last prefix is the total
-  cp_async_wait<0>();
-  __syncthreads();
-  const float cs_end = s_cs_end;
-  // row t of X times Delta_t exp(c_end - c_t), rounded back to bf16 in place
-  const float w = Delta * ex2_approx(cs_end - cs);
+// v = hi + lo with hi = bf16(v), lo = bf16(v - hi), 8 values
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+  float h[8], l[8];
 #pragma unroll
-  for (int j = 0; j < kP / 8; ++j) {
-    unsigned char* p = sX + umma::mnmajor_off(j * 8, t, kP);
-    float f[8];
-    unpack8(p, f);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) f[k] *= w;
-    *reinterpret_cast<uint4*>(p) = pack8(f);
+  for (int k = 0; k < 8; ++k) {
+    h[k] = __bfloat162float(__float2bfloat16_rn(v[k]));
+    l[k] = v[k] - h[k];
   }
-  umma::fence_proxy_async();
-  if (warp == 0) umma::tmem_alloc(&tslot, kStateCols);
-  if (t == 0) umma::mbar_init(&mbar, 1);
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  const uint32_t tbase = tslot;
-  if (t == 0) {
-    constexpr uint32_t idesc = umma::idesc_bf16(kN, kP, true, true);
-#pragma unroll 1
-    for (int kk = 0; kk < kQ / 16; ++kk)
-      umma::mma_bf16(tbase, umma::desc_mnmajor(smem_addr(sB), kk, kN), umma::desc_mnmajor(smem_addr(sX), kk, kP),
-                     idesc, kk > 0);
-    umma::mma_commit(&mbar);
-  }
-  const bool ok = __all_sync(0xffffffffu, umma::mbar_wait(&mbar, 0));
-  umma::fence_after_sync();
-  const long long bhq = ((long long)b * H + h) * a.nchunks + q;
-  if (ok) {
-    float* dst = a.ws_S + (bhq * kN + t) * kP;  // row n = t of S
-#pragma unroll
-    for (int c0 = 0; c0 < kP; c0 += 16) {
-      float v[16];
-      umma::tmem_ld16(tbase + ((uint32_t)(warp * 32) << 16) + c0, v);
-#pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-    }
-  } else if ((t & 31) == 0) {
-    atomicExch(a.ws_status, 1);
-  }
-  if (t == 0) a.ws_cs[bhq] = cs_end;
-  umma::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) umma::tmem_dealloc(tbase, kStateCols);
+  hi = pack8(h);
+  lo = pack8(l);
 }
 
-// ---- launch 2: the state entering each chunk, H_in(q+1) = exp(c_end(q)) H_in(q) + S(q), kept in
-// fp32 and written as two bf16 terms [N x P] for the output GEMMs; the final state goes to
-// h_last [P x N].
-constexpr int kPassThreads = 256;
-__global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdArgs a) {
-  constexpr int kE = kN * kP;
-  constexpr int kPer = kE / 4 / kPassThreads;  // float4 groups per thread
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const long long bh = (long long)b * a.nheads + h;
-  float4 S[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int e = (k * kPassThreads + tid) * 4, n = e / kP, p = e % kP;
-    if (a.h0) {
-      const float* h0 = a.h0 + bh * kE;  // [P][N]
-      S[k] = make_float4(h0[p * kN + n], h0[(p + 1) * kN + n], h0[(p + 2) * kN + n], h0[(p + 3) * kN + n]);
-    } else {
-      S[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  bf16* sin = static_cast<bf16*>(a.ws_Sin);
-  bf16* sin_lo = static_cast<bf16*>(a.ws_Sin_lo);
-  for (int q = 0; q < a.nchunks; ++q) {
-    const long long base = (bh * a.nchunks + q) * kE;
-    const float dec = ex2_approx(a.ws_cs[bh * a.nchunks + q]);
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = (k * kPassThreads + tid) * 4;
-      const __nv_bfloat162 h01 = __floats2bfloat162_rn(S[k].x, S[k].y), h23 = __floats2bfloat162_rn(S[k].z, S[k].w);
-      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-      const __nv_bfloat162 l01 = __floats2bfloat162_rn(S[k].x - f01.x, S[k].y - f01.y);
-      const __nv_bfloat162 l23 = __floats2bfloat162_rn(S[k].z - f23.x, S[k].w - f23.y);
-      uint2 u;
-      u.x = *reinterpret_cast<const uint32_t*>(&h01);
-      u.y = *reinterpret_cast<const uint32_t*>(&h23);
-      *reinterpret_cast<uint2*>(sin + base + e) = u;
-      u.x = *reinterpret_cast<const uint32_t*>(&l01);
-      u.y = *reinterpret_cast<const uint32_t*>(&l23);
-      *reinterpret_cast<uint2*>(sin_lo + base + e) = u;
-      const float4 d = *reinterpret_cast<const float4*>(a.ws_S + base + e);
-      S[k] = make_float4(fmaf(dec, S[k].x, d.x), fmaf(dec, S[k].y, d.y), fmaf(dec, S[k].z, d.z),
-                         fmaf(dec, S[k].w, d.w));
-    }
-  }
-  if (a.h_last) {
-    float* hl = a.h_last + bh * kE;  // [P][N]
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int e = (k * kPassThreads + tid) * 4, n = e / kP, p = e % kP;
-      hl[p * kN + n] = S[k].x;
-      hl[(p + 1) * kN + n] = S[k].y;
-      hl[(p + 2) * kN + n] = S[k].z;
-      hl[(p + 3) * kN + n] = S[k].w;
-    }
-  }
-}
-
-// ---- launch 3: y_t = sum_{s<=t} G[t][s] exp(c_t - c_s) Delta_s x_s + exp(c_t) C_t . H_in + D x_t.
-__global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdArgs a) {
+// TMA: the tiles come from three tensor maps (C and B: 4-D, X: 5-D, described at launch_ssd).
+template <bool TMA>
+__global__ void __launch_bounds__(kThreads, 2)
+    ssd_fused_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmX) {
   extern __shared__ __align__(128) unsigned char sm[];
   __shared__ uint64_t mbar;
+  __shared__ uint64_t tbar;  // TMA completion
   __shared__ uint32_t tslot;
-  __shared__ float s_wsum[4];
-  const int t = threadIdx.x, warp = t >> 5;
-  const int q = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int L = a.seqlen, H = a.nheads;
-  const int t0 = q * kQ, len = min(kQ, L - t0);
+  __shared__ float s_wsum[8];
+  __shared__ float s_z[kQ];  // lg2(Delta_s) - c_s: exp(c_t - c_s) Delta_s = 2^(c_t + z_s) in log2 units
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = tid & (kQ - 1);  // the row (step t, or state row n) of this thread
+  const int half = tid >> 7;     // which half of the row's columns
+  const int wq = warp & 3;       // TMEM lane quarter of this warp
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int L = a.seqlen, H = a.nheads, nc = a.nchunks;
+  const long long bh = (long long)b * H + h;
   const bf16* gB = static_cast<const bf16*>(a.B);
   const bf16* gC = static_cast<const bf16*>(a.C);
   const bf16* gx = static_cast<const bf16*>(a.x);
-  const long long bhq = ((long long)b * H + h) * a.nchunks + q;
-  const bf16* gS = static_cast<const bf16*>(a.ws_Sin) + bhq * kN * kP;
-  const bf16* gSl = static_cast<const bf16*>(a.ws_Sin_lo) + bhq * kN * kP;
-  unsigned char* sC = sm + ScanSmem::C;
-  unsigned char* sBG = sm + ScanSmem::BG;
-  unsigned char* sX = sm + ScanSmem::X;
-  unsigned char* sS = sm + ScanSmem::S;
-  unsigned char* sSl = sm + ScanSmem::SL;
-  float* s_cs = reinterpret_cast<float*>(sS);  // after the first GEMMs: c_t and Delta_t
-  float* s_dl = s_cs + kQ;
-
-  for (int i = t; i < kQ * kN / 8; i += kThreads) {
-    const int s = i / (kN / 8), n0 = (i % (kN / 8)) * 8;
-    const bool ok = s < len;
-    const long long g = ((long long)b * L + t0 + s) * kN + n0;
-    cp_async16(sC + umma::kmajor_off(s, n0, kN), ok ? (const void*)(gC + g) : (const void*)gC, ok ? 16u : 0u);
-    cp_async16(sBG + umma::kmajor_off(s, n0, kN), ok ? (const void*)(gB + g) : (const void*)gB, ok ? 16u : 0u);
-  }
-  for (int i = t; i < kQ * kP / 8; i += kThreads) {
-    const int s = i / (kP / 8), p0 = (i % (kP / 8)) * 8;
-    const bool ok = s < len;
-    cp_async16(sX + umma::mnmajor_off(p0, s, kP),
-               ok ? (const void*)(gx + (((long long)b * L + t0 + s) * H + h) * kP + p0) : (const void*)gx,
-               ok ? 16u : 0u);
-  }
-  for (int i = t; i < kN * kP / 8; i += kThreads) {
-    const int n = i / (kP / 8), p0 = (i % (kP / 8)) * 8;
-    cp_async16(sS + umma::mnmajor_off(p0, n, kP), gS + n * kP + p0, 16u);
-    cp_async16(sSl + umma::mnmajor_off(p0, n, kP), gSl + n * kP + p0, 16u);
-  }
-  cp_async_commit();
-  float Delta, cs;
-  chunk_decay(a, b, h, t0, len, s_wsum, Delta, cs);
-  cp_async_wait<0>();
-  umma::fence_proxy_async();
-  if (warp == 0) umma::tmem_alloc(&tslot, kScanCols);
-  if (t == 0) umma::mbar_init(&mbar, 1);
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  const uint32_t tbase = tslot;
-  const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
-  if (t == 0) {
-    constexpr uint32_t idG = umma::idesc_bf16(kQ, kQ, false, false);
-    constexpr uint32_t idOff = umma::idesc_bf16(kQ, kP, false, true);
-#pragma unroll 1
-    for (int kk = 0; kk < kN / 16; ++kk)
-      umma::mma_bf16(tbase + kColG, umma::desc_kmajor(smem_addr(sC), kk, kN),
-                     umma::desc_kmajor(smem_addr(sBG), kk, kN), idG, kk > 0);
-#pragma unroll 1
-    for (int kk = 0; kk < kN / 16; ++kk)
-      umma::mma_bf16(tbase + kColOff, umma::desc_kmajor(smem_addr(sC), kk, kN),
-                     umma::desc_mnmajor(smem_addr(sS), kk, kP), idOff, kk > 0);
-#pragma unroll 1
-    for (int kk = 0; kk < kN / 16; ++kk)
-      umma::mma_bf16(tbase + kColOff, umma::desc_kmajor(smem_addr(sC), kk, kN),
-                     umma::desc_mnmajor(smem_addr(sSl), kk, kP), idOff, true);
-    umma::mma_commit(&mbar);
-  }
-  bool ok = __all_sync(0xffffffffu, umma::mbar_wait(&mbar, 0));
-  umma::fence_after_sync();
-  // the GEMMs that read C, B and H_in have completed: their tiles take c_t, Delta_t and G'
-  s_cs[t] = cs;
-  s_dl[t] = Delta;
-  __syncthreads();
-  // G' = G masked to s <= t, times exp(c_t - c_s) Delta_s, as hi + lo bf16 terms in the places of
-  // the B and C tiles
-#pragma unroll 1
-  for (int s0 = 0; s0 < kQ; s0 += 16) {
-    float g[16];
-    if (ok) umma::tmem_ld16(trow + kColG + s0, g);
-    float v[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int s = s0 + j;
-      const float e = ex2_approx(cs - s_cs[s]) * s_dl[s];
-      v[j] = (ok && s <= t) ? g[j] * e : 0.f;
-    }
-    float hi[16], lo[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      hi[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
-      lo[j] = v[j] - hi[j];
-    }
-    *reinterpret_cast<uint4*>(sBG + umma::kmajor_off(t, s0, kQ)) = pack8(hi);
-    *reinterpret_cast<uint4*>(sBG + umma::kmajor_off(t, s0 + 8, kQ)) = pack8(hi + 8);
-    *reinterpret_cast<uint4*>(sC + umma::kmajor_off(t, s0, kQ)) = pack8(lo);
-    *reinterpret_cast<uint4*>(sC + umma::kmajor_off(t, s0 + 8, kQ)) = pack8(lo + 8);
-  }
-  umma::fence_proxy_async();
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  if (t == 0) {
-    constexpr uint32_t idDiag = umma::idesc_bf16(kQ, kP, false, true);
-#pragma unroll 1
-    for (int kk = 0; kk < kQ / 16; ++kk)
-      umma::mma_bf16(tbase + kColDiag, umma::desc_kmajor(smem_addr(sBG), kk, kQ),
-                     umma::desc_mnmajor(smem_addr(sX), kk, kP), idDiag, kk > 0);
-#pragma unroll 1
-    for (int kk = 0; kk < kQ / 16; ++kk)
-      umma::mma_bf16(tbase + kColDiag, umma::desc_kmajor(smem_addr(sC), kk, kQ),
-                     umma::desc_mnmajor(smem_addr(sX), kk, kP), idDiag, true);
-    umma::mma_commit(&mbar);
-  }
-  ok = __all_sync(0xffffffffu, umma::mbar_wait(&mbar, 1)) && ok;
-  umma::fence_after_sync();
-  if (!ok && (t & 31) == 0) atomicExch(a.ws_status, 1);
-  // epilogue: row t
-  const float et = ex2_approx(cs);
+  const bf16* gdt = static_cast<const bf16*>(a.dt);
+  unsigned char* sC = sm + Smem::C;
+  unsigned char* sB = sm + Smem::B;
+  unsigned char* sX = sm + Smem::X;
+  unsigned char* sH = sm + Smem::H;
+  unsigned char* sHL = sm + Smem::HL;
+  const float A2 = a.A[h] * kLog2e;
+  const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
   const float Dh = a.D ? a.D[h] : 0.f;
-  bf16* yrow = static_cast<bf16*>(a.y) + (((long long)b * L + t0 + t) * H + h) * kP;
-#pragma unroll 1
-  for (int p0 = 0; p0 < kP; p0 += 16) {
-    float yd[16], yo[16];
-    if (ok) {
-      umma::tmem_ld16(trow + kColDiag + p0, yd);
-      umma::tmem_ld16(trow + kColOff + p0, yo);
+
+  // C, B, X of chunk q into their tiles; rows past the sequence end are zero-filled. Copy k of
+  // thread tid: C / B row s = tid/16 + 16k, columns 8 (tid%16) ..; X row s = tid/8 + 32k, columns
+  // 8 (tid%8) .. (the core-matrix offsets of those rows and columns, written out)
+  const uint32_t cb_soff = (uint32_t)((tid / 128) * 2048 + (tid % 16) * 128 + ((tid / 16) % 8) * 16);  // + 4096 k
+  const uint32_t x_soff = (uint32_t)((tid / 64) * 1024 + (tid % 8) * 128 + ((tid / 8) % 8) * 16);     // + 4096 k
+  auto stage = [&](int q) {
+    const int t0 = q * kQ, len = min(kQ, L - t0);
+    if (TMA) {  // whole chunks only: no row of another sequence, none past the end
+      if (tid == 0) {
+        umma::fence_proxy_async();
+        umma::mbar_expect_tx(&tbar, (uint32_t)(2 * kQ * kN * 2 + kQ * kP * 2));
+        const int r8 = (int)(((long long)b * L + t0) / 8);
+        umma::tma_load_4d(sC, &tmC, 0, 0, 0, r8, &tbar);
+        umma::tma_load_4d(sB, &tmB, 0, 0, 0, r8, &tbar);
+        umma::tma_load_5d(sX, &tmX, 0, 0, 0, r8, h, &tbar);
+      }
+      return;
     }
-    float xv[16];
-    unpack8(sX + umma::mnmajor_off(p0, t, kP), *reinterpret_cast<float(*)[8]>(xv));
-    unpack8(sX + umma::mnmajor_off(p0 + 8, t, kP), *reinterpret_cast<float(*)[8]>(xv + 8));
-    float o[16];
+    const long long cbg = ((long long)b * L + t0 + tid / 16) * kN + (tid % 16) * 8;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) o[j] = ok ? fmaf(et, yo[j], yd[j]) + Dh * xv[j] : 0.f;
-    if (t < len) {
-      *reinterpret_cast<uint4*>(yrow + p0) = pack8(o);
-      *reinterpret_cast<uint4*>(yrow + p0 + 8) = pack8(o + 8);
+    for (int k = 0; k < kQ * kN / 8 / kThreads; ++k) {
+      const bool ok = tid / 16 + 16 * k < len;
+      const long long g = cbg + (long long)k * 16 * kN;
+      cp_async16(sC + cb_soff + 4096u * k, ok ? (const void*)(gC + g) : (const void*)gC, ok ? 16u : 0u);
+      cp_async16(sB + cb_soff + 4096u * k, ok ? (const void*)(gB + g) : (const void*)gB, ok ? 16u : 0u);
     }
+    const long long xg = (((long long)b * L + t0 + tid / 8) * H + h) * kP + (tid % 8) * 8;
+#pragma unroll
+    for (int k = 0; k < kQ * kP / 8 / kThreads; ++k) {
+      const bool ok = tid / 8 + 32 * k < len;
+      const long long g = xg + (long long)k * 32 * H * kP;
+      cp_async16(sX + x_soff + 4096u * k, ok ? (const void*)(gx + g) : (const void*)gx, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  auto load_dt = [&](int q) -> float {
+    const int s = q * kQ + t;
+    return s < L ? to_f32(gdt[((long long)b * L + s) * H + h]) : 0.f;
+  };
+
+  // running state: row n = t of H [N x P], columns pb .. pb + 31, fp32
+  const int pb = half * kHalfP;
+  float Hs[kHalfP];
+#pragma unroll
+  for (int p = 0; p < kHalfP; ++p) Hs[p] = a.h0 ? a.h0[(bh * kP + pb + p) * kN + t] : 0.f;
+  // its bf16 hi / lo operand tiles (element (p, n) of the B operand of Y_off)
+  auto write_state = [&]() {
+#pragma unroll
+    for (int p0 = 0; p0 < kHalfP; p0 += 8) {
+      uint4 hi, lo;
+      split8(Hs + p0, hi, lo);
+      *reinterpret_cast<uint4*>(sH + umma::mnmajor_off(pb + p0, t, kP)) = hi;
+      *reinterpret_cast<uint4*>(sHL + umma::mnmajor_off(pb + p0, t, kP)) = lo;
+    }
+  };
+  write_state();
+  float dtv = load_dt(0);
+  if (warp == 0) umma::tmem_alloc(&tslot, kCols);
+  if (tid == 0) {
+    umma::mbar_init(&mbar, 1);
+    umma::mbar_init(&tbar, 1);
   }
   umma::fence_before_sync();
   __syncthreads();
-  if (warp == 0) umma::tmem_dealloc(tbase, kScanCols);
+  umma::fence_after_sync();
+  stage(0);
+  uint32_t tparity = 0;
+  const uint32_t tbase = tslot;
+  const uint32_t trow = tbase + ((uint32_t)(wq * 32) << 16);
+  uint32_t parity = 0;
+  bool ok = true;
+
+#pragma unroll 1
+  for (int q = 0; q < nc; ++q) {
+    const int t0 = q * kQ, len = min(kQ, L - t0);
+    // ---- Delta_t and the prefix c_t (log2 units) of this chunk; the next chunk's dt in flight
+    float Delta = 0.f;
+    if (t < len) Delta = a.dt_softplus ? softplus_f<true>(dtv + bias) : dtv + bias;
+    if (q + 1 < nc) dtv = load_dt(q + 1);
+    float v = Delta * A2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) s_wsum[warp] = v;
+    __syncthreads();
+    // both halves scan all 128 steps; each reads its own half's warp totals
+    const float* ws = s_wsum + 4 * half;
+    float off = 0.f, c_end = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (w < wq) off += ws[w];
+      if (w < 3) c_end += ws[w];
+    }
+    c_end += ws[3];
+    const float cs = v + off;
+    if (half == 0) s_z[t] = lg2_approx(Delta) - cs;  // -inf past the end (Delta = 0): those columns vanish
+    if (TMA) {
+      ok = __syncthreads_and(umma::mbar_wait(&tbar, tparity)) && ok;
+      tparity ^= 1;
+      if (!ok) break;
+    } else {
+      cp_async_wait<0>();
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+
+    // ---- round A: G = C B^T, Y_off = C H_in (hi + lo)
+    if (tid == 0) {
+      constexpr uint32_t idG = umma::idesc_bf16(kQ, kQ, false, false);
+      constexpr uint32_t idOff = umma::idesc_bf16(kQ, kP, false, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kN / 16; ++kk)
+        umma::mma_bf16(tbase + kColG, umma::desc_kmajor(smem_addr(sC), kk, kN),
+                       umma::desc_kmajor(smem_addr(sB), kk, kN), idG, kk > 0);
+#pragma unroll 1
+      for (int kk = 0; kk < kN / 16; ++kk)
+        umma::mma_bf16(tbase + kColOff, umma::desc_kmajor(smem_addr(sC), kk, kN),
+                       umma::desc_mnmajor(smem_addr(sH), kk, kP), idOff, kk > 0);
+#pragma unroll 1
+      for (int kk = 0; kk < kN / 16; ++kk)
+        umma::mma_bf16(tbase + kColOff, umma::desc_kmajor(smem_addr(sC), kk, kN),
+                       umma::desc_mnmajor(smem_addr(sHL), kk, kP), idOff, true);
+      umma::mma_commit(&mbar);
+    }
+    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity)) && ok;
+    parity ^= 1;
+    umma::fence_after_sync();
+    if (!ok) break;
+
+    // ---- G' (hi into the C tile, lo into the H tiles) and B~ = Delta_s exp(c_end - c_s) B_s
+#pragma unroll 1
+    for (int j2 = 0; j2 < 2; ++j2) {
+      const int s0 = 32 * (2 * j2 + half);
+      uint4 hi[4], lo[4];
+      if (s0 < 32 * (wq + 1)) {  // some row of this warp reaches column s0
+        float g[32];
+        umma::tmem_ld32(trow + kColG + s0, g);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int s = s0 + j;
+          g[j] = s <= t ? g[j] * ex2_approx(cs + s_z[s]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) split8(g + 8 * k, hi[k], lo[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) hi[k] = lo[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        *reinterpret_cast<uint4*>(sC + umma::kmajor_off(t, s0 + 8 * k, kQ)) = hi[k];
+        *reinterpret_cast<uint4*>(sH + umma::kmajor_off(t, s0 + 8 * k, kQ)) = lo[k];
+      }
+    }
+    {
+      const float w = Delta * ex2_approx(c_end - cs);
+#pragma unroll 4
+      for (int n0 = half * (kN / 2); n0 < (half + 1) * (kN / 2); n0 += 8) {
+        unsigned char* p = sB + umma::kmajor_off(t, n0, kN);
+        float f[8];
+        unpack8(p, f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] *= w;
+        *reinterpret_cast<uint4*>(p) = pack8(f);
+      }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+
+    // ---- round B: Y_diag = G' X (hi + lo), S = B~^T X
+    if (tid == 0) {
+      constexpr uint32_t idDiag = umma::idesc_bf16(kQ, kP, false, true);
+      constexpr uint32_t idS = umma::idesc_bf16(kN, kP, true, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        umma::mma_bf16(tbase + kColDiag, umma::desc_kmajor(smem_addr(sC), kk, kQ),
+                       umma::desc_mnmajor(smem_addr(sX), kk, kP), idDiag, kk > 0);
+#pragma unroll 1
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        umma::mma_bf16(tbase + kColDiag, umma::desc_kmajor(smem_addr(sH), kk, kQ),
+                       umma::desc_mnmajor(smem_addr(sX), kk, kP), idDiag, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        umma::mma_bf16(tbase + kColS, umma::desc_mnmajor(smem_addr(sB), kk, kN),
+                       umma::desc_mnmajor(smem_addr(sX), kk, kP), idS, kk > 0);
+      umma::mma_commit(&mbar);
+    }
+    // this step's x, for the skip term, before the tile is refilled
+    uint4 xr[kHalfP / 8];
+#pragma unroll
+    for (int j = 0; j < kHalfP / 8; ++j)
+      xr[j] = *reinterpret_cast<const uint4*>(sX + umma::mnmajor_off(pb + 8 * j, t, kP));
+    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity)) && ok;
+    parity ^= 1;
+    umma::fence_after_sync();
+    if (!ok) break;
+    // every operand tile is free: bring in the next chunk while this one finishes
+    if (q + 1 < nc) stage(q + 1);
+
+    // ---- epilogue (row t) and state update (row n = t)
+    const float et = ex2_approx(cs), dec = ex2_approx(c_end);
+    bf16* yrow = static_cast<bf16*>(a.y) + (((long long)b * L + t0 + t) * H + h) * kP;
+#pragma unroll
+    for (int p0 = 0; p0 < kHalfP; p0 += 16) {
+      float yd[16], yo[16], sv[16];
+      umma::tmem_ld16x3(trow + kColDiag + pb + p0, trow + kColOff + pb + p0, trow + kColS + pb + p0, yd, yo, sv);
+      float xv[16];
+      unpack8(reinterpret_cast<const unsigned char*>(&xr[p0 / 8]), xv);
+      unpack8(reinterpret_cast<const unsigned char*>(&xr[p0 / 8 + 1]), xv + 8);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        yd[j] = fmaf(et, yo[j], yd[j]) + Dh * xv[j];
+        Hs[p0 + j] = fmaf(dec, Hs[p0 + j], sv[j]);
+      }
+      if (t < len) {
+        *reinterpret_cast<uint4*>(yrow + pb + p0) = pack8(yd);
+        *reinterpret_cast<uint4*>(yrow + pb + p0 + 8) = pack8(yd + 8);
+      }
+    }
+    write_state();
+    umma::fence_before_sync();
+  }
+
+  if (!ok) {
+    if (tid == 0) atomicExch(a.ws_status, 1);
+  } else if (a.h_last) {
+#pragma unroll
+    for (int p = 0; p < kHalfP; ++p) a.h_last[(bh * kP + pb + p) * kN + t] = Hs[p];
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) umma::tmem_dealloc(tbase, kCols);
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library does not link the
+// driver library itself)
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+// The tensor maps of the TMA path. Rows are flat (batch * seqlen + t). C, B [rows, 128]: dims
+// (n%8, row%8, n/8, row/8); X [rows, heads, 64]: dims (p%8, row%8, p/8, row/8, head). A box
+// (8, 8, all column groups, 16 row groups) is one 128-row chunk in core-matrix order.
+bool make_maps(const SsdArgs& a, CUtensorMap* mC, CUtensorMap* mB, CUtensorMap* mX) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t rows = (cuuint64_t)a.batch * a.seqlen;
+  const cuuint64_t dCB[4] = {8, 8, kN / 8, rows / 8};
+  const cuuint64_t sCB[3] = {kN * 2, 16, 8 * kN * 2};
+  const cuuint32_t bCB[4] = {8, 8, kN / 8, kQ / 8};
+  const cuuint32_t e4[4] = {1, 1, 1, 1};
+  const cuuint64_t H = (cuuint64_t)a.nheads;
+  const cuuint64_t dX[5] = {8, 8, kP / 8, rows / 8, H};
+  const cuuint64_t sX[4] = {H * kP * 2, 16, 8 * H * kP * 2, kP * 2};
+  const cuuint32_t bX[5] = {8, 8, kP / 8, kQ / 8, 1};
+  const cuuint32_t e5[5] = {1, 1, 1, 1, 1};
+  auto go = [&](CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* d, const cuuint64_t* st,
+                const cuuint32_t* bx, const cuuint32_t* el) {
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, bx, el,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  return go(mC, a.C, 4, dCB, sCB, bCB, e4) && go(mB, a.B, 4, dCB, sCB, bCB, e4) && go(mX, a.x, 5, dX, sX, bX, e5);
 }
 
 }  // namespace
@@ -402,20 +421,17 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdArgs 
 int ssd_chunk_len() { return kQ; }
 
 size_t ssd_workspace_bytes(int batch, int nheads, int nchunks) {
-  const size_t pairs = (size_t)batch * nheads * nchunks;
-  const size_t cs = (pairs * sizeof(float) + 255) & ~(size_t)255;
-  return 256 + cs + pairs * kN * kP * (sizeof(float) + 2 * sizeof(bf16));
+  (void)batch;
+  (void)nheads;
+  (void)nchunks;
+  return 256;  // the status word
 }
 
 void ssd_workspace_split(void* ws, int batch, int nheads, int nchunks, SsdArgs& a) {
-  const size_t pairs = (size_t)batch * nheads * nchunks;
-  const size_t cs = (pairs * sizeof(float) + 255) & ~(size_t)255;
-  char* p = static_cast<char*>(ws);
-  a.ws_status = reinterpret_cast<int*>(p);
-  a.ws_cs = reinterpret_cast<float*>(p + 256);
-  a.ws_S = reinterpret_cast<float*>(p + 256 + cs);
-  a.ws_Sin = p + 256 + cs + pairs * kN * kP * sizeof(float);
-  a.ws_Sin_lo = p + 256 + cs + pairs * kN * kP * (sizeof(float) + sizeof(bf16));
+  (void)batch;
+  (void)nheads;
+  (void)nchunks;
+  a.ws_status = static_cast<int*>(ws);
 }
 
 cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t stream) {
@@ -424,18 +440,22 @@ cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t stream) {
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    err = cudaFuncSetAttribute(ssd_chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, StateSmem::bytes);
+    err = cudaFuncSetAttribute(ssd_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::bytes);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(ssd_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ScanSmem::bytes);
+      err = cudaFuncSetAttribute(ssd_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::bytes);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
   err = cudaMemsetAsync(a.ws_status, 0, sizeof(int), stream);
   if (err != cudaSuccess) return err;
-  const dim3 grid(a.nchunks, a.nheads, a.batch);
-  ssd_chunk_state_kernel<<<grid, kThreads, StateSmem::bytes, stream>>>(a);
-  ssd_state_pass_kernel<<<dim3(a.nheads, a.batch), kPassThreads, 0, stream>>>(a);
-  ssd_chunk_scan_kernel<<<grid, kThreads, ScanSmem::bytes, stream>>>(a);
+  CUtensorMap mC, mB, mX;
+  const dim3 grid(a.nheads, a.batch);
+  if (a.seqlen % kQ == 0 && make_maps(a, &mC, &mB, &mX)) {
+    ssd_fused_kernel<true><<<grid, kThreads, Smem::bytes, stream>>>(a, mC, mB, mX);
+  } else {
+    memset(&mC, 0, sizeof(mC));
+    ssd_fused_kernel<false><<<grid, kThreads, Smem::bytes, stream>>>(a, mC, mC, mC);
+  }
   return cudaGetLastError();
 }
 
