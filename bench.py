@@ -138,6 +138,7 @@ _KERNEL_SOURCES = {
     "scan": ("ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
     "decode": ("ssm_decode.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
     "backward": ("ssm_scan_bwd.cu", "ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
+    "ssd": ("ssm_ssd.cu", "ssm_umma.cuh", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
 }
 
 
@@ -677,6 +678,238 @@ def run_gpu_bwd(args, w):
     return 0
 
 
+# ---------------------------------------------------------------- state-space-duality layer
+
+SSD_Q = 128  # the kernel's chunk length
+
+
+def ssd_algorithmic_bytes(w) -> int:
+    """x, dt, B, C read once, y and the final state written once, parameters read once."""
+    tok = w.batch * w.seqlen
+    return (tok * w.nheads * w.headdim * 2 * 2 + tok * w.nheads * 2 + 2 * tok * w.dstate * 2
+            + w.batch * w.nheads * w.headdim * w.dstate * 4 + w.nheads * 4 * 3)
+
+
+def ssd_flops(w):
+    """Tensor-core FLOPs of one step of the chunked dual form, per chunk of Q steps and head:
+    C B^T (2 Q^2 N), the masked product with X (2 Q^2 P), C H_in (2 Q N P) and the chunk's state
+    increment B^T X (2 N Q P). Returns (algorithmic, executed): the kernel multiplies the two
+    computed operands (G' and H_in) as hi + lo bf16 pairs, which doubles two of the four."""
+    Q, N, P = SSD_Q, w.dstate, w.headdim
+    units = w.batch * w.nheads * ((w.seqlen + Q - 1) // Q)
+    alg = 2 * Q * Q * N + 2 * Q * Q * P + 2 * Q * N * P + 2 * N * Q * P
+    exe = 2 * Q * Q * N + 4 * Q * Q * P + 4 * Q * N * P + 2 * N * Q * P
+    return units * alg, units * exe
+
+
+def _bf16_peak_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        if "bf16_tflops" in p:
+            return float(p["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    return 1800.0, "fallback"
+
+
+def ssd_config_of(w, eager: bool = False):
+    return {"workload": w.name, "kind": "ssd", "io": "bf16", "batch": w.batch, "seqlen": w.seqlen,
+            "nheads": w.nheads, "headdim": w.headdim, "d_state": w.dstate, "chunk": SSD_Q,
+            "d_model": w.d_model, "expand": w.expand, "l2": "flushed before every timed step (256 MiB write)",
+            "launch": "direct library calls" if eager else "the step's library call replayed from one CUDA graph"}
+
+
+def ssd_oracle_rate(w, target_s: float = 10.0):
+    """The fp64 oracle on a bounded sample of (batch, head) pairs at the full sequence length."""
+    import oracle
+    from selective_state_space_145_b300 import inputs
+
+    cores = oracle.oracle.default_threads()
+    p = inputs.ssd_workload_inputs(w)
+    pairs = 1
+    t0 = time.perf_counter()
+    oracle.ssd(p["x"][:1, :, :1], p["dt"][:1, :, :1], p["A"][:1], p["B"][:1], p["C"][:1], p["D"][:1],
+               p["dt_bias"][:1], True, None, nthreads=cores)
+    one = max(time.perf_counter() - t0, 1e-6)
+    heads = int(max(1, min(w.nheads, target_s / one)))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.ssd(p["x"][:1, :, :heads], p["dt"][:1, :, :heads], p["A"][:heads], p["B"][:1], p["C"][:1],
+                   p["D"][:heads], p["dt_bias"][:heads], True, None, nthreads=cores)
+        reps += 1
+        if time.perf_counter() - t0 >= target_s or reps >= 1000:
+            break
+    dt = time.perf_counter() - t0
+    pairs = reps * heads
+    ups = pairs * w.seqlen * w.headdim * w.dstate
+    return ups / dt, cores, (f"{reps} pass(es) over {heads} head(s) of one sequence x {w.seqlen} steps "
+                             f"x {w.headdim} x {w.dstate} state (fp64, {cores} threads)")
+
+
+def run_reference_ssd(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    rates, desc, cores = [], "", 1
+    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        r, cores, desc = ssd_oracle_rate(w, target_s=budget)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.mean(rates)
+    print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": ssd_config_of(w),
+                      "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+                      "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+          flush=True)
+    return 0
+
+
+def run_gpu_ssd(args, w):
+    """One ssm_ssd_fwd call per step (one kernel after clearing the status word)."""
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import dataclasses
+
+    import selective_state_space_145_b300 as ssm
+    from selective_state_space_145_b300 import inputs
+
+    p = inputs.ssd_workload_inputs(w if world == 1 else dataclasses.replace(w, seed=w.seed + 1000 * rank))
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    wsb = ssm.ssm_ssd_workspace_bytes(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, torch.bfloat16)
+    ws = torch.zeros(max(1, wsb), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(g["x"])
+    h_last = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=torch.float32, device=dev)
+
+    def call(d, yo, ho):
+        ssm.ssm_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dt_bias"], True, None, workspace=ws,
+                        out=yo, h_last=ho)
+
+    step = (lambda: call(g, y, h_last))
+    if not args.eager:
+        step = _as_graph(step, dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if int(ws[:4].view(torch.int32).item()) != 0:
+        raise RuntimeError("ssm_ssd_fwd: a tensor-core wait ran out")
+    barrier(world)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    ms = reduce_max(statistics.mean(step_ms), world, dev)
+
+    # end to end with host buffers, pipelined as for the scans: two buffer sets, uploads, calls and
+    # downloads on three streams
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    nbuf = 2
+    bufs = [{k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+            for _ in range(nbuf)]
+    outs = [{"y": torch.empty_like(y), "h_last": torch.empty_like(h_last)} for _ in range(nbuf)]
+    host_out = [{"y": torch.empty_like(host["x"]).pin_memory(), "h_last": torch.empty(h_last.shape).pin_memory()}
+                for _ in range(nbuf)]
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {name: [torch.cuda.Event() for _ in range(nbuf)] for name in ("up", "used", "down")}
+
+    def e2e_step(i):
+        k = i % nbuf
+        with torch.cuda.stream(s_up):
+            s_up.wait_event(ev["used"][k])
+            for name, v in host.items():
+                if isinstance(v, torch.Tensor):
+                    bufs[k][name].copy_(v, non_blocking=True)
+            ev["up"][k].record(s_up)
+        stream.wait_event(ev["up"][k])
+        stream.wait_event(ev["down"][k])
+        with torch.cuda.stream(stream):
+            call(bufs[k], outs[k]["y"], outs[k]["h_last"])
+            ev["used"][k].record(stream)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(ev["used"][k])
+            for name, v in outs[k].items():
+                host_out[k][name].copy_(v, non_blocking=True)
+            ev["down"][k].record(s_down)
+
+    for i in range(2 * nbuf):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    n_e2e = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_up)
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record(s_down)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, world, dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r, cores, desc = ssd_oracle_rate(w, target_s=args.cpu_seconds)
+        cpu = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    peak_gbs, peak_kind = _peaks()
+    bytes_step = ssd_algorithmic_bytes(w)
+    gbs = bytes_step / (ms * 1e-3) / 1e9
+    alg, exe = ssd_flops(w)
+    tf_peak, tf_kind = _bf16_peak_tflops()
+    tf = alg / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": w.updates * world / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": ssd_config_of(w, args.eager),
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s", "frac": tf / tf_peak,
+                     "traffic": traffic_from_profiles(w.name, "ssd"), "peak_source": tf_kind,
+                     "algorithmic_flops_per_step": alg, "executed_flops_per_step": exe,
+                     "executed_tflops": exe / (ms * 1e-3) / 1e12,
+                     "timed": "whole step (ssd_fused_kernel), CUDA events on the launching stream"},
+        "roofline_hbm": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                         "peak_source": peak_kind, "algorithmic_bytes_per_step": bytes_step},
+        "cpu_baseline": cpu,
+        "e2e": {"value": w.updates * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                "pipeline": "2 buffer sets; uploads, calls and downloads on three streams, overlapped across steps"},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+        "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -702,6 +935,15 @@ def main(argv=None):
     from selective_state_space_145_b300 import inputs
 
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    if args.workload in inputs.SSD_WORKLOADS:
+        w = inputs.SSD_WORKLOADS[args.workload]
+        if args.reverse or args.zoh or args.backward or args.chunk_len:
+            ap.error("the state-space-duality workload takes none of --reverse, --zoh, --backward, --chunk-len")
+        if args.seqlen is not None or args.batch is not None:
+            w = dataclasses.replace(w, seqlen=args.seqlen if args.seqlen is not None else w.seqlen,
+                                    batch=args.batch if args.batch is not None else w.batch)
+            w = dataclasses.replace(w, name=f"{w.name}[batch={w.batch},seqlen={w.seqlen}]")
+        return run_reference_ssd(args, w) if args.impl == "reference" else run_gpu_ssd(args, w)
     w = inputs.WORKLOADS[args.workload]
     if args.reverse and w.kind != "scan":
         ap.error("--reverse applies to the scan workloads only")
