@@ -24,13 +24,13 @@
 //             by Delta_s exp(c_end - c_s);
 //   round B:  Y_diag = G' X [Q x P] and S = B~^T X [N x P];
 //   (threads) y = Y_diag + exp(c_t) Y_off + D x; H <- exp(c_end) H + S.
+// Every tile is stored in the 128-byte swizzled layout (rows of 128 bytes in 1024-byte atoms).
 // The next chunk's C, B and X are copied in while the epilogue and the state update of the current
-// one run: when the sequence length is a multiple of the chunk, by three TMA bulk-tensor copies
-// issued by one thread, whose 4-D / 5-D boxes (8 elements, 8 rows, column groups, row groups)
-// land directly in the no-swizzle core-matrix layout; otherwise by 16-byte cp.async copies with
-// zero fill past the end. The B tile serves as
-// the K-major B operand of G and, scaled, as the MN-major A operand of S: the two layouts are the
-// same bytes. Operands the kernel computes (G' and H_in) are carried as two bf16 terms,
+// one run: when the sequence length is a multiple of the chunk, by five TMA bulk-tensor copies of
+// 128-byte rows issued by one thread (C and B as two slabs of 64 columns, X as one box), which
+// apply the swizzle themselves; otherwise by 16-byte cp.async copies with zero fill past the end.
+// The B tile serves as the K-major B operand of G and, scaled, as the MN-major A operand of S: the
+// two layouts are the same bytes. Operands the kernel computes (G' and H_in) are carried as two bf16 terms,
 // hi = bf16(v) and lo = bf16(v - hi), multiplied in two GEMMs into one accumulator: a single bf16
 // rounding of them costs up to 2^-9 of each summand, which for sums of 128 products of O(1)
 // terms that cancel exceeds the bf16-I/O tolerance on a fraction of a percent of the outputs.
@@ -55,7 +55,8 @@ static_assert(kQ == kN && 2 * kQ == kThreads, "two threads per step and per stat
 
 using bf16 = __nv_bfloat16;
 
-// Shared-memory layout (byte offsets); 112 KB, so two CTAs fit an SM.
+// Shared-memory layout (byte offsets, all 1024-aligned); 112 KB plus the small variables, so two
+// CTAs fit an SM. Every tile is 128-byte swizzled; 128 x 128 tiles are two slabs of 64 columns.
 struct Smem {
   static constexpr int C = 0;                    // C [Q x N], K-major: A operand of G and Y_off (M = t,
                                                  // K = n); after round A, G'_hi [Q x Q], K-major
@@ -65,8 +66,13 @@ struct Smem {
   static constexpr int H = X + kQ * kP * 2;      // H_in hi, lo [N x P] each, MN-major: B operand of Y_off
                                                  // (N = p, K = n); after round A, G'_lo [Q x Q], K-major
   static constexpr int HL = H + kN * kP * 2;
-  static constexpr int bytes = HL + kN * kP * 2;
+  static constexpr int MBAR = HL + kN * kP * 2;  // two mbarriers, the TMEM address, warp sums, lg2 Delta - c
+  static constexpr int TSLOT = MBAR + 16;
+  static constexpr int WSUM = TSLOT + 16;
+  static constexpr int Z = WSUM + 32;
+  static constexpr int bytes = Z + kQ * 4;
 };
+constexpr uint32_t kSlab = kQ * 128;  // bytes of a 64-column slab of a 128-row tile
 
 // TMEM columns: G [128 x 128] (Y_diag [128 x 64] after it), Y_off [128 x 64], S [128 x 64].
 constexpr uint32_t kColG = 0, kColDiag = 0, kColOff = 128, kColS = 192, kCols = 256;
@@ -100,18 +106,25 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
   lo = pack8(l);
 }
 
-// TMA: the tiles come from three tensor maps (C and B: 4-D, X: 5-D, described at launch_ssd).
+// TMA: the tiles come from three tensor maps (C and B: 2-D [rows, 128], X: 3-D [rows, heads,
+// 64]; 128-byte swizzle; described at launch_ssd).
 template <bool TMA>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fused_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmX) {
-  extern __shared__ __align__(128) unsigned char sm[];
-  __shared__ uint64_t mbar;
-  __shared__ uint64_t tbar;  // TMA completion
-  __shared__ uint32_t tslot;
-  __shared__ float s_wsum[8];
-  __shared__ float s_z[kQ];  // lg2(Delta_s) - c_s: exp(c_t - c_s) Delta_s = 2^(c_t + z_s) in log2 units
+  extern __shared__ __align__(1024) unsigned char sm[];
+  uint64_t& mbar = *reinterpret_cast<uint64_t*>(sm + Smem::MBAR);
+  uint64_t& tbar = *reinterpret_cast<uint64_t*>(sm + Smem::MBAR + 8);  // TMA completion
+  uint32_t& tslot = *reinterpret_cast<uint32_t*>(sm + Smem::TSLOT);
+  float* s_wsum = reinterpret_cast<float*>(sm + Smem::WSUM);
+  float* s_z = reinterpret_cast<float*>(sm + Smem::Z);  // lg2(Delta_s) - c_s: exp(c_t - c_s) Delta_s = 2^(c_t + z_s)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the swizzle atoms need a 1024-aligned tile base; the dynamic window starts at the CTA's
+  // shared-memory base, so this holds, but it is checked rather than assumed
+  if (smem_addr(sm) & 1023u) {
+    if (tid == 0) atomicExch(a.ws_status, 2);
+    return;
+  }
   const int t = tid & (kQ - 1);  // the row (step t, or state row n) of this thread
   const int half = tid >> 7;     // which half of the row's columns
   const int wq = warp & 3;       // TMEM lane quarter of this warp
@@ -132,37 +145,41 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float Dh = a.D ? a.D[h] : 0.f;
 
   // C, B, X of chunk q into their tiles; rows past the sequence end are zero-filled. Copy k of
-  // thread tid: C / B row s = tid/16 + 16k, columns 8 (tid%16) ..; X row s = tid/8 + 32k, columns
-  // 8 (tid%8) .. (the core-matrix offsets of those rows and columns, written out)
-  const uint32_t cb_soff = (uint32_t)((tid / 128) * 2048 + (tid % 16) * 128 + ((tid / 16) % 8) * 16);  // + 4096 k
-  const uint32_t x_soff = (uint32_t)((tid / 64) * 1024 + (tid % 8) * 128 + ((tid / 8) % 8) * 16);     // + 4096 k
+  // thread tid (cp.async path): C / B row s = tid/16 + 16k, 16-byte chunk tid%16 (slab chunk/8);
+  // X row s = tid/8 + 32k, chunk tid%8
   auto stage = [&](int q) {
     const int t0 = q * kQ, len = min(kQ, L - t0);
     if (TMA) {  // whole chunks only: no row of another sequence, none past the end
       if (tid == 0) {
         umma::fence_proxy_async();
         umma::mbar_expect_tx(&tbar, (uint32_t)(2 * kQ * kN * 2 + kQ * kP * 2));
-        const int r8 = (int)(((long long)b * L + t0) / 8);
-        umma::tma_load_4d(sC, &tmC, 0, 0, 0, r8, &tbar);
-        umma::tma_load_4d(sB, &tmB, 0, 0, 0, r8, &tbar);
-        umma::tma_load_5d(sX, &tmX, 0, 0, 0, r8, h, &tbar);
+        const int r0 = (int)((long long)b * L + t0);
+        umma::tma_load_2d(sC, &tmC, 0, r0, &tbar);
+        umma::tma_load_2d(sC + kSlab, &tmC, 64, r0, &tbar);
+        umma::tma_load_2d(sB, &tmB, 0, r0, &tbar);
+        umma::tma_load_2d(sB + kSlab, &tmB, 64, r0, &tbar);
+        umma::tma_load_3d(sX, &tmX, 0, h, r0, &tbar);
       }
       return;
     }
-    const long long cbg = ((long long)b * L + t0 + tid / 16) * kN + (tid % 16) * 8;
+    const int cch = tid % 16;
+    const long long cbg = ((long long)b * L + t0 + tid / 16) * kN + cch * 8;
 #pragma unroll
     for (int k = 0; k < kQ * kN / 8 / kThreads; ++k) {
-      const bool ok = tid / 16 + 16 * k < len;
+      const int srow = tid / 16 + 16 * k;
+      const bool ok = srow < len;
       const long long g = cbg + (long long)k * 16 * kN;
-      cp_async16(sC + cb_soff + 4096u * k, ok ? (const void*)(gC + g) : (const void*)gC, ok ? 16u : 0u);
-      cp_async16(sB + cb_soff + 4096u * k, ok ? (const void*)(gB + g) : (const void*)gB, ok ? 16u : 0u);
+      const uint32_t off = (uint32_t)(cch >> 3) * kSlab + umma::sw128_off(srow, cch & 7);
+      cp_async16(sC + off, ok ? (const void*)(gC + g) : (const void*)gC, ok ? 16u : 0u);
+      cp_async16(sB + off, ok ? (const void*)(gB + g) : (const void*)gB, ok ? 16u : 0u);
     }
     const long long xg = (((long long)b * L + t0 + tid / 8) * H + h) * kP + (tid % 8) * 8;
 #pragma unroll
     for (int k = 0; k < kQ * kP / 8 / kThreads; ++k) {
-      const bool ok = tid / 8 + 32 * k < len;
+      const int srow = tid / 8 + 32 * k;
+      const bool ok = srow < len;
       const long long g = xg + (long long)k * 32 * H * kP;
-      cp_async16(sX + x_soff + 4096u * k, ok ? (const void*)(gx + g) : (const void*)gx, ok ? 16u : 0u);
+      cp_async16(sX + umma::sw128_off(srow, tid % 8), ok ? (const void*)(gx + g) : (const void*)gx, ok ? 16u : 0u);
     }
     cp_async_commit();
   };
@@ -182,8 +199,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int p0 = 0; p0 < kHalfP; p0 += 8) {
       uint4 hi, lo;
       split8(Hs + p0, hi, lo);
-      *reinterpret_cast<uint4*>(sH + umma::mnmajor_off(pb + p0, t, kP)) = hi;
-      *reinterpret_cast<uint4*>(sHL + umma::mnmajor_off(pb + p0, t, kP)) = lo;
+      const uint32_t off = umma::sw128_off(t, (pb + p0) >> 3);  // row n = t, chunk p / 8
+      *reinterpret_cast<uint4*>(sH + off) = hi;
+      *reinterpret_cast<uint4*>(sHL + off) = lo;
     }
   };
   write_state();
@@ -247,16 +265,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       constexpr uint32_t idOff = umma::idesc_bf16(kQ, kP, false, true);
 #pragma unroll 1
       for (int kk = 0; kk < kN / 16; ++kk)
-        umma::mma_bf16(tbase + kColG, umma::desc_kmajor(smem_addr(sC), kk, kN),
-                       umma::desc_kmajor(smem_addr(sB), kk, kN), idG, kk > 0);
+        umma::mma_bf16(tbase + kColG, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
+                       umma::desc_sw128_kmajor(smem_addr(sB), kk, kSlab), idG, kk > 0);
 #pragma unroll 1
       for (int kk = 0; kk < kN / 16; ++kk)
-        umma::mma_bf16(tbase + kColOff, umma::desc_kmajor(smem_addr(sC), kk, kN),
-                       umma::desc_mnmajor(smem_addr(sH), kk, kP), idOff, kk > 0);
+        umma::mma_bf16(tbase + kColOff, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
+                       umma::desc_sw128_mnmajor(smem_addr(sH), kk, kSlab), idOff, kk > 0);
 #pragma unroll 1
       for (int kk = 0; kk < kN / 16; ++kk)
-        umma::mma_bf16(tbase + kColOff, umma::desc_kmajor(smem_addr(sC), kk, kN),
-                       umma::desc_mnmajor(smem_addr(sHL), kk, kP), idOff, true);
+        umma::mma_bf16(tbase + kColOff, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
+                       umma::desc_sw128_mnmajor(smem_addr(sHL), kk, kSlab), idOff, true);
       umma::mma_commit(&mbar);
     }
     ok = __syncthreads_and(umma::mbar_wait(&mbar, parity)) && ok;
@@ -284,16 +302,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int k = 0; k < 4; ++k) hi[k] = lo[k] = make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        *reinterpret_cast<uint4*>(sC + umma::kmajor_off(t, s0 + 8 * k, kQ)) = hi[k];
-        *reinterpret_cast<uint4*>(sH + umma::kmajor_off(t, s0 + 8 * k, kQ)) = lo[k];
+      for (int k = 0; k < 4; ++k) {  // row t, column chunk (s0 + 8k) / 8: slab s0 / 64
+        const uint32_t off = (uint32_t)(s0 >> 6) * kSlab + umma::sw128_off(t, ((s0 & 63) >> 3) + k);
+        *reinterpret_cast<uint4*>(sC + off) = hi[k];
+        *reinterpret_cast<uint4*>(sH + off) = lo[k];
       }
     }
     {
       const float w = Delta * ex2_approx(c_end - cs);
+      // row t of slab `half`: its 128 bytes (the scaling is per element, so the chunk order is
+      // free; taking chunk c ^ (t % 8) at step c spreads the 8 rows of an atom over all banks)
+      unsigned char* rowp = sB + (uint32_t)half * kSlab + (uint32_t)((t >> 3) * 1024 + (t & 7) * 128);
 #pragma unroll 4
-      for (int n0 = half * (kN / 2); n0 < (half + 1) * (kN / 2); n0 += 8) {
-        unsigned char* p = sB + umma::kmajor_off(t, n0, kN);
+      for (int c = 0; c < 8; ++c) {
+        unsigned char* p = rowp + 16 * (c ^ (t & 7));
         float f[8];
         unpack8(p, f);
 #pragma unroll
@@ -312,23 +334,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       constexpr uint32_t idS = umma::idesc_bf16(kN, kP, true, true);
 #pragma unroll 1
       for (int kk = 0; kk < kQ / 16; ++kk)
-        umma::mma_bf16(tbase + kColDiag, umma::desc_kmajor(smem_addr(sC), kk, kQ),
-                       umma::desc_mnmajor(smem_addr(sX), kk, kP), idDiag, kk > 0);
+        umma::mma_bf16(tbase + kColDiag, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
+                       umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idDiag, kk > 0);
 #pragma unroll 1
       for (int kk = 0; kk < kQ / 16; ++kk)
-        umma::mma_bf16(tbase + kColDiag, umma::desc_kmajor(smem_addr(sH), kk, kQ),
-                       umma::desc_mnmajor(smem_addr(sX), kk, kP), idDiag, true);
+        umma::mma_bf16(tbase + kColDiag, umma::desc_sw128_kmajor(smem_addr(sH), kk, kSlab),
+                       umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idDiag, true);
 #pragma unroll 1
       for (int kk = 0; kk < kQ / 16; ++kk)
-        umma::mma_bf16(tbase + kColS, umma::desc_mnmajor(smem_addr(sB), kk, kN),
-                       umma::desc_mnmajor(smem_addr(sX), kk, kP), idS, kk > 0);
+        umma::mma_bf16(tbase + kColS, umma::desc_sw128_mnmajor(smem_addr(sB), kk, kSlab),
+                       umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idS, kk > 0);
       umma::mma_commit(&mbar);
     }
     // this step's x, for the skip term, before the tile is refilled
     uint4 xr[kHalfP / 8];
 #pragma unroll
     for (int j = 0; j < kHalfP / 8; ++j)
-      xr[j] = *reinterpret_cast<const uint4*>(sX + umma::mnmajor_off(pb + 8 * j, t, kP));
+      xr[j] = *reinterpret_cast<const uint4*>(sX + umma::sw128_off(t, (pb >> 3) + j));
     ok = __syncthreads_and(umma::mbar_wait(&mbar, parity)) && ok;
     parity ^= 1;
     umma::fence_after_sync();
@@ -391,29 +413,29 @@ EncodeTiled encoder() {
   return fn;
 }
 
-// The tensor maps of the TMA path. Rows are flat (batch * seqlen + t). C, B [rows, 128]: dims
-// (n%8, row%8, n/8, row/8); X [rows, heads, 64]: dims (p%8, row%8, p/8, row/8, head). A box
-// (8, 8, all column groups, 16 row groups) is one 128-row chunk in core-matrix order.
+// The tensor maps of the TMA path, 128-byte swizzle. Rows are flat (batch * seqlen + t). C, B
+// [rows, 128]: a box of 64 columns x 128 rows is one slab; X [rows, heads, 64]: a box of
+// 64 x 1 x 128 is the whole tile of one head.
 bool make_maps(const SsdArgs& a, CUtensorMap* mC, CUtensorMap* mB, CUtensorMap* mX) {
   EncodeTiled enc = encoder();
   if (!enc) return false;
   const cuuint64_t rows = (cuuint64_t)a.batch * a.seqlen;
-  const cuuint64_t dCB[4] = {8, 8, kN / 8, rows / 8};
-  const cuuint64_t sCB[3] = {kN * 2, 16, 8 * kN * 2};
-  const cuuint32_t bCB[4] = {8, 8, kN / 8, kQ / 8};
-  const cuuint32_t e4[4] = {1, 1, 1, 1};
+  const cuuint64_t dCB[2] = {kN, rows};
+  const cuuint64_t sCB[1] = {kN * 2};
+  const cuuint32_t bCB[2] = {64, kQ};
+  const cuuint32_t e2[2] = {1, 1};
   const cuuint64_t H = (cuuint64_t)a.nheads;
-  const cuuint64_t dX[5] = {8, 8, kP / 8, rows / 8, H};
-  const cuuint64_t sX[4] = {H * kP * 2, 16, 8 * H * kP * 2, kP * 2};
-  const cuuint32_t bX[5] = {8, 8, kP / 8, kQ / 8, 1};
-  const cuuint32_t e5[5] = {1, 1, 1, 1, 1};
+  const cuuint64_t dX[3] = {kP, H, rows};
+  const cuuint64_t sX[2] = {kP * 2, H * kP * 2};
+  const cuuint32_t bX[3] = {kP, 1, kQ};
+  const cuuint32_t e3[3] = {1, 1, 1};
   auto go = [&](CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* d, const cuuint64_t* st,
                 const cuuint32_t* bx, const cuuint32_t* el) {
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, bx, el,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
-  return go(mC, a.C, 4, dCB, sCB, bCB, e4) && go(mB, a.B, 4, dCB, sCB, bCB, e4) && go(mX, a.x, 5, dX, sX, bX, e5);
+  return go(mC, a.C, 2, dCB, sCB, bCB, e2) && go(mB, a.B, 2, dCB, sCB, bCB, e2) && go(mX, a.x, 3, dX, sX, bX, e3);
 }
 
 }  // namespace

@@ -60,6 +60,32 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk, int R) {
   return smem_desc(base + (uint32_t)kk * 2u * (uint32_t)R * 16u, (uint32_t)R * 16u, 128u);
 }
 
+// ---- 128-byte swizzled operands. A tile is stored as rows of 128 bytes (64 bf16) in atoms of
+// 8 rows (1024 bytes); the 16-byte chunk c of row r sits at chunk position c ^ (r % 8) (the
+// pattern TMA's 128-byte swizzle writes). K-major operands wider than 64 in K are stored as slabs
+// of 64 columns; MN-major operands wider than 64 in M (or N) as spans of 64. Measured on a B300
+// (all-integer GEMMs exact; TMA box contents as below): K-major, the K slice kk of 16 starts
+// 32 * (kk % 4) bytes into slab kk / 4, with 1024 bytes between 8-row groups; MN-major, it
+// starts 2048 * kk bytes in (16 K rows), with the span stride as leading-dimension offset and
+// 1024 bytes between 8-row K groups.
+__host__ __device__ constexpr uint32_t sw128_off(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version 1
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+__device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t base, int kk, uint32_t slab_bytes) {
+  return desc_sw128(base + (uint32_t)(kk >> 2) * slab_bytes + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
+}
+__device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t base, int kk, uint32_t span_bytes) {
+  return desc_sw128(base + (uint32_t)kk * 2048u, span_bytes, 1024u);
+}
+
 // ---- tensor memory: one warp allocates (writing the base address to shared memory) and the
 // same warp frees; ncols is a power of two >= 32.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -122,6 +148,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(mbar)), "r"(bytes)
                : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_addr(mbar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(mbar))
+      : "memory");
 }
 __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3,
                                             uint64_t* mbar) {
