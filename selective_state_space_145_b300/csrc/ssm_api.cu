@@ -43,6 +43,8 @@ long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 // The policy splits only as far as the main pass still fits in one wave of resident CTAs:
 // q chunks give q times the CTAs, each walking 1/q of the sequence, and a second wave
 // would cost as much as it saves.
+constexpr long long kLongChunk = 3072;  // a multiple of kChunkQuantum
+
 int default_chunk_len_impl(int batch, int dim, int seqlen, bool bf16) {
   const int dt = ssm::scan_channels_per_cta();
   const long long ctas = ((dim + dt - 1) / dt) * (long long)batch;
@@ -53,7 +55,11 @@ int default_chunk_len_impl(int batch, int dim, int seqlen, bool bf16) {
   const long long qmax = (seqlen + kChunkQuantum - 1) / kChunkQuantum;
   if (q > qmax) q = qmax;
   if (q <= 1) return (int)whole;
-  return (int)round_up((seqlen + q - 1) / q, kChunkQuantum);
+  // Once the sequence is split anyway, chunks longer than kLongChunk are cut further: the extra
+  // waves of short chunks balance better than one wave of very long ones (long-scan workload,
+  // 10944 -> 3072 steps per chunk: 1.77 -> 1.69 ms).
+  const long long cl = round_up((seqlen + q - 1) / q, kChunkQuantum);
+  return (int)(cl > kLongChunk ? kLongChunk : cl);
 }
 
 // Chunk length of the backward pass: the same one-wave rule, with the backward kernel's occupancy.

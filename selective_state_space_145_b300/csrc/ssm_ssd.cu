@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float cs = v + off;
     if (half == 0) s_z[t] = lg2_approx(Delta) - cs;  // -inf past the end (Delta = 0): those columns vanish
     if (TMA) {
-      ok = __syncthreads_and(umma::mbar_wait(&tbar, tparity)) && ok;
+      ok = __syncthreads_and(umma::mbar_wait(&tbar, tparity) && ok);
       tparity ^= 1;
       if (!ok) break;
     } else {
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                        umma::desc_sw128_mnmajor(smem_addr(sHL), kk, kSlab), idOff, true);
       umma::mma_commit(&mbar);
     }
-    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity)) && ok;
+    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity) && ok);
     parity ^= 1;
     umma::fence_after_sync();
     if (!ok) break;
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int j = 0; j < kHalfP / 8; ++j)
       xr[j] = *reinterpret_cast<const uint4*>(sX + umma::sw128_off(t, (pb >> 3) + j));
-    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity)) && ok;
+    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity) && ok);
     parity ^= 1;
     umma::fence_after_sync();
     if (!ok) break;
