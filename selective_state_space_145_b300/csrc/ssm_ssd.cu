@@ -221,13 +221,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t parity = 0;
   bool ok = true;
 
-#pragma unroll 1
-  for (int q = 0; q < nc; ++q) {
-    const int t0 = q * kQ, len = min(kQ, L - t0);
-    // ---- Delta_t and the prefix c_t (log2 units) of this chunk; the next chunk's dt in flight
-    float Delta = 0.f;
-    if (t < len) Delta = a.dt_softplus ? softplus_f<true>(dtv + bias) : dtv + bias;
-    if (q + 1 < nc) dtv = load_dt(q + 1);
+  // Delta_t of chunk q (dt already loaded), the prefix c_t (log2 units) and its total, and the
+  // shared lg2(Delta_s) - c_s; one barrier, so every thread calls it
+  auto decay = [&](int q, float dtq, float& Delta, float& cs, float& c_end) {
+    const int len = min(kQ, L - q * kQ);
+    Delta = 0.f;
+    if (t < len) Delta = a.dt_softplus ? softplus_f<true>(dtq + bias) : dtq + bias;
     float v = Delta * A2;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -238,15 +237,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     // both halves scan all 128 steps; each reads its own half's warp totals
     const float* ws = s_wsum + 4 * half;
-    float off = 0.f, c_end = 0.f;
+    float off = 0.f;
+    c_end = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       if (w < wq) off += ws[w];
       if (w < 3) c_end += ws[w];
     }
     c_end += ws[3];
-    const float cs = v + off;
+    cs = v + off;
     if (half == 0) s_z[t] = lg2_approx(Delta) - cs;  // -inf past the end (Delta = 0): those columns vanish
+  };
+  float Delta, cs, c_end;
+  decay(0, dtv, Delta, cs, c_end);
+  if (nc > 1) dtv = load_dt(1);
+
+#pragma unroll 1
+  for (int q = 0; q < nc; ++q) {
+    const int t0 = q * kQ, len = min(kQ, L - t0);
     if (TMA) {
       ok = __syncthreads_and(umma::mbar_wait(&tbar, tparity) && ok);
       tparity ^= 1;
@@ -351,6 +359,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int j = 0; j < kHalfP / 8; ++j)
       xr[j] = *reinterpret_cast<const uint4*>(sX + umma::sw128_off(t, (pb >> 3) + j));
+    // the next chunk's decays while round B runs (every reader of this chunk's lg2 Delta - c has
+    // passed the barrier before round B)
+    float Delta_n = 0.f, cs_n = 0.f, c_end_n = 0.f;
+    if (q + 1 < nc) {
+      decay(q + 1, dtv, Delta_n, cs_n, c_end_n);
+      if (q + 2 < nc) dtv = load_dt(q + 2);
+    }
     ok = __syncthreads_and(umma::mbar_wait(&mbar, parity) && ok);
     parity ^= 1;
     umma::fence_after_sync();
@@ -380,6 +395,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     write_state();
     umma::fence_before_sync();
+    Delta = Delta_n;
+    cs = cs_n;
+    c_end = c_end_n;
   }
 
   if (!ok) {
