@@ -2,13 +2,7 @@
 // shared-memory matrix descriptors, the kind::f16 instruction descriptor, tensor-memory (TMEM)
 // allocation, MMA issue and commit, TMEM loads, and mbarriers with bounded waits.
 //
-// Operand layout used throughout: no swizzle, "core matrices" of 8 rows x 16 bytes stored as
-// 128 contiguous bytes. A K-major operand (K contiguous in memory) keeps 8 consecutive K
-// elements of one row in each 16-byte core row; an MN-major operand keeps 8 consecutive M (or
-// N) elements of one K row. Two byte strides place the core matrices. For both kinds of operand
-// the descriptor's leading-dimension offset is the stride between core matrices adjacent along
-// K and its stride-dimension offset the stride along M (or N): an all-integer GEMM on a B300
-// was exact with exactly that assignment, for K-major and MN-major A and B alike.
+// Operands use the 128-byte swizzled layout described at sw128_off below.
 #pragma once
 
 #include <cstdint>
@@ -17,18 +11,6 @@
 
 namespace ssm {
 namespace umma {
-
-// Shared-memory matrix descriptor (no swizzle). saddr: shared-window byte address of the first
-// core matrix; kstride: byte stride between core matrices adjacent along K; rstride: byte stride
-// between core matrices adjacent along M (or N).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t kstride, uint32_t rstride) {
-  const uint32_t lbo = kstride, sbo = rstride;
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version 1; base offset 0, relative LBO, no swizzle
-  return d;
-}
 
 // Instruction descriptor of tcgen05.mma kind::f16 for bf16 A and B, fp32 accumulation, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
@@ -39,25 +21,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          | ((b_mn_major ? 1u : 0u) << 16)
          | ((uint32_t)(N >> 3) << 17)
          | ((uint32_t)(M >> 4) << 24);
-}
-
-// Byte offset of element (r, k) of a K-major operand with K columns, and of element (r, k)
-// of an MN-major operand with R rows (r runs along M or N). Strides: K-major, 128 B along K and
-// 16*K B along r; MN-major, 128 B along r and 16*R B along K.
-__host__ __device__ constexpr uint32_t kmajor_off(int r, int k, int K) {
-  return (uint32_t)((r >> 3) * (K >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
-}
-__host__ __device__ constexpr uint32_t mnmajor_off(int r, int k, int R) {
-  return (uint32_t)((k >> 3) * (R >> 3) * 128 + (r >> 3) * 128 + (k & 7) * 16 + (r & 7) * 2);
-}
-
-// Descriptor of the K slice [16 kk, 16 kk + 16) of a K-major operand with K columns.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk, int K) {
-  return smem_desc(base + (uint32_t)kk * 256u, 128u, (uint32_t)K * 16u);
-}
-// Descriptor of the K slice [16 kk, 16 kk + 16) of an MN-major operand with R rows.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk, int R) {
-  return smem_desc(base + (uint32_t)kk * 2u * (uint32_t)R * 16u, (uint32_t)R * 16u, 128u);
 }
 
 // ---- 128-byte swizzled operands. A tile is stored as rows of 128 bytes (64 bf16) in atoms of
@@ -163,40 +126,8 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0,
       "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(mbar))
       : "memory");
 }
-__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3,
-                                            uint64_t* mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];" ::"r"(smem_addr(dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(mbar))
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, int c4,
-                                            uint64_t* mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
-      "%6}], [%7];" ::"r"(smem_addr(dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_addr(mbar))
-      : "memory");
-}
-
-// ---- TMEM -> registers: this warp's 32 lanes (lane i = row 32*(warp%4) + i), 16 consecutive
-// 32-bit columns starting at column `col` of the address.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 consecutive columns in one load, one wait.
+// ---- TMEM -> registers: this warp's 32 lanes (lane i = row 32*(warp%4) + i), consecutive
+// 32-bit columns from the address's column. 32 consecutive columns in one load, one wait.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
