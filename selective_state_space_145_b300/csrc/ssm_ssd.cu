@@ -94,16 +94,16 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   for (int k = 0; k < 4; ++k) e[k] = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
   return v;
 }
-// v = hi + lo with hi = bf16(v), lo = bf16(v - hi), 8 values
+// v = hi + lo with hi = bf16(v), lo = bf16(v - hi), 8 values, converted in pairs
 __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
-  float h[8], l[8];
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&hi);
+  __nv_bfloat162* l = reinterpret_cast<__nv_bfloat162*>(&lo);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    h[k] = __bfloat162float(__float2bfloat16_rn(v[k]));
-    l[k] = v[k] - h[k];
+  for (int k = 0; k < 4; ++k) {
+    h[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+    const float2 hf = __bfloat1622float2(h[k]);
+    l[k] = __floats2bfloat162_rn(v[2 * k] - hf.x, v[2 * k + 1] - hf.y);
   }
-  hi = pack8(h);
-  lo = pack8(l);
 }
 
 // TMA: the tiles come from three tensor maps (C and B: 2-D [rows, 128], X: 3-D [rows, heads,
