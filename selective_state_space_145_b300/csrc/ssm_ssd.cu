@@ -16,21 +16,21 @@
 // running state on the chip: fp32 in registers (row n of H is held by threads n and n + 128,
 // 32 columns each), and as the bf16 operand of the next chunk's GEMM in shared memory. Rows of
 // the tensor-memory accumulators map to threads; the two warps that share a row split its
-// columns. Per chunk, two rounds of tcgen05 GEMMs
-// (bf16 operands, fp32 accumulators in tensor memory, issued by one thread, completion through an
-// mbarrier):
+// columns. Per chunk, two rounds of tcgen05 GEMMs (bf16 operands, fp32 accumulators in tensor
+// memory, issued by one thread, completion through an mbarrier):
 //   round A:  G = C B^T [Q x Q] and Y_off = C H_in [Q x P];
 //   (threads) G' = G masked to s <= t and scaled by exp(c_t - c_s) Delta_s; B~ = B scaled per row
 //             by Delta_s exp(c_end - c_s);
 //   round B:  Y_diag = G' X [Q x P] and S = B~^T X [N x P];
 //   (threads) y = Y_diag + exp(c_t) Y_off + D x; H <- exp(c_end) H + S.
 // Every tile is stored in the 128-byte swizzled layout (rows of 128 bytes in 1024-byte atoms).
-// The next chunk's C, B and X are copied in while the epilogue and the state update of the current
-// one run: when the sequence length is a multiple of the chunk, by five TMA bulk-tensor copies of
-// 128-byte rows issued by one thread (C and B as two slabs of 64 columns, X as one box), which
-// apply the swizzle themselves; otherwise by 16-byte cp.async copies with zero fill past the end.
-// The B tile serves as the K-major B operand of G and, scaled, as the MN-major A operand of S: the
-// two layouts are the same bytes. Operands the kernel computes (G' and H_in) are carried as two bf16 terms,
+// The next chunk's C, B and X are copied in while the epilogue and the state update of the
+// current one run: when the sequence length is a multiple of the chunk, by five TMA bulk-tensor
+// copies of 128-byte rows issued by one thread (C and B as two slabs of 64 columns, X as one box),
+// which apply the swizzle themselves; otherwise by 16-byte cp.async copies with zero fill past
+// the end. The next chunk's decay prefix is computed while round B runs. The B tile serves as the
+// K-major B operand of G and, scaled, as the MN-major A operand of S: the two layouts are the
+// same bytes. Operands the kernel computes (G' and H_in) are carried as two bf16 terms,
 // hi = bf16(v) and lo = bf16(v - hi), multiplied in two GEMMs into one accumulator: a single bf16
 // rounding of them costs up to 2^-9 of each summand, which for sums of 128 products of O(1)
 // terms that cancel exceeds the bf16-I/O tolerance on a fraction of a percent of the outputs.
@@ -66,7 +66,8 @@ struct Smem {
   static constexpr int H = X + kQ * kP * 2;      // H_in hi, lo [N x P] each, MN-major: B operand of Y_off
                                                  // (N = p, K = n); after round A, G'_lo [Q x Q], K-major
   static constexpr int HL = H + kN * kP * 2;
-  static constexpr int MBAR = HL + kN * kP * 2;  // two mbarriers, the TMEM address, warp sums, lg2 Delta - c
+  static constexpr int MBAR = HL + kN * kP * 2;  // GEMM and TMA mbarriers, the TMEM address, warp
+                                                 // sums of the decay scan, lg2 Delta - c
   static constexpr int TSLOT = MBAR + 16;
   static constexpr int WSUM = TSLOT + 16;
   static constexpr int Z = WSUM + 32;
