@@ -88,3 +88,21 @@ def test_issue_floor_and_backward_bytes():
     tok, bnl = 2 * 1024 * 1024, 2 * 16 * 1024
     assert bench.bwd_algorithmic_bytes(w) == (tok * 4 * 7 + bnl * (2 * 4 + 8) + 2 * 1024 * 16 * 4 * 3
                                               + 1024 * 16 * 4 * 2 + 1024 * 4 * 4)
+
+
+def test_ssd_work_and_bytes():
+    """The state-space-duality workload's FLOP and byte accounting, spelled out."""
+    import bench
+    from selective_state_space_145_b300 import inputs
+
+    w = inputs.SSD_WORKLOADS["ssd_bf16_b8_l2048_h32_p64_n128"]
+    Q, N, P = 128, 128, 64
+    units = 8 * 32 * (2048 // Q)
+    alg, exe = bench.ssd_flops(w)
+    assert alg == units * (2 * Q * Q * N + 2 * Q * Q * P + 2 * Q * N * P + 2 * N * Q * P)
+    # the two computed operands (G' and H_in) enter as hi + lo pairs: their two GEMMs run twice
+    assert exe == alg + units * (2 * Q * Q * P + 2 * Q * N * P)
+    tok = 8 * 2048
+    assert bench.ssd_algorithmic_bytes(w) == (tok * 32 * 64 * 2 * 2 + tok * 32 * 2 + 2 * tok * 128 * 2
+                                              + 8 * 32 * 64 * 128 * 4 + 32 * 4 * 3)
+    assert w.updates == 8 * 2048 * 32 * 64 * 128
