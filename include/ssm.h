@@ -327,6 +327,16 @@ SSM_API ssm_status ssm_selective_scan_fwd_noalloc(const void* x, const void* del
  * runs one kernel (after clearing the status word) on `stream`.
  */
 SSM_API size_t ssm_ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, ssm_dtype io);
+
+/*
+ * Test hooks, process-wide, for tests only (0 = none, the default).
+ *   SSM_TEST_SSD_SKIP_MMA: ssm_ssd_fwd issues no tensor-core GEMMs, so its first wait for them
+ *   runs out (after a shortened bound, well under a second). The kernel then records status 1
+ *   in the workspace word, frees its tensor memory and returns; the results are undefined.
+ *   This exercises the bounded-wait path without faulting or hanging the GPU.
+ */
+#define SSM_TEST_SSD_SKIP_MMA 1u
+SSM_API void ssm_set_test_hooks(unsigned int flags);
 SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
                                const float* D, const float* dt_bias, int dt_softplus, const float* h0, void* y,
                                float* h_last, int batch, int seqlen, int nheads, int headdim, int dstate,

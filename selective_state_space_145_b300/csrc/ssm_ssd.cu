@@ -39,6 +39,7 @@
 #include <cuda.h>  // CUtensorMap and its encoder's signature (resolved at run time, not linked)
 #include <cuda_bf16.h>
 
+#include "../../include/ssm.h"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 #include "ssm_umma.cuh"
@@ -112,7 +113,7 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
 template <bool TMA>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fused_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmX) {
+                     const __grid_constant__ CUtensorMap tmX, const int test_skip_mma) {
   extern __shared__ __align__(1024) unsigned char sm[];
   uint64_t& mbar = *reinterpret_cast<uint64_t*>(sm + Smem::MBAR);
   uint64_t& tbar = *reinterpret_cast<uint64_t*>(sm + Smem::MBAR + 8);  // TMA completion
@@ -217,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   umma::fence_after_sync();
   stage(0);
   uint32_t tparity = 0;
+  // the test hook's waits give up sooner: nothing will complete them
+  const uint32_t wait_limit = test_skip_mma ? (1u << 12) : umma::kWaitLimit;
   const uint32_t tbase = tslot;
   const uint32_t trow = tbase + ((uint32_t)(wq * 32) << 16);
   uint32_t parity = 0;
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     umma::fence_after_sync();
 
     // ---- round A: G = C B^T, Y_off = C H_in (hi + lo)
-    if (tid == 0) {
+    if (tid == 0 && !test_skip_mma) {
       constexpr uint32_t idG = umma::idesc_bf16(kQ, kQ, false, false);
       constexpr uint32_t idOff = umma::idesc_bf16(kQ, kP, false, true);
 #pragma unroll 1
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                        umma::desc_sw128_mnmajor(smem_addr(sHL), kk, kSlab), idOff, true);
       umma::mma_commit(&mbar);
     }
-    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity) && ok);
+    ok = __syncthreads_and(umma::mbar_wait(&mbar, parity, wait_limit) && ok);
     parity ^= 1;
     umma::fence_after_sync();
     if (!ok) break;
@@ -459,6 +462,10 @@ bool make_maps(const SsdArgs& a, CUtensorMap* mC, CUtensorMap* mB, CUtensorMap* 
 
 }  // namespace
 
+namespace {
+unsigned int g_test_hooks = 0;  // SSM_TEST_* flags (ssm_set_test_hooks)
+}
+
 int ssd_chunk_len() { return kQ; }
 
 size_t ssd_workspace_bytes(int batch, int nheads, int nchunks) {
@@ -487,17 +494,23 @@ cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
+  const int skip_mma = (g_test_hooks & 1u) ? 1 : 0;
   err = cudaMemsetAsync(a.ws_status, 0, sizeof(int), stream);
   if (err != cudaSuccess) return err;
   CUtensorMap mC, mB, mX;
   const dim3 grid(a.nheads, a.batch);
-  if (a.seqlen % kQ == 0 && make_maps(a, &mC, &mB, &mX)) {
-    ssd_fused_kernel<true><<<grid, kThreads, Smem::bytes, stream>>>(a, mC, mB, mX);
+  // TMA row coordinates are 32-bit: the flat row index batch * seqlen must stay below 2^31
+  const bool tma_rows_fit = (long long)a.batch * a.seqlen < (1LL << 31);
+  if (a.seqlen % kQ == 0 && tma_rows_fit && make_maps(a, &mC, &mB, &mX)) {
+    ssd_fused_kernel<true><<<grid, kThreads, Smem::bytes, stream>>>(a, mC, mB, mX, skip_mma);
   } else {
     memset(&mC, 0, sizeof(mC));
-    ssd_fused_kernel<false><<<grid, kThreads, Smem::bytes, stream>>>(a, mC, mC, mC);
+    ssd_fused_kernel<false><<<grid, kThreads, Smem::bytes, stream>>>(a, mC, mC, mC, skip_mma);
   }
   return cudaGetLastError();
 }
 
 }  // namespace ssm
+
+// Test hooks of the C ABI (include/ssm.h): they only affect the state-space-duality launches.
+extern "C" SSM_API void ssm_set_test_hooks(unsigned int flags) { ssm::g_test_hooks = flags; }

@@ -29,7 +29,8 @@ _lib = None
 EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_scan_default_chunk_len",
            "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update",
            "ssm_selective_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_selective_scan_bwd",
-           "ssm_conv_bwd_workspace_bytes", "ssm_causal_conv1d_bwd", "ssm_ssd_workspace_bytes", "ssm_ssd_fwd")
+           "ssm_conv_bwd_workspace_bytes", "ssm_causal_conv1d_bwd", "ssm_ssd_workspace_bytes", "ssm_ssd_fwd",
+           "ssm_set_test_hooks")
 
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.ssm_selective_scan_bwd.restype = i
         L.ssm_selective_scan_bwd.argtypes = ([vp, vp, fp, vp, vp, fp, vp, fp, i, fp, vp, fp]
                                              + [vp, vp, vp, fp, fp, fp, fp, fp, fp] + [i] * 5 + [vp, sz, u, vp])
+        L.ssm_set_test_hooks.restype = None
+        L.ssm_set_test_hooks.argtypes = [u]
         L.ssm_ssd_workspace_bytes.restype = sz
         L.ssm_ssd_workspace_bytes.argtypes = [i] * 6
         L.ssm_ssd_fwd.restype = i

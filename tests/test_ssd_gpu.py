@@ -72,6 +72,17 @@ def test_ssd_softplus_off_and_no_skip(cuda_device):
     assert_close(hl, ref_h, "bf16", "h_last")
 
 
+def test_ssd_without_bias_and_skip_pointers(cuda_device):
+    """dt_bias and D absent (NULL at the ABI): the step is softplus(dt) and there is no skip term."""
+    p = inputs.ssd_inputs(1, 256, 3, seed=17, with_h0=False, with_D=False)
+    p["dt"] = (p["dt"].float() - 3.0).to(torch.bfloat16)   # softplus(dt) of the order of the workloads' steps
+    p["dt_bias"] = None
+    y, hl = _run(_dev(p, cuda_device))
+    ref, ref_h = oracle.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], None, None, True, None)
+    assert_close(y, ref, "bf16", "y")
+    assert_close(hl, ref_h, "bf16", "h_last")
+
+
 def test_ssd_deterministic_and_two_calls(cuda_device):
     p = inputs.ssd_inputs(2, 512, 2, seed=8, with_h0=True)
     g = _dev(p, cuda_device)
@@ -87,6 +98,32 @@ def test_ssd_deterministic_and_two_calls(cuda_device):
     yb, hb = _run(gb)
     assert_close(torch.cat([ya, yb], dim=1), y1.float().cpu().double().numpy(), "bf16", "two calls")
     assert_close(hb, h1.cpu().double().numpy(), "bf16", "state after two calls")
+
+
+def test_ssd_bounded_wait_reports_status(cuda_device):
+    """Failure detection without a fault: with the SSM_TEST_SSD_SKIP_MMA hook no GEMM is issued,
+    the kernel's wait for it runs out, it records status 1, frees its tensor memory and returns;
+    the context stays usable and the next call is correct."""
+    import time
+
+    ssm = _ssm()
+    p = inputs.ssd_inputs(1, 256, 1, seed=3)
+    g = _dev(p, cuda_device)
+    ws = torch.zeros(256, dtype=torch.uint8, device=cuda_device)
+    ssm.lib().ssm_set_test_hooks(1)
+    try:
+        t0 = time.time()
+        ssm.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["dt_bias"], True, None, workspace=ws)
+        torch.cuda.synchronize()
+        waited = time.time() - t0
+    finally:
+        ssm.lib().ssm_set_test_hooks(0)
+    assert int(ws[:4].view(torch.int32).item()) == 1
+    assert waited < 30.0
+    y, hl = _run(g)   # also checks that the status word is back to 0
+    ref, ref_h = oracle.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["dt_bias"], True, None)
+    assert_close(y, ref, "bf16", "y after the timed-out call")
+    assert_close(hl, ref_h, "bf16", "h_last after the timed-out call")
 
 
 def test_ssd_empty(cuda_device):
