@@ -78,6 +78,32 @@ def _as_graph(fn, dev):
     return graph.replay
 
 
+class _Packed:
+    """Named tensors laid out back to back (256-byte aligned) in one flat byte buffer, so that a
+    step's inputs (or results) cross PCIe in one copy; `views` holds the named tensors as views
+    into the buffer (non-tensor entries pass through)."""
+
+    def __init__(self, tensors, device=None, pin=False):
+        import torch
+
+        meta, off = [], 0
+        for name, v in tensors.items():
+            if isinstance(v, torch.Tensor):
+                nb = v.numel() * v.element_size()
+                meta.append((name, off, v.dtype, tuple(v.shape), nb))
+                off += (nb + 255) // 256 * 256
+        self.buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+        if pin:
+            self.buf = self.buf.pin_memory()
+        self.views = {k: v for k, v in tensors.items() if not isinstance(v, torch.Tensor)}
+        for name, o, dt, shape, nb in meta:
+            self.views[name] = self.buf[o:o + nb].view(dt).view(shape)
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+
 def alu_roofline(w, seconds: float, chunk_len: int, sms: int):
     """Scan step time against its issue floor: main + carry updates at the dispatch rate of
     sms x 4 SMSPs x 32 lanes per clock at the maximum SM clock. The per-token element-wise work
@@ -432,10 +458,15 @@ def run_gpu(args, w):
     # last download.
     e2e = None
     if rank == 0 or world > 1:
-        host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+        # every input of a step in one pinned buffer and one device buffer per set: one upload copy
+        hpack = _Packed(p, pin=True)
+        for k, v in p.items():
+            if isinstance(v, torch.Tensor):
+                hpack.views[k].copy_(v)
+        host = hpack.views
         nbuf = 2
-        bufs = [{k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
-                for _ in range(nbuf)]
+        dpacks = [_Packed(p, device=dev) for _ in range(nbuf)]
+        bufs = [dp.views for dp in dpacks]
         s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev = {name: [torch.cuda.Event() for _ in range(nbuf)] for name in ("up", "used", "done", "down")}
         if w.kind == "decode":
@@ -455,13 +486,17 @@ def run_gpu(args, w):
             def call(d, o):
                 replays[next(i for i, bb in enumerate(bufs) if bb is d)]()
 
-            def results(d, o):
-                return {"y": o["y"], "state": d["state"]}
+            def download(k):
+                host_out[k]["y"].copy_(outs[k]["y"], non_blocking=True)
+                host_out[k]["state"].copy_(bufs[k]["state"], non_blocking=True)
+
+            d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
         else:
-            outs = [{"out": torch.empty_like(out), "h_last": torch.empty_like(h_last)} for _ in range(nbuf)]
-            host_out = [{"out": torch.empty_like(host["x"]).pin_memory(),
-                         "h_last": torch.empty(w.batch, w.dim, w.dstate, dtype=torch.float32).pin_memory()}
-                        for _ in range(nbuf)]
+            # the results of a step in one device buffer and one pinned buffer: one download copy
+            res = {"out": out, "h_last": h_last}
+            opacks = [_Packed(res, device=dev) for _ in range(nbuf)]
+            outs = [op.views for op in opacks]
+            hopacks = [_Packed(res, pin=True) for _ in range(nbuf)]
 
             def call(d, o):
                 ssm.ssm_selective_scan_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
@@ -469,16 +504,16 @@ def run_gpu(args, w):
                                            workspace=ws, out=o["out"], h_last=o["h_last"],
                                            chunk_len=args.chunk_len, reverse=args.reverse, zoh=args.zoh)
 
-            def results(d, o):
-                return o
+            def download(k):
+                hopacks[k].buf.copy_(opacks[k].buf, non_blocking=True)
+
+            d2h = opacks[0].nbytes
 
         def e2e_step(i):
             k = i % nbuf
             with torch.cuda.stream(s_up):
                 s_up.wait_event(ev["used"][k])          # the call two steps back is done with buffer k
-                for name, v in host.items():
-                    if isinstance(v, torch.Tensor):
-                        bufs[k][name].copy_(v, non_blocking=True)
+                dpacks[k].buf.copy_(hpack.buf, non_blocking=True)
                 ev["up"][k].record(s_up)
             stream.wait_event(ev["up"][k])
             stream.wait_event(ev["down"][k])            # the download two steps back has read buffer k
@@ -487,12 +522,10 @@ def run_gpu(args, w):
                 ev["used"][k].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(ev["used"][k])
-                for name, v in results(bufs[k], outs[k]).items():
-                    host_out[k][name].copy_(v, non_blocking=True)
+                download(k)
                 ev["down"][k].record(s_down)
 
-        h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
-        d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+        h2d = hpack.nbytes
         for i in range(2 * nbuf):
             e2e_step(i)
         torch.cuda.synchronize(dev)
@@ -506,7 +539,7 @@ def run_gpu(args, w):
         e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, world, dev)
         e2e = {"value": updates * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
-               "pipeline": "2 buffer sets; uploads, calls and downloads on three streams, overlapped across steps"}
+               "pipeline": "2 buffer sets; one packed upload, the call(s) and one packed download per step on three streams, overlapped across steps"}
 
     if rank != 0:
         if world > 1:
@@ -824,13 +857,18 @@ def run_gpu_ssd(args, w):
 
     # end to end with host buffers, pipelined as for the scans: two buffer sets, uploads, calls and
     # downloads on three streams
-    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    # one upload and one download copy per step, as for the scans
+    hpack = _Packed(p, pin=True)
+    for k_, v in p.items():
+        if isinstance(v, torch.Tensor):
+            hpack.views[k_].copy_(v)
     nbuf = 2
-    bufs = [{k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
-            for _ in range(nbuf)]
-    outs = [{"y": torch.empty_like(y), "h_last": torch.empty_like(h_last)} for _ in range(nbuf)]
-    host_out = [{"y": torch.empty_like(host["x"]).pin_memory(), "h_last": torch.empty(h_last.shape).pin_memory()}
-                for _ in range(nbuf)]
+    dpacks = [_Packed(p, device=dev) for _ in range(nbuf)]
+    bufs = [dp.views for dp in dpacks]
+    res = {"y": y, "h_last": h_last}
+    opacks = [_Packed(res, device=dev) for _ in range(nbuf)]
+    outs = [op.views for op in opacks]
+    hopacks = [_Packed(res, pin=True) for _ in range(nbuf)]
     s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = {name: [torch.cuda.Event() for _ in range(nbuf)] for name in ("up", "used", "down")}
 
@@ -838,9 +876,7 @@ def run_gpu_ssd(args, w):
         k = i % nbuf
         with torch.cuda.stream(s_up):
             s_up.wait_event(ev["used"][k])
-            for name, v in host.items():
-                if isinstance(v, torch.Tensor):
-                    bufs[k][name].copy_(v, non_blocking=True)
+            dpacks[k].buf.copy_(hpack.buf, non_blocking=True)
             ev["up"][k].record(s_up)
         stream.wait_event(ev["up"][k])
         stream.wait_event(ev["down"][k])
@@ -849,8 +885,7 @@ def run_gpu_ssd(args, w):
             ev["used"][k].record(stream)
         with torch.cuda.stream(s_down):
             s_down.wait_event(ev["used"][k])
-            for name, v in outs[k].items():
-                host_out[k][name].copy_(v, non_blocking=True)
+            hopacks[k].buf.copy_(opacks[k].buf, non_blocking=True)
             ev["down"][k].record(s_down)
 
     for i in range(2 * nbuf):
@@ -864,8 +899,8 @@ def run_gpu_ssd(args, w):
     e1.record(s_down)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, world, dev)
-    h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
-    d2h = sum(v.numel() * v.element_size() for v in host_out[0].values())
+    h2d = hpack.nbytes
+    d2h = opacks[0].nbytes
 
     if rank != 0:
         if world > 1:
@@ -898,7 +933,7 @@ def run_gpu_ssd(args, w):
         "cpu_baseline": cpu,
         "e2e": {"value": w.updates * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
-                "pipeline": "2 buffer sets; uploads, calls and downloads on three streams, overlapped across steps"},
+                "pipeline": "2 buffer sets; one packed upload, the call(s) and one packed download per step on three streams, overlapped across steps"},
         "gpu_launches": args.steps, "clocks": clk.summary(),
         "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
     }
