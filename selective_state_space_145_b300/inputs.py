@@ -256,3 +256,88 @@ def ssd_inputs(batch: int, seqlen: int, nheads: int, headdim: int = 64, dstate: 
 
 def ssd_workload_inputs(w: SsdWorkload) -> Dict[str, Optional[torch.Tensor]]:
     return ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.seed)
+
+
+# ---- problems too large to draw on the host
+#
+# Same distributions and shapes as scan_inputs, decode_inputs and ssd_inputs, for tensors of
+# billions of elements: the per-token tensors and states are drawn directly on `device`, in their
+# storage dtype, by a generator of that device seeded with `seed`; the per-channel (or per-head)
+# parameters are drawn on the host as above and then moved. The numbers differ from the host
+# recipe's (another generator), the distributions do not.
+
+def _dev_gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _dev_normal(g: torch.Generator, shape, dtype, device, scale: float = 1.0) -> torch.Tensor:
+    t = torch.randn(shape, generator=g, dtype=dtype, device=device)
+    return t.mul_(scale) if scale != 1.0 else t
+
+
+def _channel_params(g: torch.Generator, dim: int, dstate: int, d_conv: int, device):
+    D = torch.randn(dim, generator=g)
+    dt_ = _log_uniform(g, dim, 1e-3, 0.1)
+    delta_bias = (dt_ + torch.log(-torch.expm1(-dt_))).to(torch.float32)
+    conv_w = (torch.rand(dim, d_conv, generator=g) - 0.5).contiguous() if d_conv > 0 else None
+    conv_b = torch.zeros(dim, dtype=torch.float32) if d_conv > 0 else None
+    mv = lambda t: None if t is None else t.to(device)
+    return {"D": mv(D), "delta_bias": mv(delta_bias), "A": mv(s4d_real_A(dim, dstate)), "conv_w": mv(conv_w),
+            "conv_b": mv(conv_b)}
+
+
+def scan_inputs_on(device, batch: int, dim: int, seqlen: int, dstate: int, d_conv: int = 0, io: str = "bf16",
+                   seed: int = 0) -> Dict[str, Optional[torch.Tensor]]:
+    """A prefill problem drawn on `device` (keys of scan_inputs; no h0, no conv_init)."""
+    gd = _dev_gen(seed, device)
+    dt = IO_DTYPES[io]
+    p = {
+        "x": _dev_normal(gd, (batch, dim, seqlen), dt, device),
+        "delta": _dev_normal(gd, (batch, dim, seqlen), dt, device, 0.5),
+        "z": _dev_normal(gd, (batch, dim, seqlen), dt, device),
+        "B": _dev_normal(gd, (batch, dstate, seqlen), dt, device),
+        "C": _dev_normal(gd, (batch, dstate, seqlen), dt, device),
+        "conv_init": None, "h0": None,
+    }
+    p.update(_channel_params(_gen(seed), dim, dstate, d_conv, device))
+    return p
+
+
+def decode_inputs_on(device, batch: int, dim: int, dstate: int, d_conv: int = 4, io: str = "bf16",
+                     seed: int = 0) -> Dict[str, Optional[torch.Tensor]]:
+    """One decode step drawn on `device`: x, delta, z [batch, dim]; B, C [batch, dstate];
+    state [batch, dim, dstate] fp32; conv_state [batch, dim, d_conv-1]; parameters as decode_inputs."""
+    gd = _dev_gen(seed, device)
+    dt = IO_DTYPES[io]
+    p = {
+        "x": _dev_normal(gd, (batch, dim), dt, device),
+        "delta": _dev_normal(gd, (batch, dim), dt, device, 0.5),
+        "z": _dev_normal(gd, (batch, dim), dt, device),
+        "B": _dev_normal(gd, (batch, dstate), dt, device),
+        "C": _dev_normal(gd, (batch, dstate), dt, device),
+        "state": _dev_normal(gd, (batch, dim, dstate), torch.float32, device),
+        "conv_state": _dev_normal(gd, (batch, dim, d_conv - 1), dt, device) if d_conv > 1 else None,
+    }
+    p.update(_channel_params(_gen(seed), dim, dstate, d_conv, device))
+    return p
+
+
+def ssd_inputs_on(device, batch: int, seqlen: int, nheads: int, headdim: int = 64, dstate: int = 128,
+                  seed: int = 0) -> Dict[str, Optional[torch.Tensor]]:
+    """A problem of the state-space-duality layer drawn on `device` (keys of ssd_inputs, no h0)."""
+    gd = _dev_gen(seed, device)
+    bf = torch.bfloat16
+    g = _gen(seed)
+    D = torch.randn(nheads, generator=g)
+    dt0 = _log_uniform(g, nheads, 1e-3, 0.1)
+    dt_bias = (dt0 + torch.log(-torch.expm1(-dt0))).to(torch.float32)
+    A = -(1.0 + 15.0 * torch.rand(nheads, generator=g))
+    return {
+        "x": _dev_normal(gd, (batch, seqlen, nheads, headdim), bf, device),
+        "dt": _dev_normal(gd, (batch, seqlen, nheads), bf, device, 0.5),
+        "B": _dev_normal(gd, (batch, seqlen, dstate), bf, device),
+        "C": _dev_normal(gd, (batch, seqlen, dstate), bf, device),
+        "A": A.to(device), "D": D.to(device), "dt_bias": dt_bias.to(device), "h0": None,
+    }
