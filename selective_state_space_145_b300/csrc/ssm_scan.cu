@@ -461,17 +461,24 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
     }
     __syncthreads();  // (B)
 
-    // ---- scan phase: sequential in t; steps past tl have Delta = 0 and Delta*u = 0 (identity)
+    // ---- scan phase: sequential in t; steps past tl have Delta = 0 and Delta*u = 0 (identity).
+    // kU steps per pass over the staged rows: 8 in the bf16 main pass with the conv prologue
+    // (more independent exp2 work in flight), 4 elsewhere (8 would spill in the fp32 main pass).
     {
-      const int tl4 = (tl + 3) & ~3;
-      for (int t = 0; t < tl4; t += 4) {
-        const float4 dl4 = *reinterpret_cast<const float4*>(&s_dl[c][t]);
-        const float4 du4 = *reinterpret_cast<const float4*>(&s_du[c][t]);
-        const float dl[4] = {dl4.x, dl4.y, dl4.z, dl4.w};
-        const float du[4] = {du4.x, du4.y, du4.z, du4.w};
-        float yv[4];
+      constexpr int kU = (sizeof(T) == 2 && CONV && !CARRY) ? 8 : 4;
+      const int tlu = (tl + kU - 1) & ~(kU - 1);
+      for (int t = 0; t < tlu; t += kU) {
+        float dl[kU], du[kU];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int i = 0; i < kU; i += 4) {
+          const float4 dl4 = *reinterpret_cast<const float4*>(&s_dl[c][t + i]);
+          const float4 du4 = *reinterpret_cast<const float4*>(&s_du[c][t + i]);
+          dl[i] = dl4.x; dl[i + 1] = dl4.y; dl[i + 2] = dl4.z; dl[i + 3] = dl4.w;
+          du[i] = du4.x; du[i + 1] = du4.y; du[i + 2] = du4.z; du[i + 3] = du4.w;
+        }
+        float yv[kU];
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
           const float4 bv = *reinterpret_cast<const float4*>(&s_B[t + j][4 * g]);
           const float2 dd = f2(dl[j]);
           const float2 x01 = fmul2(dd, a01), x23 = fmul2(dd, a23);
@@ -493,7 +500,13 @@ __global__ void __launch_bounds__(kThreads, 4) scan_kernel(const ScanArgs a) {
             dsum += dl[j];
           }
         }
-        if (!CARRY) store4(&s_y[g][c][t], yv);
+        if (!CARRY) {
+#pragma unroll
+          for (int i = 0; i < kU; i += 4) {
+            const float y4[4] = {yv[i], yv[i + 1], yv[i + 2], yv[i + 3]};
+            store4(&s_y[g][c][t + i], y4);
+          }
+        }
       }
     }
 
