@@ -159,7 +159,7 @@ def bwd_algorithmic_bytes(w) -> int:
 
 
 # The sources each kind of workload's kernels are built from: a traffic figure stays valid
-# while these files are unchanged.
+# while their code is unchanged (comments and whitespace do not count, see source_code_only).
 _KERNEL_SOURCES = {
     "scan": ("ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
     "decode": ("ssm_decode.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
@@ -168,11 +168,38 @@ _KERNEL_SOURCES = {
 }
 
 
+def source_code_only(text: str) -> str:
+    """C / C++ / CUDA source without its comments, with every run of whitespace collapsed to one
+    space: two sources that differ only in comments or layout compile to the same kernels and
+    give the same string. String and character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":  # literal: copy through the closing quote, honouring escapes
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kind: str = "scan") -> str:
     h = hashlib.sha256()
     for name in _KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "selective_state_space_145_b300", "csrc", name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(ROOT, "selective_state_space_145_b300", "csrc", name), encoding="utf-8") as f:
+            h.update(name.encode() + source_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -106,3 +106,19 @@ def test_ssd_work_and_bytes():
     assert bench.ssd_algorithmic_bytes(w) == (tok * 32 * 64 * 2 * 2 + tok * 32 * 2 + 2 * tok * 128 * 2
                                               + 8 * 32 * 64 * 128 * 4 + 32 * 4 * 3)
     assert w.updates == 8 * 2048 * 32 * 64 * 128
+
+
+def test_traffic_records_follow_code_not_comments():
+    """A recorded DRAM-traffic figure belongs to the code it was measured on: the source hash
+    ignores comments and layout, and changes with any code token or string literal."""
+    import bench
+
+    base = 'int f(int a) {\n  // old note\n  return a * 2; /* x */\n}\nconst char* s = "a // b";\n'
+    same = 'int f(int a)\n{\n  /* a new, longer\n     note */\n  return a * 2;   // y\n}\nconst char* s = "a // b";\n'
+    code = 'int f(int a) {\n  return a * 3;\n}\nconst char* s = "a // b";\n'
+    lit = 'int f(int a) {\n  return a * 2;\n}\nconst char* s = "a // c";\n'
+    cb = bench.source_code_only(base)
+    assert cb == bench.source_code_only(same)
+    assert cb != bench.source_code_only(code)
+    assert cb != bench.source_code_only(lit)
+    assert "old note" not in cb and '"a // b"' in cb
