@@ -34,10 +34,6 @@ int sm_count() {
 
 long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 
-// Time-chunk length. Chunking costs a carry pass over all but the last chunk, so the scan
-// runs as one chunk whenever the channels alone give every SM a CTA. Otherwise each chunk's
-// CTAs walk their steps sequentially, and short chains of many CTAs beat long chains of few:
-// take up to 16 CTAs per SM, keeping chunks at least 256 steps long.
 // Chunk length of the default policy. The scan is sequential in t within a CTA, so a
 // problem with few channels leaves most SMs idle unless the sequence is split into chunks.
 // The policy splits only as far as the main pass still fits in one wave of resident CTAs:
