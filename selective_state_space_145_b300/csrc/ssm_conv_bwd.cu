@@ -9,11 +9,15 @@
 //   dx[s] = sum_k w[k] dacc_{s+(K-1)-k};  dwindow likewise for s < 0
 //   dw[d,k] = sum_{b,t} dacc_t xs(t-(K-1)+k);  dbias[d] = sum_{b,t} dacc_t.
 //
-// Design. One thread owns 4 consecutive positions s of one row: it recomputes acc and dacc at
-// the K+3 steps that reach them, writes dx for its 4 positions, and adds the dw / dbias terms
-// of its own 4 steps. A block (1024 steps of one row) reduces those terms and writes one
-// partial; a second kernel sums the partials over sequences and segments in a fixed order.
-// The conv taps are zero-padded to 4 (w[4-K+k] holds tap k).
+// Design. A block takes 1024 consecutive steps of one row; one thread owns 4 of them. The
+// block stages x at its steps (plus a 4-step halo on each side) and then dacc at its steps
+// (plus the 3 that follow) in shared memory, so every activation is computed once: thread i
+// computes acc and dacc at its own 4 steps, and one thread adds the 3 steps past the block.
+// dx at a step takes the 4 dacc values that reach it from the staged row. Rows whose length is
+// a multiple of 4 at aligned addresses move 4 elements per load and store. Each thread adds
+// the dw / dbias terms of its own 4 steps; the block reduces them and writes one partial, and
+// a second kernel sums the partials over sequences and segments in a fixed order. The conv
+// taps are zero-padded to 4 (w[4-K+k] holds tap k).
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -23,15 +27,21 @@ namespace {
 constexpr int kCBThreads = 256;
 constexpr int kCBSeg = kCBThreads * 4;   // steps per block
 constexpr int kCBPart = kMaxConv + 1;    // partial: dw taps (padded) + dbias
+static_assert(kMaxConv == 4, "the staged halos hold 4 steps");
 
-template <typename T>
+// VEC: the row length is a multiple of 4 and x, dout, dx are aligned to 4 elements.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs a, int nseg) {
   __shared__ float red[kCBThreads / 32][kCBPart];
+  __shared__ __align__(16) float sx[kCBSeg + 8];   // x at steps base-4 .. base+kCBSeg+3
+  __shared__ __align__(16) float sda[kCBSeg + 4];  // dacc at steps base .. base+kCBSeg+3
   const int L = a.seqlen, K = a.d_conv;
   const long long c = blockIdx.x / nseg;          // channel row b * dim + d
   const int seg = blockIdx.x % nseg;
   const int d = (int)(c % a.dim);
-  const int s0 = seg * kCBSeg + threadIdx.x * 4;  // this thread's 4 positions
+  const int tid = threadIdx.x;
+  const int base = seg * kCBSeg;
+  const int s0 = base + tid * 4;                  // this thread's 4 steps
   const T* __restrict__ x = static_cast<const T*>(a.x) + c * L;
   const T* __restrict__ dout = static_cast<const T*>(a.dout) + c * L;
   const T* win = a.conv_init ? static_cast<const T*>(a.conv_init) + c * (K - 1) : nullptr;
@@ -48,38 +58,83 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
     if (s >= 0) return to_f32(x[s]);
     return (win && s >= -(K - 1)) ? to_f32(win[(K - 1) + s]) : 0.f;
   };
-
-  // x at s0-3 .. s0+6, dacc at s0 .. s0+6 (zero past L)
-  float xv[10];
+  // dacc at step t from the staged x at t-3 .. t (xw) and dout_t (zero past L)
+  auto dacc = [&](int t, const float* xw, float g) -> float {
+    if (t >= L) return 0.f;
+    float acc = cb;
 #pragma unroll
-  for (int j = 0; j < 10; ++j) xv[j] = xs(s0 - 3 + j);
-  float da[7];
-#pragma unroll
-  for (int j = 0; j < 7; ++j) {
-    const int t = s0 + j;
-    float g = 0.f;
-    if (t < L) {
-      float acc = cb;
-#pragma unroll
-      for (int i = 0; i < kMaxConv; ++i) acc = fmaf(wp[i], xv[j + i], acc);
-      g = to_f32(dout[t]);
-      if (a.apply_silu) {
-        const float sg = rcp_approx(1.0f + ex2_approx(-acc * kLog2e));
-        g *= sg * fmaf(acc, 1.0f - sg, 1.0f);
-      }
+    for (int i = 0; i < kMaxConv; ++i) acc = fmaf(wp[i], xw[i], acc);
+    if (a.apply_silu) {
+      const float sg = rcp_approx(1.0f + ex2_approx(-acc * kLog2e));
+      g *= sg * fmaf(acc, 1.0f - sg, 1.0f);
     }
-    da[j] = g;
+    return g;
+  };
+
+  // ---- stage x; own steps from registers, the halos from one warp
+  float xo[4], go[4];
+  if (VEC && s0 < L) {
+    load4(x + s0, xo);
+    load4(dout + s0, go);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool in = s0 + j < L;
+      xo[j] = in ? to_f32(x[s0 + j]) : 0.f;
+      go[j] = in ? to_f32(dout[s0 + j]) : 0.f;
+    }
   }
-  // dx at s0 .. s0+3: dx[s] = sum_i wp[i] dacc_{s+3-i}
-  T* dx = static_cast<T*>(a.dx) + c * L;
+  *reinterpret_cast<float4*>(&sx[4 + 4 * tid]) = make_float4(xo[0], xo[1], xo[2], xo[3]);
+  if (tid < 4) sx[tid] = xs(base - 4 + tid);
+  else if (tid < 8) sx[kCBSeg + tid] = xs(base + kCBSeg + tid - 4);
+  __syncthreads();
+
+  // ---- dacc at the own steps; x at s0-4 .. s0+3 is sx[4 tid .. 4 tid + 7]
+  float xv[8];
+  {
+    const float4 p = *reinterpret_cast<const float4*>(&sx[4 * tid]);
+    xv[0] = p.x; xv[1] = p.y; xv[2] = p.z; xv[3] = p.w;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) xv[4 + j] = xo[j];
+  }
+  float da[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) da[j] = dacc(s0 + j, xv + j + 1, go[j]);
+  *reinterpret_cast<float4*>(&sda[4 * tid]) = make_float4(da[0], da[1], da[2], da[3]);
+  if (tid == kCBThreads - 1) {
+    // the 3 steps past the block reach its last dx values
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int t = base + kCBSeg + j;
+      sda[kCBSeg + j] = dacc(t, &sx[kCBSeg + 1 + j], t < L ? to_f32(dout[t]) : 0.f);
+    }
+    sda[kCBSeg + 3] = 0.f;
+  }
+  __syncthreads();
+
+  // ---- dx at the own steps: dx[s] = sum_i wp[i] dacc_{s+3-i}; dacc at s0 .. s0+6
+  float dn[8];
+  {
+    const float4 q = *reinterpret_cast<const float4*>(&sda[4 * tid + 4]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dn[j] = da[j];
+    dn[4] = q.x; dn[5] = q.y; dn[6] = q.z; dn[7] = q.w;
+  }
+  float dxv[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    if (s0 + j < L) {
-      float v = 0.f;
+    float v = 0.f;
 #pragma unroll
-      for (int i = 0; i < kMaxConv; ++i) v = fmaf(wp[i], da[j + 3 - i], v);
-      dx[s0 + j] = from_f32<T>(v);
-    }
+    for (int i = 0; i < kMaxConv; ++i) v = fmaf(wp[i], dn[j + 3 - i], v);
+    dxv[j] = v;
+  }
+  T* dx = static_cast<T*>(a.dx) + c * L;
+  if (VEC && s0 < L) {
+    store4(dx + s0, dxv);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (s0 + j < L) dx[s0 + j] = from_f32<T>(dxv[j]);
   }
   // window gradient: positions -(K-1) .. -1, reached by dacc_0 .. dacc_{K-2}
   if (s0 == 0 && a.dconv_init && K > 1) {
@@ -90,7 +145,7 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
 #pragma unroll
       for (int i = 0; i < kMaxConv; ++i) {
         const int t = s + 3 - i;
-        if (t >= 0 && t < 7 && t < L) v = fmaf(wp[i], da[t], v);
+        if (t >= 0 && t < L) v = fmaf(wp[i], dn[t], v);
       }
       dw_out[j] = from_f32<T>(v);
     }
@@ -102,22 +157,22 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
 #pragma unroll
-    for (int i = 0; i < kMaxConv; ++i) part[i] = fmaf(da[j], xv[j + i], part[i]);
+    for (int i = 0; i < kMaxConv; ++i) part[i] = fmaf(da[j], xv[j + 1 + i], part[i]);
     part[kMaxConv] += da[j];
   }
   // block reduction (fixed order): warp shuffles, then warp 0 over the warps
 #pragma unroll
   for (int i = 0; i < kCBPart; ++i)
     for (int o = 16; o > 0; o >>= 1) part[i] += __shfl_xor_sync(0xffffffffu, part[i], o);
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int lane = tid % 32, warp = tid / 32;
   if (lane == 0)
 #pragma unroll
     for (int i = 0; i < kCBPart; ++i) red[warp][i] = part[i];
   __syncthreads();
-  if (threadIdx.x < kCBPart) {
-    float s = 0.f;
-    for (int w = 0; w < kCBThreads / 32; ++w) s += red[w][threadIdx.x];
-    a.ws_part[((long long)c * nseg + seg) * kCBPart + threadIdx.x] = s;
+  if (tid < kCBPart) {
+    float sum = 0.f;
+    for (int w = 0; w < kCBThreads / 32; ++w) sum += red[w][tid];
+    a.ws_part[((long long)c * nseg + seg) * kCBPart + tid] = sum;
   }
 }
 
@@ -141,7 +196,13 @@ cudaError_t launch_conv_bwd_t(const ConvBwdArgs& a, cudaStream_t stream) {
   const int nseg = (a.seqlen + kCBSeg - 1) / kCBSeg;
   const long long blocks = (long long)a.batch * a.dim * nseg;
   if (blocks > 0) {
-    conv_bwd_kernel<T><<<(unsigned)blocks, kCBThreads, 0, stream>>>(a, nseg);
+    const uintptr_t vb = 4 * sizeof(T);
+    const bool vec = a.seqlen % 4 == 0 && reinterpret_cast<uintptr_t>(a.x) % vb == 0 &&
+                     reinterpret_cast<uintptr_t>(a.dout) % vb == 0 && reinterpret_cast<uintptr_t>(a.dx) % vb == 0;
+    if (vec)
+      conv_bwd_kernel<T, true><<<(unsigned)blocks, kCBThreads, 0, stream>>>(a, nseg);
+    else
+      conv_bwd_kernel<T, false><<<(unsigned)blocks, kCBThreads, 0, stream>>>(a, nseg);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
