@@ -122,3 +122,28 @@ def test_traffic_records_follow_code_not_comments():
     assert cb != bench.source_code_only(code)
     assert cb != bench.source_code_only(lit)
     assert "old note" not in cb and '"a // b"' in cb
+
+
+@pytest.mark.parametrize("workload", ["block_f32_b2_d1024_l1024_n16_k4", "ssd_bf16_b8_l2048_h32_p64_n128"])
+def test_reference_arm_line_on_rank_zero(monkeypatch, capsys, workload):
+    """Rank 0 prints one JSON line carrying the contract's keys; the oracle's sampling is replaced
+    by a fixed rate so that only the line's assembly is under test."""
+    import json
+
+    import bench
+    from selective_state_space_145_b300 import inputs
+
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    rate = 2.5e9
+    monkeypatch.setattr(bench, "oracle_sample_rate", lambda *a, **k: (rate, 4, "stub sample"))
+    monkeypatch.setattr(bench, "ssd_oracle_rate", lambda *a, **k: (rate, 4, "stub sample"))
+    assert bench.main(["--impl", "reference", "--workload", workload, "--steps", "2", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = inputs.WORKLOADS.get(workload) or inputs.SSD_WORKLOADS[workload]
+    assert line["impl"] == "reference" and line["value"] == rate and line["config"]["workload"] == workload
+    assert line["steps"] == 2 and line["warmup"] == 3 and line["higher_is_better"] is True
+    assert abs(line["ms_per_step"] - w.updates / rate * 1e3) < 1e-9 * line["ms_per_step"]
+    assert line["cpu_baseline"] == {"value": rate, "unit": line["unit"], "cores": 4, "kind": "oracle",
+                                    "sample": "stub sample"}
+    assert line["e2e"] == {"value": rate, "unit": line["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
