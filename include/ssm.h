@@ -321,8 +321,11 @@ SSM_API ssm_status ssm_selective_scan_fwd_noalloc(const void* x, const void* del
  *   io      SSM_BF16 only (SSM_F32 returns SSM_ERR_UNSUPPORTED); headdim must be 64 and dstate
  *           128, else SSM_ERR_UNSUPPORTED
  *   workspace  device buffer of ssm_ssd_workspace_bytes(...) bytes (256), 256-byte aligned;
- *           its contents need no initialisation. After the call its first 4 bytes hold a status
- *           word: nonzero if a wait on the tensor cores ran out (results then invalid).
+ *           its contents need no initialisation. After the call (once the stream reaches it)
+ *           its first 4 bytes hold a status word: 0 on success; 1 if a wait on the tensor cores
+ *           or on a tensor-map copy ran out; 2 if the kernel's shared memory was not 1024-byte
+ *           aligned (not expected: the kernel checks rather than assumes it). On a nonzero word
+ *           y and h_last are undefined; the context stays usable.
  * x, B, C and y must be 16-byte aligned; dt 2-byte aligned. The call allocates nothing and
  * runs one kernel (after clearing the status word) on `stream`.
  */
