@@ -321,18 +321,38 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     {
-      const float w = Delta * ex2_approx(c_end - cs);
-      // row t of slab `half`: its 128 bytes (the scaling is per element, so the chunk order is
-      // free; taking chunk c ^ (t % 8) at step c spreads the 8 rows of an atom over all banks)
-      unsigned char* rowp = sB + (uint32_t)half * kSlab + (uint32_t)((t >> 3) * 1024 + (t & 7) * 128);
-#pragma unroll 4
-      for (int c = 0; c < 8; ++c) {
-        unsigned char* p = rowp + 16 * (c ^ (t & 7));
-        float f[8];
-        unpack8(p, f);
+      // B~ row r = Delta_r 2^(c_end - c_r) B_r, in half rows of 64 bytes. The scaling is per
+      // element, so the chunk order is free: taking chunk c ^ (r % 8) at step c spreads the 8
+      // rows of an atom over all banks.
+      auto scale_half = [&](int r, int slab, int hc, float w) {
+        unsigned char* rowp = sB + (uint32_t)slab * kSlab + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] *= w;
-        *reinterpret_cast<uint4*>(p) = pack8(f);
+        for (int c = 4 * hc; c < 4 * hc + 4; ++c) {
+          unsigned char* p = rowp + 16 * (c ^ (r & 7));
+          float f[8];
+          unpack8(p, f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] *= w;
+          *reinterpret_cast<uint4*>(p) = pack8(f);
+        }
+      };
+      // The G' pass above is uneven: rows are bound to warps by their TMEM lane quarter, and
+      // warps 2, 3 and 7 mask two column blocks where warps 0, 1, 5 and 6 mask one and warp 4
+      // none. Those three warps hand their B rows (row t of slab `half`) to the lighter warps;
+      // a helper takes the weight of a row it does not own from the shared lg2 Delta_r - c_r.
+      if (warp != 2 && warp != 3 && warp != 7) {
+        const float w = Delta * ex2_approx(c_end - cs);
+        scale_half(t, half, 0, w);
+        scale_half(t, half, 1, w);
+      }
+      if (warp == 4) {  // rows 64..127 of slab 0 (those of warps 2 and 3)
+        const float w2 = ex2_approx(s_z[64 + lane] + c_end), w3 = ex2_approx(s_z[96 + lane] + c_end);
+        scale_half(64 + lane, 0, 0, w2);
+        scale_half(64 + lane, 0, 1, w2);
+        scale_half(96 + lane, 0, 0, w3);
+        scale_half(96 + lane, 0, 1, w3);
+      } else if (warp == 0 || warp == 1) {  // rows 96..127 of slab 1 (those of warp 7), one half each
+        scale_half(96 + lane, 1, warp, ex2_approx(s_z[96 + lane] + c_end));
       }
     }
     umma::fence_proxy_async();
