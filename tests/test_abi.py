@@ -182,3 +182,41 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(s, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         s.lib()
+
+
+_C_PROGRAM = r"""
+#include <stdio.h>
+#include "ssm.h"
+int main(void) {
+  /* every call returns from the host-side checks: nothing touches a GPU */
+  ssm_status st = ssm_selective_scan_fwd(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, NULL, NULL, 0, NULL,
+                                         NULL, NULL, NULL, NULL, 1, 4, 8, 16, SSM_F32, 0, NULL, 0, 0u, NULL);
+  printf("%d %s %s %zu %zu\n", ssm_version(), ssm_status_string(SSM_OK), ssm_status_string(st),
+         ssm_ssd_workspace_bytes(1, 128, 1, 64, 128, SSM_BF16), ssm_ssd_workspace_bytes(1, 128, 1, 32, 128, SSM_BF16));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """A C99 program (no C++, no torch) includes include/ssm.h under -pedantic -Werror, links
+    libssm.so and calls it; the header also compiles as C++."""
+    import shutil
+    import subprocess
+
+    import selective_state_space_145_b300 as ssm
+
+    gcc = shutil.which("gcc")
+    assert gcc, "gcc is part of the toolchain"
+    src = tmp_path / "abi.c"
+    src.write_text(_C_PROGRAM)
+    libdir = os.path.dirname(ssm.LIB_PATH)
+    exe = tmp_path / "abi"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-L", libdir, "-lssm", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert out == [str(ssm.version()), "SSM_OK", "SSM_ERR_INVALID_ARG", "256", "0"]
+    gxx = shutil.which("g++")
+    if gxx:
+        subprocess.run([gxx, "-std=c++17", "-Wall", "-Wextra", "-Werror", "-x", "c++", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], check=True)
