@@ -220,3 +220,29 @@ def test_header_is_plain_c_and_links(L, tmp_path):
     if gxx:
         subprocess.run([gxx, "-std=c++17", "-Wall", "-Wextra", "-Werror", "-x", "c++", "-fsyntax-only",
                         "-I", os.path.join(ROOT, "include"), str(src)], check=True)
+
+
+def test_default_chunk_policy_one_wave_rule(L):
+    """The default chunking on a 148-SM part with 4 resident scan CTAs per SM (the figures the
+    library assumes when no device answers, and those of the B300): split a sequence only as far
+    as the main pass still fits one wave, in multiples of 64 steps, and cut chunks of a split
+    sequence to at most 3072 steps."""
+    import selective_state_space_145_b300 as ssm
+    import torch
+
+    f32, bf16 = torch.float32, torch.bfloat16
+    resident = 148 * 4
+    # fp32 block workload: 64 channel CTAs, 9 fit a wave -> 1024 / 9 rounded up to 64 -> 128
+    assert ssm.ssm_scan_default_chunk_len(2, 1024, 1024, 16, f32) == 128
+    # bf16 block workload: 512 CTAs already more than half a wave -> one chunk
+    assert ssm.ssm_scan_default_chunk_len(8, 2048, 2048, 16, bf16) == 2048
+    # long scan: 48 channel CTAs, 12 chunks of 10944 would fit; cut to 3072
+    assert ssm.ssm_scan_default_chunk_len(1, 1536, 131072, 16, bf16) == 3072
+    # small scan: 2 channel CTAs; 4 chunks of 64 steps (the sequence allows no more)
+    assert ssm.ssm_scan_default_chunk_len(1, 64, 256, 16, f32) == 64
+    for batch, dim, L_ in ((1, 1536, 32768), (3, 700, 5000), (1, 33, 70000)):
+        cl = ssm.ssm_scan_default_chunk_len(batch, dim, L_, 16, bf16)
+        ctas = (dim + 31) // 32 * batch
+        q = (L_ + cl - 1) // cl
+        assert cl % 64 == 0 and cl <= max(3072, (L_ + 63) // 64 * 64)
+        assert q == 1 or q * ctas <= resident or cl == 3072
