@@ -246,3 +246,21 @@ def test_default_chunk_policy_one_wave_rule(L):
         q = (L_ + cl - 1) // cl
         assert cl % 64 == 0 and cl <= max(3072, (L_ + 63) // 64 * 64)
         assert q == 1 or q * ctas <= resident or cl == 3072
+
+
+def test_scan_workspace_stays_far_below_a_per_step_state(L):
+    """Memory is linear in the sequence only through the chunk count: the default chunking's
+    workspace holds (chunks - 1) carries of N + 1 floats per channel, never a state per step."""
+    import selective_state_space_145_b300 as ssm
+    import torch
+
+    batch, dim, N = 1, 1536, 16
+    prev = -1
+    for L_ in (1024, 8192, 65536, 131072, 524288):
+        cl = ssm.ssm_scan_default_chunk_len(batch, dim, L_, N, torch.bfloat16)
+        ws = ssm.ssm_scan_workspace_bytes(batch, dim, L_, N, 0, torch.bfloat16)
+        q = (L_ + cl - 1) // cl
+        assert ws <= (q - 1) * batch * dim * (N + 1) * 4 + 256
+        assert ws * 100 < batch * dim * L_ * N * 4          # a per-step state would be L x N floats
+        assert ws >= prev                                     # grows with L, at most linearly
+        prev = ws
