@@ -133,3 +133,28 @@ def test_ssd_heads_do_not_interact():
     np.testing.assert_array_equal(y[:, :, 0], y2[:, :, 0])
     np.testing.assert_array_equal(y[:, :, 2], y2[:, :, 2])
     assert not np.allclose(y[:, :, 1], y2[:, :, 1])
+
+
+def test_ssd_constant_input_geometric_sum():
+    """Constant x, dt, B, C over time: H_t = Delta x B^T (1 - a^(t+1)) / (1 - a) with a = exp(Delta A),
+    so y_t = Delta (B . C) x (1 - a^(t+1)) / (1 - a) + D x (closed form, no recurrence)."""
+    rng = np.random.default_rng(11)
+    batch, L, H, P, N = 2, 50, 3, 4, 5
+    x1 = rng.standard_normal((batch, 1, H, P))
+    B1, C1 = rng.standard_normal((batch, 1, N)), rng.standard_normal((batch, 1, N))
+    dt1 = 0.3 * rng.standard_normal((batch, 1, H))
+    A = -rng.uniform(0.5, 3.0, H)
+    D = rng.standard_normal(H)
+    bias = rng.uniform(-3.0, -1.0, H)
+    p = dict(x=np.repeat(x1, L, axis=1), dt=np.repeat(dt1, L, axis=1), A=A, B=np.repeat(B1, L, axis=1),
+             C=np.repeat(C1, L, axis=1), D=D, dt_bias=bias, h0=None)
+    y, hl = oracle.ssd(**p)
+    Delta = _softplus(dt1[:, 0] + bias)                         # [b, h]
+    a = np.exp(Delta * A)
+    t = np.arange(L)[None, :, None]
+    geo = (1.0 - a[:, None, :] ** (t + 1)) / (1.0 - a[:, None, :])      # [b, t, h]
+    bc = np.einsum("bn,bn->b", B1[:, 0], C1[:, 0])[:, None, None]
+    ref = (Delta[:, None, :] * bc * geo)[..., None] * x1 + D[None, None, :, None] * x1
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+    hl_ref = (Delta * (1.0 - a ** L) / (1.0 - a))[:, :, None, None] * x1[:, 0, :, :, None] * B1[:, 0][:, None, None, :]
+    np.testing.assert_allclose(hl, hl_ref, rtol=1e-11, atol=1e-12)
