@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "block_f32_b2_d1024_l1024_n16_k4"
+DEFAULT_WORKLOAD = "longscan_bf16_b1_d1536_l131072_n16"
 METRIC = "selective-scan state updates/s (B*L*D*N) and HBM GB/s vs B300 peak"
 UNIT = "updates/s"
 FALLBACK_HBM_GBS = 6400.0
@@ -53,11 +53,16 @@ def _sm_max_mhz() -> float:
     return 2032.0
 
 
-# Issue model of one state update on this part (probes: an ex2 occupies an SMSP's dispatch for
-# two cycles, an FFMA / FMUL lane-op for one cycle per 32 lanes): main pass ex2 + 4 FMA-pipe
-# ops (Delta*A, Delta*u*B, the recurrence, the readout) = 6 cycles per 32 updates per SMSP;
-# carry pass without the readout = 5.
-CYCLES_MAIN, CYCLES_CARRY = 6, 5
+# Pipe model of one state update on this part (measured by a throughput probe on the B300:
+# ex2.approx.f32 issues at 4 cycles per warp instruction per SMSP, i.e. 32 results per clock per
+# SM; packed fma.rn.f32x2 at 2 cycles per warp instruction, overlapping fully with ex2; lg2,
+# tanh and rcp at half the ex2 rate). Every update of the main pass and of the carry pass needs
+# one exp2, so the special-function pipe alone allows 32 updates per clock per SM: that is the
+# floor the scan kernels are held against. The four FMA-pipe operations of a main-pass update
+# (Delta*A, Delta*u*B, the recurrence, the readout) cost the same four cycles per 32 updates on
+# the FMA pipe, so a perfect kernel would keep both pipes full; the per-token element-wise work
+# (conv, SiLU, softplus, gate) comes on top.
+UPDATES_PER_CLK_PER_SM = 32
 
 
 def _as_graph(fn, dev):
@@ -105,21 +110,21 @@ class _Packed:
 
 
 def alu_roofline(w, seconds: float, chunk_len: int, sms: int):
-    """Scan step time against its issue floor: main + carry updates at the dispatch rate of
-    sms x 4 SMSPs x 32 lanes per clock at the maximum SM clock. The per-token element-wise work
-    (conv, SiLU, softplus, gate) is extra, so frac stays below 1 even for a perfect scan."""
+    """Scan step time against its special-function-pipe floor: main + carry updates, one exp2
+    each, at 32 per clock per SM at the maximum SM clock. The per-token element-wise work (conv,
+    SiLU, softplus, gate) is extra, so frac stays below 1 even for a perfect scan."""
     if w.kind != "scan":
         return None
     per_t = w.batch * w.dim * w.dstate
     nchunks = (w.seqlen + chunk_len - 1) // chunk_len if w.seqlen > 0 else 1
     u_main = per_t * w.seqlen
     u_carry = per_t * min(w.seqlen, (nchunks - 1) * chunk_len) if nchunks > 1 else 0
-    lane_clk = sms * 128 * _sm_max_mhz() * 1e6
-    floor_s = (CYCLES_MAIN * u_main + CYCLES_CARRY * u_carry) / lane_clk
+    rate = sms * UPDATES_PER_CLK_PER_SM * _sm_max_mhz() * 1e6
+    floor_s = (u_main + u_carry) / rate
     return {"bound": "alu", "achieved": u_main / seconds / 1e9, "peak": u_main / floor_s / 1e9,
             "unit": "Gupdates/s", "frac": floor_s / seconds, "carry_updates": u_carry,
-            "model": f"{CYCLES_MAIN} (main) / {CYCLES_CARRY} (carry) dispatch cycles per 32 updates per SMSP; "
-                     f"{sms} SMs x 4 SMSPs at {_sm_max_mhz():.0f} MHz"}
+            "model": f"one ex2 per main or carry update at {UPDATES_PER_CLK_PER_SM} per clock per SM (measured); "
+                     f"{sms} SMs at {_sm_max_mhz():.0f} MHz"}
 
 
 def algorithmic_bytes(w) -> int:

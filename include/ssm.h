@@ -280,8 +280,9 @@ SSM_API ssm_status ssm_selective_state_update(float* state, void* conv_state, co
  * the chunk carries go to a file-scope device array of SSM_NOALLOC_SCRATCH_BYTES bytes
  * instead. The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
  * routine).
- *   - The first call on a device looks up that array's device address, with the device
- *     current; make that first call before any stream capture.
+ *   - Every call looks up that array's device address in the current device's context
+ *     (cudaGetSymbolAddress, which allocates nothing). The first call on a device also loads
+ *     the library's device code there: make that first call before any stream capture.
  *   - With chunk_len = 0 the scan uses as many chunks as fit the array (one chunk needs
  *     none). An explicit chunk_len whose carries need more than SSM_NOALLOC_SCRATCH_BYTES
  *     (see ssm_scan_workspace_bytes) returns SSM_ERR_UNSUPPORTED before anything runs.

@@ -8,11 +8,13 @@
 //
 // The array costs SSM_NOALLOC_SCRATCH_BYTES of memory on every GPU that loads the library,
 // held until the process exits. In host code the array's name is only a host-side stand-in,
-// so its device address is looked up with cudaGetSymbolAddress, once per device, by the
-// first call made with that device current.
+// so its device address is looked up with cudaGetSymbolAddress, with the caller's device
+// current. The first call on a device is the set-up: it loads the library's device code
+// into that device's context (which is why it should come before any stream capture).
+// Later calls repeat the lookup, which is a table lookup in the CUDA runtime and allocates
+// nothing; an address cached across calls could go stale once the context is destroyed
+// (cudaDeviceReset) and the module is loaded again at another address.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "../../include/ssm.h"
 
@@ -20,24 +22,12 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_scan_scratch[SSM_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of g_scan_scratch on the current device (looked up on first use).
+// Device address of g_scan_scratch in the current device's context.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&p, g_scan_scratch);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_scan_scratch);
-    if (err != cudaSuccess) return err;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

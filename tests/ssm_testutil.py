@@ -19,18 +19,43 @@ def io_of(t: torch.Tensor) -> str:
     return "bf16" if t.dtype == torch.bfloat16 else "f32"
 
 
+_BLOCK = 1 << 24  # elements compared per pass, so that full-size tensors need no large temporaries
+
+
 def assert_close(got, ref, io: str, what: str):
+    """Every element: |got - ref| <= atol + rtol |ref|. got may be a (device) tensor of any float
+    dtype or an array; ref is the fp64 oracle result. Large tensors are compared block by block."""
     rtol, atol = TOL[io]
-    got = got.detach().float().cpu().double().numpy() if hasattr(got, "detach") else np.asarray(got, np.float64)
+    if hasattr(got, "detach"):
+        got = got.detach()
+        shape = tuple(got.shape)
+        flat_got = got.reshape(-1)
+        take = lambda s, e: flat_got[s:e].float().cpu().double().numpy()
+    else:
+        arr = np.asarray(got, np.float64)
+        shape = arr.shape
+        flat_np = arr.reshape(-1)
+        take = lambda s, e: flat_np[s:e]
     ref = np.asarray(ref, dtype=np.float64)
-    assert got.shape == ref.shape, (what, got.shape, ref.shape)
-    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
-    err = np.abs(got - ref)
-    bad = err > atol + rtol * np.abs(ref)
-    if bad.any():
-        i = tuple(np.argwhere(bad)[0])
-        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside rtol={rtol} atol={atol}; first at {i}: "
-                             f"gpu={got[i]!r} oracle={ref[i]!r}; max abs err {err.max():.3e}")
+    assert shape == ref.shape, (what, shape, ref.shape)
+    flat_ref = ref.reshape(-1)
+    nbad, first, max_err = 0, None, 0.0
+    for s in range(0, flat_ref.size, _BLOCK):
+        e = min(flat_ref.size, s + _BLOCK)
+        g, r = take(s, e), flat_ref[s:e]
+        assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+        err = np.abs(g - r)
+        max_err = max(max_err, float(err.max(initial=0.0)))
+        bad = err > atol + rtol * np.abs(r)
+        if bad.any():
+            nbad += int(bad.sum())
+            if first is None:
+                j = int(np.argmax(bad))
+                first = (np.unravel_index(s + j, shape), g[j], r[j])
+    if nbad:
+        i, gv, rv = first
+        raise AssertionError(f"{what}: {nbad}/{flat_ref.size} outside rtol={rtol} atol={atol}; first at "
+                             f"{tuple(int(v) for v in i)}: gpu={gv!r} oracle={rv!r}; max abs err {max_err:.3e}")
 
 
 def to_dev(p: dict, dev) -> dict:

@@ -73,15 +73,17 @@ def test_algorithmic_bytes_match_the_stated_formula():
 
 
 def test_issue_floor_and_backward_bytes():
-    """The issue-floor model and the backward's algorithmic bytes, spelled out for one shape."""
+    """The special-function-pipe floor and the backward's algorithmic bytes, spelled out for one
+    shape."""
     import bench
     from selective_state_space_145_b300 import inputs
 
     w = inputs.WORKLOADS["block_f32_b2_d1024_l1024_n16_k4"]
     per_t = 2 * 1024 * 16
-    # 8 chunks of 128: main 1024 steps, carry 7 * 128 steps; 148 SMs x 128 lanes at 2032 MHz
+    # 8 chunks of 128: main 1024 steps, carry 7 * 128 steps; one exp2 per update at 32 per clock
+    # per SM, 148 SMs at the maximum SM clock
     r = bench.alu_roofline(w, 1e-3, 128, 148)
-    floor = (6 * per_t * 1024 + 5 * per_t * 7 * 128) / (148 * 128 * bench._sm_max_mhz() * 1e6)
+    floor = (per_t * 1024 + per_t * 7 * 128) / (148 * 32 * bench._sm_max_mhz() * 1e6)
     assert r["frac"] == pytest.approx(floor / 1e-3)
     assert r["carry_updates"] == per_t * 7 * 128
     assert bench.alu_roofline(inputs.WORKLOADS["decode_bf16_b256_d5120_n16_k4_x64"], 1e-3, 0, 148) is None
