@@ -451,7 +451,7 @@ def run_gpu(args, w):
                                        zoh=args.zoh)
 
         launches_per_step = 2 if nchunks > 1 else 1
-        kernels = ["scan_kernel<carry>", "scan_kernel<main>"] if nchunks > 1 else ["scan_kernel<main>"]
+        kernels = ["scan_carry_kernel", "scan_main_kernel"] if nchunks > 1 else ["scan_main_kernel"]
         if not args.eager:
             step = _as_graph(step, dev)
 

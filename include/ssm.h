@@ -38,7 +38,9 @@
  *     SSM_ERR_INVALID_ARG or SSM_ERR_UNSUPPORTED without touching device memory. A
  *     failed launch returns SSM_ERR_CUDA. No call aborts, prints or throws.
  *   - Empty work (batch == 0 or dim == 0) returns SSM_OK without a launch.
- *   - dstate (N) is 1..16. d_conv (K) is 1..4 when a conv weight is given.
+ *   - dstate (N) is 1..32 for the forward scan and the decode step (compiled for N <= 16
+ *     and N <= 32), 1..16 for the backward pass. d_conv (K) is 1..4 when a conv weight is
+ *     given.
  *   - Tensors named as inputs are only read; outputs must not alias inputs, except the
  *     decode state and window, which are updated in place.
  */
@@ -60,8 +62,8 @@ extern "C" {
 typedef enum {
   SSM_OK = 0,
   SSM_ERR_INVALID_ARG = 1, /* a required pointer is NULL, a size is negative, a buffer is too small */
-  SSM_ERR_UNSUPPORTED = 2, /* a valid request outside the compiled limits (dstate > 16, d_conv > 4,
-                              misaligned pointer, unknown dtype) */
+  SSM_ERR_UNSUPPORTED = 2, /* a valid request outside the compiled limits (dstate > 32, or > 16 for
+                              the backward pass; d_conv > 4, misaligned pointer, unknown dtype) */
   SSM_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
 } ssm_status;
 

@@ -34,28 +34,59 @@ int sm_count() {
 
 long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 
-// Chunk length of the default policy. The scan is sequential in t within a CTA, so a
-// problem with few channels leaves most SMs idle unless the sequence is split into chunks.
-// The policy splits only as far as the main pass still fits in one wave of resident CTAs:
-// q chunks give q times the CTAs, each walking 1/q of the sequence, and a second wave
-// would cost as much as it saves.
+// The default policy: how the main pass maps a channel onto lanes, and the chunk length.
+// The scan is sequential in t within a CTA, so a problem with few channels leaves most SMs idle
+// unless the sequence is split into chunks, and every chunk but the last costs a carry pass.
+//  * N > 16: four lanes of 8 states per channel; chunks by the one-wave rule below.
+//  * N <= 16 with enough channels that the main pass, at two lanes of 8 states per channel,
+//    fills more than half a wave of resident CTAs: two lanes per channel, one chunk.
+//  * otherwise the sequence is split, and the main pass takes one lane per channel with all 16
+//    states, which keeps every per-channel value in registers: the one-wave rule splits only as
+//    far as q chunks of CTAs still fit one wave (q times the CTAs, each walking 1/q of the
+//    sequence; a second wave would cost as much as it saves).
+// Once a sequence is split, chunks longer than kLongChunk are cut further: the extra waves of
+// short chunks balance better than one wave of very long ones.
 constexpr long long kLongChunk = 3072;  // a multiple of kChunkQuantum
 
-int default_chunk_len_impl(int batch, int dim, int seqlen, bool bf16) {
-  const int dt = ssm::scan_channels_per_cta();
-  const long long ctas = ((dim + dt - 1) / dt) * (long long)batch;
-  const long long resident = (long long)sm_count() * ssm::scan_resident_ctas_per_sm(bf16);
+struct ScanPlan {
+  int lanes;
+  int chunk_len;
+};
+
+long long scan_ctas(int batch, int dim, int lanes) {
+  const int cpc = ssm::scan_channels_per_cta(lanes);
+  return ((dim + cpc - 1) / cpc) * (long long)batch;
+}
+
+ScanPlan default_plan(int batch, int dim, int seqlen, int dstate, bool bf16) {
   const long long whole = round_up(seqlen > 0 ? seqlen : 1, kChunkQuantum);
-  if (ctas <= 0 || 2 * ctas > resident) return (int)whole;
+  int lanes = dstate > 16 ? 4 : 2;
+  long long ctas = scan_ctas(batch, dim, lanes);
+  long long resident = (long long)sm_count() * ssm::scan_resident_ctas_per_sm(bf16, lanes);
+  if (ctas <= 0 || 2 * ctas > resident) return {lanes, (int)whole};
+  if (lanes == 2) {
+    lanes = 1;
+    ctas = scan_ctas(batch, dim, lanes);
+    resident = (long long)sm_count() * ssm::scan_resident_ctas_per_sm(bf16, lanes);
+  }
   long long q = resident / ctas;
   const long long qmax = (seqlen + kChunkQuantum - 1) / kChunkQuantum;
   if (q > qmax) q = qmax;
-  if (q <= 1) return (int)whole;
-  // Once the sequence is split anyway, chunks longer than kLongChunk are cut further: the extra
-  // waves of short chunks balance better than one wave of very long ones (long-scan workload,
-  // 10944 -> 3072 steps per chunk: 1.77 -> 1.69 ms).
+  if (q <= 1) return {lanes, (int)whole};
   const long long cl = round_up((seqlen + q - 1) / q, kChunkQuantum);
-  return (int)(cl > kLongChunk ? kLongChunk : cl);
+  return {lanes, (int)(cl > kLongChunk ? kLongChunk : cl)};
+}
+
+// Lanes per channel for a given chunking: chunked problems and problems whose channels alone
+// give one warp per SMSP at one lane per channel take one lane; the rest take two (N <= 16).
+int lanes_for(int batch, int dim, int nchunks, int dstate) {
+  if (dstate > 16) return 4;
+  if (nchunks > 1 || scan_ctas(batch, dim, 1) >= 4LL * sm_count()) return 1;
+  return 2;
+}
+
+int default_chunk_len_impl(int batch, int dim, int seqlen, int dstate, bool bf16) {
+  return default_plan(batch, dim, seqlen, dstate, bf16).chunk_len;
 }
 
 // Chunk length of the backward pass: the same one-wave rule, with the backward kernel's occupancy.
@@ -97,16 +128,15 @@ const char* ssm_status_string(int status) {
 }
 
 int ssm_scan_default_chunk_len(int batch, int dim, int seqlen, int dstate, ssm_dtype io) {
-  (void)dstate;
   if (batch <= 0 || dim <= 0 || seqlen < 0) return kChunkQuantum;
-  return default_chunk_len_impl(batch, dim, seqlen, io == SSM_BF16);
+  return default_chunk_len_impl(batch, dim, seqlen, dstate, io == SSM_BF16);
 }
 
 size_t ssm_scan_workspace_bytes(int batch, int dim, int seqlen, int dstate, int chunk_len, ssm_dtype io) {
   if (batch <= 0 || dim <= 0 || seqlen <= 0 || chunk_len < 0) return 0;
   int cl = chunk_len == 0 ? ssm_scan_default_chunk_len(batch, dim, seqlen, dstate, io)
                           : (int)round_up(chunk_len, kChunkQuantum);
-  return ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl));
+  return ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl), dstate);
 }
 
 ssm_status ssm_causal_conv1d_fwd(const void* x, const float* w, const float* bias, const void* conv_init, void* out,
@@ -140,7 +170,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
   if (flags & ~(SSM_SCAN_REVERSE | SSM_SCAN_ZOH)) return SSM_ERR_INVALID_ARG;
   if (!dims_ok(batch, dim, seqlen, dstate)) return SSM_ERR_INVALID_ARG;
-  if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
+  if (dstate > ssm::kMaxDstateScan) return SSM_ERR_UNSUPPORTED;
   if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
   if (chunk_len < 0) return SSM_ERR_INVALID_ARG;
   const bool conv = conv_w != nullptr;
@@ -163,10 +193,10 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   // chunking
   int cl;
   if (chunk_len == 0) {
-    cl = default_chunk_len_impl(batch, dim, seqlen, io == SSM_BF16);
+    cl = default_chunk_len_impl(batch, dim, seqlen, dstate, io == SSM_BF16);
     // lower the chunk count until the given workspace suffices
     while (nchunks_for(seqlen, cl) > 1 &&
-           ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl)) >
+           ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl), dstate) >
                (workspace ? workspace_bytes : 0)) {
       const int q = nchunks_for(seqlen, cl) - 1;
       cl = (int)round_up((seqlen + q - 1) / q, kChunkQuantum);
@@ -177,7 +207,8 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   }
   const int nchunks = nchunks_for(seqlen, cl);
   if (nchunks > 65535) return SSM_ERR_INVALID_ARG;
-  const size_t need = ssm::scan_workspace_bytes((long long)batch * dim, nchunks);
+  const int lanes = lanes_for(batch, dim, nchunks, dstate);
+  const size_t need = ssm::scan_workspace_bytes((long long)batch * dim, nchunks, dstate);
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return SSM_ERR_UNSUPPORTED;
@@ -194,6 +225,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
           aligned(out, 16) && (!z || aligned(z, 16));
   a.chunk_len = cl;
   a.nchunks = nchunks;
+  a.lanes = lanes;
   a.reverse = (flags & SSM_SCAN_REVERSE) ? 1 : 0;
   a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
   ssm::scan_workspace_split(workspace, (long long)batch * dim, nchunks, &a.ws_S, &a.ws_h);
@@ -208,7 +240,7 @@ ssm_status ssm_selective_state_update(float* state, void* conv_state, const void
   if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
   if (flags & ~SSM_SCAN_ZOH) return SSM_ERR_INVALID_ARG;
   if (batch < 0 || dim < 0 || dstate < 1) return SSM_ERR_INVALID_ARG;
-  if (dstate > kMaxDstate) return SSM_ERR_UNSUPPORTED;
+  if (dstate > ssm::kMaxDstateScan) return SSM_ERR_UNSUPPORTED;
   if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
   const bool conv = conv_w != nullptr;
   if (conv) {
@@ -292,7 +324,7 @@ ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float*
     f.batch = batch; f.dim = dim; f.seqlen = seqlen; f.dstate = dstate; f.bf16 = io == SSM_BF16;
     f.vec = ((long long)seqlen * (long long)es) % 16 == 0 && aligned(u, 16) && aligned(delta, 16) &&
             aligned(B, 16) && aligned(C, 16);
-    f.chunk_len = cl; f.nchunks = nchunks; f.reverse = 0; f.zoh = 0;
+    f.chunk_len = cl; f.nchunks = nchunks; f.lanes = 1; f.reverse = 0; f.zoh = 0;
     f.ws_S = const_cast<float*>(a.fS); f.ws_h = const_cast<float*>(a.fh);
     if (ssm::launch_scan_carry(f, st) != cudaSuccess) return SSM_ERR_CUDA;
   }

@@ -10,8 +10,8 @@
 //
 // HBM-bound: the fp32 state is read and written once (128 of the ~150 bytes a channel moves).
 // The fast kernel gives one thread a whole channel (16 states) and keeps the channel's
-// parameters in registers across sequences; the general kernel (any N, any alignment) gives
-// four threads a channel. The conv width is a compile-time constant in both.
+// parameters in registers across sequences; the general kernel (any N <= 32, any alignment)
+// gives four threads a channel. The conv width is a compile-time constant in both.
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -19,13 +19,13 @@ namespace ssm {
 namespace {
 
 // ---------------------------------------------------------------- one channel's step
-// For the four threads that own a channel (this thread holds states 4g .. 4g+3).
+// For the four threads that own a channel (this thread holds states SPT g .. SPT g + SPT-1).
 // KC = d_conv (0: no conv); the window holds K1 = KC - 1 raw inputs. Returns this thread's
 // part of C.h.
-template <typename T, int KC, bool ZOH>
+template <typename T, int KC, bool ZOH, int SPT>
 __device__ __forceinline__ float channel_step(const DecodeArgs& a, int d, float xv, float dv, const T* win,
-                                              float (&h)[4], const float (&av)[4], const float (&bv)[4],
-                                              const float (&cv)[4], float& u) {
+                                              float (&h)[SPT], const float (&av)[SPT], const float (&bv)[SPT],
+                                              const float (&cv)[SPT], float& u) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   constexpr int K1 = KC > 0 ? KC - 1 : 0;
   u = xv;
@@ -43,7 +43,7 @@ __device__ __forceinline__ float channel_step(const DecodeArgs& a, int d, float 
   const float dl2 = Delta * kLog2e;  // exp(Delta A) = 2^(Delta log2(e) A)
   float part = 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < SPT; ++j) {
     const float x = dl2 * av[j];
     const float e = ex2_approx(x);
     // input term: Euler Delta B u, or zero-order hold expm1(Delta A)/A B u
@@ -55,12 +55,13 @@ __device__ __forceinline__ float channel_step(const DecodeArgs& a, int d, float 
 }
 
 // ---------------------------------------------------------------- general kernel
-// Any N <= 16 and any alignment. Grid (ceil(dim / 64), batch): one CTA covers 64 channels of
-// one sequence, four threads per channel.
+// Any N <= 4 SPT (SPT = 4: N <= 16, SPT = 8: N <= 32) and any alignment. Grid
+// (ceil(dim / 64), batch): one CTA covers 64 channels of one sequence, four threads per
+// channel, SPT states per thread.
 constexpr int kDecThreads = 256;
 constexpr int kDecCh = kDecThreads / 4;
 
-template <typename T, int KC, bool ZOH>
+template <typename T, int KC, bool ZOH, int SPT>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a) {
   constexpr int K1 = KC > 0 ? KC - 1 : 0;
   const int c = threadIdx.x / 4, g = threadIdx.x % 4;
@@ -69,16 +70,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a)
   const bool valid = d < a.dim;
   const int N = a.dstate;
   const long long cc = b * a.dim + d;
-  float h[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f}, bv[4] = {0.f, 0.f, 0.f, 0.f},
-        cv[4] = {0.f, 0.f, 0.f, 0.f};
+  float h[SPT], av[SPT], bv[SPT], cv[SPT];
+#pragma unroll
+  for (int j = 0; j < SPT; ++j) h[j] = av[j] = bv[j] = cv[j] = 0.f;
   T win[K1 > 0 ? K1 : 1];
   float xv = 0.f, dv = 0.f, zv = 0.f;
   if (valid) {
     const T* Bb = static_cast<const T*>(a.B) + b * N;
     const T* Cb = static_cast<const T*>(a.C) + b * N;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = 4 * g + j;
+    for (int j = 0; j < SPT; ++j) {
+      const int n = SPT * g + j;
       if (n < N) {
         h[j] = a.state[cc * N + n];
         av[j] = a.A[(long long)d * N + n];
@@ -96,13 +98,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a)
   // window before any of them overwrites a slot
   __syncwarp();
   float u = 0.f;
-  float part = valid ? channel_step<T, KC, ZOH>(a, d, xv, dv, win, h, av, bv, cv, u) : 0.f;
+  float part = valid ? channel_step<T, KC, ZOH, SPT>(a, d, xv, dv, win, h, av, bv, cv, u) : 0.f;
   part += __shfl_xor_sync(0xffffffffu, part, 1);
   part += __shfl_xor_sync(0xffffffffu, part, 2);
   if (!valid) return;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (4 * g + j < N) a.state[cc * N + 4 * g + j] = h[j];
+  for (int j = 0; j < SPT; ++j)
+    if (SPT * g + j < N) a.state[cc * N + SPT * g + j] = h[j];
   if (g == 0) {
     float y = fmaf(a.D ? a.D[d] : 0.f, u, part);
     if (a.z) y *= silu_f(zv);
@@ -341,7 +343,8 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
 template <typename T, int KC, bool ZOH>
 cudaError_t launch_general(const DecodeArgs& a, cudaStream_t stream) {
   dim3 grid((a.dim + kDecCh - 1) / kDecCh, a.batch);
-  decode_kernel<T, KC, ZOH><<<grid, kDecThreads, 0, stream>>>(a);
+  if (a.dstate > 16) decode_kernel<T, KC, ZOH, 8><<<grid, kDecThreads, 0, stream>>>(a);
+  else decode_kernel<T, KC, ZOH, 4><<<grid, kDecThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -7,8 +7,10 @@
 
 namespace ssm {
 
-// Largest state size the kernels hold in registers.
+// Largest state size the decode and backward kernels hold in registers.
 constexpr int kMaxDstate = 16;
+// Largest state size of the forward scan (two compile-time geometries: N <= 16 and N <= 32).
+constexpr int kMaxDstateScan = 32;
 // Largest conv width; narrower filters are zero-padded on the old side to this width.
 constexpr int kMaxConv = 4;
 // Chunk lengths are multiples of the scan's time tile.
@@ -37,10 +39,11 @@ struct ScanArgs {
   int vec;               // 1: 16-byte vector path is legal for every per-token tensor
   int chunk_len;         // multiple of kChunkQuantum, >= 1 chunk
   int nchunks;
+  int lanes;             // lanes per channel of the main pass: 1 (N <= 16), 2 (N <= 16) or 4 (N <= 32)
   int reverse;           // 1: the scan runs from t = L-1 down to t = 0
   int zoh;               // 1: zero-order-hold input term expm1(Delta A)/A B u
   float* ws_S;           // [nchunks-1][batch*dim] sum of Delta per chunk
-  float* ws_h;           // [nchunks-1][batch*dim][kMaxDstate] chunk end state from zero
+  float* ws_h;           // [nchunks-1][batch*dim][scan_state_stride(dstate)] chunk end state from zero
 };
 
 struct ConvArgs {
@@ -146,13 +149,16 @@ struct ScanBwdArgs {
   float* ws_dbias;       // [nchunks][batch][dim]
 };
 
-// Channels one scan CTA covers.
-int scan_channels_per_cta();
-// CTAs of the main scan kernel resident per SM (occupancy query; 4 without a device)
-int scan_resident_ctas_per_sm(bool bf16);
+// Channels one main-pass CTA covers with `lanes` lanes per channel (1, 2 or 4).
+int scan_channels_per_cta(int lanes);
+// CTAs of that main-pass kernel resident per SM (occupancy query; the shared-memory limit
+// without a device)
+int scan_resident_ctas_per_sm(bool bf16, int lanes);
+// Per-channel stride of the chunk end states in the scan workspace: 16 for N <= 16, else 32.
+int scan_state_stride(int dstate);
 
 // Workspace layout of the chunked scan.
-size_t scan_workspace_bytes(long long channels, int nchunks);
+size_t scan_workspace_bytes(long long channels, int nchunks, int dstate);
 void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, float** h);
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);

@@ -73,7 +73,7 @@ def test_scan_argument_checks(L):
     assert _scan(L, out=None) == 1
     assert _scan(L, seqlen=-1) == 1
     assert _scan(L, dstate=0) == 1
-    assert _scan(L, dstate=17) == 2
+    assert _scan(L, dstate=33) == 2  # the forward scan holds up to 32 states
     assert _scan(L, io=7) == 2
     assert _scan(L, sp=2) == 1
     assert _scan(L, conv_w=FAKE, d_conv=5) == 2
@@ -133,8 +133,8 @@ def test_decode_and_conv_argument_checks(L):
     bad[0] = None
     assert f(*bad) == 1                            # state missing
     bad = list(base)
-    bad[17] = 32
-    assert f(*bad) == 2                            # dstate > 16
+    bad[17] = 33
+    assert f(*bad) == 2                            # dstate > 32
     bad = list(base)
     bad[1] = None
     assert f(*bad) == 1                            # conv window missing with a conv
@@ -223,29 +223,35 @@ def test_header_is_plain_c_and_links(L, tmp_path):
 
 
 def test_default_chunk_policy_one_wave_rule(L):
-    """The default chunking on a 148-SM part with 4 resident scan CTAs per SM (the figures the
-    library assumes when no device answers, and those of the B300): split a sequence only as far
-    as the main pass still fits one wave, in multiples of 64 steps, and cut chunks of a split
-    sequence to at most 3072 steps."""
+    """The default chunking on a 148-SM part with the resident CTAs the shared-memory limit
+    allows (the figures the library assumes when no device answers). A main-pass CTA is one
+    warp. With two lanes of 8 states per channel it covers 16 channels, and 7 bf16 or 5 fp32
+    CTAs fit an SM; a problem whose CTAs then fill more than half a wave runs unchunked.
+    Otherwise the sequence is split and the main pass takes whole channels per lane (two
+    channels of 16 states per lane, 64 channels per CTA, 16-step tiles, 9 bf16 or 5 fp32 CTAs
+    per SM): split only as far as the chunks' CTAs still fit one wave, in multiples of 64
+    steps, and cut chunks of a split sequence to at most 3072 steps."""
     import selective_state_space_145_b300 as ssm
     import torch
 
     f32, bf16 = torch.float32, torch.bfloat16
-    resident = 148 * 4
-    # fp32 block workload: 64 channel CTAs, 9 fit a wave -> 1024 / 9 rounded up to 64 -> 128
-    assert ssm.ssm_scan_default_chunk_len(2, 1024, 1024, 16, f32) == 128
-    # bf16 block workload: 512 CTAs already more than half a wave -> one chunk
+    resident1 = {f32: 148 * 5, bf16: 148 * 9}
+    # fp32 block workload: 128 two-lane CTAs fit easily -> split; 32 whole-channel CTAs, 23
+    # chunks would fit a wave, the sequence allows 16 -> chunks of 64
+    assert ssm.ssm_scan_default_chunk_len(2, 1024, 1024, 16, f32) == 64
+    # bf16 block workload: 1024 two-lane CTAs already more than half a wave -> one chunk
     assert ssm.ssm_scan_default_chunk_len(8, 2048, 2048, 16, bf16) == 2048
-    # long scan: 48 channel CTAs, 12 chunks of 10944 would fit; cut to 3072
-    assert ssm.ssm_scan_default_chunk_len(1, 1536, 131072, 16, bf16) == 3072
-    # small scan: 2 channel CTAs; 4 chunks of 64 steps (the sequence allows no more)
+    # long scan: 24 whole-channel CTAs, 55 chunks fit a wave -> 131072 / 55 rounded up to 64
+    assert ssm.ssm_scan_default_chunk_len(1, 1536, 131072, 16, bf16) == 2432
+    # small scan: 1 whole-channel CTA; 4 chunks of 64 steps (the sequence allows no more)
     assert ssm.ssm_scan_default_chunk_len(1, 64, 256, 16, f32) == 64
-    for batch, dim, L_ in ((1, 1536, 32768), (3, 700, 5000), (1, 33, 70000)):
-        cl = ssm.ssm_scan_default_chunk_len(batch, dim, L_, 16, bf16)
-        ctas = (dim + 31) // 32 * batch
-        q = (L_ + cl - 1) // cl
-        assert cl % 64 == 0 and cl <= max(3072, (L_ + 63) // 64 * 64)
-        assert q == 1 or q * ctas <= resident or cl == 3072
+    for io in (f32, bf16):
+        for batch, dim, L_ in ((1, 1536, 32768), (3, 700, 5000), (1, 33, 70000)):
+            cl = ssm.ssm_scan_default_chunk_len(batch, dim, L_, 16, io)
+            ctas = (dim + 63) // 64 * batch
+            q = (L_ + cl - 1) // cl
+            assert cl % 64 == 0 and cl <= max(3072, (L_ + 63) // 64 * 64)
+            assert q == 1 or q * ctas <= resident1[io] or cl == 3072
 
 
 def test_scan_workspace_stays_far_below_a_per_step_state(L):
@@ -261,6 +267,8 @@ def test_scan_workspace_stays_far_below_a_per_step_state(L):
         ws = ssm.ssm_scan_workspace_bytes(batch, dim, L_, N, 0, torch.bfloat16)
         q = (L_ + cl - 1) // cl
         assert ws <= (q - 1) * batch * dim * (N + 1) * 4 + 256
-        assert ws * 100 < batch * dim * L_ * N * 4          # a per-step state would be L x N floats
+        # a per-step state would be L x N floats; chunks of at least 64 steps keep the carries
+        # (N + 1 floats per chunk) at least 64 N / (N + 1) ~ 60 times smaller
+        assert ws * 50 < batch * dim * L_ * N * 4
         assert ws >= prev                                     # grows with L, at most linearly
         prev = ws

@@ -53,7 +53,7 @@ def test_decode_steps_replay_from_a_graph(cuda_device):
 
 
 def test_chunked_scan_replays_from_a_graph(cuda_device):
-    """The chunked forward (carry kernel + programmatic-dependent main kernel) under capture."""
+    """The chunked forward (carry kernel, then main kernel) under capture."""
     import selective_state_space_145_b300 as ssm
 
     p = inputs.scan_inputs(2, 64, 1024, 16, 4, "f32", seed=9, with_h0=True)

@@ -33,10 +33,15 @@ SMALL = [
     (2, 40, 96, 5, 3, "bf16", True, True, True, 0),          # N < 16, K < 4
     (3, 130, 200, 16, 4, "bf16", False, False, False, 64),   # 4 chunks, ragged last chunk
     (2, 33, 333, 7, 2, "f32", True, True, True, 64),         # chunks + ragged + odd N
-    (1, 20000, 40, 16, 4, "bf16", True, False, False, 0),    # many channels: 4 states per thread
-    (2, 5000, 300, 16, 4, "f32", True, True, True, 128),     # 4 states per thread, chunked
+    (1, 20000, 40, 16, 4, "bf16", True, False, False, 0),    # many channel tiles
+    (2, 5000, 300, 16, 4, "f32", True, True, True, 128),     # many channel tiles, chunked
     (1, 3, 1, 1, 4, "f32", True, True, True, 0),             # L = 1, N = 1
     (1, 8, 3, 16, 4, "bf16", False, True, False, 0),         # L < K-1: the window comes from conv_init
+    # more than 16 states: four lanes of 8 states per channel (main pass), two lanes of 16 (carry)
+    (1, 40, 200, 17, 0, "f32", True, False, True, 0),        # N = 17, one chunk
+    (2, 24, 333, 24, 3, "f32", True, True, True, 64),        # N = 24, chunks, ragged
+    (2, 50, 300, 32, 4, "bf16", True, True, True, 128),      # N = 32, chunks, conv
+    (1, 3000, 64, 32, 4, "bf16", False, False, False, 0),    # N = 32, many channel tiles
 ]
 
 
@@ -129,6 +134,8 @@ REVERSE = [
     (1, 70, 130, 16, 0, "bf16", True, False, 0),     # element-wise path, no conv
     (2, 64, 196, 16, 4, "f32", False, False, 64),    # chunks of 64, last chunk 4 steps
     (1, 8, 3, 16, 4, "bf16", False, True, 0),        # L < K-1: the window comes from conv_init
+    (2, 30, 300, 32, 4, "bf16", True, True, 128),    # N = 32, chunks
+    (1, 20, 97, 20, 0, "f32", True, False, 64),      # N = 20, element-wise path, chunks
 ]
 
 
@@ -214,6 +221,9 @@ DECODE_SMALL = [
     (2, 33, 5, 2, "f32", 4),     # N not a multiple of 4: element-wise state path
     (4, 64, 16, 4, "f32", 3),
     (1, 7, 16, 1, "bf16", 2),    # K = 1: no window
+    (2, 40, 17, 4, "f32", 3),    # more than 16 states: 8 states per thread
+    (3, 33, 24, 3, "bf16", 4),
+    (2, 70, 32, 4, "f32", 3),
 ]
 
 
@@ -281,6 +291,7 @@ ZOH = [
     (2, 33, 101, 7, 3, "f32", 64, False),        # element-wise path, chunks, N < 16
     (2, 48, 300, 16, 4, "f32", 64, True),        # backward + ZOH, chunked
     (1, 70, 130, 16, 0, "bf16", 0, True),
+    (2, 20, 200, 32, 4, "f32", 64, False),       # N = 32, chunks
 ]
 
 
