@@ -266,6 +266,44 @@ SSM_API ssm_status ssm_selective_state_update(float* state, void* conv_state, co
                                       ssm_dtype io, unsigned int flags, void* stream);
 
 /*
+ * Segment aggregate of the selective scan, for scans split across sequence segments (a long
+ * prompt processed in parts on several GPUs, or in parts on one). "Mamba" (ozercemkelahmet.com),
+ * "Deployment notes": long prompts are processed in chunks that pass the state on; the
+ * associative operator that makes the segments independent is the composition of the affine
+ * maps h -> a h + b of "Mamba" (inferensys.com glossary), the parallel-scan paragraph.
+ *
+ * For one segment of a sequence (the tokens t0 .. t0+seqlen-1 of each (batch, channel)),
+ * with the arguments and layouts of ssm_selective_scan_fwd (x, delta, B, conv prologue,
+ * delta_bias / softplus, flags SSM_SCAN_REVERSE and SSM_SCAN_ZOH):
+ *   S_out [batch, dim] float32          = sum over the segment of Delta_t (natural units), so
+ *                                         that exp(A[d,n] S) is the segment's decay of state n;
+ *   h_out [batch, dim, dstate] float32  = the state at the segment's end when it starts at zero.
+ * The state after the segment from an initial state h is exp(A S) h + h_out (elementwise per
+ * state), so segments can be aggregated independently and composed in order afterwards
+ * (ssm_scan_compose). conv_init is the conv window before the segment: the last d_conv-1 raw
+ * inputs of the previous segment (or of the stream before the sequence).
+ * The workspace holds per-chunk partial aggregates: ssm_scan_aggregate_workspace_bytes bytes,
+ * 256-byte aligned; a smaller one returns SSM_ERR_INVALID_ARG. seqlen == 0 writes zeros.
+ */
+SSM_API size_t ssm_scan_aggregate_workspace_bytes(int batch, int dim, int seqlen, int dstate, ssm_dtype io);
+SSM_API ssm_status ssm_selective_scan_aggregate(const void* x, const void* delta, const float* A, const void* B,
+                                                const float* delta_bias, int delta_softplus, const float* conv_w,
+                                                const float* conv_b, int d_conv, const void* conv_init, float* S_out,
+                                                float* h_out, int batch, int dim, int seqlen, int dstate,
+                                                ssm_dtype io, void* workspace, size_t workspace_bytes,
+                                                unsigned int flags, void* stream);
+
+/*
+ * Composition of segment aggregates: h_out = the state after nseg segments that start from
+ * h0, i.e. h = exp(A S_j) h + b_j for j = 0 .. nseg-1 with h = h0 (zeros when h0 is NULL).
+ *   S  [nseg, batch, dim] float32, b [nseg, batch, dim, dstate] float32 (from
+ *   ssm_selective_scan_aggregate, segment after segment); A [dim, dstate]; h0 and h_out
+ *   [batch, dim, dstate] float32 (h_out may alias h0). nseg == 0 copies h0 (or writes zeros).
+ */
+SSM_API ssm_status ssm_scan_compose(const float* S, const float* b, const float* A, const float* h0, float* h_out,
+                                    int nseg, int batch, int dim, int dstate, void* stream);
+
+/*
  * Size in bytes of the fixed device array that ssm_selective_scan_fwd_noalloc uses as its
  * chunk-carry scratch. Every GPU that loads the library holds this much memory until exit.
  */

@@ -14,8 +14,10 @@ from .ssm import (  # noqa: F401
     ssm_causal_conv1d_bwd,
     ssm_causal_conv1d_fwd,
     ssm_scan_bwd_workspace_bytes,
+    ssm_scan_compose,
     ssm_scan_default_chunk_len,
     ssm_scan_workspace_bytes,
+    ssm_selective_scan_aggregate,
     ssm_selective_scan_bwd,
     ssm_selective_scan_fwd,
     ssm_selective_state_update,
@@ -34,6 +36,8 @@ __all__ = [
     "ssm_scan_bwd_workspace_bytes",
     "ssm_scan_default_chunk_len",
     "ssm_scan_workspace_bytes",
+    "ssm_selective_scan_aggregate",
+    "ssm_scan_compose",
     "ssm_ssd_fwd",
     "ssm_ssd_workspace_bytes",
     "version",

@@ -77,11 +77,14 @@ ScanPlan default_plan(int batch, int dim, int seqlen, int dstate, bool bf16) {
   return {lanes, (int)(cl > kLongChunk ? kLongChunk : cl)};
 }
 
-// Lanes per channel for a given chunking: chunked problems and problems whose channels alone
-// give one warp per SMSP at one lane per channel take one lane; the rest take two (N <= 16).
+// Lanes per channel for a given chunking (N <= 16): whole channels per lane when the chunks'
+// whole-channel CTAs are at least one per SM (chunked problems and problems with many
+// channels), two lanes per channel otherwise: a tiny problem (say 64 channels, 256 steps) is
+// bound by the serial work per lane, which two lanes of 8 states halve (20 against 30 us).
 int lanes_for(int batch, int dim, int nchunks, int dstate) {
   if (dstate > 16) return 4;
-  if (nchunks > 1 || scan_ctas(batch, dim, 1) >= 4LL * sm_count()) return 1;
+  const long long w1 = scan_ctas(batch, dim, 1) * nchunks;
+  if ((nchunks > 1 && w1 >= sm_count()) || w1 >= 4LL * sm_count()) return 1;
   return 2;
 }
 
@@ -230,6 +233,97 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
   ssm::scan_workspace_split(workspace, (long long)batch * dim, nchunks, &a.ws_S, &a.ws_h);
   return ssm::launch_scan(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// Chunking of a segment aggregate: as many chunks as one wave of carry CTAs holds, in
+// multiples of kChunkQuantum, at most kLongChunk steps each.
+int aggregate_chunk_len(int batch, int dim, int seqlen, int dstate, bool bf16) {
+  const int cpc = ssm::scan_carry_channels_per_cta(dstate);
+  const long long ctas = ((dim + cpc - 1) / cpc) * (long long)batch;
+  const long long resident = (long long)sm_count() * ssm::scan_carry_resident_ctas_per_sm(bf16, dstate);
+  long long q = ctas > 0 ? resident / ctas : 1;
+  const long long qmax = (seqlen + kChunkQuantum - 1) / kChunkQuantum;
+  if (q > qmax) q = qmax;
+  if (q < 1) q = 1;
+  const long long cl = round_up((seqlen + q - 1) / q, kChunkQuantum);
+  return (int)(cl > kLongChunk ? kLongChunk : cl);
+}
+
+size_t ssm_scan_aggregate_workspace_bytes(int batch, int dim, int seqlen, int dstate, ssm_dtype io) {
+  if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate < 1) return 0;
+  const int cl = aggregate_chunk_len(batch, dim, seqlen, dstate, io == SSM_BF16);
+  return ssm::scan_workspace_bytes((long long)batch * dim, nchunks_for(seqlen, cl) + 1, dstate);
+}
+
+ssm_status ssm_selective_scan_aggregate(const void* x, const void* delta, const float* A, const void* B,
+                                        const float* delta_bias, int delta_softplus, const float* conv_w,
+                                        const float* conv_b, int d_conv, const void* conv_init, float* S_out,
+                                        float* h_out, int batch, int dim, int seqlen, int dstate, ssm_dtype io,
+                                        void* workspace, size_t workspace_bytes, unsigned int flags, void* stream) {
+  if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
+  if (flags & ~(SSM_SCAN_REVERSE | SSM_SCAN_ZOH)) return SSM_ERR_INVALID_ARG;
+  if (!dims_ok(batch, dim, seqlen, dstate)) return SSM_ERR_INVALID_ARG;
+  if (dstate > ssm::kMaxDstateScan) return SSM_ERR_UNSUPPORTED;
+  if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+  const bool conv = conv_w != nullptr;
+  if (conv || conv_init) {
+    if (d_conv < 1) return SSM_ERR_INVALID_ARG;
+    if (d_conv > kMaxConv) return SSM_ERR_UNSUPPORTED;
+  }
+  if (!conv && (conv_b || conv_init)) return SSM_ERR_INVALID_ARG;
+  if ((long long)batch * dim == 0) return SSM_OK;
+  if (!A || !S_out || !h_out || (seqlen > 0 && (!x || !delta || !B))) return SSM_ERR_INVALID_ARG;
+  const size_t es = io_bytes(io);
+  const void* io_ptrs[] = {x, delta, B, conv_init};
+  for (const void* p : io_ptrs)
+    if (p && !aligned(p, es)) return SSM_ERR_UNSUPPORTED;
+  const void* f_ptrs[] = {A, delta_bias, conv_w, conv_b, S_out, h_out};
+  for (const void* p : f_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long BD = (long long)batch * dim;
+  if (seqlen == 0) {  // no tokens: nothing decays and nothing enters
+    if (cudaMemsetAsync(S_out, 0, BD * sizeof(float), st) != cudaSuccess ||
+        cudaMemsetAsync(h_out, 0, BD * dstate * sizeof(float), st) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    return SSM_OK;
+  }
+  const int cl = aggregate_chunk_len(batch, dim, seqlen, dstate, io == SSM_BF16);
+  const int nchunks = nchunks_for(seqlen, cl);
+  if (nchunks > 65535) return SSM_ERR_INVALID_ARG;
+  const size_t need = ssm::scan_workspace_bytes(BD, nchunks + 1, dstate);
+  if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return SSM_ERR_UNSUPPORTED;
+  ssm::ScanArgs a{};
+  a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = nullptr; a.D = nullptr; a.z = nullptr;
+  a.delta_bias = delta_bias; a.delta_softplus = delta_softplus; a.conv_w = conv_w; a.conv_b = conv_b;
+  a.d_conv = d_conv; a.conv_init = conv_init; a.h0 = nullptr; a.out = nullptr; a.h_last = nullptr;
+  a.conv_state_out = nullptr;
+  a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.dstate = dstate; a.bf16 = io == SSM_BF16;
+  const bool rows16 = ((long long)seqlen * (long long)es) % 16 == 0;
+  a.vec = rows16 && aligned(x, 16) && aligned(delta, 16) && aligned(B, 16);
+  a.chunk_len = cl;
+  a.nchunks = nchunks;
+  a.lanes = 1;
+  a.reverse = (flags & SSM_SCAN_REVERSE) ? 1 : 0;
+  a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
+  ssm::scan_workspace_split(workspace, BD, nchunks + 1, &a.ws_S, &a.ws_h);
+  return ssm::launch_scan_aggregate(a, S_out, h_out, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_scan_compose(const float* S, const float* b, const float* A, const float* h0, float* h_out, int nseg,
+                            int batch, int dim, int dstate, void* stream) {
+  if (nseg < 0 || batch < 0 || dim < 0 || dstate < 1) return SSM_ERR_INVALID_ARG;
+  if (dstate > ssm::kMaxDstateScan) return SSM_ERR_UNSUPPORTED;
+  if ((long long)batch * dim == 0) return SSM_OK;
+  if (!A || !h_out || (nseg > 0 && (!S || !b))) return SSM_ERR_INVALID_ARG;
+  const void* f_ptrs[] = {S, b, A, h0, h_out};
+  for (const void* p : f_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_UNSUPPORTED;
+  return ssm::launch_scan_compose(S, b, A, h0, h_out, nseg, batch, dim, dstate, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SSM_OK
+             : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_selective_state_update(float* state, void* conv_state, const void* x, const void* delta,

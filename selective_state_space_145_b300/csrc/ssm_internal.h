@@ -163,6 +163,16 @@ void scan_workspace_split(void* ws, long long channels, int nchunks, float** S, 
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
 
+// Segment aggregates (sequence-parallel scans): the carry kernel over all of the segment's
+// chunks, then a fold into S_out [batch*dim] (sum of Delta) and h_out [batch*dim, dstate] (end
+// state from zero). The workspace holds a.nchunks carries (scan_workspace_bytes(channels,
+// a.nchunks + 1, dstate) bytes, split with scan_workspace_split the same way).
+cudaError_t launch_scan_aggregate(const ScanArgs& a, float* S_out, float* h_out, cudaStream_t stream);
+cudaError_t launch_scan_compose(const float* S, const float* b, const float* A, const float* h0, float* h_out,
+                                int nseg, int batch, int dim, int dstate, cudaStream_t stream);
+int scan_carry_resident_ctas_per_sm(bool bf16, int dstate);
+int scan_carry_channels_per_cta(int dstate);
+
 // State-space-duality layer: chunk length, workspace layout and launch.
 int ssd_chunk_len();
 size_t ssd_workspace_bytes(int batch, int nheads, int nchunks);

@@ -942,7 +942,7 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
 // ---------------------------------------------------------------- carry pass
 
 template <typename T, int G, int K, bool CONV, bool VEC, bool REV, bool ZOH>
-__global__ void __launch_bounds__(32, 8) scan_carry_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(32, 16) scan_carry_kernel(const ScanArgs a) {
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   using Geo = CarryGeo<G, K>;
   using Lay = CarryLayout<T, G, K>;
@@ -1134,11 +1134,11 @@ cudaError_t launch_main(const ScanArgs& a, cudaStream_t stream) {
 }
 
 template <typename T, int G, int K, bool CONV, bool VEC, bool REV, bool ZOH>
-cudaError_t launch_carry(const ScanArgs& a, cudaStream_t stream) {
+cudaError_t launch_carry(const ScanArgs& a, cudaStream_t stream, int ncarry) {
   cudaError_t err = prepare_carry<T, G, K, CONV, VEC, REV, ZOH>();
   if (err != cudaSuccess) return err;
   constexpr int cpw = CarryGeo<G, K>::kCPW;
-  const dim3 grid((a.dim + cpw - 1) / cpw, a.batch, a.nchunks - 1);
+  const dim3 grid((a.dim + cpw - 1) / cpw, a.batch, ncarry);
   scan_carry_kernel<T, G, K, CONV, VEC, REV, ZOH><<<grid, 32, CarryLayout<T, G, K>::bytes, stream>>>(a);
   return cudaGetLastError();
 }
@@ -1165,8 +1165,8 @@ template <typename T, bool CONV, bool VEC, bool REV, bool ZOH>
 cudaError_t launch_pair(const ScanArgs& a, cudaStream_t stream) {
   const bool big = a.dstate > 16;
   if (a.nchunks > 1) {
-    cudaError_t err = big ? launch_carry<T, 2, 1, CONV, VEC, REV, ZOH>(a, stream)
-                          : launch_carry<T, 1, 1, CONV, VEC, REV, ZOH>(a, stream);
+    cudaError_t err = big ? launch_carry<T, 2, 1, CONV, VEC, REV, ZOH>(a, stream, a.nchunks - 1)
+                          : launch_carry<T, 1, 1, CONV, VEC, REV, ZOH>(a, stream, a.nchunks - 1);
     if (err != cudaSuccess) return err;
   }
   // The main pass follows the carry pass in stream order. Launched as its programmatic
@@ -1219,7 +1219,121 @@ int resident_main1_ctas() {
   return n;
 }
 
+// ---------------------------------------------------------------- segment aggregates
+
+// Folds the carries of a segment's q chunks into the segment's aggregate: S = sum_j S_j (log2
+// units in, natural units out) and h = 2^(A S_j) h + h_j over j = 0 .. q-1 from h = 0, the
+// segment's end state from a zero state. One thread per (channel, state).
+__global__ void aggregate_fold_kernel(const float* __restrict__ S, const float* __restrict__ hs,
+                                      const float* __restrict__ A, float* __restrict__ S_out,
+                                      float* __restrict__ h_out, long long BD, int dim, int N, int NS, int nq) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= BD * N) return;
+  const long long cc = i / N;
+  const int n = (int)(i % N);
+  const int d = (int)(cc % dim);
+  const float a = A[(long long)d * N + n];
+  float sum = 0.f, h = 0.f;
+  for (int j = 0; j < nq; ++j) {
+    const float sj = S[(long long)j * BD + cc];
+    h = fmaf(ex2_approx(a * sj), h, hs[((long long)j * BD + cc) * NS + n]);
+    sum += sj;
+  }
+  h_out[cc * N + n] = h;
+  if (n == 0) S_out[cc] = sum * kLn2;
+}
+
+// Composition of segment aggregates onto an initial state: h = exp(A S_j) h + b_j for
+// j = 0 .. nseg-1 (S in natural units). One thread per (channel, state).
+__global__ void compose_kernel(const float* __restrict__ S, const float* __restrict__ b, const float* __restrict__ A,
+                               const float* __restrict__ h0, float* __restrict__ h_out, long long BD, int dim, int N,
+                               int nseg) {
+  const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (i >= BD * N) return;
+  const long long cc = i / N;
+  const int n = (int)(i % N);
+  const int d = (int)(cc % dim);
+  const float a = A[(long long)d * N + n] * kLog2e;
+  float h = h0 ? h0[cc * N + n] : 0.f;
+  for (int j = 0; j < nseg; ++j)
+    h = fmaf(ex2_approx(a * S[(long long)j * BD + cc]), h, b[((long long)j * BD + cc) * N + n]);
+  h_out[cc * N + n] = h;
+}
+
+template <typename T, bool CONV, bool VEC, bool REV, bool ZOH>
+cudaError_t launch_aggregate_t(const ScanArgs& a, float* S_out, float* h_out, cudaStream_t stream) {
+  // every chunk of the segment, the last one included, goes through the carry kernel
+  const bool big = a.dstate > 16;
+  cudaError_t err = big ? launch_carry<T, 2, 1, CONV, VEC, REV, ZOH>(a, stream, a.nchunks)
+                        : launch_carry<T, 1, 1, CONV, VEC, REV, ZOH>(a, stream, a.nchunks);
+  if (err != cudaSuccess) return err;
+  const long long BD = (long long)a.batch * a.dim;
+  const long long n = BD * a.dstate;
+  const int threads = 256;
+  aggregate_fold_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
+      a.ws_S, a.ws_h, a.A, S_out, h_out, BD, a.dim, a.dstate, scan_state_stride(a.dstate), a.nchunks);
+  return cudaGetLastError();
+}
+
+template <typename T, bool REV, bool ZOH>
+cudaError_t aggregate_opts(const ScanArgs& a, float* S_out, float* h_out, cudaStream_t s) {
+  const bool conv = a.conv_w != nullptr;
+  if (conv)
+    return a.vec ? launch_aggregate_t<T, true, true, REV, ZOH>(a, S_out, h_out, s)
+                 : launch_aggregate_t<T, true, false, REV, ZOH>(a, S_out, h_out, s);
+  return a.vec ? launch_aggregate_t<T, false, true, REV, ZOH>(a, S_out, h_out, s)
+               : launch_aggregate_t<T, false, false, REV, ZOH>(a, S_out, h_out, s);
+}
+
+template <typename T>
+cudaError_t aggregate_dispatch(const ScanArgs& a, float* S_out, float* h_out, cudaStream_t s) {
+  if (a.zoh)
+    return a.reverse ? aggregate_opts<T, true, true>(a, S_out, h_out, s) : aggregate_opts<T, false, true>(a, S_out, h_out, s);
+  return a.reverse ? aggregate_opts<T, true, false>(a, S_out, h_out, s) : aggregate_opts<T, false, false>(a, S_out, h_out, s);
+}
+
 }  // namespace
+
+int scan_carry_resident_ctas_per_sm(bool bf16, int dstate) {
+  int n = 0;
+  cudaError_t e;
+  if (dstate > 16)
+    e = bf16 ? (prepare_carry<__nv_bfloat16, 2, 1, false, true, false, false>(),
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_carry_kernel<__nv_bfloat16, 2, 1, false, true, false, false>,
+                                                              32, CarryLayout<__nv_bfloat16, 2, 1>::bytes))
+             : (prepare_carry<float, 2, 1, false, true, false, false>(),
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_carry_kernel<float, 2, 1, false, true, false, false>, 32,
+                                                              CarryLayout<float, 2, 1>::bytes));
+  else
+    e = bf16 ? (prepare_carry<__nv_bfloat16, 1, 1, false, true, false, false>(),
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_carry_kernel<__nv_bfloat16, 1, 1, false, true, false, false>,
+                                                              32, CarryLayout<__nv_bfloat16, 1, 1>::bytes))
+             : (prepare_carry<float, 1, 1, false, true, false, false>(),
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_carry_kernel<float, 1, 1, false, true, false, false>, 32,
+                                                              CarryLayout<float, 1, 1>::bytes));
+  if (e != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 16;  // no device to ask: the register limit the kernel is built for
+  }
+  return n;
+}
+
+int scan_carry_channels_per_cta(int dstate) { return dstate > 16 ? CarryGeo<2, 1>::kCPW : CarryGeo<1, 1>::kCPW; }
+
+cudaError_t launch_scan_aggregate(const ScanArgs& a, float* S_out, float* h_out, cudaStream_t stream) {
+  if (a.bf16) return aggregate_dispatch<__nv_bfloat16>(a, S_out, h_out, stream);
+  return aggregate_dispatch<float>(a, S_out, h_out, stream);
+}
+
+cudaError_t launch_scan_compose(const float* S, const float* b, const float* A, const float* h0, float* h_out,
+                                int nseg, int batch, int dim, int dstate, cudaStream_t stream) {
+  const long long BD = (long long)batch * dim;
+  const long long n = BD * dstate;
+  const int threads = 256;
+  compose_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(S, b, A, h0, h_out, BD, dim, dstate,
+                                                                                   nseg);
+  return cudaGetLastError();
+}
 
 int scan_channels_per_cta(int lanes) {
   return lanes == 1 ? Main1Layout<float, kMain1K>::kCPW : (lanes == 2 ? MainGeo<2>::kCPW : MainGeo<4>::kCPW);
@@ -1256,10 +1370,10 @@ cudaError_t launch_scan_carry(const ScanArgs& a, cudaStream_t stream) {
   // the forward carries alone (chunks 0 .. nchunks-2), forward time, Euler, no conv, N <= 16
   if (a.nchunks <= 1) return cudaSuccess;
   if (a.bf16)
-    return a.vec ? launch_carry<__nv_bfloat16, 1, 1, false, true, false, false>(a, stream)
-                 : launch_carry<__nv_bfloat16, 1, 1, false, false, false, false>(a, stream);
-  return a.vec ? launch_carry<float, 1, 1, false, true, false, false>(a, stream)
-               : launch_carry<float, 1, 1, false, false, false, false>(a, stream);
+    return a.vec ? launch_carry<__nv_bfloat16, 1, 1, false, true, false, false>(a, stream, a.nchunks - 1)
+                 : launch_carry<__nv_bfloat16, 1, 1, false, false, false, false>(a, stream, a.nchunks - 1);
+  return a.vec ? launch_carry<float, 1, 1, false, true, false, false>(a, stream, a.nchunks - 1)
+               : launch_carry<float, 1, 1, false, false, false, false>(a, stream, a.nchunks - 1);
 }
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {

@@ -30,7 +30,8 @@ EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_sca
            "ssm_scan_workspace_bytes", "ssm_selective_scan_fwd", "ssm_selective_state_update",
            "ssm_selective_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_selective_scan_bwd",
            "ssm_conv_bwd_workspace_bytes", "ssm_causal_conv1d_bwd", "ssm_ssd_workspace_bytes", "ssm_ssd_fwd",
-           "ssm_set_test_hooks")
+           "ssm_set_test_hooks", "ssm_scan_aggregate_workspace_bytes", "ssm_selective_scan_aggregate",
+           "ssm_scan_compose")
 
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -88,6 +89,13 @@ def lib() -> ctypes.CDLL:
         L.ssm_ssd_workspace_bytes.argtypes = [i] * 6
         L.ssm_ssd_fwd.restype = i
         L.ssm_ssd_fwd.argtypes = [vp, vp, fp, vp, vp, fp, fp, i, fp, vp, fp] + [i] * 6 + [vp, sz, vp]
+        L.ssm_scan_aggregate_workspace_bytes.restype = sz
+        L.ssm_scan_aggregate_workspace_bytes.argtypes = [i] * 5
+        L.ssm_selective_scan_aggregate.restype = i
+        L.ssm_selective_scan_aggregate.argtypes = ([vp, vp, fp, vp, fp, i, fp, fp, i, vp, fp, fp] + [i] * 5
+                                                   + [vp, sz, u, vp])
+        L.ssm_scan_compose.restype = i
+        L.ssm_scan_compose.argtypes = [fp, fp, fp, fp, fp, i, i, i, i, vp]
         L.ssm_selective_state_update.restype = i
         L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
                                                  i, i, i, i, u, vp]
@@ -260,6 +268,54 @@ def ssm_selective_scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor
     if return_conv_state:
         res = res + (conv_state_out,)
     return res
+
+
+def ssm_selective_scan_aggregate(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                                 delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+                                 conv_w: Optional[torch.Tensor] = None, conv_b: Optional[torch.Tensor] = None,
+                                 conv_init: Optional[torch.Tensor] = None, reverse: bool = False,
+                                 zoh: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Aggregate of one sequence segment: (S [batch, dim], h [batch, dim, dstate]), the sum of
+    Delta over the segment and the state at its end from a zero state (include/ssm.h)."""
+    batch, dim, L = x.shape
+    N = A.shape[1]
+    dev, io = x.device, x.dtype
+    K = conv_w.shape[1] if conv_w is not None else 0
+    _need(x, "x", (batch, dim, L), io, dev)
+    _need(delta, "delta", (batch, dim, L), io, dev)
+    _need(A, "A", (dim, N), torch.float32, dev)
+    _need(B, "B", (batch, N, L), io, dev)
+    _need(delta_bias, "delta_bias", (dim,), torch.float32, dev, optional=True)
+    if conv_w is not None:
+        _need(conv_w, "conv_w", (dim, K), torch.float32, dev)
+    _need(conv_b, "conv_b", (dim,), torch.float32, dev, optional=True)
+    _need(conv_init, "conv_init", (batch, dim, K - 1), io, dev, optional=True)
+    S = torch.empty(batch, dim, dtype=torch.float32, device=dev)
+    h = torch.empty(batch, dim, N, dtype=torch.float32, device=dev)
+    need = int(lib().ssm_scan_aggregate_workspace_bytes(batch, dim, L, N, _io_code(x)))
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib().ssm_selective_scan_aggregate(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(conv_w),
+        _ptr(conv_b), K, _ptr(conv_init), _ptr(S), _ptr(h), batch, dim, L, N, _io_code(x), _ptr(ws), need,
+        (SCAN_REVERSE if reverse else 0) | (SCAN_ZOH if zoh else 0), _stream(dev))
+    _check("ssm_selective_scan_aggregate", st)
+    return S, h
+
+
+def ssm_scan_compose(S: torch.Tensor, b: torch.Tensor, A: torch.Tensor,
+                     h0: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The state after segments with aggregates S [nseg, batch, dim], b [nseg, batch, dim, dstate]
+    (in order), starting from h0 [batch, dim, dstate] (zeros when None)."""
+    nseg, batch, dim = S.shape
+    N = A.shape[1]
+    dev = A.device
+    _need(S, "S", (nseg, batch, dim), torch.float32, dev)
+    _need(b, "b", (nseg, batch, dim, N), torch.float32, dev)
+    _need(h0, "h0", (batch, dim, N), torch.float32, dev, optional=True)
+    h = torch.empty(batch, dim, N, dtype=torch.float32, device=dev)
+    _check("ssm_scan_compose", lib().ssm_scan_compose(_ptr(S), _ptr(b), _ptr(A), _ptr(h0), _ptr(h), nseg, batch, dim,
+                                                      N, _stream(dev)))
+    return h
 
 
 def ssm_ssd_workspace_bytes(batch: int, seqlen: int, nheads: int, headdim: int, dstate: int, io) -> int:
