@@ -386,6 +386,25 @@ SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, co
                                float* h_last, int batch, int seqlen, int nheads, int headdim, int dstate,
                                ssm_dtype io, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Range checks of the debug build.
+ *
+ * libssm_debug.so is this library compiled with SSM_DEBUG_BOUNDS: before each global-memory
+ * access of the scan (main, carry, segment aggregate and composition), decode and conv
+ * kernels, the element range it touches is tested against the size of its tensor, as the
+ * call's arguments give them. An access outside its tensor is skipped (a load reads zero) and
+ * sets a bit of a device error word; nothing traps. Bits: 1 scan, 2 decode, 4 conv, 8 segment
+ * aggregate / composition.
+ *
+ * ssm_debug_bounds_status synchronises the device (a blocking copy from the word), stores the
+ * word's bits in *flags_out and, when clear is 1, resets them to zero. It returns
+ * SSM_ERR_UNSUPPORTED from the release library (libssm.so), which has no checks compiled in,
+ * SSM_ERR_INVALID_ARG for a NULL flags_out or a clear other than 0 or 1, and SSM_ERR_CUDA if
+ * the copy fails. A zero word after a call means that every checked access of it lay inside
+ * its tensor.
+ */
+SSM_API ssm_status ssm_debug_bounds_status(unsigned int* flags_out, int clear);
+
 #ifdef __cplusplus
 }
 #endif

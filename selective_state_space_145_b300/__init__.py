@@ -7,10 +7,14 @@ The binding loads the library on first use and raises if it is missing.
 """
 
 from .ssm import (  # noqa: F401
+    DEBUG_LIB_PATH,
     EXPORTS,
     LIB_PATH,
     SSMError,
+    debug_bounds_status,
     lib,
+    library_path,
+    select_library,
     ssm_causal_conv1d_bwd,
     ssm_causal_conv1d_fwd,
     ssm_scan_bwd_workspace_bytes,
@@ -42,5 +46,8 @@ __all__ = [
     "ssm_ssd_workspace_bytes",
     "version",
     "status_string",
+    "select_library",
+    "library_path",
+    "debug_bounds_status",
     "SSMError",
 ]

@@ -3,6 +3,10 @@
 Every .cu file under csrc/ is compiled to an object in _build/ (in parallel) and the
 objects are linked into selective_state_space_145_b300/libssm.so. A rebuild happens when
 any source or header is newer than the library.
+
+The debug variant, libssm_debug.so (objects in _build/debug/), is the same sources compiled
+with SSM_DEBUG_BOUNDS: every checked global access is range-tested against its tensor and a
+violation sets a device error word (ssm_debug_bounds_status) instead of touching memory.
 """
 
 from __future__ import annotations
@@ -19,6 +23,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libssm.so")
+DEBUG_LIB = os.path.join(HERE, "libssm_debug.so")
+VARIANTS = {"release": (LIB, BUILD, []), "debug": (DEBUG_LIB, os.path.join(BUILD, "debug"), ["-DSSM_DEBUG_BOUNDS"])}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -41,23 +47,26 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(variant: str = "release") -> bool:
+    lib = VARIANTS[variant][0]
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libssm.so if needed; return its path. Raises on a compiler error."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, variant: str = "release") -> str:
+    """Compile and link libssm.so (variant "release") or libssm_debug.so (variant "debug") if
+    needed; return its path. Raises on a compiler error."""
+    lib, bdir, vflags = VARIANTS[variant]
+    if not force and up_to_date(variant):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + vflags + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc] + ARCH + flags + ["-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -70,17 +79,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None,
+                variant="debug" if "--debug" in sys.argv else "release"))

@@ -228,6 +228,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
           aligned(out, 16) && (!z || aligned(z, 16));
   a.chunk_len = cl;
   a.nchunks = nchunks;
+  a.ws_chunks = nchunks - 1;
   a.lanes = lanes;
   a.reverse = (flags & SSM_SCAN_REVERSE) ? 1 : 0;
   a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
@@ -304,6 +305,7 @@ ssm_status ssm_selective_scan_aggregate(const void* x, const void* delta, const 
   a.vec = rows16 && aligned(x, 16) && aligned(delta, 16) && aligned(B, 16);
   a.chunk_len = cl;
   a.nchunks = nchunks;
+  a.ws_chunks = nchunks;
   a.lanes = 1;
   a.reverse = (flags & SSM_SCAN_REVERSE) ? 1 : 0;
   a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
@@ -418,7 +420,7 @@ ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float*
     f.batch = batch; f.dim = dim; f.seqlen = seqlen; f.dstate = dstate; f.bf16 = io == SSM_BF16;
     f.vec = ((long long)seqlen * (long long)es) % 16 == 0 && aligned(u, 16) && aligned(delta, 16) &&
             aligned(B, 16) && aligned(C, 16);
-    f.chunk_len = cl; f.nchunks = nchunks; f.lanes = 1; f.reverse = 0; f.zoh = 0;
+    f.chunk_len = cl; f.nchunks = nchunks; f.ws_chunks = nchunks - 1; f.lanes = 1; f.reverse = 0; f.zoh = 0;
     f.ws_S = const_cast<float*>(a.fS); f.ws_h = const_cast<float*>(a.fh);
     if (ssm::launch_scan_carry(f, st) != cudaSuccess) return SSM_ERR_CUDA;
   }
@@ -510,6 +512,18 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   a.batch = batch; a.seqlen = seqlen; a.nheads = nheads; a.nchunks = (int)nchunks;
   ssm::ssd_workspace_split(workspace, batch, nheads, (int)nchunks, a);
   return ssm::launch_ssd(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_debug_bounds_status(unsigned int* flags_out, int clear) {
+  if (!flags_out || (clear != 0 && clear != 1)) return SSM_ERR_INVALID_ARG;
+  unsigned scan = 0, decode = 0, conv = 0;
+  cudaError_t e = ssm::scan_bounds_flags(&scan, clear != 0);
+  if (e == cudaErrorNotSupported) return SSM_ERR_UNSUPPORTED;  // a release build: no checks compiled in
+  if (e == cudaSuccess) e = ssm::decode_bounds_flags(&decode, clear != 0);
+  if (e == cudaSuccess) e = ssm::conv_bounds_flags(&conv, clear != 0);
+  if (e != cudaSuccess) return SSM_ERR_CUDA;
+  *flags_out = scan | decode | conv;
+  return SSM_OK;
 }
 
 }  // extern "C"

@@ -8,6 +8,7 @@
 // Memory-bound: one thread produces 4 consecutive outputs of one row from one 4-element
 // vector load plus the previous vector (an L1/L2 hit) for the K-1 halo, so every input
 // element comes from HBM once and every output is written once.
+#include "ssm_bounds.cuh"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -28,12 +29,18 @@ __global__ void __launch_bounds__(kConvThreads) conv_kernel(const ConvArgs a) {
     const long long c = idx / nseg;
     const int t0 = (int)(idx % nseg) * 4;
     const int d = (int)(c % a.dim);
+    // debug build: the row, its taps and its window must lie inside their tensors
+    const long long tok = total / nseg * L;
+    if (!in_bounds(c * L + t0, min(4, L - t0), tok, kBoundsConv) ||
+        !in_bounds((long long)d * K, K, (long long)a.dim * K, kBoundsConv) ||
+        !in_bounds(c * (K - 1), K - 1, total / nseg * (K - 1), kBoundsConv))
+      continue;
     float w[kMaxConv] = {0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k < K; ++k) w[kMaxConv - K + k] = a.w[(long long)d * K + k];
     const float cb = a.bias ? a.bias[d] : 0.f;
     const T* row = x + c * L;
     float win[7];  // x[t0-3 .. t0+3]
-    if (VEC) {
+    if (VEC && in_bounds(c * L + t0, 4, tok, kBoundsConv)) {
       float cur[4];
       load4(row + t0, cur);
 #pragma unroll
@@ -72,7 +79,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_kernel(const ConvArgs a) {
       acc = fmaf(w[3], win[j + 3], acc);
       o[j] = a.apply_silu ? silu_f(acc) : acc;
     }
-    if (VEC) {
+    if (VEC && in_bounds(c * L + t0, 4, tok, kBoundsConv)) {
       store4(out + c * L + t0, o);
     } else {
 #pragma unroll
@@ -97,6 +104,16 @@ cudaError_t launch_t(const ConvArgs& a, cudaStream_t stream) {
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream) {
   if (a.bf16) return a.vec ? launch_t<__nv_bfloat16, true>(a, stream) : launch_t<__nv_bfloat16, false>(a, stream);
   return a.vec ? launch_t<float, true>(a, stream) : launch_t<float, false>(a, stream);
+}
+
+cudaError_t conv_bounds_flags(unsigned* out, bool clear) {
+#ifdef SSM_DEBUG_BOUNDS
+  return bounds_flags_read(out, clear);
+#else
+  (void)out;
+  (void)clear;
+  return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace ssm

@@ -12,6 +12,7 @@
 // The fast kernel gives one thread a whole channel (16 states) and keeps the channel's
 // parameters in registers across sequences; the general kernel (any N <= 32, any alignment)
 // gives four threads a channel. The conv width is a compile-time constant in both.
+#include "ssm_bounds.cuh"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -67,9 +68,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a)
   const int c = threadIdx.x / 4, g = threadIdx.x % 4;
   const int d = blockIdx.x * kDecCh + c;
   const long long b = blockIdx.y;
-  const bool valid = d < a.dim;
   const int N = a.dstate;
   const long long cc = b * a.dim + d;
+  const long long BD = (long long)a.batch * a.dim;
+  // in the debug build, a channel whose rows fall outside any tensor is flagged and skipped
+  const bool valid = d < a.dim && in_bounds(cc, 1, BD, kBoundsDecode) &&
+                     in_bounds(cc * N, N, BD * N, kBoundsDecode) &&
+                     in_bounds((long long)d * N, N, (long long)a.dim * N, kBoundsDecode) &&
+                     in_bounds(b * N, N, (long long)a.batch * N, kBoundsDecode) &&
+                     in_bounds(cc * K1, K1, BD * K1, kBoundsDecode) &&
+                     in_bounds((long long)d * KC, KC, (long long)a.dim * KC, kBoundsDecode);
   float h[SPT], av[SPT], bv[SPT], cv[SPT];
 #pragma unroll
   for (int j = 0; j < SPT; ++j) h[j] = av[j] = bv[j] = cv[j] = 0.f;
@@ -162,13 +170,15 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
   const int nvalid = min(kTileCh, dim - d0);
   const int d = d0 + tid;
   const bool valid = tid < nvalid;
+  const long long BD = (long long)a.batch * dim;
 
   // ---- this channel's parameters, once
   float a2[kMaxDstate];
   float bias = 0.f, Dd = 0.f, cb = 0.f, w[KC > 0 ? KC : 1];
 #pragma unroll
   for (int k = 0; k < (KC > 0 ? KC : 1); ++k) w[k] = 0.f;
-  if (valid) {
+  if (valid && in_bounds((long long)d * kMaxDstate, kMaxDstate, (long long)dim * kMaxDstate, kBoundsDecode) &&
+      in_bounds((long long)d * KC, KC, (long long)dim * KC, kBoundsDecode)) {
 #pragma unroll
     for (int i = 0; i < kMaxDstate; i += 4) {
       const float4 q = *reinterpret_cast<const float4*>(a.A + (long long)d * kMaxDstate + i);
@@ -200,7 +210,8 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
     for (int k = 0; k < 4; ++k) {
       const int e = tid + k * kTileCh;
       const int ch = e >> 2, part = e & 3;
-      const bool ok = ch < nvalid;
+      const bool ok = ch < nvalid &&
+                      in_bounds((c0 + ch) * kMaxDstate + 4 * part, 4, BD * kMaxDstate, kBoundsDecode);
       cp_async16(&S.st[slot][ch][4 * part], ok ? (const void*)(a.state + (c0 + ch) * kMaxDstate + 4 * part)
                                                 : (const void*)a.state, ok ? 16u : 0u);
     }
@@ -212,19 +223,22 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
         const T* base = arr == 0 ? gx : (arr == 1 ? gd : gz);
         T* dst = arr == 0 ? S.x[slot] : (arr == 1 ? S.dl[slot] : S.z[slot]);
         const int n = nvalid - first;
-        const unsigned bytes = (base == nullptr || n <= 0) ? 0u : (n >= EPC ? 16u : (unsigned)(n * ES));
+        unsigned bytes = (base == nullptr || n <= 0) ? 0u : (n >= EPC ? 16u : (unsigned)(n * ES));
+        if (bytes && !in_bounds(c0 + first, bytes / ES, BD, kBoundsDecode)) bytes = 0u;
         cp_async16(dst + first, bytes ? (const void*)(base + c0 + first) : (const void*)a.state, bytes);
       } else if (e < (3 + K1) * kCpa) {
         const int first = (e - 3 * kCpa) * EPC;
         const int n = nvalid * K1 - first;
-        const unsigned bytes = n <= 0 ? 0u : (n >= EPC ? 16u : (unsigned)(n * ES));
+        unsigned bytes = n <= 0 ? 0u : (n >= EPC ? 16u : (unsigned)(n * ES));
+        if (bytes && !in_bounds(c0 * K1 + first, bytes / ES, BD * K1, kBoundsDecode)) bytes = 0u;
         cp_async16(S.win[slot] + first, bytes ? (const void*)(gw + c0 * K1 + first) : (const void*)a.state, bytes);
       } else {
         const int q = e - (3 + K1) * kCpa;               // 0 .. kBC-1
         const int half = kBC / 2;
-        const T* src = q < half ? gB + (long long)b * kMaxDstate + q * EPC
-                                : gC + (long long)b * kMaxDstate + (q - half) * EPC;
-        cp_async16(S.bc[slot] + q * EPC, src, 16u);
+        const long long i = (long long)b * kMaxDstate + (q < half ? q : q - half) * EPC;
+        const bool ok = in_bounds(i, EPC, (long long)a.batch * kMaxDstate, kBoundsDecode);
+        cp_async16(S.bc[slot] + q * EPC, ok ? (const void*)((q < half ? gB : gC) + i) : (const void*)a.state,
+                   ok ? 16u : 0u);
       }
     }
   };
@@ -308,7 +322,7 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
 #pragma unroll
       for (int k = 0; k < K1; ++k) S.win[slot][tid * K1 + k] = nw[k];
     }
-    if (valid) {
+    if (valid && in_bounds(cc, 1, BD, kBoundsDecode)) {
       float y = fmaf(Dd, u, y0 + y1);
       if (gz) y *= silu_f(to_f32(S.z[slot][tid]));
       static_cast<T*>(a.y)[cc] = from_f32<T>(y);
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
       for (int k = 0; k < 4; ++k) {  // state: chunk e -> channel e / 4, quarter e % 4
         const int e = tid + k * kTileCh;
         const int ch = e >> 2, part = e & 3;
-        if (ch < nvalid)
+        if (ch < nvalid && in_bounds((c0 + ch) * kMaxDstate + 4 * part, 4, BD * kMaxDstate, kBoundsDecode))
           *reinterpret_cast<float4*>(a.state + (c0 + ch) * kMaxDstate + 4 * part) =
               *reinterpret_cast<const float4*>(&S.st[slot][ch][4 * part]);
       }
@@ -329,6 +343,7 @@ __global__ void __launch_bounds__(kTileCh) decode_tile_kernel(const DecodeArgs a
         const int nel = nvalid * K1;
         for (int e = tid; e * EPC < nel; e += kTileCh) {
           const int first = e * EPC;
+          if (!in_bounds(c0 * K1 + first, min(EPC, nel - first), BD * K1, kBoundsDecode)) continue;
           if (first + EPC <= nel) {
             *reinterpret_cast<uint4*>(cs + first) = *reinterpret_cast<const uint4*>(S.win[slot] + first);
           } else {
@@ -413,6 +428,16 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                          al(a.B, 16) && al(a.C, 16) && al(a.x, 16) && al(a.delta, 16) && al(a.z, 16) &&
                          (a.conv_w == nullptr || al(a.conv_state, 16));
   return a.bf16 ? dispatch_t<__nv_bfloat16>(a, stream_ok, stream) : dispatch_t<float>(a, stream_ok, stream);
+}
+
+cudaError_t decode_bounds_flags(unsigned* out, bool clear) {
+#ifdef SSM_DEBUG_BOUNDS
+  return bounds_flags_read(out, clear);
+#else
+  (void)out;
+  (void)clear;
+  return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace ssm

@@ -42,8 +42,9 @@ struct ScanArgs {
   int lanes;             // lanes per channel of the main pass: 1 (N <= 16), 2 (N <= 16) or 4 (N <= 32)
   int reverse;           // 1: the scan runs from t = L-1 down to t = 0
   int zoh;               // 1: zero-order-hold input term expm1(Delta A)/A B u
-  float* ws_S;           // [nchunks-1][batch*dim] sum of Delta per chunk
-  float* ws_h;           // [nchunks-1][batch*dim][scan_state_stride(dstate)] chunk end state from zero
+  int ws_chunks;         // carry entries the workspace holds (nchunks-1; nchunks for a segment aggregate)
+  float* ws_S;           // [ws_chunks][batch*dim] sum of Delta per chunk
+  float* ws_h;           // [ws_chunks][batch*dim][scan_state_stride(dstate)] chunk end state from zero
 };
 
 struct ConvArgs {
@@ -188,5 +189,11 @@ cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 size_t conv_bwd_workspace_bytes(int batch, int dim, int seqlen);
 cudaError_t launch_conv_bwd(const ConvBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Bounds-check error words of the debug build (ssm_bounds.cuh), one per translation unit;
+// cudaErrorNotSupported without SSM_DEBUG_BOUNDS.
+cudaError_t scan_bounds_flags(unsigned* out, bool clear);
+cudaError_t decode_bounds_flags(unsigned* out, bool clear);
+cudaError_t conv_bounds_flags(unsigned* out, bool clear);
 
 }  // namespace ssm

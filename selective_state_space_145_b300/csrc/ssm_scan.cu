@@ -43,6 +43,7 @@
 // The per-step state never leaves registers.
 #include <algorithm>
 
+#include "ssm_bounds.cuh"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -62,6 +63,23 @@ template <typename T, int TT>
 __host__ __device__ constexpr int row_stride() { return sizeof(T) == 2 ? TT + 8 : TT + 4; }
 
 constexpr size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+// Element counts of the tensors a scan call touches (for the debug build's range checks).
+struct Extents {
+  long long tok, bc, st, dn, win, wsS, wsH;
+};
+__device__ __forceinline__ Extents extents_of(const ScanArgs& a) {
+  const long long BD = (long long)a.batch * a.dim;
+  Extents e;
+  e.tok = BD * a.seqlen;
+  e.bc = (long long)a.batch * a.dstate * a.seqlen;
+  e.st = BD * a.dstate;
+  e.dn = (long long)a.dim * a.dstate;
+  e.win = BD * (a.d_conv > 1 ? a.d_conv - 1 : 0);
+  e.wsS = (long long)a.ws_chunks * BD;
+  e.wsH = e.wsS * (a.dstate <= 16 ? 16 : 32);
+  return e;
+}
 
 // Main-pass geometry: G lanes per channel, 8 states per lane.
 template <int G>
@@ -164,20 +182,30 @@ struct Stager {
       const int r0 = k * kRPC;           // first row of the step: fixes the array at compile time
       const T* src = nullptr;
       bool ok = tin;
+      long long idx = 0, ext = 0;  // element offset of the chunk in its tensor, and the tensor's size
       if (r0 < CPW) {
         ok = ok && d0 + (r0 % CPW) + lrow < a.dim;
-        src = static_cast<const T*>(a.x) + off_c + (long long)(r0 % CPW) * L;
+        idx = off_c + (long long)(r0 % CPW) * L;
+        src = static_cast<const T*>(a.x) + idx;
       } else if (r0 < 2 * CPW) {
         ok = ok && d0 + (r0 % CPW) + lrow < a.dim;
-        src = static_cast<const T*>(a.delta) + off_c + (long long)(r0 % CPW) * L;
+        idx = off_c + (long long)(r0 % CPW) * L;
+        src = static_cast<const T*>(a.delta) + idx;
       } else if (HAS_Z && r0 < 3 * CPW) {
         ok = ok && has_z && d0 + (r0 % CPW) + lrow < a.dim;
-        src = static_cast<const T*>(a.z) + off_c + (long long)(r0 % CPW) * L;
+        idx = off_c + (long long)(r0 % CPW) * L;
+        src = static_cast<const T*>(a.z) + idx;
       } else {
         const int rb = r0 - (HAS_Z ? 3 : 2) * CPW;
         const int n0 = rb % NR;
         ok = ok && n0 + lrow < a.dstate;
-        src = static_cast<const T*>(rb < NR ? a.B : a.C) + off_n + (long long)n0 * L;
+        idx = off_n + (long long)n0 * L;
+        src = static_cast<const T*>(rb < NR ? a.B : a.C) + idx;
+      }
+      if (ok) {
+        const Extents ex = extents_of(a);
+        ext = (r0 < (HAS_Z ? 3 : 2) * CPW) ? ex.tok : ex.bc;
+        ok = in_bounds(idx + seg, kEPC, ext, kBoundsScan);
       }
       cp_async16(&slot[r][col], ok ? (const void*)(src + seg) : a.x, ok ? 16u : 0u);
     }
@@ -196,25 +224,33 @@ struct Stager {
       const int r0 = k * kRPC;
       const T* src = nullptr;
       bool ok = true;
+      long long idx = 0;
       if (r0 < CPW) {
         ok = d0 + (r0 % CPW) + lrow < a.dim;
-        src = static_cast<const T*>(a.x) + off_c + (long long)(r0 % CPW) * L;
+        idx = off_c + (long long)(r0 % CPW) * L;
+        src = static_cast<const T*>(a.x) + idx;
       } else if (r0 < 2 * CPW) {
         ok = d0 + (r0 % CPW) + lrow < a.dim;
-        src = static_cast<const T*>(a.delta) + off_c + (long long)(r0 % CPW) * L;
+        idx = off_c + (long long)(r0 % CPW) * L;
+        src = static_cast<const T*>(a.delta) + idx;
       } else if (HAS_Z && r0 < 3 * CPW) {
         ok = has_z && d0 + (r0 % CPW) + lrow < a.dim;
-        src = static_cast<const T*>(a.z) + off_c + (long long)(r0 % CPW) * L;
+        idx = off_c + (long long)(r0 % CPW) * L;
+        src = static_cast<const T*>(a.z) + idx;
       } else {
         const int rb = r0 - (HAS_Z ? 3 : 2) * CPW;
         const int n0 = rb % NR;
         ok = n0 + lrow < a.dstate;
-        src = static_cast<const T*>(rb < NR ? a.B : a.C) + off_n + (long long)n0 * L;
+        idx = off_n + (long long)n0 * L;
+        src = static_cast<const T*>(rb < NR ? a.B : a.C) + idx;
       }
+      const Extents ex = extents_of(a);
+      const long long ext = (r0 < (HAS_Z ? 3 : 2) * CPW) ? ex.tok : ex.bc;
 #pragma unroll
       for (int e = 0; e < kEPC; ++e) {
         const bool in = REV ? col + e >= TT - tl : col + e < tl;
-        slot[r][col + e] = (ok && in) ? src[seg + e] : from_f32<T>(0.f);
+        slot[r][col + e] =
+            (ok && in && in_bounds(idx + seg + e, 1, ext, kBoundsScan)) ? src[seg + e] : from_f32<T>(0.f);
       }
     }
   }
@@ -289,10 +325,10 @@ struct ChannelParams {
 template <bool CONV>
 __device__ __forceinline__ ChannelParams channel_params(const ScanArgs& a, int d, bool valid) {
   ChannelParams p{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (valid) {
+  if (valid && in_bounds(d, 1, a.dim, kBoundsScan)) {
     p.bias = a.delta_bias ? a.delta_bias[d] : 0.f;
     p.Dd = a.D ? a.D[d] : 0.f;
-    if (CONV) {
+    if (CONV && in_bounds((long long)d * a.d_conv, a.d_conv, (long long)a.dim * a.d_conv, kBoundsScan)) {
       const int K = a.d_conv;
       const float* wp = a.conv_w + (long long)d * K;
       p.w3 = wp[K - 1];
@@ -315,8 +351,9 @@ __device__ __forceinline__ void halo_at(const ScanArgs& a, long long cc, int t_b
   if (!valid) return;
   const int K = a.d_conv, L = a.seqlen;
   const T* gx = static_cast<const T*>(a.x);
+  const Extents ex = extents_of(a);
   if (q == 0) {
-    if (a.conv_init) {
+    if (a.conv_init && in_bounds(cc * (K - 1), K - 1, ex.win, kBoundsScan)) {
       const T* ci = static_cast<const T*>(a.conv_init) + cc * (K - 1);
       if (K >= 2) hv[2] = to_f32(ci[K - 2]);
       if (K >= 3) hv[1] = to_f32(ci[K - 3]);
@@ -324,9 +361,11 @@ __device__ __forceinline__ void halo_at(const ScanArgs& a, long long cc, int t_b
     }
   } else {
     auto real_t = [&](int tau) { return REV ? L - 1 - tau : tau; };
-    hv[0] = to_f32(gx[cc * L + real_t(t_begin - 3)]);
-    hv[1] = to_f32(gx[cc * L + real_t(t_begin - 2)]);
-    hv[2] = to_f32(gx[cc * L + real_t(t_begin - 1)]);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const long long i = cc * L + real_t(t_begin - 3 + j);
+      if (in_bounds(i, 1, ex.tok, kBoundsScan)) hv[j] = to_f32(gx[i]);
+    }
   }
 }
 
@@ -334,6 +373,7 @@ __device__ __forceinline__ void halo_at(const ScanArgs& a, long long cc, int t_b
 
 template <typename T, int G, bool CONV, bool VEC, bool REV, bool ZOH>
 __global__ void __launch_bounds__(32) scan_main_kernel(const ScanArgs a) {
+  const Extents ex = extents_of(a);  // tensor sizes for the range checks of the debug build
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   using Geo = MainGeo<G>;
   using Lay = MainLayout<T, G>;
@@ -393,8 +433,9 @@ __global__ void __launch_bounds__(32) scan_main_kernel(const ScanArgs a) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int n0 = 8 * g + 2 * k;
-    av[k] = make_float2((valid && n0 < N) ? a.A[(long long)d * N + n0] : 0.f,
-                        (valid && n0 + 1 < N) ? a.A[(long long)d * N + n0 + 1] : 0.f);
+    const bool arow = valid && in_bounds((long long)d * N, N, ex.dn, kBoundsScan);
+    av[k] = make_float2((arow && n0 < N) ? a.A[(long long)d * N + n0] : 0.f,
+                        (arow && n0 + 1 < N) ? a.A[(long long)d * N + n0 + 1] : 0.f);
     h[k] = make_float2(0.f, 0.f);
     ia[k] = make_float2(0.f, 0.f);
     if (ZOH) {
@@ -403,7 +444,7 @@ __global__ void __launch_bounds__(32) scan_main_kernel(const ScanArgs a) {
     }
   }
   if (valid) {
-    if (a.h0) {
+    if (a.h0 && in_bounds(cc * N, N, ex.st, kBoundsScan)) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int n0 = 8 * g + 2 * k;
@@ -417,8 +458,9 @@ __global__ void __launch_bounds__(32) scan_main_kernel(const ScanArgs a) {
       float4 hb[2][2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const bool in = j0 + k < q;
-        const long long e = (long long)(in ? j0 + k : 0) * BD + cc;
+        const long long e = (long long)(j0 + k < q ? j0 + k : 0) * BD + cc;
+        const bool in = j0 + k < q && in_bounds(e, 1, ex.wsS, kBoundsScan) &&
+                        in_bounds(e * NS + 8 * g, 8, ex.wsH, kBoundsScan);
         Sj[k] = in ? a.ws_S[e] : 0.f;
         const float4* hp = reinterpret_cast<const float4*>(a.ws_h + e * NS + 8 * g);
         hb[k][0] = in ? hp[0] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -599,26 +641,29 @@ __global__ void __launch_bounds__(32) scan_main_kernel(const ScanArgs a) {
             float r[kBlk];
 #pragma unroll
             for (int j = 0; j < kBlk; ++j) r[j] = o[kBlk - 1 - j];
-            store8(orow + (L - t0 - tt - kBlk), r);
+            if (ptr_in(static_cast<T*>(a.out), orow + (L - t0 - tt - kBlk), kBlk, ex.tok, kBoundsScan))
+              store8(orow + (L - t0 - tt - kBlk), r);
           } else if (VEC && tt + 4 <= tl) {  // fp32 rows can end on a 4-step boundary
             const float r4[4] = {o[3], o[2], o[1], o[0]};
-            store4(orow + (L - t0 - tt - 4), r4);
+            if (ptr_in(static_cast<T*>(a.out), orow + (L - t0 - tt - 4), 4, ex.tok, kBoundsScan))
+              store4(orow + (L - t0 - tt - 4), r4);
           } else {
 #pragma unroll
             for (int j = 0; j < kBlk; ++j)
-              if (tt + j < tl) orow[L - 1 - (t0 + tt + j)] = from_f32<T>(o[j]);
+              if (tt + j < tl && ptr_in(static_cast<T*>(a.out), orow + (L - 1 - (t0 + tt + j)), 1, ex.tok, kBoundsScan))
+                orow[L - 1 - (t0 + tt + j)] = from_f32<T>(o[j]);
           }
         } else {
           T* dst = orow + t0 + tt;
           if (VEC && tt + kBlk <= tl) {
-            store8(dst, o);
+            if (ptr_in(static_cast<T*>(a.out), dst, kBlk, ex.tok, kBoundsScan)) store8(dst, o);
           } else if (VEC && tt + 4 <= tl) {  // fp32 rows can end on a 4-step boundary
             const float o4[4] = {o[0], o[1], o[2], o[3]};
-            store4(dst, o4);
+            if (ptr_in(static_cast<T*>(a.out), dst, 4, ex.tok, kBoundsScan)) store4(dst, o4);
           } else {
 #pragma unroll
             for (int j = 0; j < kBlk; ++j)
-              if (tt + j < tl) dst[j] = from_f32<T>(o[j]);
+              if (tt + j < tl && ptr_in(static_cast<T*>(a.out), dst + j, 1, ex.tok, kBoundsScan)) dst[j] = from_f32<T>(o[j]);
           }
         }
       }
@@ -627,7 +672,7 @@ __global__ void __launch_bounds__(32) scan_main_kernel(const ScanArgs a) {
 
   // ---- chunk results
   if (valid && q == a.nchunks - 1) {
-    if (a.h_last) {
+    if (a.h_last && in_bounds(cc * N, N, ex.st, kBoundsScan)) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int n0 = 8 * g + 2 * k;
@@ -641,10 +686,14 @@ __global__ void __launch_bounds__(32) scan_main_kernel(const ScanArgs a) {
       const int K1 = a.d_conv - 1;
       for (int j = g; j < K1; j += G) {
         const int s = L - K1 + j;
-        T v;
-        if (s >= 0) v = gx[cc * L + (REV ? L - 1 - s : s)];
-        else v = a.conv_init ? static_cast<const T*>(a.conv_init)[cc * K1 + (K1 + s)] : from_f32<T>(0.f);
-        static_cast<T*>(a.conv_state_out)[cc * K1 + j] = v;
+        T v = from_f32<T>(0.f);
+        if (s >= 0) {
+          const long long i = cc * L + (REV ? L - 1 - s : s);
+          if (in_bounds(i, 1, ex.tok, kBoundsScan)) v = gx[i];
+        } else if (a.conv_init && in_bounds(cc * K1 + (K1 + s), 1, ex.win, kBoundsScan)) {
+          v = static_cast<const T*>(a.conv_init)[cc * K1 + (K1 + s)];
+        }
+        if (in_bounds(cc * K1 + j, 1, ex.win, kBoundsScan)) static_cast<T*>(a.conv_state_out)[cc * K1 + j] = v;
       }
     }
   }
@@ -678,6 +727,7 @@ struct Main1Layout {
 // per lane, which matters because broadcast shared loads contend with the exp2 and FMA work.
 template <typename T, int K, bool CONV, bool VEC, bool REV, bool ZOH>
 __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
+  const Extents ex = extents_of(a);  // tensor sizes for the range checks of the debug build
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   using Lay = Main1Layout<T, K>;
   constexpr int CPW = Lay::kCPW;
@@ -725,8 +775,9 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int n0 = 2 * k;
-      av[kc][k] = make_float2((valid[kc] && n0 < N) ? a.A[(long long)d * N + n0] : 0.f,
-                              (valid[kc] && n0 + 1 < N) ? a.A[(long long)d * N + n0 + 1] : 0.f);
+      const bool arow = valid[kc] && in_bounds((long long)d * N, N, ex.dn, kBoundsScan);
+      av[kc][k] = make_float2((arow && n0 < N) ? a.A[(long long)d * N + n0] : 0.f,
+                              (arow && n0 + 1 < N) ? a.A[(long long)d * N + n0 + 1] : 0.f);
       h[kc][k] = make_float2(0.f, 0.f);
       ia[kc][k] = make_float2(0.f, 0.f);
       if (ZOH) {
@@ -734,7 +785,7 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
         ia[kc][k] = make_float2(inv(av[kc][k].x), inv(av[kc][k].y));
       }
     }
-    if (valid[kc] && a.h0) {
+    if (valid[kc] && a.h0 && in_bounds(cc[kc] * N, N, ex.st, kBoundsScan)) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int n0 = 2 * k;
@@ -750,6 +801,7 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
       if (!valid[kc]) continue;
       for (int j = 0; j < q; ++j) {
         const long long e = (long long)j * BD + cc[kc];
+        if (!in_bounds(e, 1, ex.wsS, kBoundsScan) || !in_bounds(e * 16, 16, ex.wsH, kBoundsScan)) continue;
         const float Sj = a.ws_S[e];
         const float4* hp = reinterpret_cast<const float4*>(a.ws_h + e * 16);
         float4 hb[4];
@@ -884,26 +936,29 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
             float r[kBlk];
 #pragma unroll
             for (int j = 0; j < kBlk; ++j) r[j] = o[kBlk - 1 - j];
-            store8(orow + (L - t0 - tt - kBlk), r);
+            if (ptr_in(static_cast<T*>(a.out), orow + (L - t0 - tt - kBlk), kBlk, ex.tok, kBoundsScan))
+              store8(orow + (L - t0 - tt - kBlk), r);
           } else if (VEC && tt + 4 <= tl) {  // fp32 rows can end on a 4-step boundary
             const float r4[4] = {o[3], o[2], o[1], o[0]};
-            store4(orow + (L - t0 - tt - 4), r4);
+            if (ptr_in(static_cast<T*>(a.out), orow + (L - t0 - tt - 4), 4, ex.tok, kBoundsScan))
+              store4(orow + (L - t0 - tt - 4), r4);
           } else {
 #pragma unroll
             for (int j = 0; j < kBlk; ++j)
-              if (tt + j < tl) orow[L - 1 - (t0 + tt + j)] = from_f32<T>(o[j]);
+              if (tt + j < tl && ptr_in(static_cast<T*>(a.out), orow + (L - 1 - (t0 + tt + j)), 1, ex.tok, kBoundsScan))
+                orow[L - 1 - (t0 + tt + j)] = from_f32<T>(o[j]);
           }
         } else {
           T* dst = orow + t0 + tt;
           if (VEC && full) {
-            store8(dst, o);
+            if (ptr_in(static_cast<T*>(a.out), dst, kBlk, ex.tok, kBoundsScan)) store8(dst, o);
           } else if (VEC && tt + 4 <= tl) {
             const float o4[4] = {o[0], o[1], o[2], o[3]};
-            store4(dst, o4);
+            if (ptr_in(static_cast<T*>(a.out), dst, 4, ex.tok, kBoundsScan)) store4(dst, o4);
           } else {
 #pragma unroll
             for (int j = 0; j < kBlk; ++j)
-              if (tt + j < tl) dst[j] = from_f32<T>(o[j]);
+              if (tt + j < tl && ptr_in(static_cast<T*>(a.out), dst + j, 1, ex.tok, kBoundsScan)) dst[j] = from_f32<T>(o[j]);
           }
         }
       }
@@ -915,7 +970,7 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
 #pragma unroll
     for (int kc = 0; kc < K; ++kc) {
       if (!valid[kc]) continue;
-      if (a.h_last) {
+      if (a.h_last && in_bounds(cc[kc] * N, N, ex.st, kBoundsScan)) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int n0 = 2 * k;
@@ -929,10 +984,14 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
         const int K1 = a.d_conv - 1;
         for (int j = 0; j < K1; ++j) {
           const int s = L - K1 + j;
-          T v;
-          if (s >= 0) v = gx[cc[kc] * L + (REV ? L - 1 - s : s)];
-          else v = a.conv_init ? static_cast<const T*>(a.conv_init)[cc[kc] * K1 + (K1 + s)] : from_f32<T>(0.f);
-          static_cast<T*>(a.conv_state_out)[cc[kc] * K1 + j] = v;
+          T v = from_f32<T>(0.f);
+          if (s >= 0) {
+            const long long i = cc[kc] * L + (REV ? L - 1 - s : s);
+            if (in_bounds(i, 1, ex.tok, kBoundsScan)) v = gx[i];
+          } else if (a.conv_init && in_bounds(cc[kc] * K1 + (K1 + s), 1, ex.win, kBoundsScan)) {
+            v = static_cast<const T*>(a.conv_init)[cc[kc] * K1 + (K1 + s)];
+          }
+          if (in_bounds(cc[kc] * K1 + j, 1, ex.win, kBoundsScan)) static_cast<T*>(a.conv_state_out)[cc[kc] * K1 + j] = v;
         }
       }
     }
@@ -943,6 +1002,7 @@ __global__ void __launch_bounds__(32, 8) scan_main1_kernel(const ScanArgs a) {
 
 template <typename T, int G, int K, bool CONV, bool VEC, bool REV, bool ZOH>
 __global__ void __launch_bounds__(32, 16) scan_carry_kernel(const ScanArgs a) {
+  const Extents ex = extents_of(a);  // tensor sizes for the range checks of the debug build
   constexpr bool PRECISE = IoTraits<T>::kPrecise;
   using Geo = CarryGeo<G, K>;
   using Lay = CarryLayout<T, G, K>;
@@ -994,8 +1054,9 @@ __global__ void __launch_bounds__(32, 16) scan_carry_kernel(const ScanArgs a) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int n0 = 16 * g + 2 * k;
-      av[kc][k] = make_float2((valid[kc] && n0 < N) ? a.A[(long long)d * N + n0] : 0.f,
-                              (valid[kc] && n0 + 1 < N) ? a.A[(long long)d * N + n0 + 1] : 0.f);
+      const bool arow = valid[kc] && in_bounds((long long)d * N, N, ex.dn, kBoundsScan);
+      av[kc][k] = make_float2((arow && n0 < N) ? a.A[(long long)d * N + n0] : 0.f,
+                              (arow && n0 + 1 < N) ? a.A[(long long)d * N + n0 + 1] : 0.f);
       h[kc][k] = make_float2(0.f, 0.f);
       ia[kc][k] = make_float2(0.f, 0.f);
       if (ZOH) {
@@ -1087,13 +1148,14 @@ __global__ void __launch_bounds__(32, 16) scan_carry_kernel(const ScanArgs a) {
 
 #pragma unroll
   for (int kc = 0; kc < K; ++kc) {
-    if (valid[kc]) {
+    const long long e = (long long)q * BD + cc[kc];
+    if (valid[kc] && in_bounds(e * NS + 16 * g, 16, ex.wsH, kBoundsScan) && in_bounds(e, 1, ex.wsS, kBoundsScan)) {
       // lane g's 16 states lie at 16g .. 16g+15 of the channel's stride (16 for G = 1, 32 for G = 2)
-      float4* hp = reinterpret_cast<float4*>(a.ws_h + ((long long)q * BD + cc[kc]) * NS + 16 * g);
+      float4* hp = reinterpret_cast<float4*>(a.ws_h + e * NS + 16 * g);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         hp[k] = make_float4(h[kc][2 * k].x, h[kc][2 * k].y, h[kc][2 * k + 1].x, h[kc][2 * k + 1].y);
-      if (g == 0) a.ws_S[(long long)q * BD + cc[kc]] = dsum[kc];
+      if (g == 0) a.ws_S[e] = dsum[kc];
     }
   }
 }
@@ -1232,11 +1294,15 @@ __global__ void aggregate_fold_kernel(const float* __restrict__ S, const float* 
   const long long cc = i / N;
   const int n = (int)(i % N);
   const int d = (int)(cc % dim);
+  if (!in_bounds((long long)d * N + n, 1, (long long)dim * N, kBoundsSegment)) return;
   const float a = A[(long long)d * N + n];
   float sum = 0.f, h = 0.f;
   for (int j = 0; j < nq; ++j) {
-    const float sj = S[(long long)j * BD + cc];
-    h = fmaf(ex2_approx(a * sj), h, hs[((long long)j * BD + cc) * NS + n]);
+    const long long e = (long long)j * BD + cc;
+    if (!in_bounds(e, 1, nq * BD, kBoundsSegment) || !in_bounds(e * NS + n, 1, nq * BD * NS, kBoundsSegment))
+      continue;
+    const float sj = S[e];
+    h = fmaf(ex2_approx(a * sj), h, hs[e * NS + n]);
     sum += sj;
   }
   h_out[cc * N + n] = h;
@@ -1253,10 +1319,15 @@ __global__ void compose_kernel(const float* __restrict__ S, const float* __restr
   const long long cc = i / N;
   const int n = (int)(i % N);
   const int d = (int)(cc % dim);
+  if (!in_bounds((long long)d * N + n, 1, (long long)dim * N, kBoundsSegment)) return;
   const float a = A[(long long)d * N + n] * kLog2e;
   float h = h0 ? h0[cc * N + n] : 0.f;
-  for (int j = 0; j < nseg; ++j)
-    h = fmaf(ex2_approx(a * S[(long long)j * BD + cc]), h, b[((long long)j * BD + cc) * N + n]);
+  for (int j = 0; j < nseg; ++j) {
+    const long long e = (long long)j * BD + cc;
+    if (!in_bounds(e, 1, nseg * BD, kBoundsSegment) || !in_bounds(e * N + n, 1, nseg * BD * N, kBoundsSegment))
+      continue;
+    h = fmaf(ex2_approx(a * S[e]), h, b[e * N + n]);
+  }
   h_out[cc * N + n] = h;
 }
 
@@ -1379,6 +1450,16 @@ cudaError_t launch_scan_carry(const ScanArgs& a, cudaStream_t stream) {
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
   if (a.bf16) return dispatch<__nv_bfloat16>(a, stream);
   return dispatch<float>(a, stream);
+}
+
+cudaError_t scan_bounds_flags(unsigned* out, bool clear) {
+#ifdef SSM_DEBUG_BOUNDS
+  return bounds_flags_read(out, clear);
+#else
+  (void)out;
+  (void)clear;
+  return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace ssm

@@ -5,6 +5,8 @@ the C entry point of the same name on the current torch stream with raw device p
 Every step of the computation runs in the library's kernels; nothing here computes.
 The library must have been built (``__graft_entry__.build()`` or ``python -m
 selective_state_space_145_b300.build``): a missing library raises, there is no fallback.
+``select_library("debug")`` points every call at libssm_debug.so, the range-checked build
+(``debug_bounds_status`` reads its error word).
 """
 
 from __future__ import annotations
@@ -17,6 +19,10 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libssm.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libssm_debug.so")
+_LIB_KINDS = ("release", "debug")
+_lib_kind = "release"
+_loaded = {}
 
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA = 0, 1, 2, 3
 SSM_F32, SSM_BF16 = 0, 1
@@ -31,7 +37,10 @@ EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_sca
            "ssm_selective_scan_fwd_noalloc", "ssm_scan_bwd_workspace_bytes", "ssm_selective_scan_bwd",
            "ssm_conv_bwd_workspace_bytes", "ssm_causal_conv1d_bwd", "ssm_ssd_workspace_bytes", "ssm_ssd_fwd",
            "ssm_set_test_hooks", "ssm_scan_aggregate_workspace_bytes", "ssm_selective_scan_aggregate",
-           "ssm_scan_compose")
+           "ssm_scan_compose", "ssm_debug_bounds_status")
+
+# Bits of the debug build's error word (include/ssm.h).
+BOUNDS_SCAN, BOUNDS_DECODE, BOUNDS_CONV, BOUNDS_SEGMENT = 1, 2, 4, 8
 
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -49,14 +58,31 @@ class SSMError(RuntimeError):
         self.status = status
 
 
+def select_library(kind: str) -> None:
+    """Route every following call to libssm.so ("release", the default) or libssm_debug.so
+    ("debug"). Both may stay loaded; each is loaded once."""
+    global _lib, _lib_kind
+    if kind not in _LIB_KINDS:
+        raise ValueError(f"unknown library kind {kind!r}")
+    _lib_kind = kind
+    _lib = _loaded.get(kind)
+
+
+def library_path() -> str:
+    """Path of the library the calls go to."""
+    return LIB_PATH if _lib_kind == "release" else DEBUG_LIB_PATH
+
+
 def lib() -> ctypes.CDLL:
-    """Load libssm.so once; raise if it has not been built."""
+    """Load the selected library once; raise if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
-                               "(python -m selective_state_space_145_b300.build)")
-        L = ctypes.CDLL(LIB_PATH)
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                               "(python -m selective_state_space_145_b300.build"
+                               + (" --debug)" if _lib_kind == "debug" else ")"))
+        L = ctypes.CDLL(path)
         vp, fp, i, sz, u = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
         L.ssm_version.restype = i
         L.ssm_version.argtypes = []
@@ -99,8 +125,19 @@ def lib() -> ctypes.CDLL:
         L.ssm_selective_state_update.restype = i
         L.ssm_selective_state_update.argtypes = [fp, vp, vp, vp, fp, vp, vp, fp, vp, fp, i, fp, fp, i, vp,
                                                  i, i, i, i, u, vp]
+        L.ssm_debug_bounds_status.restype = i
+        L.ssm_debug_bounds_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
         _lib = L
+        _loaded[_lib_kind] = L
     return _lib
+
+
+def debug_bounds_status(clear: bool = True) -> int:
+    """The debug library's error word (0: no checked access left its tensor), cleared when
+    `clear`. Synchronises the device. Raises SSMError(SSM_ERR_UNSUPPORTED) on the release library."""
+    word = ctypes.c_uint(0)
+    _check("ssm_debug_bounds_status", lib().ssm_debug_bounds_status(ctypes.byref(word), 1 if clear else 0))
+    return int(word.value)
 
 
 def version() -> int:

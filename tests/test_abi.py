@@ -272,3 +272,49 @@ def test_scan_workspace_stays_far_below_a_per_step_state(L):
         assert ws * 50 < batch * dim * L_ * N * 4
         assert ws >= prev                                     # grows with L, at most linearly
         prev = ws
+
+
+def test_release_library_has_no_bounds_checks(L):
+    """ssm_debug_bounds_status answers SSM_ERR_UNSUPPORTED from the release library (no check
+    compiled in, no CUDA call made) and rejects a NULL word or a bad clear flag."""
+    word = ctypes.c_uint(7)
+    assert L.ssm_debug_bounds_status(ctypes.byref(word), 0) == 2
+    assert word.value == 7
+    assert L.ssm_debug_bounds_status(None, 0) == 1
+    assert L.ssm_debug_bounds_status(ctypes.byref(word), 2) == 1
+
+
+def test_debug_library_builds_and_exports_every_symbol():
+    """libssm_debug.so (SSM_DEBUG_BOUNDS) builds, loads beside the release library and exports
+    the same entry points; its argument checks are the release library's."""
+    from selective_state_space_145_b300 import build
+
+    path = build.build(variant="debug")
+    D = ctypes.CDLL(path)
+    for name in _declared_symbols():
+        assert hasattr(D, name), name
+    D.ssm_version.restype = ctypes.c_int
+    import selective_state_space_145_b300 as ssm
+
+    assert D.ssm_version() == ssm.version()
+    D.ssm_debug_bounds_status.restype = ctypes.c_int
+    assert D.ssm_debug_bounds_status(None, 0) == 1  # host-side argument check, before any CUDA call
+    D.ssm_scan_workspace_bytes.restype = ctypes.c_size_t
+    assert D.ssm_scan_workspace_bytes(1, 1536, 131072, 16, 1, 0) == ssm.lib().ssm_scan_workspace_bytes(
+        1, 1536, 131072, 16, 1, 0)
+
+
+def test_library_selection_routes_the_binding():
+    import selective_state_space_145_b300 as ssm
+
+    try:
+        ssm.select_library("debug")
+        assert ssm.library_path() == ssm.DEBUG_LIB_PATH
+        ssm.select_library("release")
+        assert ssm.library_path() == ssm.LIB_PATH
+        with pytest.raises(ValueError):
+            ssm.select_library("fast")
+    finally:
+        ssm.select_library("release")
+    with pytest.raises(ssm.SSMError, match="UNSUPPORTED"):
+        ssm.debug_bounds_status()
