@@ -166,9 +166,9 @@ def bwd_algorithmic_bytes(w) -> int:
 # The sources each kind of workload's kernels are built from: a traffic figure stays valid
 # while their code is unchanged (comments and whitespace do not count, see source_code_only).
 _KERNEL_SOURCES = {
-    "scan": ("ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
-    "decode": ("ssm_decode.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
-    "backward": ("ssm_scan_bwd.cu", "ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
+    "scan": ("ssm_scan.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h", "ssm_bounds.cuh"),
+    "decode": ("ssm_decode.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h", "ssm_bounds.cuh"),
+    "backward": ("ssm_scan_bwd.cu", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h", "ssm_bounds.cuh"),
     "ssd": ("ssm_ssd.cu", "ssm_umma.cuh", "ssm_api.cu", "ssm_device.cuh", "ssm_internal.h"),
 }
 
@@ -731,8 +731,8 @@ def run_gpu_bwd(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profiles(w.name + "#backward", "backward"), "peak_source": peak_kind,
                      "algorithmic_bytes_per_step": bytes_step,
-                     "timed": "whole step (scan_bwd_kernel + scan_bwd_reduce_kernel)"},
-        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+                     "timed": "whole step (scan_bwd_ckpt_kernel + scan_bwd_kernel + scan_bwd_reduce_kernel)"},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 3 * args.steps, "clocks": clk.summary(),
         "conv_backward_ms": conv_ms,
         "conv_backward_gbs": (None if conv_ms is None else
                               w.batch * w.dim * w.seqlen * (2 if w.io == "bf16" else 4) * 3 / (conv_ms * 1e-3) / 1e9),

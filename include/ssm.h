@@ -173,8 +173,9 @@ SSM_API ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, cons
                                   size_t workspace_bytes, unsigned int flags, void* stream);
 
 /*
- * Workspace bytes ssm_selective_scan_bwd needs (about 4 bytes per (b, d, t) for the state
- * checkpoints plus the per-channel-tile partial sums of dB, dC).
+ * Workspace bytes ssm_selective_scan_bwd needs: about 8.5 bytes per (b, d, t) for the state
+ * checkpoints (16 fp32 states and a sum every 8 steps), 4 bytes per (b, 32-channel tile, t, n)
+ * for the partial sums of dB and dC, and the per-chunk aggregates and partial dA, dD, dbias.
  */
 SSM_API size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int dstate, ssm_dtype io);
 
@@ -199,9 +200,11 @@ SSM_API size_t ssm_scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int 
  *   du, ddelta [batch, dim, seqlen] io;  dz [batch, dim, seqlen] io, required when z != NULL;
  *   dA [dim, dstate], dB, dC [batch, dstate, seqlen], dD [dim], ddelta_bias [dim],
  *   dh0 [batch, dim, dstate], all float32; dD, ddelta_bias and dh0 may be NULL (not computed).
- * The intermediate states are recomputed from checkpoints the call writes to the workspace
- * (ssm_scan_bwd_workspace_bytes, 256-byte aligned, no initialisation needed). Channel and
- * sequence sums are formed in a fixed order, so the results are deterministic.
+ * The call makes two passes over the data: a forward pass writes a state checkpoint every 8
+ * steps to the workspace (ssm_scan_bwd_workspace_bytes, 256-byte aligned, no initialisation
+ * needed), then a reverse pass recomputes each 4 steps' states from them and walks the
+ * adjoint back. Channel and sequence sums are formed in a fixed order, so the results are
+ * deterministic.
  *   flags  must be 0: SSM_SCAN_REVERSE and SSM_SCAN_ZOH have no backward pass here
  *          (SSM_ERR_UNSUPPORTED); unknown bits are SSM_ERR_INVALID_ARG.
  */
@@ -390,11 +393,11 @@ SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, co
  * Range checks of the debug build.
  *
  * libssm_debug.so is this library compiled with SSM_DEBUG_BOUNDS: before each global-memory
- * access of the scan (main, carry, segment aggregate and composition), decode and conv
- * kernels, the element range it touches is tested against the size of its tensor, as the
- * call's arguments give them. An access outside its tensor is skipped (a load reads zero) and
- * sets a bit of a device error word; nothing traps. Bits: 1 scan, 2 decode, 4 conv, 8 segment
- * aggregate / composition.
+ * access of the scan (main, carry, segment aggregate and composition), decode, conv and scan
+ * backward kernels, the element range it touches is tested against the size of its tensor, as
+ * the call's arguments give them. An access outside its tensor is skipped (a load reads zero)
+ * and sets a bit of a device error word; nothing traps. Bits: 1 scan, 2 decode, 4 conv,
+ * 8 segment aggregate / composition, 16 scan backward.
  *
  * ssm_debug_bounds_status synchronises the device (a blocking copy from the word), stores the
  * word's bits in *flags_out and, when clear is 1, resets them to zero. It returns

@@ -92,17 +92,21 @@ int default_chunk_len_impl(int batch, int dim, int seqlen, int dstate, bool bf16
   return default_plan(batch, dim, seqlen, dstate, bf16).chunk_len;
 }
 
-// Chunk length of the backward pass: the same one-wave rule, with the backward kernel's occupancy.
+// Chunk length of the backward pass: as many chunks as fill one wave of the reverse kernel
+// (its occupancy), in whole tiles of scan_bwd_tile_steps() steps and at least kBwdMinChunk steps.
+constexpr int kBwdMinChunk = 32;
 int bwd_chunk_len(int batch, int dim, int seqlen, bool bf16) {
-  const long long ctas = ((dim + 31) / 32) * (long long)batch;
+  const int quantum = ssm::scan_bwd_tile_steps();
+  const long long ctas = (long long)((dim + ssm::scan_bwd_channels_per_cta() - 1) / ssm::scan_bwd_channels_per_cta()) *
+                         batch;
   const long long resident = (long long)sm_count() * ssm::scan_bwd_resident_ctas_per_sm(bf16);
-  const long long whole = round_up(seqlen > 0 ? seqlen : 1, kChunkQuantum);
+  const long long whole = round_up(seqlen > 0 ? seqlen : 1, quantum);
   if (ctas <= 0 || 2 * ctas > resident) return (int)whole;
   long long q = resident / ctas;
-  const long long qmax = (seqlen + kChunkQuantum - 1) / kChunkQuantum;
+  const long long qmax = (seqlen + kBwdMinChunk - 1) / kBwdMinChunk;
   if (q > qmax) q = qmax;
   if (q <= 1) return (int)whole;
-  return (int)round_up((seqlen + q - 1) / q, kChunkQuantum);
+  return (int)round_up((seqlen + q - 1) / q, quantum);
 }
 
 int nchunks_for(int seqlen, int chunk_len) {
@@ -398,6 +402,7 @@ ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float*
   // time is cut into chunks when the channels alone leave SMs idle (as in the forward pass)
   const int cl = bwd_chunk_len(batch, dim, seqlen, io == SSM_BF16);
   const int nchunks = nchunks_for(seqlen, cl);
+  if (nchunks > 65535) return SSM_ERR_INVALID_ARG;
   const size_t need = ssm::scan_bwd_workspace_bytes(batch, dim, seqlen, nchunks);
   if (!workspace || workspace_bytes < need) return SSM_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return SSM_ERR_UNSUPPORTED;
@@ -407,23 +412,15 @@ ssm_status ssm_selective_scan_bwd(const void* u, const void* delta, const float*
   a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD;
   a.ddelta_bias = ddelta_bias; a.dh0 = dh0;
   a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.dstate = dstate; a.bf16 = io == SSM_BF16;
+  bool vec = ((long long)seqlen * (long long)es) % 16 == 0;
+  const void* vec_ptrs[] = {u, delta, B, C, z, dout, du, ddelta, dz};
+  for (const void* p : vec_ptrs)
+    if (p && !aligned(p, 16)) vec = false;
+  a.vec = vec;
   a.chunk_len = cl;
   a.nchunks = nchunks;
   ssm::scan_bwd_workspace_split(workspace, batch, dim, seqlen, nchunks, a);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (nchunks > 1) {
-    // forward carries of chunks 0 .. nchunks-2: the chunk-start states of the checkpoint pass
-    ssm::ScanArgs f;
-    f.x = u; f.delta = delta; f.A = A; f.B = B; f.C = C; f.D = nullptr; f.z = nullptr; f.delta_bias = delta_bias;
-    f.delta_softplus = delta_softplus; f.conv_w = nullptr; f.conv_b = nullptr; f.d_conv = 0; f.conv_init = nullptr;
-    f.h0 = nullptr; f.out = nullptr; f.h_last = nullptr; f.conv_state_out = nullptr;
-    f.batch = batch; f.dim = dim; f.seqlen = seqlen; f.dstate = dstate; f.bf16 = io == SSM_BF16;
-    f.vec = ((long long)seqlen * (long long)es) % 16 == 0 && aligned(u, 16) && aligned(delta, 16) &&
-            aligned(B, 16) && aligned(C, 16);
-    f.chunk_len = cl; f.nchunks = nchunks; f.ws_chunks = nchunks - 1; f.lanes = 1; f.reverse = 0; f.zoh = 0;
-    f.ws_S = const_cast<float*>(a.fS); f.ws_h = const_cast<float*>(a.fh);
-    if (ssm::launch_scan_carry(f, st) != cudaSuccess) return SSM_ERR_CUDA;
-  }
   return ssm::launch_scan_bwd(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
@@ -516,13 +513,14 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
 
 ssm_status ssm_debug_bounds_status(unsigned int* flags_out, int clear) {
   if (!flags_out || (clear != 0 && clear != 1)) return SSM_ERR_INVALID_ARG;
-  unsigned scan = 0, decode = 0, conv = 0;
+  unsigned scan = 0, decode = 0, conv = 0, bwd = 0;
   cudaError_t e = ssm::scan_bounds_flags(&scan, clear != 0);
   if (e == cudaErrorNotSupported) return SSM_ERR_UNSUPPORTED;  // a release build: no checks compiled in
   if (e == cudaSuccess) e = ssm::decode_bounds_flags(&decode, clear != 0);
   if (e == cudaSuccess) e = ssm::conv_bounds_flags(&conv, clear != 0);
+  if (e == cudaSuccess) e = ssm::scan_bwd_bounds_flags(&bwd, clear != 0);
   if (e != cudaSuccess) return SSM_ERR_CUDA;
-  *flags_out = scan | decode | conv;
+  *flags_out = scan | decode | conv | bwd;
   return SSM_OK;
 }
 

@@ -17,6 +17,7 @@ constexpr unsigned kBoundsScan = 1u;       // scan main and carry passes
 constexpr unsigned kBoundsDecode = 2u;     // decode state update
 constexpr unsigned kBoundsConv = 4u;       // standalone causal conv
 constexpr unsigned kBoundsSegment = 8u;    // segment aggregate fold and composition
+constexpr unsigned kBoundsBackward = 16u;  // scan backward: checkpoint, reverse and reduction kernels
 
 // [first, first + count) lies within [0, extent).
 __host__ __device__ constexpr bool range_ok(long long first, long long count, long long extent) {

@@ -136,15 +136,15 @@ struct ScanBwdArgs {
   float* dh0;
   int batch, dim, seqlen, dstate;
   int bf16;
-  int chunk_len;         // multiple of 64; the sequence is cut into nchunks chunks
+  int vec;               // 16-byte staging: row bytes a multiple of 16, bases 16-byte aligned
+  int chunk_len;         // multiple of the 8-step tile; the sequence is cut into nchunks chunks
   int nchunks;
-  const float* fS;       // forward carries [nchunks-1][batch*dim]: sum of Delta' per chunk
-  const float* fh;       // [nchunks-1][batch*dim][16]: chunk end state from zero
-  float* bS;             // backward carries [nchunks][batch*dim] (chunk 0 unused): sum of Delta'
-  float* bh;             // [nchunks][batch*dim][16]: adjoint leaving the chunk's start, from zero
-  float* ws_ckpt;        // [batch][channel tiles][tiles][128 threads] float4: state before each tile
-  float* ws_dB;          // [batch][channel tiles][16][seqlen] per-CTA channel sums
-  float* ws_dC;
+  float* ws_ck;          // [batch][channel tiles][tiles] checkpoints: states from zero at the chunk
+                         //   start and sums of Delta', before every 8-step tile
+  float* fS;             // [nchunks][batch*dim]: sum of Delta' of the chunk
+  float* fh;             // [nchunks][batch*dim][16]: chunk end state from a zero start
+  float* bh;             // [nchunks][batch*dim][16]: adjoint leaving the chunk start, zero at its end
+  float* ws_dBC;         // [batch][channel tiles][seqlen][32]: per-tile channel sums (dB at n, dC at 16+n)
   float* ws_dA;          // [nchunks][batch][dim][16]
   float* ws_dD;          // [nchunks][batch][dim]
   float* ws_dbias;       // [nchunks][batch][dim]
@@ -184,6 +184,8 @@ cudaError_t launch_scan_carry(const ScanArgs& a, cudaStream_t stream);
 size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int nchunks);
 void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, int nchunks, ScanBwdArgs& a);
 int scan_bwd_resident_ctas_per_sm(bool bf16);
+int scan_bwd_tile_steps();
+int scan_bwd_channels_per_cta();
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& a, cudaStream_t stream);
 size_t conv_bwd_workspace_bytes(int batch, int dim, int seqlen);
@@ -195,5 +197,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t scan_bounds_flags(unsigned* out, bool clear);
 cudaError_t decode_bounds_flags(unsigned* out, bool clear);
 cudaError_t conv_bounds_flags(unsigned* out, bool clear);
+cudaError_t scan_bwd_bounds_flags(unsigned* out, bool clear);
 
 }  // namespace ssm

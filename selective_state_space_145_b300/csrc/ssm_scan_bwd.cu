@@ -12,508 +12,753 @@
 //   dDelta_t = sum_n g_t (A Abar_t h_{t-1} + B_t u_t),  ddelta_t = dDelta_t sigmoid(delta_t + bias),
 //   dA += g_t Delta_t Abar_t h_{t-1},  dB_t += g_t Delta_t u_t,  dC_t += dy_t h_t,  dD += dy_t u_t,
 //   dh0 = Abar_0 g_0.
+// Abar_t h_{t-1} is taken as h_t - Delta_t B_t u_t, so the adjoint needs the states h_t alone.
 //
-// Design. One CTA = 32 channels of one sequence, the whole sequence, 128 threads; thread
-// (c, g) holds states 4g .. 4g+3 of channel c, as in the forward kernel.
-//  * Checkpoint pass: the forward recurrence (no readout) over the sequence, writing the state
-//    before every 16-step tile to the workspace. Each tile's global loads are issued into
-//    registers one tile ahead, so they complete while the previous tile computes.
-//  * Reverse pass, tile by tile from the end: stage the tile's u, delta, z, dout rows and B, C;
-//    recompute h_t of the tile's steps from its checkpoint into shared memory, with the
-//    readout partials that give y_t; then dy, dz; the channel sums of dC_t over the CTA's 32
-//    channels; the adjoint walk (backward over the tile, four states per thread in registers),
-//    which leaves g_t in the slot of h_t; the channel sums of dB_t; and du, ddelta.
-//  * dA, dD and dbias accumulate per channel in registers. dB, dC, dA, dD, dbias are written as
-//    per-CTA partials and summed over channel tiles / sequences by a second kernel in a fixed
-//    order (deterministic, no atomics).
+// Design: two passes over the data, then a reduction. Every CTA is one warp; lane c owns
+// channel d0 + c of one sequence with its 16 states in registers; time is cut into chunks
+// (a multiple of the 8-step tile) when the channels alone leave SMs idle.
+//  * Checkpoint pass (scan_bwd_ckpt_kernel), per chunk, forward in time from a zero state.
+//    At the start of every 8-step tile it writes the state so far and the sum of Delta' so
+//    far (Delta' = Delta log2 e); at the chunk's end the chunk's aggregate (sum of Delta', end
+//    state). With several chunks it also folds the chunk's adjoint aggregate on the way: the
+//    adjoint that leaves the chunk's start when its end receives zero,
+//    sum_t 2^(A S_t) C_t dy_t with S_t the sum of Delta' up to and including step t.
+//  * Reverse pass (scan_bwd_kernel), per chunk, tiles from the chunk's end to its start.
+//    The chunk's start state h_in is h0 composed with the aggregates of the chunks before it;
+//    the adjoint entering its end is dh_last composed with the adjoint aggregates of the
+//    chunks after it. A tile's start state is 2^(A S) h_in + (its checkpoint). A tile is two
+//    4-step sub-tiles: a sub-tile's forward states are recomputed into registers, then the
+//    adjoint walks back over them. The tile's per-(step, channel) inputs are staged once by
+//    cp.async and transposed to fp32 [step][lane] (conflict-free per-step reads); B and C to
+//    fp32 [step][32] (broadcast reads). dB_t and dC_t (sums over the CTA's 32 channels) go
+//    through a shared-memory transpose: each lane writes its 32 products as a row, then sums
+//    one column. Outputs du, ddelta, dz leave as one 16-byte row segment per lane and tile.
+//  * Reduction (scan_bwd_reduce_kernel): dB, dC over the channel tiles; dA, dD, dbias over the
+//    chunks and sequences; in a fixed order, so results are deterministic.
+#include "ssm_bounds.cuh"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
 namespace {
 
-constexpr int kBThreads = 128;
-constexpr int kBDT = 32;        // channels per CTA
-constexpr int kBT = 16;         // steps per tile
-constexpr int kBTP = kBT + 1;   // padded row of the per-(channel, step) arrays
-static_assert(kBThreads == kBDT * 4, "four threads per channel");
-constexpr int kOut = kBT * kMaxDstate / kBThreads;  // (step, state) channel sums per thread
-static_assert(kOut == 2, "channel sums: two states (one 8-byte load) per thread");
+constexpr int kW = 32;            // channels per CTA: one warp, one channel per lane
+constexpr int kTB = 8;            // steps per tile (the checkpoint spacing)
+constexpr int kSub = 4;           // steps per sub-tile (forward states kept in registers)
+constexpr int kNS = kMaxDstate;   // states per lane
+static_assert(kTB == 2 * kSub, "a tile is two sub-tiles");
+static_assert(kNS == 16, "16 states per lane");
 
-struct BwdSmem {
-  float4 hist[kBT][kBThreads];        // h_t of the tile, then the adjoint g_t
-  float Bt[kBT][kMaxDstate];          // B, C of the tile, fp32, t-major
-  float Ct[kBT][kMaxDstate];
-  float dl[kBDT][kBTP];               // Delta' = Delta log2(e)
-  float Dl[kBDT][kBTP];               // Delta
-  float uu[kBDT][kBTP];               // u
-  float du[kBDT][kBTP];               // Delta u
-  float sg[kBDT][kBTP];               // dDelta / d(delta)
-  float dy[kBDT][kBTP];               // dL/dy
-  float dout[kBDT][kBTP];
-  float zz[kBDT][kBTP];
-  float p0[4][kBDT][kBTP];            // per-state-group partials: readout, then du
-  float p1[4][kBDT][kBTP];            // per-state-group partials of dDelta
+// Checkpoint of one (CTA, tile): the 32 channels' states at the tile start, from a zero state at
+// the chunk start (states 4k .. 4k+3 of lane c at h[k][c]), and the sums of Delta' from the
+// chunk start to the tile start.
+struct Ckpt {
+  float4 h[4][kW];
+  float S[kW];
+};
+static_assert(sizeof(Ckpt) % 16 == 0, "checkpoints move in 16-byte pieces");
+
+// Raw rows of one tile in shared memory: kCh per-channel arrays (32 rows each), then kSt
+// per-state arrays (16 rows each); kTB elements per row at a stride of RS elements (16 bytes
+// for bf16; 48 for fp32, so that lane c's two 16-byte reads of row c are conflict-free).
+template <typename T, int kCh, int kSt>
+struct Rows {
+  static constexpr int kEPC = 16 / (int)sizeof(T);  // elements per 16-byte piece
+  static constexpr int kCPR = kTB / kEPC;           // pieces per row
+  static constexpr int RS = sizeof(T) == 2 ? kTB : kTB + 4;
+  static constexpr int kRows = kCh * kW + kSt * kNS;
+  static constexpr int kBytes = kRows * RS * (int)sizeof(T);
 };
 
-// ADJ: the adjoint carry of one chunk (chunks 1 .. nchunks-1): the adjoint walked backward over
-// the chunk from zero with its own dy_t C_t inputs, and the chunk's sum of Delta', so that every
-// chunk can start from the composed adjoint of the chunks after it.
-template <typename T, bool ADJ>
-__global__ void __launch_bounds__(kBThreads, 3) scan_bwd_kernel(const ScanBwdArgs a) {
-  constexpr bool PRECISE = IoTraits<T>::kPrecise;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  BwdSmem& S = *reinterpret_cast<BwdSmem*>(smem_raw);
-  const int tid = threadIdx.x;
-  const int c = tid % kBDT, g = tid / kBDT;
-  const int dtile = blockIdx.x, b = blockIdx.y;
-  const int d0 = dtile * kBDT, d = d0 + c;
+template <typename T>
+__device__ __forceinline__ const T* pick4(int k, const T* p0, const T* p1, const T* p2, const T* p3) {
+  return k == 0 ? p0 : (k == 1 ? p1 : (k == 2 ? p2 : p3));
+}
+
+// Stages steps [t0, t0 + kTB) of channel arrays c0..c3 (channels d0 .. d0+31 of sequence b) and
+// state arrays s0, s1 (states 0..15 of sequence b) into `ring`; zeros past L, dim, N or for a
+// NULL array. VEC: 16-byte cp.async pieces (the caller commits the group); else plain loads.
+template <typename T, int kCh, int kSt, bool VEC>
+__device__ __forceinline__ void stage_tile(T* ring, const ScanBwdArgs& a, const T* c0, const T* c1, const T* c2,
+                                           const T* c3, const T* s0, const T* s1, int b, int d0, int t0, int lane) {
+  using R = Rows<T, kCh, kSt>;
   const int L = a.seqlen, N = a.dstate, dim = a.dim;
-  const bool valid = d < dim;
-  const long long cc = (long long)b * dim + d;
-  const int ntiles = (L + kBT - 1) / kBT;
-  const int Q = a.nchunks;
-  const int q = ADJ ? blockIdx.z + 1 : blockIdx.z;   // chunk; chunk boundaries are tile boundaries
-  const int it_begin = q * (a.chunk_len / kBT);
-  const int it_end = min(ntiles, it_begin + a.chunk_len / kBT);
-  const long long BD = (long long)a.batch * dim;
-  const long long cta = (long long)b * gridDim.x + dtile;
-  float4* ckpt = reinterpret_cast<float4*>(a.ws_ckpt) + cta * (long long)ntiles * kBThreads;
-
-  const T* gu = static_cast<const T*>(a.u);
-  const T* gdel = static_cast<const T*>(a.delta);
-  const T* gz = static_cast<const T*>(a.z);
-  const T* gdo = static_cast<const T*>(a.dout);
-  const T* gB = static_cast<const T*>(a.B);
-  const T* gC = static_cast<const T*>(a.C);
-
-  const float Dd = (valid && a.D) ? a.D[d] : 0.f;
-  float An[4];  // A of this thread's states (Delta is staged in log2 units)
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int n = 4 * g + k;
-    An[k] = (valid && n < N) ? a.A[(long long)d * N + n] : 0.f;
-  }
-
-  // ---- staging of tile `it`, in two halves: fetch() issues the global loads into registers
-  // (so the next tile's loads are in flight while this tile computes); put() derives Delta,
-  // its softplus derivative and Delta u and stores everything to shared memory (zeros past
-  // L / dim / N: identity steps with Delta = 0 and u = 0).
-  constexpr int kPE = kBDT * kBT / kBThreads;           // per-(channel, step) elements per thread
-  constexpr int kPB = kBT * kMaxDstate / kBThreads;     // B / C elements per thread
-  struct Fetched {
-    float u[kPE], dv[kPE], z[kPE], dout[kPE], B[kPB], C[kPB];
-  };
-  auto fetch = [&](int it, bool need_all, Fetched& f) {
-    const int t0 = it * kBT;
-#pragma unroll
-    for (int k = 0; k < kPE; ++k) {
-      const int e = tid + k * kBThreads;
-      const int ch = e / kBT, s = e % kBT, t = t0 + s;
-      const bool in = d0 + ch < dim && t < L;
-      const long long idx = ((long long)b * dim + d0 + ch) * L + t;
-      f.u[k] = in ? to_f32(gu[idx]) : 0.f;
-      f.dv[k] = in ? to_f32(gdel[idx]) : 0.f;
-      f.z[k] = (in && need_all && gz) ? to_f32(gz[idx]) : 0.f;
-      f.dout[k] = (in && need_all) ? to_f32(gdo[idx]) : 0.f;
+  const long long tok = (long long)a.batch * dim * L, bcx = (long long)a.batch * N * L;
+  constexpr int kPer = VEC ? R::kCPR : kTB;   // copies per row
+  constexpr int kLen = VEC ? R::kEPC : 1;     // elements per copy
+#pragma unroll 1
+  for (int i = lane; i < R::kRows * kPer; i += kW) {
+    const int r = i / kPer, j = i % kPer;
+    const int t = t0 + j * kLen;
+    const T* src;
+    long long idx, ext;
+    bool ok = t < L;
+    if (r < kCh * kW) {
+      const int c = r % kW;
+      src = pick4<T>(r / kW, c0, c1, c2, c3);
+      ok = ok && d0 + c < dim;
+      idx = ((long long)b * dim + d0 + c) * L + t;
+      ext = tok;
+    } else {
+      const int rr = r - kCh * kW, n = rr % kNS;
+      src = rr / kNS == 0 ? s0 : s1;
+      ok = ok && n < N;
+      idx = ((long long)b * N + n) * L + t;
+      ext = bcx;
     }
-#pragma unroll
-    for (int k = 0; k < kPB; ++k) {
-      const int e = tid + k * kBThreads;
-      const int n = e / kBT, s = e % kBT, t = t0 + s;
-      const bool in = n < N && t < L;
-      const long long idx = ((long long)b * N + n) * L + t;
-      f.B[k] = in ? to_f32(gB[idx]) : 0.f;
-      f.C[k] = (in && need_all) ? to_f32(gC[idx]) : 0.f;
+    ok = ok && src != nullptr && in_bounds(idx, kLen, ext, kBoundsBackward);
+    T* dst = ring + r * R::RS + j * kLen;
+    if (VEC) {
+      cp_async16(dst, ok ? (const void*)(src + idx) : (const void*)c0, ok ? 16u : 0u);
+    } else {
+      *dst = ok ? src[idx] : from_f32<T>(0.f);
     }
-  };
-  auto put = [&](int it, const Fetched& f) {
-    const int t0 = it * kBT;
-#pragma unroll
-    for (int k = 0; k < kPE; ++k) {
-      const int e = tid + k * kBThreads;
-      const int ch = e / kBT, s = e % kBT, t = t0 + s;
-      const bool in = d0 + ch < dim && t < L;
-      float D = 0.f, sgv = 0.f;
-      if (in) {
-        const float v = f.dv[k] + ((a.delta_bias) ? a.delta_bias[d0 + ch] : 0.f);
-        if (a.delta_softplus) {
-          D = softplus_f<PRECISE>(v);
-          sgv = rcp_approx(1.0f + ex2_approx(-v * kLog2e));
-        } else {
-          D = v;
-          sgv = 1.0f;
-        }
-      }
-      S.Dl[ch][s] = D;
-      S.dl[ch][s] = D * kLog2e;
-      S.uu[ch][s] = f.u[k];
-      S.du[ch][s] = D * f.u[k];
-      S.sg[ch][s] = sgv;
-      S.zz[ch][s] = f.z[k];
-      S.dout[ch][s] = f.dout[k];
-    }
-#pragma unroll
-    for (int k = 0; k < kPB; ++k) {
-      const int e = tid + k * kBThreads;
-      const int n = e / kBT, s = e % kBT;
-      S.Bt[s][n] = f.B[k];
-      S.Ct[s][n] = f.C[k];
-    }
-  };
-  Fetched fb;
-
-  // ---- checkpoint pass: the state before every tile of the chunk, from the chunk's start
-  // state h0 o carry_0 o ... o carry_{q-1} (forward carries: a = 2^(A sum Delta'), b = end state)
-  float h[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) h[k] = (valid && a.h0 && 4 * g + k < N) ? a.h0[cc * N + 4 * g + k] : 0.f;
-  if (!ADJ && valid) {
-    for (int j = 0; j < q; ++j) {
-      const float Sj = a.fS[(long long)j * BD + cc];
-      const float4 hb = *reinterpret_cast<const float4*>(a.fh + ((long long)j * BD + cc) * kMaxDstate + 4 * g);
-      const float hbv[4] = {hb.x, hb.y, hb.z, hb.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) h[k] = fmaf(ex2_approx(Sj * An[k]), h[k], hbv[k]);
-    }
-  }
-  if (!ADJ && it_begin < it_end) fetch(it_begin, false, fb);
-  for (int it = it_begin; it < (ADJ ? it_begin : it_end); ++it) {
-    ckpt[(long long)it * kBThreads + tid] = make_float4(h[0], h[1], h[2], h[3]);
-    __syncthreads();  // previous tile's smem reads are done
-    put(it, fb);
-    if (it + 1 < it_end) fetch(it + 1, false, fb);
-    __syncthreads();
-    for (int s = 0; s < kBT; ++s) {
-      const float x = S.dl[c][s], w = S.du[c][s];
-      const float4 B4 = *reinterpret_cast<const float4*>(&S.Bt[s][4 * g]);
-      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) h[k] = fmaf(ex2_approx(x * An[k]), h[k], w * Bv[k]);
-    }
-  }
-
-  // ---- reverse pass. The adjoint entering the chunk's end: dh_last composed with the adjoint
-  // carries of chunks nchunks-1 .. q+1 (ADJ: zero)
-  float gad[4] = {0.f, 0.f, 0.f, 0.f};
-  if (!ADJ) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) gad[k] = (valid && a.dh_last && 4 * g + k < N) ? a.dh_last[cc * N + 4 * g + k] : 0.f;
-    if (valid) {
-      for (int j = Q - 1; j > q; --j) {
-        const float Sj = a.bS[(long long)j * BD + cc];
-        const float4 gb = *reinterpret_cast<const float4*>(a.bh + ((long long)j * BD + cc) * kMaxDstate + 4 * g);
-        const float gbv[4] = {gb.x, gb.y, gb.z, gb.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) gad[k] = fmaf(ex2_approx(Sj * An[k]), gad[k], gbv[k]);
-      }
-    }
-  }
-  float dsum = 0.f;  // ADJ: the chunk's sum of Delta (log2 units)
-  float dA_acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float dD_acc = 0.f, dbias_acc = 0.f;
-  // channel sums: thread -> step tid / (16 / kOut), states n0 .. n0 + kOut - 1 of one group
-  const int rs = tid / (kMaxDstate / kOut), rn0 = kOut * (tid % (kMaxDstate / kOut));
-  const int rg = rn0 / 4, rk = rn0 % 4;
-  if (it_begin < it_end) fetch(it_end - 1, true, fb);
-  for (int it = it_end - 1; it >= it_begin; --it) {
-    const int t0 = it * kBT;
-    const int tl = min(kBT, L - t0);
-    __syncthreads();  // the previous tile is done with shared memory
-    put(it, fb);
-    const float4 hs = ADJ ? make_float4(0.f, 0.f, 0.f, 0.f) : ckpt[(long long)it * kBThreads + tid];
-    if (it > it_begin) fetch(it - 1, true, fb);
-    __syncthreads();
-    if (ADJ) {
-      // dy only (no y needed), then the adjoint from zero over the tile
-      constexpr int kSPT0 = kBT / 4;
-      for (int s = kSPT0 * g; s < kSPT0 * g + kSPT0; ++s) {
-        const float dov = S.dout[c][s];
-        float dyv = dov;
-        if (gz) {
-          const float zv = S.zz[c][s];
-          dyv = dov * zv * rcp_approx(1.0f + ex2_approx(-zv * kLog2e));
-        }
-        S.dy[c][s] = dyv;
-      }
-      __syncthreads();
-      for (int s = kBT - 1; s >= 0; --s) {
-        const float dyv = S.dy[c][s], x = S.dl[c][s];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) gad[k] = ex2_approx(x * An[k]) * fmaf(S.Ct[s][4 * g + k], dyv, gad[k]);
-        dsum += x;
-      }
-      continue;
-    }
-    // recompute h_t of the tile, with this group's readout partial
-    {
-      float hh[4] = {hs.x, hs.y, hs.z, hs.w};
-      for (int s = 0; s < kBT; ++s) {
-        const float x = S.dl[c][s], w = S.du[c][s];
-        const float4 B4 = *reinterpret_cast<const float4*>(&S.Bt[s][4 * g]);
-        const float4 C4 = *reinterpret_cast<const float4*>(&S.Ct[s][4 * g]);
-        const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
-        float p = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          hh[k] = fmaf(ex2_approx(x * An[k]), hh[k], w * Bv[k]);
-          p = fmaf(Cv[k], hh[k], p);
-        }
-        S.hist[s][tid] = make_float4(hh[0], hh[1], hh[2], hh[3]);
-        S.p0[g][c][s] = p;
-      }
-    }
-    __syncthreads();
-    // y, dy, dz for this thread's steps of channel c
-    constexpr int kSPT = kBT / 4;  // steps per thread
-    for (int s = kSPT * g; s < kSPT * g + kSPT; ++s) {
-      const float y = S.p0[0][c][s] + S.p0[1][c][s] + S.p0[2][c][s] + S.p0[3][c][s] + Dd * S.uu[c][s];
-      const float dov = S.dout[c][s];
-      float dyv = dov;
-      if (gz) {
-        const float zv = S.zz[c][s];
-        const float sz = rcp_approx(1.0f + ex2_approx(-zv * kLog2e));
-        dyv = dov * zv * sz;
-        if (valid && s < tl)
-          static_cast<T*>(a.dz)[cc * L + t0 + s] = from_f32<T>(dov * y * sz * (1.0f + zv * (1.0f - sz)));
-      }
-      S.dy[c][s] = dyv;
-      dD_acc = fmaf(dyv, S.uu[c][s], dD_acc);
-    }
-    __syncthreads();
-    // dC_t[n] over the CTA's channels (this thread: step rs, states rn0, rn0 + 1)
-    {
-      float acc0 = 0.f, acc1 = 0.f;
-      for (int j = 0; j < kBDT; ++j) {
-        const int ch = (j + tid) % kBDT;
-        const float2 hv = reinterpret_cast<const float2*>(&S.hist[rs][rg * kBDT + ch])[rk / 2];
-        const float dyv = S.dy[ch][rs];
-        acc0 = fmaf(dyv, hv.x, acc0);
-        acc1 = fmaf(dyv, hv.y, acc1);
-      }
-      if (rs < tl) {
-        float* out = a.ws_dC + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
-        if (rn0 < N) out[(long long)rn0 * L + t0 + rs] = acc0;
-        if (rn0 + 1 < N) out[(long long)(rn0 + 1) * L + t0 + rs] = acc1;
-      }
-    }
-    __syncthreads();  // dC has read every h_t; the adjoint walk overwrites them
-    // adjoint walk: steps kBT-1 .. 0 of the tile
-    // per state: g_t = g + C dy; with gB = g_t B and t1 = g_t Abar h_{t-1},
-    //   du part = Delta sum gB,  dDelta part = sum A t1 + u sum gB,  dA += Delta t1,  g <- Abar g_t
-    for (int s = kBT - 1; s >= 0; --s) {
-      const float dyv = S.dy[c][s], x = S.dl[c][s], Dl = S.Dl[c][s], uv = S.uu[c][s];
-      const float4 hp4 = s > 0 ? S.hist[s - 1][tid] : hs;
-      const float4 B4 = *reinterpret_cast<const float4*>(&S.Bt[s][4 * g]);
-      const float4 C4 = *reinterpret_cast<const float4*>(&S.Ct[s][4 * g]);
-      const float hp[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
-      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
-      float sgb = 0.f, sat = 0.f, gt[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float e = ex2_approx(x * An[k]);
-        gt[k] = fmaf(Cv[k], dyv, gad[k]);
-        sgb = fmaf(gt[k], Bv[k], sgb);
-        const float t1 = gt[k] * (e * hp[k]);
-        sat = fmaf(An[k], t1, sat);
-        dA_acc[k] = fmaf(Dl, t1, dA_acc[k]);
-        gad[k] = e * gt[k];
-      }
-      S.hist[s][tid] = make_float4(gt[0], gt[1], gt[2], gt[3]);
-      S.p0[g][c][s] = Dl * sgb;
-      S.p1[g][c][s] = fmaf(uv, sgb, sat);
-    }
-    __syncthreads();
-    // dB_t[n] over the CTA's channels from g_t and Delta u
-    {
-      float acc0 = 0.f, acc1 = 0.f;
-      for (int j = 0; j < kBDT; ++j) {
-        const int ch = (j + tid) % kBDT;
-        const float2 gv = reinterpret_cast<const float2*>(&S.hist[rs][rg * kBDT + ch])[rk / 2];
-        const float w = S.du[ch][rs];
-        acc0 = fmaf(w, gv.x, acc0);
-        acc1 = fmaf(w, gv.y, acc1);
-      }
-      if (rs < tl) {
-        float* out = a.ws_dB + (((long long)b * gridDim.x + dtile) * kMaxDstate) * L;
-        if (rn0 < N) out[(long long)rn0 * L + t0 + rs] = acc0;
-        if (rn0 + 1 < N) out[(long long)(rn0 + 1) * L + t0 + rs] = acc1;
-      }
-    }
-    // du, ddelta for this thread's steps of channel c
-    for (int s = kSPT * g; s < kSPT * g + kSPT; ++s) {
-      if (!valid || s >= tl) continue;
-      const float duv = Dd * S.dy[c][s] + S.p0[0][c][s] + S.p0[1][c][s] + S.p0[2][c][s] + S.p0[3][c][s];
-      const float dD = (S.p1[0][c][s] + S.p1[1][c][s] + S.p1[2][c][s] + S.p1[3][c][s]) * S.sg[c][s];
-      static_cast<T*>(a.du)[cc * L + t0 + s] = from_f32<T>(duv);
-      static_cast<T*>(a.ddelta)[cc * L + t0 + s] = from_f32<T>(dD);
-      dbias_acc += dD;
-    }
-  }
-
-  // ---- per-channel results
-  if (ADJ) {
-    if (valid) {
-      *reinterpret_cast<float4*>(a.bh + ((long long)q * BD + cc) * kMaxDstate + 4 * g) =
-          make_float4(gad[0], gad[1], gad[2], gad[3]);
-      if (g == 0) a.bS[(long long)q * BD + cc] = dsum;
-    }
-    return;
-  }
-  if (valid) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int n = 4 * g + k;
-      if (n < N) {
-        if (a.dh0 && q == 0) a.dh0[cc * N + n] = gad[k];
-        a.ws_dA[((long long)q * BD + cc) * N + n] = dA_acc[k];
-      }
-    }
-  }
-  // dD and dbias: the four threads of a channel each hold a quarter of every tile's steps
-  __syncthreads();
-  S.p0[g][c][0] = dD_acc;
-  S.p1[g][c][0] = dbias_acc;
-  __syncthreads();
-  if (g == 0 && valid) {
-    a.ws_dD[(long long)q * BD + cc] = S.p0[0][c][0] + S.p0[1][c][0] + S.p0[2][c][0] + S.p0[3][c][0];
-    a.ws_dbias[(long long)q * BD + cc] = S.p1[0][c][0] + S.p1[1][c][0] + S.p1[2][c][0] + S.p1[3][c][0];
   }
 }
 
-// Sums of the per-CTA partials, in a fixed order:
-//   dB, dC [b, n, t] over the channel tiles of sequence b; dA [d, n], dD, dbias [d] over b.
-__global__ void scan_bwd_reduce_kernel(const ScanBwdArgs a, int ndt) {
-  const long long L = a.seqlen, N = a.dstate;
-  const long long nBC = (long long)a.batch * N * L;
+// The checkpoint record of tile `it`: 136 16-byte pieces.
+__device__ __forceinline__ void stage_ckpt(Ckpt* dst, const Ckpt* src, long long rec, long long nrec, int lane) {
+  if (!in_bounds(rec, 1, nrec, kBoundsBackward)) return;
+  const char* s = reinterpret_cast<const char*>(src + rec);
+  char* d = reinterpret_cast<char*>(dst);
+#pragma unroll 1
+  for (int i = lane; i < (int)(sizeof(Ckpt) / 16); i += kW) cp_async16(d + 16 * i, s + 16 * i, 16u);
+}
+
+__device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(ex2_approx(x.x), ex2_approx(x.y)); }
+
+// ---------------------------------------------------------------- checkpoint pass
+// ADJ: also the chunk's adjoint aggregate (needs dout, z and C).
+template <typename T, bool VEC, bool ADJ>
+__global__ void __launch_bounds__(kW, 16) scan_bwd_ckpt_kernel(const ScanBwdArgs a) {
+  constexpr bool PRECISE = IoTraits<T>::kPrecise;
+  constexpr int kCh = ADJ ? 4 : 2, kSt = ADJ ? 2 : 1;
+  using R = Rows<T, kCh, kSt>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  auto ring = [&](int slot) { return reinterpret_cast<T*>(smem_raw + slot * R::kBytes); };
+  float (*const BC)[kW] = reinterpret_cast<float (*)[kW]>(smem_raw + 2 * R::kBytes);
+
+  const int lane = threadIdx.x;
+  const int dtile = blockIdx.x, b = blockIdx.y, q = blockIdx.z;
+  const int ndt = gridDim.x;
+  const int d0 = dtile * kW, d = d0 + lane;
+  const int L = a.seqlen, N = a.dstate, dim = a.dim;
+  const bool valid = d < dim;
+  const long long BD = (long long)a.batch * dim, cc = (long long)b * dim + d;
+  const int ntiles = (L + kTB - 1) / kTB;
+  const int it_begin = q * (a.chunk_len / kTB);
+  const int it_end = min(ntiles, it_begin + a.chunk_len / kTB);
+  const T* gu = static_cast<const T*>(a.u);
+  const T* gdl = static_cast<const T*>(a.delta);
+  const T* gdo = static_cast<const T*>(a.dout);
+  const T* gz = static_cast<const T*>(a.z);
+  const T* gB = static_cast<const T*>(a.B);
+  const T* gC = static_cast<const T*>(a.C);
+  Ckpt* const ck = reinterpret_cast<Ckpt*>(a.ws_ck);
+  const long long nrec = (long long)a.batch * ndt * ntiles;
+  const long long rec0 = ((long long)b * ndt + dtile) * ntiles;
+
+  const bool arow = valid && in_bounds((long long)d * N, N, (long long)dim * N, kBoundsBackward);
+  float2 An[kNS / 2];
+#pragma unroll
+  for (int k = 0; k < kNS / 2; ++k)
+    An[k] = make_float2(arow && 2 * k < N ? a.A[(long long)d * N + 2 * k] : 0.f,
+                        arow && 2 * k + 1 < N ? a.A[(long long)d * N + 2 * k + 1] : 0.f);
+  const float bias = (valid && a.delta_bias) ? a.delta_bias[d] : 0.f;
+
+  float2 h[kNS / 2], g[kNS / 2];
+#pragma unroll
+  for (int k = 0; k < kNS / 2; ++k) h[k] = g[k] = make_float2(0.f, 0.f);
+  float S = 0.f;
+
+  if (it_begin < it_end) {
+    stage_tile<T, kCh, kSt, VEC>(ring(0), a, gu, gdl, gdo, gz, gB, gC, b, d0, it_begin * kTB, lane);
+    cp_async_commit();
+  }
+#pragma unroll 1
+  for (int it = it_begin; it < it_end; ++it) {
+    const int t0 = it * kTB, tl = min(kTB, L - t0);
+    // the checkpoint of this tile: the state and the sum of Delta' before it
+    if (in_bounds(rec0 + it, 1, nrec, kBoundsBackward)) {
+      Ckpt& c = ck[rec0 + it];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) c.h[k][lane] = make_float4(h[2 * k].x, h[2 * k].y, h[2 * k + 1].x, h[2 * k + 1].y);
+      c.S[lane] = S;
+    }
+    if (it + 1 < it_end)
+      stage_tile<T, kCh, kSt, VEC>(ring((it + 1 - it_begin) & 1), a, gu, gdl, gdo, gz, gB, gC, b, d0, t0 + kTB, lane);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncwarp();  // (A) this tile's rows have landed for every lane; every lane is done with BC
+    const T* rg = ring((it - it_begin) & 1);
+    float x[kTB], du[kTB], dy[kTB];
+    {
+      float uv[kTB], dv[kTB];
+      load8(rg + (0 * kW + lane) * R::RS, uv);
+      load8(rg + (1 * kW + lane) * R::RS, dv);
+      float dov[kTB], zv[kTB];
+      if (ADJ) {
+        load8(rg + (2 * kW + lane) * R::RS, dov);
+        load8(rg + (3 * kW + lane) * R::RS, zv);
+      }
+#pragma unroll
+      for (int s = 0; s < kTB; ++s) {
+        const bool in = valid && s < tl;
+        const float v = dv[s] + bias;
+        const float Dl = a.delta_softplus ? softplus_f<PRECISE>(v) : v;
+        x[s] = in ? Dl * kLog2e : 0.f;
+        du[s] = in ? Dl * uv[s] : 0.f;
+        if (ADJ) dy[s] = in ? (gz ? dov[s] * silu_f(zv[s]) : dov[s]) : 0.f;
+      }
+      // B (and C) rows, transposed to [step][state] (C at 16 + n)
+      if (lane < kSt * kNS) {
+        float bv[kTB];
+        load8(rg + (kCh * kW + lane) * R::RS, bv);
+#pragma unroll
+        for (int s = 0; s < kTB; ++s) BC[s][lane] = bv[s];
+      }
+    }
+    __syncwarp();  // (B) BC visible
+#pragma unroll
+    for (int s = 0; s < kTB; ++s) {
+      S += x[s];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 B4 = *reinterpret_cast<const float4*>(&BC[s][4 * k4]);
+        const float2 Bv[2] = {make_float2(B4.x, B4.y), make_float2(B4.z, B4.w)};
+        float2 Cv[2];
+        if (ADJ) {
+          const float4 C4 = *reinterpret_cast<const float4*>(&BC[s][kNS + 4 * k4]);
+          Cv[0] = make_float2(C4.x, C4.y);
+          Cv[1] = make_float2(C4.z, C4.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int k = 2 * k4 + i;
+          h[k] = ffma2(ex2x2(fmul2(f2(x[s]), An[k])), h[k], fmul2(f2(du[s]), Bv[i]));
+          if (ADJ) g[k] = ffma2(ex2x2(fmul2(f2(S), An[k])), fmul2(Cv[i], f2(dy[s])), g[k]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  // the chunk's aggregates: [nchunks][batch * dim] sums, [nchunks][batch * dim][16] states
+  const long long e = (long long)q * BD + cc;
+  if (valid && in_bounds(e, 1, (long long)a.nchunks * BD, kBoundsBackward)) {
+    a.fS[e] = S;
+    float4* fh = reinterpret_cast<float4*>(a.fh + e * kNS);
+    float4* bh = reinterpret_cast<float4*>(a.bh + e * kNS);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      fh[k] = make_float4(h[2 * k].x, h[2 * k].y, h[2 * k + 1].x, h[2 * k + 1].y);
+      if (ADJ) bh[k] = make_float4(g[2 * k].x, g[2 * k].y, g[2 * k + 1].x, g[2 * k + 1].y);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- reverse pass
+
+template <typename T>
+struct RevSmem {
+  using R = Rows<T, 4, 2>;                 // u, delta, dout, z; B, C
+  static constexpr int ring = 0;
+  static constexpr int ck = ring + R::kBytes;
+  static constexpr int arr = ck + (int)sizeof(Ckpt);  // x, u, dy, gz, sg: [5][kTB][kW] fp32
+  static constexpr int bc = arr + 5 * kTB * kW * 4;   // [kTB][kW]: B at n, C at 16 + n
+  static constexpr int hst = bc + kTB * kW * 4;       // float4 [4][kW]: the tile's start state
+  static constexpr int hin = hst + 4 * kW * 16;       // float4 [4][kW]: the chunk's start state
+  static constexpr int red = hin + 4 * kW * 16;       // [kW][kRed]: dB / dC products, one row per lane
+  static constexpr int kRed = 2 * kNS + 4;
+  static constexpr int bytes = red + kW * kRed * 4;
+};
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kW, 12) scan_bwd_kernel(const ScanBwdArgs a) {
+  constexpr bool PRECISE = IoTraits<T>::kPrecise;
+  using Lay = RevSmem<T>;
+  using R = typename Lay::R;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  T* const ring = reinterpret_cast<T*>(smem_raw + Lay::ring);
+  Ckpt& cks = *reinterpret_cast<Ckpt*>(smem_raw + Lay::ck);
+  float (*const X)[kW] = reinterpret_cast<float (*)[kW]>(smem_raw + Lay::arr);      // Delta'
+  float (*const U)[kW] = X + kTB;      // u; after the adjoint step: du
+  float (*const DY)[kW] = X + 2 * kTB; // dL/dy
+  float (*const GZ)[kW] = X + 3 * kTB; // dout silu'(z); after the forward step: dz
+  float (*const SG)[kW] = X + 4 * kTB; // sigmoid(delta + bias); after the adjoint step: ddelta
+  float (*const BC)[kW] = reinterpret_cast<float (*)[kW]>(smem_raw + Lay::bc);
+  float4 (*const hst)[kW] = reinterpret_cast<float4 (*)[kW]>(smem_raw + Lay::hst);
+  float4 (*const hin)[kW] = reinterpret_cast<float4 (*)[kW]>(smem_raw + Lay::hin);
+  float (*const red)[Lay::kRed] = reinterpret_cast<float (*)[Lay::kRed]>(smem_raw + Lay::red);
+
+  const int lane = threadIdx.x;
+  const int dtile = blockIdx.x, b = blockIdx.y, q = blockIdx.z;
+  const int ndt = gridDim.x, Q = a.nchunks;
+  const int d0 = dtile * kW, d = d0 + lane;
+  const int L = a.seqlen, N = a.dstate, dim = a.dim;
+  const bool valid = d < dim;
+  const long long BD = (long long)a.batch * dim, cc = (long long)b * dim + d;
+  const int ntiles = (L + kTB - 1) / kTB;
+  const int it_begin = q * (a.chunk_len / kTB);
+  const int it_end = min(ntiles, it_begin + a.chunk_len / kTB);
+  const bool has_z = a.z != nullptr;
+  const T* gu = static_cast<const T*>(a.u);
+  const T* gdl = static_cast<const T*>(a.delta);
+  const T* gdo = static_cast<const T*>(a.dout);
+  const T* gz = static_cast<const T*>(a.z);
+  const T* gB = static_cast<const T*>(a.B);
+  const T* gC = static_cast<const T*>(a.C);
+  const Ckpt* const ck = reinterpret_cast<const Ckpt*>(a.ws_ck);
+  const long long nrec = (long long)a.batch * ndt * ntiles;
+  const long long rec0 = ((long long)b * ndt + dtile) * ntiles;
+  const long long tok = BD * L;
+  const long long nagg = (long long)Q * BD;
+
+  // prefetch the last tile of the chunk while the carries are composed
+  if (it_begin < it_end) {
+    stage_tile<T, 4, 2, VEC>(ring, a, gu, gdl, gdo, gz, gB, gC, b, d0, (it_end - 1) * kTB, lane);
+    stage_ckpt(&cks, ck, rec0 + it_end - 1, nrec, lane);
+  }
+  cp_async_commit();
+
+  const bool arow = valid && in_bounds((long long)d * N, N, (long long)dim * N, kBoundsBackward);
+  const bool srow = valid && in_bounds(cc * N, N, BD * N, kBoundsBackward);
+  float2 An[kNS / 2];
+#pragma unroll
+  for (int k = 0; k < kNS / 2; ++k)
+    An[k] = make_float2(arow && 2 * k < N ? a.A[(long long)d * N + 2 * k] : 0.f,
+                        arow && 2 * k + 1 < N ? a.A[(long long)d * N + 2 * k + 1] : 0.f);
+  const float bias = (valid && a.delta_bias) ? a.delta_bias[d] : 0.f;
+  const float Dd = (valid && a.D) ? a.D[d] : 0.f;
+
+  // ---- the chunk's start state: h0 composed with the aggregates of chunks 0 .. q-1
+  const bool need_hin = q > 0 || a.h0 != nullptr;
+  if (need_hin) {
+    float2 h[kNS / 2];
+#pragma unroll
+    for (int k = 0; k < kNS / 2; ++k)
+      h[k] = make_float2(srow && a.h0 && 2 * k < N ? a.h0[cc * N + 2 * k] : 0.f,
+                         srow && a.h0 && 2 * k + 1 < N ? a.h0[cc * N + 2 * k + 1] : 0.f);
+#pragma unroll 1
+    for (int j = 0; j < q; ++j) {
+      const long long e = (long long)j * BD + cc;
+      if (!valid || !in_bounds(e, 1, nagg, kBoundsBackward)) break;
+      const float Sj = a.fS[e];
+      const float4* hp = reinterpret_cast<const float4*>(a.fh + e * kNS);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 v = hp[k4];
+        h[2 * k4] = ffma2(ex2x2(fmul2(f2(Sj), An[2 * k4])), h[2 * k4], make_float2(v.x, v.y));
+        h[2 * k4 + 1] = ffma2(ex2x2(fmul2(f2(Sj), An[2 * k4 + 1])), h[2 * k4 + 1], make_float2(v.z, v.w));
+      }
+    }
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4)
+      hin[k4][lane] = make_float4(h[2 * k4].x, h[2 * k4].y, h[2 * k4 + 1].x, h[2 * k4 + 1].y);
+  }
+  // ---- the adjoint entering the chunk's end: dh_last composed with chunks nchunks-1 .. q+1
+  float2 gad[kNS / 2];
+#pragma unroll
+  for (int k = 0; k < kNS / 2; ++k)
+    gad[k] = make_float2(srow && a.dh_last && 2 * k < N ? a.dh_last[cc * N + 2 * k] : 0.f,
+                         srow && a.dh_last && 2 * k + 1 < N ? a.dh_last[cc * N + 2 * k + 1] : 0.f);
+#pragma unroll 1
+  for (int j = Q - 1; j > q; --j) {
+    const long long e = (long long)j * BD + cc;
+    if (!valid || !in_bounds(e, 1, nagg, kBoundsBackward)) break;
+    const float Sj = a.fS[e];
+    const float4* gp = reinterpret_cast<const float4*>(a.bh + e * kNS);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const float4 v = gp[k4];
+      gad[2 * k4] = ffma2(ex2x2(fmul2(f2(Sj), An[2 * k4])), gad[2 * k4], make_float2(v.x, v.y));
+      gad[2 * k4 + 1] = ffma2(ex2x2(fmul2(f2(Sj), An[2 * k4 + 1])), gad[2 * k4 + 1], make_float2(v.z, v.w));
+    }
+  }
+
+  float2 dA[kNS / 2];
+#pragma unroll
+  for (int k = 0; k < kNS / 2; ++k) dA[k] = make_float2(0.f, 0.f);
+  float dD_acc = 0.f, dbias_acc = 0.f;
+  float* const dbc = a.ws_dBC + ((long long)b * ndt + dtile) * (long long)L * (2 * kNS);
+
+  // one forward step of the recomputation: h <- 2^(Delta' A) h + Delta u B; with Y, also
+  // y_t = C.h_t + D u_t and dz_t = y_t dout_t silu'(z_t) (into GZ)
+  auto fwd_step = [&](int s, float2 (&h)[kNS / 2], bool Y) {
+    const float xv = X[s][lane], uv = U[s][lane];
+    const float duv = xv * kLn2 * uv;
+    float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const float4 B4 = *reinterpret_cast<const float4*>(&BC[s][4 * k4]);
+      const float2 Bv[2] = {make_float2(B4.x, B4.y), make_float2(B4.z, B4.w)};
+      float2 Cv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      if (Y) {
+        const float4 C4 = *reinterpret_cast<const float4*>(&BC[s][kNS + 4 * k4]);
+        Cv[0] = make_float2(C4.x, C4.y);
+        Cv[1] = make_float2(C4.z, C4.w);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k = 2 * k4 + i;
+        h[k] = ffma2(ex2x2(fmul2(f2(xv), An[k])), h[k], fmul2(f2(duv), Bv[i]));
+        if (Y) y2 = ffma2(Cv[i], h[k], y2);
+      }
+    }
+    if (Y && has_z) GZ[s][lane] = fmaf(Dd, uv, y2.x + y2.y) * GZ[s][lane];
+  };
+
+  // one adjoint step over the state hs = h_t: gradients of step t, then the adjoint moves to t-1
+  auto adj_step = [&](int s, int t, const float2 (&hs)[kNS / 2]) {
+    const float xv = X[s][lane], uv = U[s][lane], dyv = DY[s][lane], sgv = SG[s][lane];
+    const float Dl = xv * kLn2, duv = Dl * uv;
+    float2 sgb = make_float2(0.f, 0.f), sat = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const float4 B4 = *reinterpret_cast<const float4*>(&BC[s][4 * k4]);
+      const float4 C4 = *reinterpret_cast<const float4*>(&BC[s][kNS + 4 * k4]);
+      const float2 Bv[2] = {make_float2(B4.x, B4.y), make_float2(B4.z, B4.w)};
+      const float2 Cv[2] = {make_float2(C4.x, C4.y), make_float2(C4.z, C4.w)};
+      float2 pb[2], pc[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k = 2 * k4 + i;
+        const float2 gt = ffma2(Cv[i], f2(dyv), gad[k]);          // g_t = g + C_t dy_t
+        const float2 m = ffma2(f2(-duv), Bv[i], hs[k]);            // Abar_t h_{t-1} = h_t - Delta u B
+        const float2 tm = fmul2(gt, m);
+        sat = ffma2(An[k], tm, sat);
+        dA[k] = ffma2(f2(Dl), tm, dA[k]);
+        sgb = ffma2(gt, Bv[i], sgb);
+        pb[i] = fmul2(gt, f2(duv));                               // dB_t term g_t Delta u
+        pc[i] = fmul2(hs[k], f2(dyv));                            // dC_t term dy h_t
+        gad[k] = fmul2(ex2x2(fmul2(f2(xv), An[k])), gt);          // g <- Abar_t g_t
+      }
+      *reinterpret_cast<float4*>(&red[lane][4 * k4]) = make_float4(pb[0].x, pb[0].y, pb[1].x, pb[1].y);
+      *reinterpret_cast<float4*>(&red[lane][kNS + 4 * k4]) = make_float4(pc[0].x, pc[0].y, pc[1].x, pc[1].y);
+    }
+    const float sgbs = sgb.x + sgb.y;
+    const float ddv = fmaf(uv, sgbs, sat.x + sat.y) * sgv;
+    U[s][lane] = fmaf(Dd, dyv, Dl * sgbs);  // du
+    SG[s][lane] = ddv;                      // ddelta
+    dD_acc = fmaf(dyv, uv, dD_acc);
+    dbias_acc += ddv;
+    __syncwarp();  // (R1) every lane's products are in its row
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int c = 0; c < kW; c += 4) {
+      s0 += red[c][lane];
+      s1 += red[c + 1][lane];
+      s2 += red[c + 2][lane];
+      s3 += red[c + 3][lane];
+    }
+    if (t < L && in_bounds((long long)t * (2 * kNS) + lane, 1, (long long)L * (2 * kNS), kBoundsBackward))
+      dbc[(long long)t * (2 * kNS) + lane] = (s0 + s1) + (s2 + s3);
+    __syncwarp();  // (R2) every column is read before the next step's rows
+  };
+
+#pragma unroll 1
+  for (int it = it_end - 1; it >= it_begin; --it) {
+    const int t0 = it * kTB, tl = min(kTB, L - t0);
+    cp_async_wait<0>();
+    __syncwarp();  // (A) this tile's rows and checkpoint have landed; every lane is done with BC
+    // ---- per-(step, channel) values of lane's channel, [step][lane] in fp32
+    {
+      float uv[kTB], dv[kTB], dov[kTB], zv[kTB];
+      load8(ring + (0 * kW + lane) * R::RS, uv);
+      load8(ring + (1 * kW + lane) * R::RS, dv);
+      load8(ring + (2 * kW + lane) * R::RS, dov);
+      load8(ring + (3 * kW + lane) * R::RS, zv);
+#pragma unroll
+      for (int s = 0; s < kTB; ++s) {
+        const bool in = valid && s < tl;
+        const float v = dv[s] + bias;
+        float Dl = v, sg = 1.f;
+        if (a.delta_softplus) {
+          Dl = softplus_f<PRECISE>(v);
+          sg = rcp_approx(1.0f + ex2_approx(-v * kLog2e));
+        }
+        float dy = dov[s], gzv = 0.f;
+        if (has_z) {
+          const float sz = rcp_approx(1.0f + ex2_approx(-zv[s] * kLog2e));
+          dy = dov[s] * zv[s] * sz;
+          gzv = dov[s] * sz * (1.0f + zv[s] * (1.0f - sz));
+        }
+        X[s][lane] = in ? Dl * kLog2e : 0.f;
+        U[s][lane] = in ? uv[s] : 0.f;
+        DY[s][lane] = in ? dy : 0.f;
+        GZ[s][lane] = in ? gzv : 0.f;
+        SG[s][lane] = in ? sg : 0.f;
+      }
+      float bv[kTB];
+      load8(ring + (4 * kW + lane) * R::RS, bv);
+#pragma unroll
+      for (int s = 0; s < kTB; ++s) BC[s][lane] = bv[s];
+      // the tile's start state: 2^(A S) h_in + the checkpoint from zero
+      const float Sck = cks.S[lane];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        float4 v = cks.h[k4][lane];
+        if (need_hin) {
+          const float4 hi = hin[k4][lane];
+          const float2 e0 = ex2x2(fmul2(f2(Sck), An[2 * k4])), e1 = ex2x2(fmul2(f2(Sck), An[2 * k4 + 1]));
+          v = make_float4(fmaf(e0.x, hi.x, v.x), fmaf(e0.y, hi.y, v.y), fmaf(e1.x, hi.z, v.z), fmaf(e1.y, hi.w, v.w));
+        }
+        hst[k4][lane] = v;
+      }
+    }
+    __syncwarp();  // (B) BC visible; the ring and the checkpoint slot are free
+    if (it > it_begin) {
+      stage_tile<T, 4, 2, VEC>(ring, a, gu, gdl, gdo, gz, gB, gC, b, d0, t0 - kTB, lane);
+      stage_ckpt(&cks, ck, rec0 + it - 1, nrec, lane);
+    }
+    cp_async_commit();
+
+    // ---- sub-tile 1 (steps 4..7) from the state after step 3, then sub-tile 0 from the tile start
+#pragma unroll 1
+    for (int half = 1; half >= 0; --half) {
+      const int s0 = half * kSub;
+      float2 hist[kSub][kNS / 2];
+      float2 h[kNS / 2];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 v = hst[k4][lane];
+        h[2 * k4] = make_float2(v.x, v.y);
+        h[2 * k4 + 1] = make_float2(v.z, v.w);
+      }
+      if (half == 1) {
+#pragma unroll
+        for (int s = 0; s < kSub; ++s) fwd_step(s, h, false);
+      }
+#pragma unroll
+      for (int j = 0; j < kSub; ++j) {
+        fwd_step(s0 + j, h, true);
+#pragma unroll
+        for (int k = 0; k < kNS / 2; ++k) hist[j][k] = h[k];
+      }
+#pragma unroll
+      for (int j = kSub - 1; j >= 0; --j) adj_step(s0 + j, t0 + s0 + j, hist[j]);
+    }
+
+    // ---- du, ddelta, dz of the tile: one row segment per lane
+    if (valid) {
+      float o[3][kTB];
+#pragma unroll
+      for (int s = 0; s < kTB; ++s) {
+        o[0][s] = U[s][lane];
+        o[1][s] = SG[s][lane];
+        o[2][s] = GZ[s][lane];
+      }
+      T* const dst[3] = {static_cast<T*>(a.du), static_cast<T*>(a.ddelta), static_cast<T*>(a.dz)};
+      const long long base = cc * L + t0;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        if (k == 2 && !has_z) continue;
+        if (VEC && tl == kTB) {
+          if (in_bounds(base, kTB, tok, kBoundsBackward)) store8(dst[k] + base, o[k]);
+        } else if (VEC && tl == 4) {
+          const float o4[4] = {o[k][0], o[k][1], o[k][2], o[k][3]};
+          if (in_bounds(base, 4, tok, kBoundsBackward)) store4(dst[k] + base, o4);
+        } else {
+#pragma unroll
+          for (int s = 0; s < kTB; ++s)
+            if (s < tl && in_bounds(base + s, 1, tok, kBoundsBackward)) dst[k][base + s] = from_f32<T>(o[k][s]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // ---- per-channel results of the chunk
+  if (valid) {
+    if (q == 0 && a.dh0 && srow) {
+#pragma unroll
+      for (int k = 0; k < kNS / 2; ++k) {
+        if (2 * k < N) a.dh0[cc * N + 2 * k] = gad[k].x;
+        if (2 * k + 1 < N) a.dh0[cc * N + 2 * k + 1] = gad[k].y;
+      }
+    }
+    const long long e = (long long)q * BD + cc;
+    if (in_bounds(e, 1, nagg, kBoundsBackward)) {
+      float4* dap = reinterpret_cast<float4*>(a.ws_dA + e * kNS);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4)
+        dap[k4] = make_float4(dA[2 * k4].x, dA[2 * k4].y, dA[2 * k4 + 1].x, dA[2 * k4 + 1].y);
+      a.ws_dD[e] = dD_acc;
+      a.ws_dbias[e] = dbias_acc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- reduction
+// Blocks [0, nbc): dB, dC [b, n, t] for 32 steps of one sequence, summed over the channel tiles
+// in order (one warp reads one step's row of 32 sums per tile), transposed through shared
+// memory so that each (n) row segment is written whole. The other blocks: dA [d, n], dD [d],
+// ddelta_bias [d], summed over chunks and sequences in order, one thread per output.
+constexpr int kRedThreads = 256;
+
+__global__ void __launch_bounds__(kRedThreads) scan_bwd_reduce_kernel(const ScanBwdArgs a, int ndt, int nbc) {
+  __shared__ float tile[32][33];
+  const int L = a.seqlen, N = a.dstate;
+  if ((int)blockIdx.x < nbc) {
+    const int tblocks = (L + 31) / 32;
+    const int b = blockIdx.x / tblocks, tb = blockIdx.x % tblocks;
+    const int w = threadIdx.x / 32, v = threadIdx.x % 32;
+    const long long nws = (long long)a.batch * ndt * L * (2 * kNS);
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int dt = 0; dt < ndt; ++dt) {
+      const long long row0 = ((long long)b * ndt + dt) * L;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = tb * 32 + w + 8 * i;
+        const long long idx = (row0 + t) * (2 * kNS) + v;
+        if (t < L && in_bounds(idx, 1, nws, kBoundsBackward)) s[i] += a.ws_dBC[idx];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tile[w + 8 * i][v] = s[i];
+    __syncthreads();
+    for (int o = threadIdx.x; o < 32 * 32; o += kRedThreads) {
+      const int vv = o / 32, tt = o % 32, t = tb * 32 + tt, n = vv % kNS;
+      if (t < L && n < N) (vv < kNS ? a.dB : a.dC)[((long long)b * N + n) * L + t] = tile[tt][vv];
+    }
+    return;
+  }
   const long long nA = (long long)a.dim * N;
-  const long long total = 2 * nBC + nA + 2LL * a.dim;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    if (i < 2 * nBC) {
-      const bool isC = i >= nBC;
-      const long long j = isC ? i - nBC : i;
-      const long long b = j / (N * L), r = j % (N * L);
-      const float* src = isC ? a.ws_dC : a.ws_dB;
+  const long long total = nA + 2LL * a.dim;
+  const long long QB = (long long)a.nchunks * a.batch;
+  for (long long i = (blockIdx.x - nbc) * (long long)kRedThreads + threadIdx.x; i < total;
+       i += (long long)(gridDim.x - nbc) * kRedThreads) {
+    if (i < nA) {
+      const long long dd = i / N, n = i % N;
       float s = 0.f;
-      for (int dt = 0; dt < ndt; ++dt) s += src[((b * ndt + dt) * kMaxDstate) * L + r];
-      (isC ? a.dC : a.dB)[j] = s;
-    } else if (i < 2 * nBC + nA) {
-      const long long j = i - 2 * nBC;  // d * N + n
-      float s = 0.f;
-      for (int qb = 0; qb < a.nchunks * a.batch; ++qb) s += a.ws_dA[(long long)qb * nA + j];
-      a.dA[j] = s;
+      for (long long qb = 0; qb < QB; ++qb) s += a.ws_dA[(qb * a.dim + dd) * kNS + n];
+      a.dA[i] = s;
     } else {
-      const long long j = i - 2 * nBC - nA;
+      const long long j = i - nA;
       const bool isBias = j >= a.dim;
       const long long dd = isBias ? j - a.dim : j;
       const float* src = isBias ? a.ws_dbias : a.ws_dD;
       float s = 0.f;
-      for (int qb = 0; qb < a.nchunks * a.batch; ++qb) s += src[(long long)qb * a.dim + dd];
+      for (long long qb = 0; qb < QB; ++qb) s += src[qb * a.dim + dd];
       float* dst = isBias ? a.ddelta_bias : a.dD;
       if (dst) dst[dd] = s;
     }
   }
 }
 
-template <typename T, bool ADJ>
-cudaError_t prepare_bwd() {
-  static int configured[64] = {0};
+// ---------------------------------------------------------------- launch
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes, int (&configured)[64]) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(scan_bwd_kernel<T, ADJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(BwdSmem));
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
   return err;
 }
 
-template <typename T>
-cudaError_t launch_bwd_t(const ScanBwdArgs& a, cudaStream_t stream) {
-  const size_t smem = sizeof(BwdSmem);
-  cudaError_t err = prepare_bwd<T, false>();
+template <typename T, bool VEC, bool ADJ>
+cudaError_t launch_ckpt(const ScanBwdArgs& a, dim3 grid, cudaStream_t stream) {
+  static int configured[64] = {0};
+  using R = Rows<T, ADJ ? 4 : 2, ADJ ? 2 : 1>;
+  const int smem = 2 * R::kBytes + kTB * kW * 4;
+  cudaError_t err = set_smem(scan_bwd_ckpt_kernel<T, VEC, ADJ>, smem, configured);
   if (err != cudaSuccess) return err;
-  const int ndt = (a.dim + kBDT - 1) / kBDT;
-  if (a.nchunks > 1) {
-    // adjoint carries of chunks 1 .. nchunks-1 (the forward carries are already on the stream)
-    err = prepare_bwd<T, true>();
-    if (err != cudaSuccess) return err;
-    scan_bwd_kernel<T, true><<<dim3(ndt, a.batch, a.nchunks - 1), kBThreads, smem, stream>>>(a);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-  }
-  scan_bwd_kernel<T, false><<<dim3(ndt, a.batch, a.nchunks), kBThreads, smem, stream>>>(a);
+  scan_bwd_ckpt_kernel<T, VEC, ADJ><<<grid, kW, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T, bool VEC>
+cudaError_t prepare_rev() {
+  static int configured[64] = {0};
+  return set_smem(scan_bwd_kernel<T, VEC>, RevSmem<T>::bytes, configured);
+}
+
+template <typename T, bool VEC>
+cudaError_t launch_bwd_t(const ScanBwdArgs& a, cudaStream_t stream) {
+  const int ndt = (a.dim + kW - 1) / kW;
+  const dim3 grid(ndt, a.batch, a.nchunks);
+  cudaError_t err = a.nchunks > 1 ? launch_ckpt<T, VEC, true>(a, grid, stream) : launch_ckpt<T, VEC, false>(a, grid, stream);
+  if (err != cudaSuccess) return err;
+  err = prepare_rev<T, VEC>();
+  if (err != cudaSuccess) return err;
+  scan_bwd_kernel<T, VEC><<<grid, kW, RevSmem<T>::bytes, stream>>>(a);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const long long total = 2LL * a.batch * a.dstate * a.seqlen + (long long)a.dim * a.dstate + 2LL * a.dim;
-  const int threads = 256;
-  long long blocks = (total + threads - 1) / threads;
-  if (blocks > 148 * 16) blocks = 148 * 16;
-  if (blocks < 1) blocks = 1;
-  scan_bwd_reduce_kernel<<<(unsigned)blocks, threads, 0, stream>>>(a, ndt);
+  const long long nbc = (long long)a.batch * ((a.seqlen + 31) / 32);
+  long long np = ((long long)a.dim * (a.dstate + 2) + kRedThreads - 1) / kRedThreads;
+  if (np > 148 * 4) np = 148 * 4;
+  if (np < 1) np = 1;
+  scan_bwd_reduce_kernel<<<(unsigned)(nbc + np), kRedThreads, 0, stream>>>(a, ndt, (int)nbc);
   return cudaGetLastError();
 }
 
 template <typename T>
-int bwd_resident() {
+int rev_resident() {
   int n = 0;
-  if (prepare_bwd<T, false>() != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_bwd_kernel<T, false>, kBThreads, sizeof(BwdSmem)) !=
+  if (prepare_rev<T, true>() != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_bwd_kernel<T, true>, kW, RevSmem<T>::bytes) !=
           cudaSuccess ||
       n <= 0) {
     cudaGetLastError();
-    return 3;  // no device to ask: the figure the kernel is built for
+    return sizeof(T) == 2 ? 11 : 9;  // no device to ask: what registers and shared memory allow
   }
   return n;
 }
 
-auto up256 = [](long long v) { return (size_t)((v + 255) & ~255LL); };
+size_t up256(long long v) { return (size_t)((v + 255) & ~255LL); }
 
 }  // namespace
 
-int scan_bwd_resident_ctas_per_sm(bool bf16) { return bf16 ? bwd_resident<__nv_bfloat16>() : bwd_resident<float>(); }
+int scan_bwd_resident_ctas_per_sm(bool bf16) { return bf16 ? rev_resident<__nv_bfloat16>() : rev_resident<float>(); }
 
-int scan_bwd_channels_per_cta() { return kBDT; }
+int scan_bwd_channels_per_cta() { return kW; }
+
+int scan_bwd_tile_steps() { return kTB; }
 
 size_t scan_bwd_workspace_bytes(int batch, int dim, int seqlen, int nchunks) {
-  const long long ndt = (dim + kBDT - 1) / kBDT;
-  const long long ntiles = (seqlen + kBT - 1) / kBT;
+  const long long ndt = (dim + kW - 1) / kW;
+  const long long ntiles = (seqlen + kTB - 1) / kTB;
   const long long BD = (long long)batch * dim;
   const long long Q = nchunks < 1 ? 1 : nchunks;
-  size_t s = up256(batch * ndt * ntiles * kBThreads * 16LL);             // checkpoints
-  s += 2 * up256(batch * ndt * (long long)kMaxDstate * seqlen * 4LL);     // dB, dC partials
-  s += up256(Q * BD * kMaxDstate * 4LL);                                  // dA partials
-  s += 2 * up256(Q * BD * 4LL);                                           // dD, dbias partials
-  s += up256((Q - 1) * BD * 4LL) + up256((Q - 1) * BD * kMaxDstate * 4LL); // forward carries
-  s += up256(Q * BD * 4LL) + up256(Q * BD * kMaxDstate * 4LL);             // adjoint carries
+  size_t s = up256(batch * ndt * ntiles * (long long)sizeof(Ckpt));  // checkpoints
+  s += up256(Q * BD * 4LL) + 2 * up256(Q * BD * kNS * 4LL);         // chunk aggregates fS, fh, bh
+  s += up256(batch * ndt * (long long)seqlen * 2 * kNS * 4LL);      // dB, dC per channel tile
+  s += up256(Q * BD * kNS * 4LL) + 2 * up256(Q * BD * 4LL);         // dA, dD, dbias per chunk
   return s;
 }
 
 void scan_bwd_workspace_split(void* ws, int batch, int dim, int seqlen, int nchunks, ScanBwdArgs& a) {
-  const long long ndt = (dim + kBDT - 1) / kBDT;
-  const long long ntiles = (seqlen + kBT - 1) / kBT;
+  const long long ndt = (dim + kW - 1) / kW;
+  const long long ntiles = (seqlen + kTB - 1) / kTB;
   const long long BD = (long long)batch * dim;
   const long long Q = nchunks < 1 ? 1 : nchunks;
   char* p = static_cast<char*>(ws);
   auto take = [&](size_t bytes) { char* r = p; p += bytes; return reinterpret_cast<float*>(r); };
-  a.ws_ckpt = take(up256(batch * ndt * ntiles * kBThreads * 16LL));
-  a.ws_dB = take(up256(batch * ndt * (long long)kMaxDstate * seqlen * 4LL));
-  a.ws_dC = take(up256(batch * ndt * (long long)kMaxDstate * seqlen * 4LL));
-  a.ws_dA = take(up256(Q * BD * kMaxDstate * 4LL));
+  a.ws_ck = take(up256(batch * ndt * ntiles * (long long)sizeof(Ckpt)));
+  a.fS = take(up256(Q * BD * 4LL));
+  a.fh = take(up256(Q * BD * kNS * 4LL));
+  a.bh = take(up256(Q * BD * kNS * 4LL));
+  a.ws_dBC = take(up256(batch * ndt * (long long)seqlen * 2 * kNS * 4LL));
+  a.ws_dA = take(up256(Q * BD * kNS * 4LL));
   a.ws_dD = take(up256(Q * BD * 4LL));
   a.ws_dbias = take(up256(Q * BD * 4LL));
-  float* fS = take(up256((Q - 1) * BD * 4LL));
-  float* fh = take(up256((Q - 1) * BD * kMaxDstate * 4LL));
-  a.fS = fS;
-  a.fh = fh;
-  a.bS = take(up256(Q * BD * 4LL));
-  a.bh = take(up256(Q * BD * kMaxDstate * 4LL));
 }
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream) {
-  if (a.bf16) return launch_bwd_t<__nv_bfloat16>(a, stream);
-  return launch_bwd_t<float>(a, stream);
+  if (a.bf16) return a.vec ? launch_bwd_t<__nv_bfloat16, true>(a, stream) : launch_bwd_t<__nv_bfloat16, false>(a, stream);
+  return a.vec ? launch_bwd_t<float, true>(a, stream) : launch_bwd_t<float, false>(a, stream);
+}
+
+cudaError_t scan_bwd_bounds_flags(unsigned* out, bool clear) {
+#ifdef SSM_DEBUG_BOUNDS
+  return bounds_flags_read(out, clear);
+#else
+  (void)out;
+  (void)clear;
+  return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace ssm

@@ -53,6 +53,9 @@ CASES = [
     (1, 64, 96, 7, "f32", False, False, False, False, False),  # options off, N < 16
     (2, 70, 129, 16, "bf16", True, True, True, True, True),   # 3 channel tiles, ragged
     (3, 5, 1, 16, "f32", True, True, True, True, True),       # L = 1
+    (2, 40, 100, 16, "f32", True, True, True, True, True),    # vector path, last tile of 4 steps
+    (1, 33, 704, 5, "bf16", True, False, True, True, True),   # vector path, chunks, N < 16
+    (2, 64, 264, 16, "bf16", False, True, False, False, True),  # vector path, no gate / bias / h0
 ]
 
 

@@ -1,6 +1,6 @@
 """The small odd-shape parity cases again, through libssm_debug.so: the library compiled with
-SSM_DEBUG_BOUNDS, in which every checked global access of the scan, segment, decode and conv
-kernels is range-tested against its tensor and an access outside it sets a bit of a device
+SSM_DEBUG_BOUNDS, in which every checked global access of the scan, segment, decode, conv and
+scan-backward kernels is range-tested against its tensor and an access outside it sets a bit of a device
 error word instead of touching memory.
 
 Each case must still match the fp64 oracle (the checks skip nothing on a correct call) and must
@@ -9,6 +9,7 @@ leave the error word at zero.
 
 import pytest
 
+import test_backward_gpu as bwd
 import test_parity_gpu as par
 import test_shard_gpu as seg
 
@@ -81,3 +82,15 @@ def test_debug_segments(debug_lib, cuda_device, io, N, K, L):
     seg.test_aggregate_matches_oracle(cuda_device, io, N, K, L)
     seg.test_compose_matches_oracle(cuda_device)
     _clean(debug_lib, "segment aggregate / compose")
+
+
+@pytest.mark.parametrize("case", bwd.CASES, ids=lambda c: "b{}_d{}_l{}_n{}_{}_z{}_D{}_bias{}_h0{}_dh{}".format(*c))
+def test_debug_backward(debug_lib, cuda_device, case):
+    bwd.test_backward_matches_oracle(cuda_device, case)
+    _clean(debug_lib, "scan backward")
+
+
+def test_debug_backward_chunked(debug_lib, cuda_device):
+    bwd.test_backward_chunked_long(cuda_device, "bf16")
+    bwd.test_backward_empty_sequence(cuda_device)
+    _clean(debug_lib, "scan backward, chunked / empty")
