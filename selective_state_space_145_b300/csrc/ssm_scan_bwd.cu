@@ -20,9 +20,10 @@
 //  * Checkpoint pass (scan_bwd_ckpt_kernel), per chunk, forward in time from a zero state.
 //    At the start of every 8-step tile it writes the state so far and the sum of Delta' so
 //    far (Delta' = Delta log2 e); at the chunk's end the chunk's aggregate (sum of Delta', end
-//    state). With several chunks it also folds the chunk's adjoint aggregate on the way: the
-//    adjoint that leaves the chunk's start when its end receives zero,
-//    sum_t 2^(A S_t) C_t dy_t with S_t the sum of Delta' up to and including step t.
+//    state). With several chunks, every chunk after the first also folds its adjoint aggregate
+//    on the way: the adjoint that leaves the chunk's start when its end receives zero,
+//    sum_t P_t C_t dy_t with P_t = Abar_start ... Abar_t, a running product of the Abar the
+//    state update computes anyway.
 //  * Reverse pass (scan_bwd_kernel), per chunk, tiles from the chunk's end to its start.
 //    The chunk's start state h_in is h0 composed with the aggregates of the chunks before it;
 //    the adjoint entering its end is dh_last composed with the adjoint aggregates of the
@@ -166,13 +167,21 @@ __global__ void __launch_bounds__(kW, 16) scan_bwd_ckpt_kernel(const ScanBwdArgs
                         arow && 2 * k + 1 < N ? a.A[(long long)d * N + 2 * k + 1] : 0.f);
   const float bias = (valid && a.delta_bias) ? a.delta_bias[d] : 0.f;
 
-  float2 h[kNS / 2], g[kNS / 2];
+  // the first chunk's adjoint aggregate is never composed: skip its inputs and arithmetic
+  const bool adj = ADJ && q > 0;
+  const T* const gdo_s = adj ? gdo : nullptr;
+  const T* const gz_s = adj ? gz : nullptr;
+  const T* const gC_s = adj ? gC : nullptr;
+  float2 h[kNS / 2], g[kNS / 2], P[kNS / 2];
 #pragma unroll
-  for (int k = 0; k < kNS / 2; ++k) h[k] = g[k] = make_float2(0.f, 0.f);
+  for (int k = 0; k < kNS / 2; ++k) {
+    h[k] = g[k] = make_float2(0.f, 0.f);
+    P[k] = make_float2(1.f, 1.f);
+  }
   float S = 0.f;
 
   if (it_begin < it_end) {
-    stage_tile<T, kCh, kSt, VEC>(ring(0), a, gu, gdl, gdo, gz, gB, gC, b, d0, it_begin * kTB, lane);
+    stage_tile<T, kCh, kSt, VEC>(ring(0), a, gu, gdl, gdo_s, gz_s, gB, gC_s, b, d0, it_begin * kTB, lane);
     cp_async_commit();
   }
 #pragma unroll 1
@@ -186,7 +195,8 @@ __global__ void __launch_bounds__(kW, 16) scan_bwd_ckpt_kernel(const ScanBwdArgs
       c.S[lane] = S;
     }
     if (it + 1 < it_end)
-      stage_tile<T, kCh, kSt, VEC>(ring((it + 1 - it_begin) & 1), a, gu, gdl, gdo, gz, gB, gC, b, d0, t0 + kTB, lane);
+      stage_tile<T, kCh, kSt, VEC>(ring((it + 1 - it_begin) & 1), a, gu, gdl, gdo_s, gz_s, gB, gC_s, b, d0, t0 + kTB,
+                                   lane);
     cp_async_commit();
     cp_async_wait<1>();
     __syncwarp();  // (A) this tile's rows have landed for every lane; every lane is done with BC
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(kW, 16) scan_bwd_ckpt_kernel(const ScanBwdArgs
         const float Dl = a.delta_softplus ? softplus_f<PRECISE>(v) : v;
         x[s] = in ? Dl * kLog2e : 0.f;
         du[s] = in ? Dl * uv[s] : 0.f;
-        if (ADJ) dy[s] = in ? (gz ? dov[s] * silu_f(zv[s]) : dov[s]) : 0.f;
+        if (ADJ) dy[s] = (in && adj) ? (gz ? dov[s] * silu_f(zv[s]) : dov[s]) : 0.f;
       }
       // B (and C) rows, transposed to [step][state] (C at 16 + n)
       if (lane < kSt * kNS) {
@@ -235,8 +245,12 @@ __global__ void __launch_bounds__(kW, 16) scan_bwd_ckpt_kernel(const ScanBwdArgs
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int k = 2 * k4 + i;
-          h[k] = ffma2(ex2x2(fmul2(f2(x[s]), An[k])), h[k], fmul2(f2(du[s]), Bv[i]));
-          if (ADJ) g[k] = ffma2(ex2x2(fmul2(f2(S), An[k])), fmul2(Cv[i], f2(dy[s])), g[k]);
+          const float2 e = ex2x2(fmul2(f2(x[s]), An[k]));
+          h[k] = ffma2(e, h[k], fmul2(f2(du[s]), Bv[i]));
+          if (ADJ) {
+            P[k] = fmul2(P[k], e);
+            g[k] = ffma2(P[k], fmul2(Cv[i], f2(dy[s])), g[k]);
+          }
         }
       }
     }
@@ -589,58 +603,65 @@ __global__ void __launch_bounds__(kW, 12) scan_bwd_kernel(const ScanBwdArgs a) {
 }
 
 // ---------------------------------------------------------------- reduction
-// Blocks [0, nbc): dB, dC [b, n, t] for 32 steps of one sequence, summed over the channel tiles
-// in order (one warp reads one step's row of 32 sums per tile), transposed through shared
-// memory so that each (n) row segment is written whole. The other blocks: dA [d, n], dD [d],
-// ddelta_bias [d], summed over chunks and sequences in order, one thread per output.
+// Blocks [0, nbc): dB, dC [b, n, t] for 8 steps of one sequence (one warp per step, lane v for
+// sum v of the step's 32), summed over the channel tiles in order, 8 tiles' loads in flight at
+// a time; written through shared memory as 8-step row pieces. The other blocks: dA [d, n],
+// dD [d], ddelta_bias [d], summed over chunks and sequences in order, one thread per output.
 constexpr int kRedThreads = 256;
+constexpr int kRedSteps = kRedThreads / 32;
+
+__device__ __forceinline__ float sum_strided(const float* src, long long stride, int n) {
+  float acc = 0.f;
+  int i = 0;
+  for (; i + 8 <= n; i += 8) {
+    float r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) r[j] = src[(i + j) * stride];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc += r[j];
+  }
+  for (; i < n; ++i) acc += src[i * stride];
+  return acc;
+}
 
 __global__ void __launch_bounds__(kRedThreads) scan_bwd_reduce_kernel(const ScanBwdArgs a, int ndt, int nbc) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[kRedSteps][33];
   const int L = a.seqlen, N = a.dstate;
   if ((int)blockIdx.x < nbc) {
-    const int tblocks = (L + 31) / 32;
+    const int tblocks = (L + kRedSteps - 1) / kRedSteps;
     const int b = blockIdx.x / tblocks, tb = blockIdx.x % tblocks;
     const int w = threadIdx.x / 32, v = threadIdx.x % 32;
-    const long long nws = (long long)a.batch * ndt * L * (2 * kNS);
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int dt = 0; dt < ndt; ++dt) {
-      const long long row0 = ((long long)b * ndt + dt) * L;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = tb * 32 + w + 8 * i;
-        const long long idx = (row0 + t) * (2 * kNS) + v;
-        if (t < L && in_bounds(idx, 1, nws, kBoundsBackward)) s[i] += a.ws_dBC[idx];
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tile[w + 8 * i][v] = s[i];
+    const int t = tb * kRedSteps + w;
+    const long long stride = (long long)L * (2 * kNS);
+    const long long first = ((long long)b * ndt * L + t) * (2 * kNS) + v;
+    const long long nws = (long long)a.batch * ndt * stride;
+    float acc = 0.f;
+    if (t < L && in_bounds(first, 1, nws, kBoundsBackward) &&
+        in_bounds(first + (ndt - 1) * stride, 1, nws, kBoundsBackward))
+      acc = sum_strided(a.ws_dBC + first, stride, ndt);
+    tile[w][v] = acc;
     __syncthreads();
-    for (int o = threadIdx.x; o < 32 * 32; o += kRedThreads) {
-      const int vv = o / 32, tt = o % 32, t = tb * 32 + tt, n = vv % kNS;
-      if (t < L && n < N) (vv < kNS ? a.dB : a.dC)[((long long)b * N + n) * L + t] = tile[tt][vv];
+    {
+      const int vv = threadIdx.x / kRedSteps, tt = threadIdx.x % kRedSteps, t2 = tb * kRedSteps + tt;
+      const int n = vv % kNS;
+      if (t2 < L && n < N) (vv < kNS ? a.dB : a.dC)[((long long)b * N + n) * L + t2] = tile[tt][vv];
     }
     return;
   }
   const long long nA = (long long)a.dim * N;
   const long long total = nA + 2LL * a.dim;
-  const long long QB = (long long)a.nchunks * a.batch;
+  const int QB = a.nchunks * a.batch;
   for (long long i = (blockIdx.x - nbc) * (long long)kRedThreads + threadIdx.x; i < total;
        i += (long long)(gridDim.x - nbc) * kRedThreads) {
     if (i < nA) {
       const long long dd = i / N, n = i % N;
-      float s = 0.f;
-      for (long long qb = 0; qb < QB; ++qb) s += a.ws_dA[(qb * a.dim + dd) * kNS + n];
-      a.dA[i] = s;
+      a.dA[i] = sum_strided(a.ws_dA + dd * kNS + n, (long long)a.dim * kNS, QB);
     } else {
       const long long j = i - nA;
       const bool isBias = j >= a.dim;
       const long long dd = isBias ? j - a.dim : j;
-      const float* src = isBias ? a.ws_dbias : a.ws_dD;
-      float s = 0.f;
-      for (long long qb = 0; qb < QB; ++qb) s += src[qb * a.dim + dd];
       float* dst = isBias ? a.ddelta_bias : a.dD;
-      if (dst) dst[dd] = s;
+      if (dst) dst[dd] = sum_strided((isBias ? a.ws_dbias : a.ws_dD) + dd, a.dim, QB);
     }
   }
 }
@@ -686,7 +707,7 @@ cudaError_t launch_bwd_t(const ScanBwdArgs& a, cudaStream_t stream) {
   scan_bwd_kernel<T, VEC><<<grid, kW, RevSmem<T>::bytes, stream>>>(a);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const long long nbc = (long long)a.batch * ((a.seqlen + 31) / 32);
+  const long long nbc = (long long)a.batch * ((a.seqlen + kRedSteps - 1) / kRedSteps);
   long long np = ((long long)a.dim * (a.dstate + 2) + kRedThreads - 1) / kRedThreads;
   if (np > 148 * 4) np = 148 * 4;
   if (np < 1) np = 1;

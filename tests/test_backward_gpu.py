@@ -2,11 +2,16 @@
 adjoint, gradient by gradient, on seeded problems that span several channel tiles, several
 16-step tiles, ragged tails and the optional terms.
 
-Gradients are sums (over time, channels or sequences) whose terms can cancel, so each element
-is compared as |gpu - oracle| <= rtol |oracle| + atol * scale, scale = the largest magnitude in
-that gradient tensor: fp32 I/O rtol 1e-4 / atol 1e-5, bf16 I/O (du, ddelta, dz rounded to bf16)
-rtol 2e-2 / atol 1e-2, the scan's own bounds applied to the tensor's scale.
+Every element of every gradient is held to the scan's own per-element bounds,
+|gpu - oracle| <= rtol |oracle| + atol: fp32 I/O rtol 1e-4 / atol 1e-5, bf16 I/O (du, ddelta, dz
+rounded to bf16) rtol 2e-2 / atol 1e-2. With SSM_GRAD_REPORT set to a file path, each comparison
+appends one JSON line with the largest ratio err / (rtol |oracle| + atol), and the same ratio
+with atol scaled by the tensor's largest magnitude (the looser criterion sums with
+cancellation would otherwise need).
 """
+
+import json
+import os
 
 import numpy as np
 import pytest
@@ -29,11 +34,25 @@ def _assert_grad(got, ref, io, what):
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     scale = max(float(np.abs(ref).max()) if ref.size else 0.0, 1e-30)
     err = np.abs(got - ref)
-    bad = err > rtol * np.abs(ref) + atol * scale
+    _report(what, io, err, ref, rtol, atol, scale)
+    bad = err > rtol * np.abs(ref) + atol
     if bad.any():
         i = tuple(np.argwhere(bad)[0])
         raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside; first at {i}: gpu={got[i]!r} "
-                             f"oracle={ref[i]!r}; max err {err.max():.3e}, scale {scale:.3e}")
+                             f"oracle={ref[i]!r}; max err {err.max():.3e}")
+
+
+def _report(what, io, err, ref, rtol, atol, scale):
+    """Per-element figures against rtol |ref| + atol, appended to $SSM_GRAD_REPORT if set."""
+    path = os.environ.get("SSM_GRAD_REPORT")
+    if not path or err.size == 0:
+        return
+    ratio = err / (rtol * np.abs(ref) + atol)
+    rec = {"grad": what, "io": io, "n": int(err.size), "within_elem": float(np.mean(ratio <= 1.0)),
+           "max_ratio_elem": float(ratio.max()), "max_err": float(err.max()), "scale": scale,
+           "max_ratio_scaled": float((err / (rtol * np.abs(ref) + atol * scale)).max())}
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
 
 
 def _problem(batch, dim, L, N, io, seed, with_z=True, with_D=True, with_bias=True, with_h0=True):
