@@ -393,11 +393,13 @@ SSM_API ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, co
  * Range checks of the debug build.
  *
  * libssm_debug.so is this library compiled with SSM_DEBUG_BOUNDS: before each global-memory
- * access of the scan (main, carry, segment aggregate and composition), decode, conv and scan
- * backward kernels, the element range it touches is tested against the size of its tensor, as
- * the call's arguments give them. An access outside its tensor is skipped (a load reads zero)
- * and sets a bit of a device error word; nothing traps. Bits: 1 scan, 2 decode, 4 conv,
- * 8 segment aggregate / composition, 16 scan backward.
+ * access of the scan (main, carry, segment aggregate and composition), decode, conv (forward
+ * and backward), scan backward and state-space-duality kernels, the element range it touches
+ * is tested against the size of its tensor, as the call's arguments give them (the duality
+ * kernel's bulk tensor copies are clipped by their tensor maps instead). An access outside its
+ * tensor is skipped (a load reads zero) and sets a bit of a device error word; nothing traps.
+ * Bits: 1 scan, 2 decode, 4 conv, 8 segment aggregate / composition, 16 scan backward,
+ * 32 state-space duality.
  *
  * ssm_debug_bounds_status synchronises the device (a blocking copy from the word), stores the
  * word's bits in *flags_out and, when clear is 1, resets them to zero. It returns

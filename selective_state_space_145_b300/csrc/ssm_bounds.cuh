@@ -15,9 +15,10 @@ namespace ssm {
 // Bits of the error word, one per kernel family.
 constexpr unsigned kBoundsScan = 1u;       // scan main and carry passes
 constexpr unsigned kBoundsDecode = 2u;     // decode state update
-constexpr unsigned kBoundsConv = 4u;       // standalone causal conv
+constexpr unsigned kBoundsConv = 4u;       // standalone causal conv, forward and backward
 constexpr unsigned kBoundsSegment = 8u;    // segment aggregate fold and composition
 constexpr unsigned kBoundsBackward = 16u;  // scan backward: checkpoint, reverse and reduction kernels
+constexpr unsigned kBoundsSsd = 32u;       // state-space-duality layer (its plain copies and stores)
 
 // [first, first + count) lies within [0, extent).
 __host__ __device__ constexpr bool range_ok(long long first, long long count, long long extent) {

@@ -18,6 +18,7 @@
 // the dw / dbias terms of its own 4 steps; the block reduces them and writes one partial, and
 // a second kernel sums the partials over sequences and segments in a fixed order. The conv
 // taps are zero-padded to 4 (w[4-K+k] holds tap k).
+#include "ssm_bounds.cuh"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -45,6 +46,15 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
   const T* __restrict__ x = static_cast<const T*>(a.x) + c * L;
   const T* __restrict__ dout = static_cast<const T*>(a.dout) + c * L;
   const T* win = a.conv_init ? static_cast<const T*>(a.conv_init) + c * (K - 1) : nullptr;
+  // debug build: the block's row, window row, taps and partial slot lie inside their tensors
+  // (the test is uniform over the block, so a skipped block skips its barriers as a whole)
+  {
+    const long long rows = (long long)a.batch * a.dim;
+    if (!in_bounds(c * L, L, rows * L, kBoundsConv) || !in_bounds((long long)d * K, K, (long long)a.dim * K, kBoundsConv) ||
+        !in_bounds(c * (K - 1), K - 1, rows * (K - 1), kBoundsConv) ||
+        !in_bounds(((long long)c * nseg + seg) * kCBPart, kCBPart, rows * nseg * kCBPart, kBoundsConv))
+      return;
+  }
 
   float wp[kMaxConv];
 #pragma unroll
@@ -184,8 +194,12 @@ __global__ void conv_bwd_reduce_kernel(const ConvBwdArgs a, int nseg) {
     const int d = i / (K + 1), k = i % (K + 1);
     const int slot = k < K ? kMaxConv - K + k : kMaxConv;  // padded tap, or dbias
     float s = 0.f;
+    const long long nparts = (long long)a.batch * a.dim * nseg * kCBPart;
     for (int b = 0; b < a.batch; ++b)
-      for (int g = 0; g < nseg; ++g) s += a.ws_part[(((long long)b * a.dim + d) * nseg + g) * kCBPart + slot];
+      for (int g = 0; g < nseg; ++g) {
+        const long long j = (((long long)b * a.dim + d) * nseg + g) * kCBPart + slot;
+        if (in_bounds(j, 1, nparts, kBoundsConv)) s += a.ws_part[j];
+      }
     if (k < K) a.dw[(long long)d * K + k] = s;
     else if (a.dbias) a.dbias[d] = s;
   }
@@ -221,6 +235,16 @@ size_t conv_bwd_workspace_bytes(int batch, int dim, int seqlen) {
 cudaError_t launch_conv_bwd(const ConvBwdArgs& a, cudaStream_t stream) {
   if (a.bf16) return launch_conv_bwd_t<__nv_bfloat16>(a, stream);
   return launch_conv_bwd_t<float>(a, stream);
+}
+
+cudaError_t conv_bwd_bounds_flags(unsigned* out, bool clear) {
+#ifdef SSM_DEBUG_BOUNDS
+  return bounds_flags_read(out, clear);
+#else
+  (void)out;
+  (void)clear;
+  return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace ssm

@@ -198,5 +198,7 @@ cudaError_t scan_bounds_flags(unsigned* out, bool clear);
 cudaError_t decode_bounds_flags(unsigned* out, bool clear);
 cudaError_t conv_bounds_flags(unsigned* out, bool clear);
 cudaError_t scan_bwd_bounds_flags(unsigned* out, bool clear);
+cudaError_t conv_bwd_bounds_flags(unsigned* out, bool clear);
+cudaError_t ssd_bounds_flags(unsigned* out, bool clear);
 
 }  // namespace ssm

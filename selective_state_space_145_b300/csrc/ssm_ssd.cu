@@ -40,6 +40,7 @@
 #include <cuda_bf16.h>
 
 #include "../../include/ssm.h"
+#include "ssm_bounds.cuh"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 #include "ssm_umma.cuh"
@@ -142,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* sX = sm + Smem::X;
   unsigned char* sH = sm + Smem::H;
   unsigned char* sHL = sm + Smem::HL;
+  // element counts for the range checks of the debug build (the TMA copies are clipped by their
+  // tensor maps instead)
+  const long long nCB = (long long)a.batch * L * kN, nX = (long long)a.batch * L * H * kP;
+  const long long nDt = (long long)a.batch * L * H, nSt = (long long)a.batch * H * kP * kN;
   const float A2 = a.A[h] * kLog2e;
   const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
   const float Dh = a.D ? a.D[h] : 0.f;
@@ -169,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int k = 0; k < kQ * kN / 8 / kThreads; ++k) {
       const int srow = tid / 16 + 16 * k;
-      const bool ok = srow < len;
       const long long g = cbg + (long long)k * 16 * kN;
+      const bool ok = srow < len && in_bounds(g, 8, nCB, kBoundsSsd);
       const uint32_t off = (uint32_t)(cch >> 3) * kSlab + umma::sw128_off(srow, cch & 7);
       cp_async16(sC + off, ok ? (const void*)(gC + g) : (const void*)gC, ok ? 16u : 0u);
       cp_async16(sB + off, ok ? (const void*)(gB + g) : (const void*)gB, ok ? 16u : 0u);
@@ -179,22 +184,25 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int k = 0; k < kQ * kP / 8 / kThreads; ++k) {
       const int srow = tid / 8 + 32 * k;
-      const bool ok = srow < len;
       const long long g = xg + (long long)k * 32 * H * kP;
+      const bool ok = srow < len && in_bounds(g, 8, nX, kBoundsSsd);
       cp_async16(sX + umma::sw128_off(srow, tid % 8), ok ? (const void*)(gx + g) : (const void*)gx, ok ? 16u : 0u);
     }
     cp_async_commit();
   };
   auto load_dt = [&](int q) -> float {
     const int s = q * kQ + t;
-    return s < L ? to_f32(gdt[((long long)b * L + s) * H + h]) : 0.f;
+    const long long i = ((long long)b * L + s) * H + h;
+    return (s < L && in_bounds(i, 1, nDt, kBoundsSsd)) ? to_f32(gdt[i]) : 0.f;
   };
 
   // running state: row n = t of H [N x P], columns pb .. pb + 31, fp32
   const int pb = half * kHalfP;
   float Hs[kHalfP];
+  // this thread's state elements: (bh, p, t) for p = pb .. pb + 31, stride kN
+  const bool st_ok = in_bounds((bh * kP + pb) * kN + t, (long long)(kHalfP - 1) * kN + 1, nSt, kBoundsSsd);
 #pragma unroll
-  for (int p = 0; p < kHalfP; ++p) Hs[p] = a.h0 ? a.h0[(bh * kP + pb + p) * kN + t] : 0.f;
+  for (int p = 0; p < kHalfP; ++p) Hs[p] = (a.h0 && st_ok) ? a.h0[(bh * kP + pb + p) * kN + t] : 0.f;
   // its bf16 hi / lo operand tiles (element (p, n) of the B operand of Y_off)
   auto write_state = [&]() {
 #pragma unroll
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         yd[j] = fmaf(et, yo[j], yd[j]) + Dh * xv[j];
         Hs[p0 + j] = fmaf(dec, Hs[p0 + j], sv[j]);
       }
-      if (t < len) {
+      if (t < len && in_bounds((((long long)b * L + t0 + t) * H + h) * kP + pb + p0, 16, nX, kBoundsSsd)) {
         *reinterpret_cast<uint4*>(yrow + pb + p0) = pack8(yd);
         *reinterpret_cast<uint4*>(yrow + pb + p0 + 8) = pack8(yd + 8);
       }
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (!ok) {
     if (tid == 0) atomicExch(a.ws_status, 1);
-  } else if (a.h_last) {
+  } else if (a.h_last && st_ok) {
 #pragma unroll
     for (int p = 0; p < kHalfP; ++p) a.h_last[(bh * kP + pb + p) * kN + t] = Hs[p];
   }
@@ -528,6 +536,16 @@ cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t stream) {
     ssd_fused_kernel<false><<<grid, kThreads, Smem::bytes, stream>>>(a, mC, mC, mC, skip_mma);
   }
   return cudaGetLastError();
+}
+
+cudaError_t ssd_bounds_flags(unsigned* out, bool clear) {
+#ifdef SSM_DEBUG_BOUNDS
+  return bounds_flags_read(out, clear);
+#else
+  (void)out;
+  (void)clear;
+  return cudaErrorNotSupported;
+#endif
 }
 
 }  // namespace ssm

@@ -40,7 +40,7 @@ EXPORTS = ("ssm_version", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_sca
            "ssm_scan_compose", "ssm_debug_bounds_status")
 
 # Bits of the debug build's error word (include/ssm.h).
-BOUNDS_SCAN, BOUNDS_DECODE, BOUNDS_CONV, BOUNDS_SEGMENT, BOUNDS_BACKWARD = 1, 2, 4, 8, 16
+BOUNDS_SCAN, BOUNDS_DECODE, BOUNDS_CONV, BOUNDS_SEGMENT, BOUNDS_BACKWARD, BOUNDS_SSD = 1, 2, 4, 8, 16, 32
 
 # Bytes of the fixed device scratch array ssm_selective_scan_fwd_noalloc uses (include/ssm.h).
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024

@@ -1,6 +1,6 @@
 """The small odd-shape parity cases again, through libssm_debug.so: the library compiled with
-SSM_DEBUG_BOUNDS, in which every checked global access of the scan, segment, decode, conv and
-scan-backward kernels is range-tested against its tensor and an access outside it sets a bit of a device
+SSM_DEBUG_BOUNDS, in which every checked global access of the scan, segment, decode, conv
+(forward and backward), scan-backward and state-space-duality kernels is range-tested against its tensor and an access outside it sets a bit of a device
 error word instead of touching memory.
 
 Each case must still match the fp64 oracle (the checks skip nothing on a correct call) and must
@@ -12,6 +12,7 @@ import pytest
 import test_backward_gpu as bwd
 import test_parity_gpu as par
 import test_shard_gpu as seg
+import test_ssd_gpu as ssd
 
 pytestmark = pytest.mark.gpu
 
@@ -94,3 +95,15 @@ def test_debug_backward_chunked(debug_lib, cuda_device):
     bwd.test_backward_chunked_long(cuda_device, "bf16")
     bwd.test_backward_empty_sequence(cuda_device)
     _clean(debug_lib, "scan backward, chunked / empty")
+
+
+@pytest.mark.parametrize("case", bwd.CONV_CASES, ids=lambda c: "b{}_d{}_l{}_k{}_{}_win{}_silu{}".format(*c))
+def test_debug_conv_backward(debug_lib, cuda_device, case):
+    bwd.test_conv_backward_matches_oracle(cuda_device, case)
+    _clean(debug_lib, "conv backward")
+
+
+@pytest.mark.parametrize("case", ssd.CASES, ids=lambda c: "b{}_l{}_h{}_h0{}".format(*c))
+def test_debug_ssd(debug_lib, cuda_device, case):
+    ssd.test_ssd_matches_oracle(cuda_device, case)
+    _clean(debug_lib, "state-space duality")
