@@ -9,14 +9,15 @@
 //   dx[s] = sum_k w[k] dacc_{s+(K-1)-k};  dwindow likewise for s < 0
 //   dw[d,k] = sum_{b,t} dacc_t xs(t-(K-1)+k);  dbias[d] = sum_{b,t} dacc_t.
 //
-// Design. A block takes 1024 consecutive steps of one row; one thread owns 4 of them. The
-// block stages x at its steps (plus a 4-step halo on each side) and then dacc at its steps
-// (plus the 3 that follow) in shared memory, so every activation is computed once: thread i
-// computes acc and dacc at its own 4 steps, and one thread adds the 3 steps past the block.
-// dx at a step takes the 4 dacc values that reach it from the staged row. Rows whose length is
-// a multiple of 4 at aligned addresses move 4 elements per load and store. Each thread adds
-// the dw / dbias terms of its own 4 steps; the block reduces them and writes one partial, and
-// a second kernel sums the partials over sequences and segments in a fixed order. The conv
+// Design. A block takes 1024 consecutive steps of one row; one thread owns 16 bytes of each
+// input row: 8 steps (bf16, 128 threads) or 4 (fp32, 256 threads). The block stages x at its
+// steps (plus a 4-step halo on each side) and then dacc at its steps (plus the 3 that follow)
+// in shared memory, so every activation is computed once: each thread computes acc and dacc at
+// its own steps, and one thread adds the 3 steps past the block. dx at a step takes the 4 dacc
+// values that reach it from the staged row. Rows whose length is a multiple of the thread's
+// steps at 16-byte aligned addresses move them with one 16-byte load or store. Each thread
+// adds the dw / dbias terms of its own steps; the block reduces them and writes one partial,
+// and a second kernel sums the partials over sequences and segments in a fixed order. The conv
 // taps are zero-padded to 4 (w[4-K+k] holds tap k).
 #include "ssm_bounds.cuh"
 #include "ssm_device.cuh"
@@ -25,14 +26,22 @@
 namespace ssm {
 namespace {
 
-constexpr int kCBThreads = 256;
-constexpr int kCBSeg = kCBThreads * 4;   // steps per block
+constexpr int kCBSeg = 1024;             // steps per block
+constexpr int kCBMaxThreads = 256;
 constexpr int kCBPart = kMaxConv + 1;    // partial: dw taps (padded) + dbias
 static_assert(kMaxConv == 4, "the staged halos hold 4 steps");
 
-// VEC: the row length is a multiple of 4 and x, dout, dx are aligned to 4 elements.
+template <typename T>
+struct CBGeo {
+  static constexpr int kSpt = 16 / (int)sizeof(T);   // steps per thread: one 16-byte piece
+  static constexpr int kThreads = kCBSeg / kSpt;
+};
+
+// VEC: the row length is a multiple of the thread's steps and x, dout, dx are 16-byte aligned.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs a, int nseg) {
+__global__ void __launch_bounds__(kCBMaxThreads) conv_bwd_kernel(const ConvBwdArgs a, int nseg) {
+  constexpr int kCBSpt = CBGeo<T>::kSpt;
+  constexpr int kCBThreads = CBGeo<T>::kThreads;
   __shared__ float red[kCBThreads / 32][kCBPart];
   __shared__ __align__(16) float sx[kCBSeg + 8];   // x at steps base-4 .. base+kCBSeg+3
   __shared__ __align__(16) float sda[kCBSeg + 4];  // dacc at steps base .. base+kCBSeg+3
@@ -42,7 +51,7 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
   const int d = (int)(c % a.dim);
   const int tid = threadIdx.x;
   const int base = seg * kCBSeg;
-  const int s0 = base + tid * 4;                  // this thread's 4 steps
+  const int s0 = base + tid * kCBSpt;             // this thread's steps
   const T* __restrict__ x = static_cast<const T*>(a.x) + c * L;
   const T* __restrict__ dout = static_cast<const T*>(a.dout) + c * L;
   const T* win = a.conv_init ? static_cast<const T*>(a.conv_init) + c * (K - 1) : nullptr;
@@ -82,35 +91,44 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
   };
 
   // ---- stage x; own steps from registers, the halos from one warp
-  float xo[4], go[4];
+  float xo[kCBSpt], go[kCBSpt];
   if (VEC && s0 < L) {
-    load4(x + s0, xo);
-    load4(dout + s0, go);
+    if constexpr (kCBSpt == 8) {
+      load8(x + s0, xo);
+      load8(dout + s0, go);
+    } else {
+      load4(x + s0, xo);
+      load4(dout + s0, go);
+    }
   } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kCBSpt; ++j) {
       const bool in = s0 + j < L;
       xo[j] = in ? to_f32(x[s0 + j]) : 0.f;
       go[j] = in ? to_f32(dout[s0 + j]) : 0.f;
     }
   }
-  *reinterpret_cast<float4*>(&sx[4 + 4 * tid]) = make_float4(xo[0], xo[1], xo[2], xo[3]);
+#pragma unroll
+  for (int j = 0; j < kCBSpt; j += 4)
+    *reinterpret_cast<float4*>(&sx[4 + kCBSpt * tid + j]) = make_float4(xo[j], xo[j + 1], xo[j + 2], xo[j + 3]);
   if (tid < 4) sx[tid] = xs(base - 4 + tid);
   else if (tid < 8) sx[kCBSeg + tid] = xs(base + kCBSeg + tid - 4);
   __syncthreads();
 
-  // ---- dacc at the own steps; x at s0-4 .. s0+3 is sx[4 tid .. 4 tid + 7]
-  float xv[8];
+  // ---- dacc at the own steps; x at s0-4 .. s0-1 is sx[kCBSpt tid .. kCBSpt tid + 3]
+  float xv[kCBSpt + 4];
   {
-    const float4 p = *reinterpret_cast<const float4*>(&sx[4 * tid]);
+    const float4 p = *reinterpret_cast<const float4*>(&sx[kCBSpt * tid]);
     xv[0] = p.x; xv[1] = p.y; xv[2] = p.z; xv[3] = p.w;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) xv[4 + j] = xo[j];
+    for (int j = 0; j < kCBSpt; ++j) xv[4 + j] = xo[j];
   }
-  float da[4];
+  float da[kCBSpt];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) da[j] = dacc(s0 + j, xv + j + 1, go[j]);
-  *reinterpret_cast<float4*>(&sda[4 * tid]) = make_float4(da[0], da[1], da[2], da[3]);
+  for (int j = 0; j < kCBSpt; ++j) da[j] = dacc(s0 + j, xv + j + 1, go[j]);
+#pragma unroll
+  for (int j = 0; j < kCBSpt; j += 4)
+    *reinterpret_cast<float4*>(&sda[kCBSpt * tid + j]) = make_float4(da[j], da[j + 1], da[j + 2], da[j + 3]);
   if (tid == kCBThreads - 1) {
     // the 3 steps past the block reach its last dx values
 #pragma unroll
@@ -122,17 +140,17 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
   }
   __syncthreads();
 
-  // ---- dx at the own steps: dx[s] = sum_i wp[i] dacc_{s+3-i}; dacc at s0 .. s0+6
-  float dn[8];
+  // ---- dx at the own steps: dx[s] = sum_i wp[i] dacc_{s+3-i}; dacc at s0 .. s0+kCBSpt+2
+  float dn[kCBSpt + 4];
   {
-    const float4 q = *reinterpret_cast<const float4*>(&sda[4 * tid + 4]);
+    const float4 q = *reinterpret_cast<const float4*>(&sda[kCBSpt * tid + kCBSpt]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dn[j] = da[j];
-    dn[4] = q.x; dn[5] = q.y; dn[6] = q.z; dn[7] = q.w;
+    for (int j = 0; j < kCBSpt; ++j) dn[j] = da[j];
+    dn[kCBSpt] = q.x; dn[kCBSpt + 1] = q.y; dn[kCBSpt + 2] = q.z; dn[kCBSpt + 3] = q.w;
   }
-  float dxv[4];
+  float dxv[kCBSpt];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < kCBSpt; ++j) {
     float v = 0.f;
 #pragma unroll
     for (int i = 0; i < kMaxConv; ++i) v = fmaf(wp[i], dn[j + 3 - i], v);
@@ -140,10 +158,14 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
   }
   T* dx = static_cast<T*>(a.dx) + c * L;
   if (VEC && s0 < L) {
-    store4(dx + s0, dxv);
+    if constexpr (kCBSpt == 8) {
+      store8(dx + s0, dxv);
+    } else {
+      store4(dx + s0, dxv);
+    }
   } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < kCBSpt; ++j)
       if (s0 + j < L) dx[s0 + j] = from_f32<T>(dxv[j]);
   }
   // window gradient: positions -(K-1) .. -1, reached by dacc_0 .. dacc_{K-2}
@@ -160,12 +182,12 @@ __global__ void __launch_bounds__(kCBThreads) conv_bwd_kernel(const ConvBwdArgs 
       dw_out[j] = from_f32<T>(v);
     }
   }
-  // this thread's dw / dbias terms (its own 4 steps only)
+  // this thread's dw / dbias terms (its own 8 steps only)
   float part[kCBPart];
 #pragma unroll
   for (int i = 0; i < kCBPart; ++i) part[i] = 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < kCBSpt; ++j) {
 #pragma unroll
     for (int i = 0; i < kMaxConv; ++i) part[i] = fmaf(da[j], xv[j + 1 + i], part[i]);
     part[kMaxConv] += da[j];
@@ -210,13 +232,13 @@ cudaError_t launch_conv_bwd_t(const ConvBwdArgs& a, cudaStream_t stream) {
   const int nseg = (a.seqlen + kCBSeg - 1) / kCBSeg;
   const long long blocks = (long long)a.batch * a.dim * nseg;
   if (blocks > 0) {
-    const uintptr_t vb = 4 * sizeof(T);
-    const bool vec = a.seqlen % 4 == 0 && reinterpret_cast<uintptr_t>(a.x) % vb == 0 &&
+    const uintptr_t vb = 16;
+    const bool vec = a.seqlen % CBGeo<T>::kSpt == 0 && reinterpret_cast<uintptr_t>(a.x) % vb == 0 &&
                      reinterpret_cast<uintptr_t>(a.dout) % vb == 0 && reinterpret_cast<uintptr_t>(a.dx) % vb == 0;
     if (vec)
-      conv_bwd_kernel<T, true><<<(unsigned)blocks, kCBThreads, 0, stream>>>(a, nseg);
+      conv_bwd_kernel<T, true><<<(unsigned)blocks, CBGeo<T>::kThreads, 0, stream>>>(a, nseg);
     else
-      conv_bwd_kernel<T, false><<<(unsigned)blocks, kCBThreads, 0, stream>>>(a, nseg);
+      conv_bwd_kernel<T, false><<<(unsigned)blocks, CBGeo<T>::kThreads, 0, stream>>>(a, nseg);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
