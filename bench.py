@@ -371,14 +371,14 @@ def run_reference(args, w):
             "ms_per_step_basis": "one whole step of the workload at the oracle's sampled rate",
             "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, args.reverse, args.zoh),
+            "config": config_of(w, args.reverse, args.zoh, s4d_real=args.s4d_real),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def config_of(w, reverse: bool = False, zoh: bool = False, eager: bool = False):
+def config_of(w, reverse: bool = False, zoh: bool = False, eager: bool = False, s4d_real: bool = False):
     c = {"workload": w.name, "kind": w.kind, "io": w.io, "batch": w.batch, "d_inner": w.dim, "seqlen": w.seqlen,
          "d_state": w.dstate, "d_conv": w.d_conv, "l2": "flushed before every timed step (256 MiB write)",
          "launch": "direct library calls" if eager else "the step's library calls replayed from one CUDA graph"}
@@ -386,6 +386,9 @@ def config_of(w, reverse: bool = False, zoh: bool = False, eager: bool = False):
         c["direction"] = "backward (SSM_SCAN_REVERSE)"
     if zoh:
         c["discretisation"] = "zero-order hold (SSM_SCAN_ZOH)"
+    if s4d_real:
+        c["a_structure"] = ("opt-in S4D-real path (SSM_SCAN_S4D_REAL): Abar_n = Abar_0^(n+1), valid because the "
+                            "workload's A is -(n+1); not the generic measurement")
     if w.d_model:
         c.update({"d_model": w.d_model, "expand": w.expand})
     if w.kind == "decode":
@@ -448,10 +451,11 @@ def run_gpu(args, w):
             ssm.ssm_selective_scan_fwd(g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"],
                                        True, g["conv_w"], g["conv_b"], None, None, workspace=ws, out=out,
                                        h_last=h_last, chunk_len=args.chunk_len, reverse=args.reverse,
-                                       zoh=args.zoh)
+                                       zoh=args.zoh, s4d_real=args.s4d_real)
 
         launches_per_step = 2 if nchunks > 1 else 1
-        kernels = ["scan_carry_kernel", "scan_main_kernel"] if nchunks > 1 else ["scan_main_kernel"]
+        main = "scan_main1_kernel or scan_main_kernel (the plan's main pass)"
+        kernels = ["scan_carry_kernel", main] if nchunks > 1 else [main]
         if not args.eager:
             step = _as_graph(step, dev)
 
@@ -536,7 +540,8 @@ def run_gpu(args, w):
                 ssm.ssm_selective_scan_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
                                            d["delta_bias"], True, d["conv_w"], d["conv_b"], None, None,
                                            workspace=ws, out=o["out"], h_last=o["h_last"],
-                                           chunk_len=args.chunk_len, reverse=args.reverse, zoh=args.zoh)
+                                           chunk_len=args.chunk_len, reverse=args.reverse, zoh=args.zoh,
+                                           s4d_real=args.s4d_real)
 
             def download(k):
                 hopacks[k].buf.copy_(opacks[k].buf, non_blocking=True)
@@ -591,7 +596,7 @@ def run_gpu(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": config_of(w, args.reverse, args.zoh, args.eager),
+        "config": config_of(w, args.reverse, args.zoh, args.eager, args.s4d_real),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profiles(w.name, w.kind), "peak_source": peak_kind,
@@ -997,6 +1002,8 @@ def main(argv=None):
                     help="scan chunk length (0 = the library's default policy)")
     ap.add_argument("--reverse", action="store_true", help="time the backward scan (SSM_SCAN_REVERSE)")
     ap.add_argument("--zoh", action="store_true", help="zero-order-hold discretisation (SSM_SCAN_ZOH)")
+    ap.add_argument("--s4d-real", action="store_true",
+                    help="the opt-in S4D-real path (SSM_SCAN_S4D_REAL); labelled in config, never the default")
     ap.add_argument("--backward", action="store_true", help="time the scan's backward pass")
     ap.add_argument("--eager", action="store_true",
                     help="time direct library calls instead of replaying the step from a CUDA graph")
@@ -1008,8 +1015,9 @@ def main(argv=None):
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     if args.workload in inputs.SSD_WORKLOADS:
         w = inputs.SSD_WORKLOADS[args.workload]
-        if args.reverse or args.zoh or args.backward or args.chunk_len:
-            ap.error("the state-space-duality workload takes none of --reverse, --zoh, --backward, --chunk-len")
+        if args.reverse or args.zoh or args.backward or args.chunk_len or args.s4d_real:
+            ap.error("the state-space-duality workload takes none of --reverse, --zoh, --backward, --chunk-len, "
+                     "--s4d-real")
         if args.seqlen is not None or args.batch is not None:
             w = dataclasses.replace(w, seqlen=args.seqlen if args.seqlen is not None else w.seqlen,
                                     batch=args.batch if args.batch is not None else w.batch)
@@ -1018,6 +1026,8 @@ def main(argv=None):
     w = inputs.WORKLOADS[args.workload]
     if args.reverse and w.kind != "scan":
         ap.error("--reverse applies to the scan workloads only")
+    if args.s4d_real and (w.kind != "scan" or args.backward):
+        ap.error("--s4d-real applies to the forward scan workloads only")
     if args.seqlen is not None or args.batch is not None:
         w = dataclasses.replace(w, seqlen=args.seqlen if args.seqlen is not None else w.seqlen,
                                 batch=args.batch if args.batch is not None else w.batch)

@@ -10,6 +10,9 @@ from .ssm import (  # noqa: F401
     DEBUG_LIB_PATH,
     EXPORTS,
     LIB_PATH,
+    SCAN_REVERSE,
+    SCAN_S4D_REAL,
+    SCAN_ZOH,
     SSMError,
     debug_bounds_status,
     lib,

@@ -175,7 +175,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
                                   int dim, int seqlen, int dstate, ssm_dtype io, int chunk_len, void* workspace,
                                   size_t workspace_bytes, unsigned int flags, void* stream) {
   if (!io_ok(io)) return SSM_ERR_UNSUPPORTED;
-  if (flags & ~(SSM_SCAN_REVERSE | SSM_SCAN_ZOH)) return SSM_ERR_INVALID_ARG;
+  if (flags & ~(SSM_SCAN_REVERSE | SSM_SCAN_ZOH | SSM_SCAN_S4D_REAL)) return SSM_ERR_INVALID_ARG;
   if (!dims_ok(batch, dim, seqlen, dstate)) return SSM_ERR_INVALID_ARG;
   if (dstate > ssm::kMaxDstateScan) return SSM_ERR_UNSUPPORTED;
   if (delta_softplus != 0 && delta_softplus != 1) return SSM_ERR_INVALID_ARG;
@@ -238,6 +238,7 @@ ssm_status ssm_selective_scan_fwd(const void* x, const void* delta, const float*
   a.lanes = lanes;
   a.reverse = (flags & SSM_SCAN_REVERSE) ? 1 : 0;
   a.zoh = (flags & SSM_SCAN_ZOH) ? 1 : 0;
+  a.s4d = (flags & SSM_SCAN_S4D_REAL) && !(flags & SSM_SCAN_ZOH) ? 1 : 0;
   ssm::scan_workspace_split(workspace, (long long)batch * dim, nchunks, &a.ws_S, &a.ws_h);
   return ssm::launch_scan(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

@@ -42,6 +42,7 @@ struct ScanArgs {
   int lanes;             // lanes per channel of the main pass: 1 (N <= 16), 2 (N <= 16) or 4 (N <= 32)
   int reverse;           // 1: the scan runs from t = L-1 down to t = 0
   int zoh;               // 1: zero-order-hold input term expm1(Delta A)/A B u
+  int s4d;               // 1: take Abar_n = Abar_0^(n+1) where every channel of a CTA has A[d,n] = (n+1) A[d,0]
   int ws_chunks;         // carry entries the workspace holds (nchunks-1; nchunks for a segment aggregate)
   float* ws_S;           // [ws_chunks][batch*dim] sum of Delta per chunk
   float* ws_h;           // [ws_chunks][batch*dim][scan_state_stride(dstate)] chunk end state from zero

@@ -81,7 +81,8 @@ def test_scan_argument_checks(L):
     assert _scan(L, conv_b=FAKE) == 1              # conv bias without conv weight
     assert _scan(L, x=FAKE + 2) == 2               # misaligned fp32 pointer
     assert _scan(L, chunk_len=-5) == 1
-    assert _scan(L, flags=4) == 1                  # unknown option bit
+    assert _scan(L, flags=8) == 1                  # unknown option bit
+    assert _scan(L, flags=4, batch=0) == 0         # SSM_SCAN_S4D_REAL is a scan option
     assert _scan(L, flags=1, x=None) == 1          # reverse: same checks
     assert _scan(L, seqlen=1 << 20, chunk_len=64, batch=1, dim=4) == 1   # chunked: workspace missing
     # empty work: no launch, OK
@@ -318,3 +319,15 @@ def test_library_selection_routes_the_binding():
         ssm.select_library("release")
     with pytest.raises(ssm.SSMError, match="UNSUPPORTED"):
         ssm.debug_bounds_status()
+
+
+def test_s4d_real_bit_only_on_the_scan(L):
+    """SSM_SCAN_S4D_REAL is an option of ssm_selective_scan_fwd; the segment aggregate and the
+    decode step refuse it on the host (SSM_ERR_INVALID_ARG)."""
+    import selective_state_space_145_b300 as ssm
+
+    assert ssm.SCAN_S4D_REAL == 4
+    assert L.ssm_selective_scan_aggregate(None, None, None, None, None, 1, None, None, 0, None, None, None,
+                                          1, 8, 16, 16, 0, None, 0, ssm.SCAN_S4D_REAL, None) == 1
+    assert L.ssm_selective_state_update(None, None, None, None, None, None, None, None, None, None, 1, None, None, 0,
+                                        None, 1, 8, 16, 0, ssm.SCAN_S4D_REAL, None) == 1
