@@ -109,3 +109,35 @@ def test_ssd_past_int32_indices(cuda_device, L):
         assert_close(hl[b:b + 1, sl], ref_h, "bf16", f"h_last b{b} h{h}")
     del p, y, hl
     _free()
+
+
+def test_backward_past_int32_indices(cuda_device):
+    """Scan backward, bf16, 4 x 16384 channels x 32800 steps: u, delta, z, dout and the three
+    per-token gradients hold 2.15e9 elements each, and the 8-step checkpoints 18 GB. Every
+    per-channel gradient (du, ddelta, dz, dh0; dA, dD, ddelta_bias, which sum over the channel's
+    sequences) of the sampled channels against the oracle; dB and dC sum over all channels and are
+    covered by the smaller backward tests."""
+    ssm = _ssm()
+    batch, dim, L, N = 4, 16384, 32800, 16
+    assert batch * dim * L > INT31
+    p = inputs.scan_inputs_on(cuda_device, batch, dim, L, N, 0, "bf16", seed=2034)
+    gen = torch.Generator(device=cuda_device).manual_seed(2035)
+    dout = torch.randn(batch, dim, L, generator=gen, device=cuda_device).to(torch.bfloat16)
+    dhl = torch.randn(batch, dim, N, generator=gen, device=cuda_device)
+    g = ssm.ssm_selective_scan_bwd(p["x"], p["delta"], p["A"], p["B"], p["C"], dout, p["D"], p["z"], p["delta_bias"],
+                                   True, None, dhl)
+    torch.cuda.synchronize()
+    # (b * dim + d) * L >= 2^31 for b = 3 and d past about 10000
+    for d in (0, 8000, 16383):
+        assert d < 16383 or (3 * dim + d) * L > INT31
+        sl = lambda t: t[:, d:d + 1].cpu()
+        ref = oracle.selective_scan_bwd(sl(p["x"]), sl(p["delta"]), p["A"][d:d + 1].cpu(), p["B"].cpu(), p["C"].cpu(),
+                                        sl(dout), p["D"][d:d + 1].cpu(), sl(p["z"]), p["delta_bias"][d:d + 1].cpu(),
+                                        True, None, sl(dhl), nthreads=oracle.oracle.default_threads())
+        for k in ("du", "ddelta", "dz", "dh0"):
+            assert_close(g[k][:, d:d + 1], ref[k], "bf16", f"{k}[:, {d}]")
+        assert_close(g["dA"][d:d + 1], ref["dA"], "bf16", f"dA[{d}]")
+        assert_close(g["dD"][d:d + 1], ref["dD"], "bf16", f"dD[{d}]")
+        assert_close(g["ddelta_bias"][d:d + 1], ref["ddelta_bias"], "bf16", f"ddelta_bias[{d}]")
+    del p, g, dout, dhl
+    _free()

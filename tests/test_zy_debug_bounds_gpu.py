@@ -11,6 +11,7 @@ import pytest
 
 import test_backward_gpu as bwd
 import test_parity_gpu as par
+import test_s4d_gpu as s4d
 import test_shard_gpu as seg
 import test_ssd_gpu as ssd
 
@@ -107,3 +108,9 @@ def test_debug_conv_backward(debug_lib, cuda_device, case):
 def test_debug_ssd(debug_lib, cuda_device, case):
     ssd.test_ssd_matches_oracle(cuda_device, case)
     _clean(debug_lib, "state-space duality")
+
+
+@pytest.mark.parametrize("case", s4d.CASES, ids=lambda c: "b{}_d{}_l{}_n{}_k{}_{}_cl{}_rev{}".format(*c))
+def test_debug_s4d_real(debug_lib, cuda_device, case):
+    s4d.test_s4d_matches_oracle_and_takes_the_powers(cuda_device, case)
+    _clean(debug_lib, "S4D-real scan")
