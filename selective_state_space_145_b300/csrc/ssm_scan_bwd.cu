@@ -71,49 +71,49 @@ struct Rows {
   static constexpr int kBytes = kRows * RS * (int)sizeof(T);
 };
 
-template <typename T>
-__device__ __forceinline__ const T* pick4(int k, const T* p0, const T* p1, const T* p2, const T* p3) {
-  return k == 0 ? p0 : (k == 1 ? p1 : (k == 2 ? p2 : p3));
+// One row of a tile: steps [t0, t0 + kTB) of row `rowbase` of `arr` (zeros past L or when !ok).
+template <typename T, int RS, bool VEC>
+__device__ __forceinline__ void copy_row(T* dst, const T* arr, long long rowbase, bool ok, long long ext, int t0,
+                                         int L, const void* fallback) {
+  constexpr int kEPC = 16 / (int)sizeof(T);
+  if (VEC) {
+#pragma unroll
+    for (int j = 0; j < kTB / kEPC; ++j) {
+      const int t = t0 + j * kEPC;
+      const bool v = ok && t < L && in_bounds(rowbase + t, kEPC, ext, kBoundsBackward);
+      cp_async16(dst + j * kEPC, v ? (const void*)(arr + rowbase + t) : fallback, v ? 16u : 0u);
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < kTB; ++s) {
+      const int t = t0 + s;
+      dst[s] = (ok && t < L && in_bounds(rowbase + t, 1, ext, kBoundsBackward)) ? arr[rowbase + t] : from_f32<T>(0.f);
+    }
+  }
 }
 
-// Stages steps [t0, t0 + kTB) of channel arrays c0..c3 (channels d0 .. d0+31 of sequence b) and
-// state arrays s0, s1 (states 0..15 of sequence b) into `ring`; zeros past L, dim, N or for a
-// NULL array. VEC: 16-byte cp.async pieces (the caller commits the group); else plain loads.
+// Stages steps [t0, t0 + kTB) of channel arrays c0..c3 (lane c copies its own channel d0 + c of
+// sequence b in each) and state arrays s0, s1 (lanes 0..15 rows n of s0, lanes 16..31 of s1)
+// into `ring`; zeros past L, dim, N or for a NULL array. VEC: 16-byte cp.async pieces (the
+// caller commits the group); else plain loads.
 template <typename T, int kCh, int kSt, bool VEC>
 __device__ __forceinline__ void stage_tile(T* ring, const ScanBwdArgs& a, const T* c0, const T* c1, const T* c2,
                                            const T* c3, const T* s0, const T* s1, int b, int d0, int t0, int lane) {
   using R = Rows<T, kCh, kSt>;
   const int L = a.seqlen, N = a.dstate, dim = a.dim;
   const long long tok = (long long)a.batch * dim * L, bcx = (long long)a.batch * N * L;
-  constexpr int kPer = VEC ? R::kCPR : kTB;   // copies per row
-  constexpr int kLen = VEC ? R::kEPC : 1;     // elements per copy
-#pragma unroll 1
-  for (int i = lane; i < R::kRows * kPer; i += kW) {
-    const int r = i / kPer, j = i % kPer;
-    const int t = t0 + j * kLen;
-    const T* src;
-    long long idx, ext;
-    bool ok = t < L;
-    if (r < kCh * kW) {
-      const int c = r % kW;
-      src = pick4<T>(r / kW, c0, c1, c2, c3);
-      ok = ok && d0 + c < dim;
-      idx = ((long long)b * dim + d0 + c) * L + t;
-      ext = tok;
-    } else {
-      const int rr = r - kCh * kW, n = rr % kNS;
-      src = rr / kNS == 0 ? s0 : s1;
-      ok = ok && n < N;
-      idx = ((long long)b * N + n) * L + t;
-      ext = bcx;
-    }
-    ok = ok && src != nullptr && in_bounds(idx, kLen, ext, kBoundsBackward);
-    T* dst = ring + r * R::RS + j * kLen;
-    if (VEC) {
-      cp_async16(dst, ok ? (const void*)(src + idx) : (const void*)c0, ok ? 16u : 0u);
-    } else {
-      *dst = ok ? src[idx] : from_f32<T>(0.f);
-    }
+  const long long crow = ((long long)b * dim + d0 + lane) * L;
+  const bool cvalid = d0 + lane < dim;
+#pragma unroll
+  for (int m = 0; m < kCh; ++m) {
+    const T* arr = m == 0 ? c0 : (m == 1 ? c1 : (m == 2 ? c2 : c3));  // m is known once unrolled
+    copy_row<T, R::RS, VEC>(ring + (m * kW + lane) * R::RS, arr, crow, cvalid && arr != nullptr, tok, t0, L, c0);
+  }
+  if (lane < kSt * kNS) {
+    const int n = lane % kNS;
+    const T* sarr = lane < kNS ? s0 : s1;
+    copy_row<T, R::RS, VEC>(ring + (kCh * kW + lane) * R::RS, sarr, ((long long)b * N + n) * L,
+                            n < N && sarr != nullptr, bcx, t0, L, c0);
   }
 }
 
