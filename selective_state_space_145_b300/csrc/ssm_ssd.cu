@@ -31,10 +31,18 @@
 // the end. The next chunk's decay prefix is computed while round B runs. The B tile serves as the
 // K-major B operand of G and, scaled, as the MN-major A operand of S: the two layouts are the
 // same bytes. Operands the kernel computes (G' and H_in) are carried as two bf16 terms,
-// hi = bf16(v) and lo = bf16(v - hi), multiplied in two GEMMs into one accumulator: a single bf16
-// rounding of them costs up to 2^-9 of each summand, which for sums of 128 products of O(1)
-// terms that cancel exceeds the bf16-I/O tolerance on a fraction of a percent of the outputs.
+// hi = bf16(v) and lo = bf16(v - hi): a single bf16 rounding of them costs up to 2^-9 of each
+// summand, which for sums of 128 products of O(1) terms that cancel exceeds the bf16-I/O
+// tolerance on a fraction of a percent of the outputs. G' hi and lo are two GEMMs into one
+// accumulator. The H_in hi and lo tiles are adjacent 64-column spans of one MN-major operand, so
+// C H_in is one GEMM of N = 128 whose two halves the epilogue adds.
+//
+// Each tcgen05.mma costs its issuing thread tens of cycles whatever its size, so the MMA loops are
+// unrolled (constant descriptor offsets) and the GEMMs are merged where they share an operand.
+// Two CTAs share an SM and its shared-memory bandwidth, which the operand reads, the TMA copies
+// and the thread passes together nearly fill.
 #include <cstring>
+#include <type_traits>
 
 #include <cuda.h>  // CUtensorMap and its encoder's signature (resolved at run time, not linked)
 #include <cuda_bf16.h>
@@ -77,8 +85,9 @@ struct Smem {
 };
 constexpr uint32_t kSlab = kQ * 128;  // bytes of a 64-column slab of a 128-row tile
 
-// TMEM columns: G [128 x 128] (Y_diag [128 x 64] after it), Y_off [128 x 64], S [128 x 64].
-constexpr uint32_t kColG = 0, kColDiag = 0, kColOff = 128, kColS = 192, kCols = 256;
+// TMEM columns: G [128 x 128] in round A, then Y_diag [128 x 64] and S [128 x 64] in its place in
+// round B; C H_in hi and lo [128 x 64] each, side by side.
+constexpr uint32_t kColG = 0, kColDiag = 0, kColS = 64, kColOff = 128, kColOffLo = 192, kCols = 256;
 
 __device__ __forceinline__ void unpack8(const unsigned char* p, float* f) {
   const uint4 v = *reinterpret_cast<const uint4*>(p);
@@ -190,10 +199,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     cp_async_commit();
   };
-  auto load_dt = [&](int q) -> float {
+  auto load_dt = [&](int q) -> bf16 {
     const int s = q * kQ + t;
     const long long i = ((long long)b * L + s) * H + h;
-    return (s < L && in_bounds(i, 1, nDt, kBoundsSsd)) ? to_f32(gdt[i]) : 0.f;
+    return (s < L && in_bounds(i, 1, nDt, kBoundsSsd)) ? gdt[i] : __float2bfloat16_rn(0.f);
   };
 
   // running state: row n = t of H [N x P], columns pb .. pb + 31, fp32
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
   write_state();
-  float dtv = load_dt(0);
+  bf16 dtv = load_dt(0);
   if (warp == 0) umma::tmem_alloc(&tslot, kCols);
   if (tid == 0) {
     umma::mbar_init(&mbar, 1);
@@ -261,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (half == 0) s_z[t] = lg2_approx(Delta) - cs;  // -inf past the end (Delta = 0): those columns vanish
   };
   float Delta, cs, c_end;
-  decay(0, dtv, Delta, cs, c_end);
+  decay(0, to_f32(dtv), Delta, cs, c_end);
   if (nc > 1) dtv = load_dt(1);
 
 #pragma unroll 1
@@ -279,22 +288,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     umma::fence_after_sync();
 
-    // ---- round A: G = C B^T, Y_off = C H_in (hi + lo)
+    // ---- round A: G = C B^T, Y_off = C [H_in hi | H_in lo] (one N = 128 GEMM)
     if (tid == 0 && !test_skip_mma) {
       constexpr uint32_t idG = umma::idesc_bf16(kQ, kQ, false, false);
-      constexpr uint32_t idOff = umma::idesc_bf16(kQ, kP, false, true);
-#pragma unroll 1
+      constexpr uint32_t idOff = umma::idesc_bf16(kQ, 2 * kP, false, true);
+#pragma unroll
       for (int kk = 0; kk < kN / 16; ++kk)
         umma::mma_bf16(tbase + kColG, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
                        umma::desc_sw128_kmajor(smem_addr(sB), kk, kSlab), idG, kk > 0);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < kN / 16; ++kk)
         umma::mma_bf16(tbase + kColOff, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
                        umma::desc_sw128_mnmajor(smem_addr(sH), kk, kSlab), idOff, kk > 0);
-#pragma unroll 1
-      for (int kk = 0; kk < kN / 16; ++kk)
-        umma::mma_bf16(tbase + kColOff, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
-                       umma::desc_sw128_mnmajor(smem_addr(sHL), kk, kSlab), idOff, true);
       umma::mma_commit(&mbar);
     }
     ok = __syncthreads_and(umma::mbar_wait(&mbar, parity, wait_limit) && ok);
@@ -303,17 +308,33 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!ok) break;
 
     // ---- G' (hi into the C tile, lo into the H tiles) and B~ = Delta_s exp(c_end - c_s) B_s
+    // Column block s0 of row t: G'[t, s] = G[t, s] 2^(c_t + lg2 Delta_s - c_s) for s <= t. The
+    // warp's rows are 32 wq .. 32 wq + 31: a block left of its diagonal needs no mask, one right
+    // of it is zero.
 #pragma unroll 1
     for (int j2 = 0; j2 < 2; ++j2) {
       const int s0 = 32 * (2 * j2 + half);
       uint4 hi[4], lo[4];
-      if (s0 < 32 * (wq + 1)) {  // some row of this warp reaches column s0
+      if (s0 <= 32 * wq) {
         float g[32];
         umma::tmem_ld32(trow + kColG + s0, g);
+        const float4* zq = reinterpret_cast<const float4*>(s_z + s0);
+        const bool diag = s0 == 32 * wq;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int s = s0 + j;
-          g[j] = s <= t ? g[j] * ex2_approx(cs + s_z[s]) : 0.f;
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 z = zq[j4];
+          const float2 a0 = fadd2(f2(cs), make_float2(z.x, z.y)), a1 = fadd2(f2(cs), make_float2(z.z, z.w));
+          float2 v0 = fmul2(make_float2(g[4 * j4], g[4 * j4 + 1]), make_float2(ex2_approx(a0.x), ex2_approx(a0.y)));
+          float2 v1 = fmul2(make_float2(g[4 * j4 + 2], g[4 * j4 + 3]), make_float2(ex2_approx(a1.x), ex2_approx(a1.y)));
+          if (diag) {  // exp2 of a masked entry may overflow; the select drops it
+            const int s = s0 + 4 * j4;
+            v0 = make_float2(s <= t ? v0.x : 0.f, s + 1 <= t ? v0.y : 0.f);
+            v1 = make_float2(s + 2 <= t ? v1.x : 0.f, s + 3 <= t ? v1.y : 0.f);
+          }
+          g[4 * j4] = v0.x;
+          g[4 * j4 + 1] = v0.y;
+          g[4 * j4 + 2] = v1.x;
+          g[4 * j4 + 3] = v1.y;
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) split8(g + 8 * k, hi[k], lo[k]);
@@ -329,38 +350,39 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     {
-      // B~ row r = Delta_r 2^(c_end - c_r) B_r, in half rows of 64 bytes. The scaling is per
-      // element, so the chunk order is free: taking chunk c ^ (r % 8) at step c spreads the 8
-      // rows of an atom over all banks.
-      auto scale_half = [&](int r, int slab, int hc, float w) {
+      // B~ row r = Delta_r 2^(c_end - c_r) B_r, NC 16-byte chunks from chunk c0 on. Every load
+      // is issued before the first store (the stores could alias the loads as far as the
+      // compiler knows). Chunk c of row r sits at position c ^ (r % 8) of the swizzled row.
+      auto scale = [&](auto nc_tag, int r, int slab, int c0, float w) {
+        constexpr int NC = decltype(nc_tag)::value;
         unsigned char* rowp = sB + (uint32_t)slab * kSlab + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+        uint4 v[NC];
 #pragma unroll
-        for (int c = 4 * hc; c < 4 * hc + 4; ++c) {
-          unsigned char* p = rowp + 16 * (c ^ (r & 7));
-          float f[8];
-          unpack8(p, f);
+        for (int c = 0; c < NC; ++c) v[c] = *reinterpret_cast<const uint4*>(rowp + 16 * ((c0 + c) ^ (r & 7)));
 #pragma unroll
-          for (int k = 0; k < 8; ++k) f[k] *= w;
-          *reinterpret_cast<uint4*>(p) = pack8(f);
+        for (int c = 0; c < NC; ++c) {
+          __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&v[c]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 x = fmul2(__bfloat1622float2(e[k]), f2(w));
+            e[k] = __floats2bfloat162_rn(x.x, x.y);
+          }
         }
+#pragma unroll
+        for (int c = 0; c < NC; ++c) *reinterpret_cast<uint4*>(rowp + 16 * ((c0 + c) ^ (r & 7))) = v[c];
       };
+      using Row = std::integral_constant<int, 8>;
+      using Half = std::integral_constant<int, 4>;
       // The G' pass above is uneven: rows are bound to warps by their TMEM lane quarter, and
       // warps 2, 3 and 7 mask two column blocks where warps 0, 1, 5 and 6 mask one and warp 4
       // none. Those three warps hand their B rows (row t of slab `half`) to the lighter warps;
       // a helper takes the weight of a row it does not own from the shared lg2 Delta_r - c_r.
-      if (warp != 2 && warp != 3 && warp != 7) {
-        const float w = Delta * ex2_approx(c_end - cs);
-        scale_half(t, half, 0, w);
-        scale_half(t, half, 1, w);
-      }
+      if (warp != 2 && warp != 3 && warp != 7) scale(Row{}, t, half, 0, Delta * ex2_approx(c_end - cs));
       if (warp == 4) {  // rows 64..127 of slab 0 (those of warps 2 and 3)
-        const float w2 = ex2_approx(s_z[64 + lane] + c_end), w3 = ex2_approx(s_z[96 + lane] + c_end);
-        scale_half(64 + lane, 0, 0, w2);
-        scale_half(64 + lane, 0, 1, w2);
-        scale_half(96 + lane, 0, 0, w3);
-        scale_half(96 + lane, 0, 1, w3);
+        scale(Row{}, 64 + lane, 0, 0, ex2_approx(s_z[64 + lane] + c_end));
+        scale(Row{}, 96 + lane, 0, 0, ex2_approx(s_z[96 + lane] + c_end));
       } else if (warp == 0 || warp == 1) {  // rows 96..127 of slab 1 (those of warp 7), one half each
-        scale_half(96 + lane, 1, warp, ex2_approx(s_z[96 + lane] + c_end));
+        scale(Half{}, 96 + lane, 1, 4 * warp, ex2_approx(s_z[96 + lane] + c_end));
       }
     }
     umma::fence_proxy_async();
@@ -372,15 +394,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) {
       constexpr uint32_t idDiag = umma::idesc_bf16(kQ, kP, false, true);
       constexpr uint32_t idS = umma::idesc_bf16(kN, kP, true, true);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < kQ / 16; ++kk)
         umma::mma_bf16(tbase + kColDiag, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
                        umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idDiag, kk > 0);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < kQ / 16; ++kk)
         umma::mma_bf16(tbase + kColDiag, umma::desc_sw128_kmajor(smem_addr(sH), kk, kSlab),
                        umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idDiag, true);
-#pragma unroll 1
+#pragma unroll
       for (int kk = 0; kk < kQ / 16; ++kk)
         umma::mma_bf16(tbase + kColS, umma::desc_sw128_mnmajor(smem_addr(sB), kk, kSlab),
                        umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idS, kk > 0);
@@ -395,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // passed the barrier before round B)
     float Delta_n = 0.f, cs_n = 0.f, c_end_n = 0.f;
     if (q + 1 < nc) {
-      decay(q + 1, dtv, Delta_n, cs_n, c_end_n);
+      decay(q + 1, to_f32(dtv), Delta_n, cs_n, c_end_n);
       if (q + 2 < nc) dtv = load_dt(q + 2);
     }
     ok = __syncthreads_and(umma::mbar_wait(&mbar, parity) && ok);
@@ -409,21 +431,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float et = ex2_approx(cs), dec = ex2_approx(c_end);
     bf16* yrow = static_cast<bf16*>(a.y) + (((long long)b * L + t0 + t) * H + h) * kP;
 #pragma unroll
-    for (int p0 = 0; p0 < kHalfP; p0 += 16) {
-      float yd[16], yo[16], sv[16];
-      umma::tmem_ld16x3(trow + kColDiag + pb + p0, trow + kColOff + pb + p0, trow + kColS + pb + p0, yd, yo, sv);
-      float xv[16];
+    for (int p0 = 0; p0 < kHalfP; p0 += 8) {
+      float yd[8], yo[8], sv[8], yl[8];
+      umma::tmem_ld8x4(trow + kColDiag + pb + p0, trow + kColOff + pb + p0, trow + kColS + pb + p0,
+                       trow + kColOffLo + pb + p0, yd, yo, sv, yl);
+      float xv[8];
       unpack8(reinterpret_cast<const unsigned char*>(&xr[p0 / 8]), xv);
-      unpack8(reinterpret_cast<const unsigned char*>(&xr[p0 / 8 + 1]), xv + 8);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        yd[j] = fmaf(et, yo[j], yd[j]) + Dh * xv[j];
+      for (int j = 0; j < 8; ++j) {
+        yd[j] = fmaf(et, yo[j] + yl[j], yd[j]) + Dh * xv[j];
         Hs[p0 + j] = fmaf(dec, Hs[p0 + j], sv[j]);
       }
-      if (t < len && in_bounds((((long long)b * L + t0 + t) * H + h) * kP + pb + p0, 16, nX, kBoundsSsd)) {
+      if (t < len && in_bounds((((long long)b * L + t0 + t) * H + h) * kP + pb + p0, 8, nX, kBoundsSsd))
         *reinterpret_cast<uint4*>(yrow + pb + p0) = pack8(yd);
-        *reinterpret_cast<uint4*>(yrow + pb + p0 + 8) = pack8(yd + 8);
-      }
     }
     write_state();
     umma::fence_before_sync();
