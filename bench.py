@@ -765,12 +765,13 @@ def ssd_algorithmic_bytes(w) -> int:
 def ssd_flops(w):
     """Tensor-core FLOPs of one step of the chunked dual form, per chunk of Q steps and head:
     C B^T (2 Q^2 N), the masked product with X (2 Q^2 P), C H_in (2 Q N P) and the chunk's state
-    increment B^T X (2 N Q P). Returns (algorithmic, executed): the kernel multiplies the two
-    computed operands (G' and H_in) as hi + lo bf16 pairs, which doubles two of the four."""
+    increment B^T X (2 N Q P). Returns (algorithmic, executed): the kernel multiplies the three
+    operands it computes (G', H_in and the decay-scaled B) as hi + lo bf16 pairs, which doubles
+    three of the four."""
     Q, N, P = SSD_Q, w.dstate, w.headdim
     units = w.batch * w.nheads * ((w.seqlen + Q - 1) // Q)
     alg = 2 * Q * Q * N + 2 * Q * Q * P + 2 * Q * N * P + 2 * N * Q * P
-    exe = 2 * Q * Q * N + 4 * Q * Q * P + 4 * Q * N * P + 2 * N * Q * P
+    exe = 2 * Q * Q * N + 4 * Q * Q * P + 4 * Q * N * P + 4 * N * Q * P
     return units * alg, units * exe
 
 

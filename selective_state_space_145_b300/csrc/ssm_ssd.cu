@@ -19,28 +19,32 @@
 // columns. Per chunk, two rounds of tcgen05 GEMMs (bf16 operands, fp32 accumulators in tensor
 // memory, issued by one thread, completion through an mbarrier):
 //   round A:  G = C B^T [Q x Q] and Y_off = C H_in [Q x P];
-//   (threads) G' = G masked to s <= t and scaled by exp(c_t - c_s) Delta_s; B~ = B scaled per row
-//             by Delta_s exp(c_end - c_s);
-//   round B:  Y_diag = G' X [Q x P] and S = B~^T X [N x P];
-//   (threads) y = Y_diag + exp(c_t) Y_off + D x; H <- exp(c_end) H + S.
-// Every tile is stored in the 128-byte swizzled layout (rows of 128 bytes in 1024-byte atoms).
-// The next chunk's C, B and X are copied in while the epilogue and the state update of the
-// current one run: when the sequence length is a multiple of the chunk, by five TMA bulk-tensor
-// copies of 128-byte rows issued by one thread (C and B as two slabs of 64 columns, X as one box),
-// which apply the swizzle themselves; otherwise by 16-byte cp.async copies with zero fill past
-// the end. The next chunk's decay prefix is computed while round B runs. The B tile serves as the
-// K-major B operand of G and, scaled, as the MN-major A operand of S: the two layouts are the
-// same bytes. Operands the kernel computes (G' and H_in) are carried as two bf16 terms,
-// hi = bf16(v) and lo = bf16(v - hi): a single bf16 rounding of them costs up to 2^-9 of each
-// summand, which for sums of 128 products of O(1) terms that cancel exceeds the bf16-I/O
-// tolerance on a fraction of a percent of the outputs. G' hi and lo are two GEMMs into one
+//   (threads) G' = G masked to s <= t and scaled by exp(c_t - c_s) Delta_s, into tensor memory as
+//             the A operand of Y_diag; exp(c_t) Y_off into Y_diag's accumulator; B~ = B scaled
+//             per row by Delta_s exp(c_end - c_s);
+//   round B:  Y_diag += G' X [Q x P] and S = B~^T X [N x P];
+//   (threads) y = Y_diag + D x; H <- exp(c_end) H + S.
+// Every shared-memory tile is stored in the 128-byte swizzled layout (rows of 128 bytes in
+// 1024-byte atoms). The next chunk's C, B and X are copied in while the epilogue and the state
+// update of the current one run: when the sequence length is a multiple of the chunk, by five TMA
+// bulk-tensor copies of 128-byte rows issued by one thread (C and B as two slabs of 64 columns, X
+// as one box), which apply the swizzle themselves; otherwise by 16-byte cp.async copies with zero
+// fill past the end. The next chunk's decay prefix is computed while round B runs.
+//
+// Precision. The three operands the kernel computes (G', H_in and B~) are carried as two bf16
+// terms, hi = bf16(v) and lo = bf16(v - hi), each multiplied by the same bf16 input: a single bf16
+// rounding costs up to 2^-9 of each summand, which for sums of 128 products of O(1) terms that
+// cancel exceeds the bf16-I/O tolerance. For G' and H_in that happened on a fraction of a percent
+// of the outputs; for B~, whose error the state carries from chunk to chunk, on 2 of the 33.5
+// million outputs of the 8 x 2048 x 32-head workload. G' hi and lo are two GEMMs into one
 // accumulator. The H_in hi and lo tiles are adjacent 64-column spans of one MN-major operand, so
-// C H_in is one GEMM of N = 128 whose two halves the epilogue adds.
+// C H_in is one GEMM of N = 128 whose halves are added when exp(c_t) Y_off is formed. B~ hi
+// replaces B in its tile (B serves as the K-major B operand of G and, scaled, as the MN-major A
+// operand of S: the same bytes); B~ lo goes to the C tile, free after round A since G' lives in
+// tensor memory.
 //
 // Each tcgen05.mma costs its issuing thread tens of cycles whatever its size, so the MMA loops are
-// unrolled (constant descriptor offsets) and the GEMMs are merged where they share an operand.
-// Two CTAs share an SM and its shared-memory bandwidth, which the operand reads, the TMA copies
-// and the thread passes together nearly fill.
+// unrolled (constant descriptor offsets). Two CTAs share an SM and its shared-memory bandwidth.
 #include <cstring>
 #include <type_traits>
 
@@ -85,9 +89,11 @@ struct Smem {
 };
 constexpr uint32_t kSlab = kQ * 128;  // bytes of a 64-column slab of a 128-row tile
 
-// TMEM columns: G [128 x 128] in round A, then Y_diag [128 x 64] and S [128 x 64] in its place in
-// round B; C H_in hi and lo [128 x 64] each, side by side.
-constexpr uint32_t kColG = 0, kColDiag = 0, kColS = 64, kColOff = 128, kColOffLo = 192, kCols = 256;
+// TMEM columns. Round A: G [128 x 128] at 0, C [H_in hi | H_in lo] [128 x 128] at 128. The G'
+// pass writes G' in G's place as the A operand of Y_diag (bf16 pairs, hi and lo of column block b
+// at 32 b and 32 b + 16), and 2^(c_t) Y_off into columns 192..255, where round B's Y_diag
+// GEMMs accumulate onto it; S [128 x 64] takes columns 128..191.
+constexpr uint32_t kColG = 0, kColOff = 128, kColOffLo = 192, kColDiag = 192, kColS = 128, kCols = 256;
 
 __device__ __forceinline__ void unpack8(const unsigned char* p, float* f) {
   const uint4 v = *reinterpret_cast<const uint4*>(p);
@@ -116,6 +122,16 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
     const float2 hf = __bfloat1622float2(h[k]);
     l[k] = __floats2bfloat162_rn(v[2 * k] - hf.x, v[2 * k + 1] - hf.y);
   }
+}
+
+// The pair v = hi + lo as bf16x2 terms (the first element in the low half): hi = bf16(v),
+// lo = bf16(v - hi).
+__device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(v.x - hf.x, v.y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // TMA: the tiles come from three tensor maps (C and B: 2-D [rows, 128], X: 3-D [rows, heads,
@@ -307,14 +323,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     umma::fence_after_sync();
     if (!ok) break;
 
-    // ---- G' (hi into the C tile, lo into the H tiles) and B~ = Delta_s exp(c_end - c_s) B_s
-    // Column block s0 of row t: G'[t, s] = G[t, s] 2^(c_t + lg2 Delta_s - c_s) for s <= t. The
-    // warp's rows are 32 wq .. 32 wq + 31: a block left of its diagonal needs no mask, one right
-    // of it is zero.
+    // ---- G' into TMEM, 2^(c_t) Y_off into Y_diag's accumulator, B~ = Delta_s 2^(c_end - c_s) B_s
+    // Column block b = 2 j2 + half (steps s0 = 32 b ..) of row t: G'[t, s] = G[t, s]
+    // 2^(c_t + lg2 Delta_s - c_s) for s <= t, written as bf16 pairs (hi to columns 32 b ..,
+    // lo to 32 b + 16 ..) in the columns of G this thread has just read. The warp's rows are
+    // 32 wq .. 32 wq + 31: a block left of its diagonal needs no mask, one right of it is zero.
 #pragma unroll 1
     for (int j2 = 0; j2 < 2; ++j2) {
       const int s0 = 32 * (2 * j2 + half);
-      uint4 hi[4], lo[4];
+      uint32_t hi[16], lo[16];
       if (s0 <= 32 * wq) {
         float g[32];
         umma::tmem_ld32(trow + kColG + s0, g);
@@ -331,81 +348,105 @@ __global__ void __launch_bounds__(kThreads, 2)
             v0 = make_float2(s <= t ? v0.x : 0.f, s + 1 <= t ? v0.y : 0.f);
             v1 = make_float2(s + 2 <= t ? v1.x : 0.f, s + 3 <= t ? v1.y : 0.f);
           }
-          g[4 * j4] = v0.x;
-          g[4 * j4 + 1] = v0.y;
-          g[4 * j4 + 2] = v1.x;
-          g[4 * j4 + 3] = v1.y;
+          split2(v0, hi[2 * j4], lo[2 * j4]);
+          split2(v1, hi[2 * j4 + 1], lo[2 * j4 + 1]);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) split8(g + 8 * k, hi[k], lo[k]);
       } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) hi[k] = lo[k] = make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
       }
+      umma::tmem_st16(trow + kColG + s0, hi);
+      umma::tmem_st16(trow + kColG + s0 + 16, lo);
+    }
+    {
+      // Y_diag's accumulator starts as 2^(c_t) (C H_in hi + C H_in lo): this thread's columns of
+      // row t, read and rewritten by this thread alone
+      const float et = ex2_approx(cs);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // row t, column chunk (s0 + 8k) / 8: slab s0 / 64
-        const uint32_t off = (uint32_t)(s0 >> 6) * kSlab + umma::sw128_off(t, ((s0 & 63) >> 3) + k);
-        *reinterpret_cast<uint4*>(sC + off) = hi[k];
-        *reinterpret_cast<uint4*>(sH + off) = lo[k];
+      for (int c0 = 0; c0 < kHalfP; c0 += 16) {
+        float oh[16], ol[16];
+        umma::tmem_ld16x2(trow + kColOff + pb + c0, trow + kColOffLo + pb + c0, oh, ol);
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(et * (oh[j] + ol[j]));
+        umma::tmem_st16(trow + kColDiag + pb + c0, v);
       }
     }
     {
-      // B~ row r = Delta_r 2^(c_end - c_r) B_r, NC 16-byte chunks from chunk c0 on. Every load
-      // is issued before the first store (the stores could alias the loads as far as the
-      // compiler knows). Chunk c of row r sits at position c ^ (r % 8) of the swizzled row.
+      // B~ row r = w_r B_r as hi = bf16(v) in place in the B tile and lo = bf16(v - hi) at the
+      // same position of the spent C tile: the MN-major A operands of S's two GEMMs. NC 16-byte
+      // chunks of row r from chunk c0 on; every load is issued before the first store (the
+      // stores could alias the loads as far as the compiler knows). Chunk c of row r sits at
+      // position c ^ (r % 8) of the swizzled row.
       auto scale = [&](auto nc_tag, int r, int slab, int c0, float w) {
         constexpr int NC = decltype(nc_tag)::value;
-        unsigned char* rowp = sB + (uint32_t)slab * kSlab + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+        const uint32_t rowo = (uint32_t)slab * kSlab + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
         uint4 v[NC];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) v[c] = *reinterpret_cast<const uint4*>(rowp + 16 * ((c0 + c) ^ (r & 7)));
+        for (int c = 0; c < NC; ++c) v[c] = *reinterpret_cast<const uint4*>(sB + rowo + 16 * ((c0 + c) ^ (r & 7)));
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&v[c]);
+          uint32_t* e = reinterpret_cast<uint32_t*>(&v[c]);
+          uint4 l;
+          uint32_t* le = reinterpret_cast<uint32_t*>(&l);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 x = fmul2(__bfloat1622float2(e[k]), f2(w));
-            e[k] = __floats2bfloat162_rn(x.x, x.y);
+            const float2 x = fmul2(__bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&e[k])), f2(w));
+            split2(x, e[k], le[k]);
           }
+          *reinterpret_cast<uint4*>(sC + rowo + 16 * ((c0 + c) ^ (r & 7))) = l;
         }
 #pragma unroll
-        for (int c = 0; c < NC; ++c) *reinterpret_cast<uint4*>(rowp + 16 * ((c0 + c) ^ (r & 7))) = v[c];
+        for (int c = 0; c < NC; ++c) *reinterpret_cast<uint4*>(sB + rowo + 16 * ((c0 + c) ^ (r & 7))) = v[c];
       };
-      using Row = std::integral_constant<int, 8>;
-      using Half = std::integral_constant<int, 4>;
-      // The G' pass above is uneven: rows are bound to warps by their TMEM lane quarter, and
-      // warps 2, 3 and 7 mask two column blocks where warps 0, 1, 5 and 6 mask one and warp 4
-      // none. Those three warps hand their B rows (row t of slab `half`) to the lighter warps;
-      // a helper takes the weight of a row it does not own from the shared lg2 Delta_r - c_r.
-      if (warp != 2 && warp != 3 && warp != 7) scale(Row{}, t, half, 0, Delta * ex2_approx(c_end - cs));
-      if (warp == 4) {  // rows 64..127 of slab 0 (those of warps 2 and 3)
-        scale(Row{}, 64 + lane, 0, 0, ex2_approx(s_z[64 + lane] + c_end));
-        scale(Row{}, 96 + lane, 0, 0, ex2_approx(s_z[96 + lane] + c_end));
-      } else if (warp == 0 || warp == 1) {  // rows 96..127 of slab 1 (those of warp 7), one half each
-        scale(Half{}, 96 + lane, 1, 4 * warp, ex2_approx(s_z[96 + lane] + c_end));
+      // The G' pass above is uneven: rows are bound to warps by their TMEM lane quarter; warps 2,
+      // 3 and 7 mask two column blocks, warps 0, 1, 5 and 6 one, warp 4 none. The B rows are
+      // dealt out against that (in 16-byte chunks, about as costly as a sixth of a block):
+      // warp w's own rows are row t of slab `half`, 8 chunks; warps 2, 3 and 7 keep chunks
+      // 0..3 of theirs, warp 4 takes chunks 4..7 of warps 2 and 3, and chunks 4..7 of warp 7's
+      // rows go one each to warps 0, 1, 5 and 6.
+      using C8 = std::integral_constant<int, 8>;
+      using C4 = std::integral_constant<int, 4>;
+      using C1 = std::integral_constant<int, 1>;
+      const float w_own = Delta * ex2_approx(c_end - cs);
+      if (warp == 2 || warp == 3 || warp == 7) {
+        scale(C4{}, t, half, 0, w_own);
+      } else {
+        scale(C8{}, t, half, 0, w_own);
+        if (warp == 4) {  // chunks 4..7 of rows 64..127 of slab 0 (warps 2 and 3)
+          scale(C4{}, 64 + lane, 0, 4, ex2_approx(s_z[64 + lane] + c_end));
+          scale(C4{}, 96 + lane, 0, 4, ex2_approx(s_z[96 + lane] + c_end));
+        } else {  // one of chunks 4..7 of rows 96..127 of slab 1 (warp 7)
+          const int c0 = warp == 0 ? 4 : warp == 1 ? 5 : warp == 5 ? 6 : 7;
+          scale(C1{}, 96 + lane, 1, c0, ex2_approx(s_z[96 + lane] + c_end));
+        }
       }
     }
+    umma::tmem_wait_st();
     umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
 
-    // ---- round B: Y_diag = G' X (hi + lo), S = B~^T X
+    // ---- round B: Y_diag += G' X (A from TMEM, hi + lo), S = B~^T X (hi + lo)
     if (tid == 0) {
       constexpr uint32_t idDiag = umma::idesc_bf16(kQ, kP, false, true);
       constexpr uint32_t idS = umma::idesc_bf16(kN, kP, true, true);
 #pragma unroll
-      for (int kk = 0; kk < kQ / 16; ++kk)
-        umma::mma_bf16(tbase + kColDiag, umma::desc_sw128_kmajor(smem_addr(sC), kk, kSlab),
-                       umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idDiag, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < kQ / 16; ++kk)
-        umma::mma_bf16(tbase + kColDiag, umma::desc_sw128_kmajor(smem_addr(sH), kk, kSlab),
-                       umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idDiag, true);
+      for (int kk = 0; kk < kQ / 16; ++kk) {  // K slice kk: steps 16 kk .., block kk / 2
+        const uint32_t a = tbase + kColG + 32u * (kk >> 1) + 8u * (kk & 1);
+        const uint64_t bx = umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab);
+        umma::mma_bf16_ta(tbase + kColDiag, a, bx, idDiag, true);
+        umma::mma_bf16_ta(tbase + kColDiag, a + 16u, bx, idDiag, true);
+      }
 #pragma unroll
       for (int kk = 0; kk < kQ / 16; ++kk)
         umma::mma_bf16(tbase + kColS, umma::desc_sw128_mnmajor(smem_addr(sB), kk, kSlab),
                        umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idS, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        umma::mma_bf16(tbase + kColS, umma::desc_sw128_mnmajor(smem_addr(sC), kk, kSlab),
+                       umma::desc_sw128_mnmajor(smem_addr(sX), kk, kSlab), idS, true);
       umma::mma_commit(&mbar);
     }
     // this step's x, for the skip term, before the tile is refilled
@@ -428,18 +469,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (q + 1 < nc) stage(q + 1);
 
     // ---- epilogue (row t) and state update (row n = t)
-    const float et = ex2_approx(cs), dec = ex2_approx(c_end);
+    const float dec = ex2_approx(c_end);
     bf16* yrow = static_cast<bf16*>(a.y) + (((long long)b * L + t0 + t) * H + h) * kP;
 #pragma unroll
     for (int p0 = 0; p0 < kHalfP; p0 += 8) {
-      float yd[8], yo[8], sv[8], yl[8];
-      umma::tmem_ld8x4(trow + kColDiag + pb + p0, trow + kColOff + pb + p0, trow + kColS + pb + p0,
-                       trow + kColOffLo + pb + p0, yd, yo, sv, yl);
+      float yd[8], sv[8];
+      umma::tmem_ld8x2(trow + kColDiag + pb + p0, trow + kColS + pb + p0, yd, sv);
       float xv[8];
       unpack8(reinterpret_cast<const unsigned char*>(&xr[p0 / 8]), xv);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        yd[j] = fmaf(et, yo[j] + yl[j], yd[j]) + Dh * xv[j];
+        yd[j] = fmaf(Dh, xv[j], yd[j]);
         Hs[p0 + j] = fmaf(dec, Hs[p0 + j], sv[j]);
       }
       if (t < len && in_bounds((((long long)b * L + t0 + t) * H + h) * kP + pb + p0, 8, nX, kBoundsSsd))

@@ -102,8 +102,9 @@ def test_ssd_work_and_bytes():
     units = 8 * 32 * (2048 // Q)
     alg, exe = bench.ssd_flops(w)
     assert alg == units * (2 * Q * Q * N + 2 * Q * Q * P + 2 * Q * N * P + 2 * N * Q * P)
-    # the two computed operands (G' and H_in) enter as hi + lo pairs: their two GEMMs run twice
-    assert exe == alg + units * (2 * Q * Q * P + 2 * Q * N * P)
+    # the three computed operands (G', H_in and the decay-scaled B) enter as hi + lo pairs: their
+    # three GEMMs run twice
+    assert exe == alg + units * (2 * Q * Q * P + 2 * Q * N * P + 2 * N * Q * P)
     tok = 8 * 2048
     assert bench.ssd_algorithmic_bytes(w) == (tok * 32 * 64 * 2 * 2 + tok * 32 * 2 + 2 * tok * 128 * 2
                                               + 8 * 32 * 64 * 128 * 4 + 32 * 4 * 3)

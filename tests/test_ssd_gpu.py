@@ -1,9 +1,11 @@
 """GPU parity of the multi-head SSM with one decay per head (the state-space-duality layer, run on
 the tcgen05 tensor cores), called through the C ABI, against the fp64 oracle on the same seeded
 inputs: whole small problems (one chunk, several chunks, a ragged last chunk, one step, with and
-without an initial state or softplus) and sampled heads of the full-size workload. Tolerance is
+without an initial state or softplus) and every head of the full-size workload. Tolerance is
 the bf16-I/O bound: |gpu - oracle| <= 1e-2 + 2e-2 |oracle| on y and on the final state.
 """
+
+import os
 
 import numpy as np
 import pytest
@@ -138,16 +140,15 @@ def test_ssd_empty(cuda_device):
     assert torch.count_nonzero(hl) == 0
 
 
-def test_ssd_workload_sampled_heads(cuda_device):
-    """The full-size workload in the benchmark's launch configuration; two (batch, head) pairs
-    are recomputed by the oracle (heads are independent, so a head's slice is exact)."""
+def test_ssd_workload_every_head(cuda_device):
+    """The full-size workload in the benchmark's launch configuration, every output and every
+    final state against the oracle (4.3e9 state updates: well under a second on the host's
+    cores)."""
     w = inputs.SSD_WORKLOADS["ssd_bf16_b8_l2048_h32_p64_n128"]
     p = inputs.ssd_workload_inputs(w)
     y, hl = _run(_dev(p, cuda_device))
     y, hl = y.cpu(), hl.cpu()
-    for b, h in ((0, 0), (w.batch - 1, w.nheads - 1)):
-        sl = slice(h, h + 1)
-        ref, ref_h = oracle.ssd(p["x"][b:b + 1, :, sl], p["dt"][b:b + 1, :, sl], p["A"][sl], p["B"][b:b + 1],
-                                p["C"][b:b + 1], p["D"][sl], p["dt_bias"][sl], True, None)
-        assert_close(y[b:b + 1, :, sl], ref, "bf16", f"y b{b} h{h}")
-        assert_close(hl[b:b + 1, sl], ref_h, "bf16", f"h_last b{b} h{h}")
+    ref, ref_h = oracle.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["dt_bias"], True, None,
+                            nthreads=os.cpu_count() or 1)
+    assert_close(y, ref, "bf16", "y")
+    assert_close(hl, ref_h, "bf16", "h_last")
