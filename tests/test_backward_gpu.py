@@ -203,3 +203,31 @@ def test_block_backward_chain(cuda_device):
     _assert_grad(gc["dx"], rc["dx"], "f32", "dx")
     _assert_grad(gc["dw"], rc["dw"], "f32", "dconv_w")
     _assert_grad(gc["dbias"], rc["dbias"], "f32", "dconv_b")
+
+
+@pytest.mark.parametrize("name", ["block_f32_b2_d1024_l1024_n16_k4", "block_bf16_b8_d2048_l2048_n16_k4"])
+def test_backward_workload_whole(cuda_device, name):
+    """The backward pass on a block workload at full size, in the benchmark's configuration (x
+    taken as the scan input u, the same seeded dout and dh_last): every element of every gradient
+    against the fp64 adjoint at the per-element bounds."""
+    import selective_state_space_145_b300 as ssm
+
+    w = inputs.WORKLOADS[name]
+    p = inputs.workload_inputs(w)
+    gen = torch.Generator().manual_seed(w.seed + 7)
+    dout = torch.randn(w.batch, w.dim, w.seqlen, generator=gen).to(p["x"].dtype)
+    dhl = torch.randn(w.batch, w.dim, w.dstate, generator=gen)
+    g = to_dev(p, cuda_device)
+    got = ssm.ssm_selective_scan_bwd(g["x"], g["delta"], g["A"], g["B"], g["C"], dout.to(cuda_device), g["D"], g["z"],
+                                     g["delta_bias"], True, g["h0"], dhl.to(cuda_device))
+    got = {k: (v.cpu() if v is not None else None) for k, v in got.items()}
+    del g
+    torch.cuda.synchronize()
+    ref = oracle.selective_scan_bwd(p["x"], p["delta"], p["A"], p["B"], p["C"], dout, p["D"], p["z"],
+                                    p["delta_bias"], True, p["h0"], dhl, nthreads=oracle.oracle.default_threads())
+    for k in GRADS:
+        if ref[k] is None:
+            assert got[k] is None, k
+            continue
+        _assert_grad(got[k], ref[k], w.io, k)
+        ref[k] = None
