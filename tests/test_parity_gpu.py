@@ -338,14 +338,14 @@ def test_zoh_decode_matches_oracle_and_scan(cuda_device, io):
 # Every output element of every workload is compared with the oracle: the oracle runs on all host
 # threads (about a second for the largest workload on a 16-core host), so no sampling is needed.
 
-def _workload_scan_whole(name, cuda_device):
+def _workload_scan_whole(name, cuda_device, reverse=False, zoh=False):
     w = inputs.WORKLOADS[name]
     p = inputs.workload_inputs(w)
     g = to_dev(p, cuda_device)
-    out, hL = gpu_scan(g)   # default chunking: the launch configuration the benchmark times
+    out, hL = gpu_scan(g, reverse=reverse, zoh=zoh)   # default chunking: the launch configuration the benchmark times
     torch.cuda.synchronize()
     del g
-    ref, refL = oracle_scan(p)
+    ref, refL = oracle_scan(p, reverse=reverse, zoh=zoh)
     del p
     assert_close(out, ref, w.io, f"{name} out")
     del ref
@@ -368,6 +368,15 @@ def test_workload_block_bf16_whole(cuda_device):
 @pytest.mark.slow
 def test_workload_longscan_bf16_whole(cuda_device):
     _workload_scan_whole("longscan_bf16_b1_d1536_l131072_n16", cuda_device)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["block_bf16_b8_d2048_l2048_n16_k4", "longscan_bf16_b1_d1536_l131072_n16"])
+@pytest.mark.parametrize("mode", ["reverse", "zoh"])
+def test_workload_options_whole(cuda_device, name, mode):
+    """The backward-direction scan and the ZOH rule on the bf16 workloads at full size, in the
+    launch configurations `bench.py --reverse` / `--zoh` time: every output against the oracle."""
+    _workload_scan_whole(name, cuda_device, reverse=mode == "reverse", zoh=mode == "zoh")
 
 
 @pytest.mark.slow
