@@ -231,3 +231,26 @@ def test_backward_workload_whole(cuda_device, name):
             continue
         _assert_grad(got[k], ref[k], w.io, k)
         ref[k] = None
+
+
+@pytest.mark.parametrize("name", ["block_f32_b2_d1024_l1024_n16_k4", "block_bf16_b8_d2048_l2048_n16_k4"])
+def test_conv_backward_workload_whole(cuda_device, name):
+    """The conv prologue's backward on a block workload at full size (the workload's x, conv
+    weights and window, a seeded dout): every element of dx, dconv_w, dconv_b and the window
+    gradient against the oracle at the per-element bounds."""
+    import selective_state_space_145_b300 as ssm
+
+    w = inputs.WORKLOADS[name]
+    p = inputs.workload_inputs(w)
+    gen = torch.Generator().manual_seed(w.seed + 9)
+    dout = torch.randn(w.batch, w.dim, w.seqlen, generator=gen).to(p["x"].dtype)
+    win = p.get("conv_init")
+    got = ssm.ssm_causal_conv1d_bwd(p["x"].to(cuda_device), p["conv_w"].to(cuda_device), dout.to(cuda_device),
+                                    p["conv_b"].to(cuda_device), win.to(cuda_device) if win is not None else None)
+    ref = oracle.causal_conv1d_bwd(p["x"], p["conv_w"], dout, p["conv_b"], win,
+                                   nthreads=oracle.oracle.default_threads())
+    _assert_grad(got["dx"], ref["dx"], w.io, "dx")
+    _assert_grad(got["dw"], ref["dw"], w.io, "dconv_w")
+    _assert_grad(got["dbias"], ref["dbias"], w.io, "dconv_b")
+    if win is not None:
+        _assert_grad(got["dconv_init"], ref["dwindow"], w.io, "dconv_init")

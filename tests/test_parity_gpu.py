@@ -380,9 +380,11 @@ def test_workload_options_whole(cuda_device, name, mode):
 
 
 @pytest.mark.slow
-def test_workload_decode_whole(cuda_device):
+@pytest.mark.parametrize("zoh", [False, True], ids=["euler", "zoh"])
+def test_workload_decode_whole(cuda_device, zoh):
     """The decode workload: 64 consecutive steps on every (sequence, channel); y of every step,
-    the final state and the final window against the oracle stepping the same inputs."""
+    the final state and the final window against the oracle stepping the same inputs (Euler, and
+    the ZOH rule that `bench.py --zoh` times)."""
     ssm = _ssm()
     w = inputs.WORKLOADS["decode_bf16_b256_d5120_n16_k4_x64"]
     q = inputs.workload_inputs(w)
@@ -392,10 +394,10 @@ def test_workload_decode_whole(cuda_device):
     for t in range(w.steps):
         y = ssm.ssm_selective_state_update(g["state"], g["conv_state"], g["x"][t], g["delta"][t], g["A"], g["B"][t],
                                            g["C"][t], g["D"], g["z"][t], g["delta_bias"], True, g["conv_w"],
-                                           g["conv_b"])
+                                           g["conv_b"], zoh=zoh)
         yr, state, win = oracle.state_update(state, win, q["x"][t], q["delta"][t], q["A"], q["B"][t], q["C"][t],
                                              q["D"], q["z"][t], q["delta_bias"], True, q["conv_w"], q["conv_b"],
-                                             nthreads=oracle.oracle.default_threads())
+                                             nthreads=oracle.oracle.default_threads(), zoh=zoh)
         assert_close(y, yr, "bf16", f"decode y step {t}")
     assert_close(g["state"], state, "bf16", "decode state after 64 steps")
     # the window holds raw inputs: moved bit for bit
