@@ -152,3 +152,15 @@ def test_ssd_workload_every_head(cuda_device):
                             nthreads=os.cpu_count() or 1)
     assert_close(y, ref, "bf16", "y")
     assert_close(hl, ref_h, "bf16", "h_last")
+
+
+def test_ssd_ragged_every_head(cuda_device):
+    """The cp.async copy path (a sequence length that is not a multiple of the 128-step chunk)
+    on a mid-size problem with an initial state: 16 chunks, a ragged last one, 32 heads; every
+    output and every final state against the oracle."""
+    p = inputs.ssd_inputs(2, 2000, 32, seed=2024, with_h0=True)
+    y, hl = _run(_dev(p, cuda_device))
+    ref, ref_h = oracle.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["dt_bias"], True, p["h0"],
+                            nthreads=os.cpu_count() or 1)
+    assert_close(y.cpu(), ref, "bf16", "y")
+    assert_close(hl.cpu(), ref_h, "bf16", "h_last")
