@@ -42,6 +42,7 @@ SMALL = [
     (2, 24, 333, 24, 3, "f32", True, True, True, 64),        # N = 24, chunks, ragged
     (2, 50, 300, 32, 4, "bf16", True, True, True, 128),      # N = 32, chunks, conv
     (1, 3000, 64, 32, 4, "bf16", False, False, False, 0),    # N = 32, many channel tiles
+    (1, 1536, 8192, 32, 4, "bf16", True, True, False, 0),    # N = 32, long: the default plan's many chunks
 ]
 
 
